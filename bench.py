@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark of neighborhood attention forward + backward on GB300.
+
+One step = one pass of the whole path on one batch of synthetic input resident in HBM:
+forward (O, LSE), then the backward's Delta prologue, dQ pass and dK/dV pass.  The headline
+workload is the 2D 1024x1024 / 9x9 / 8 heads x 32 bf16 problem of NATTEN issue #161 ("Backward pass
+is very slow towards much tokens and large kernels", the user's benchmark script, loss = O.sum(),
+so dO = 1).  Useful FLOPs follow the maintainer's arithmetic-intensity count in that thread:
+4*N*K*D*heads forward (QK^T and PV) and 10*N*K*D*heads backward.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead (bounded samples).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from neighborhood_attention_fwd_gb300 import inputs as nain  # noqa: E402
+
+METRIC = "NA fwd+bwd ms and useful TFLOP/s (1 GB300), % of roofline"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------------------------
+# Work and traffic model
+# ---------------------------------------------------------------------------------------------
+
+def useful_flops(w):
+    nkdh = float(w.tokens) * w.keys_per_query * w.D * w.heads
+    return 4.0 * nkdh, 10.0 * nkdh
+
+
+def kernel_bytes(w):
+    """Algorithmic bytes each kernel must move (read inputs once, write outputs once)."""
+    s = 2 if w.dtype == "bf16" else 4
+    rows = float(w.tokens) * w.heads
+    t = rows * w.D * s
+    return {"fwd": 4 * t + 4 * rows,            # q, k, v in; o out; lse out
+            "delta": 2 * t + 4 * rows,          # o, dO in; delta out
+            "dq": 5 * t + 8 * rows,             # q, k, v, dO in; dQ out; lse, delta in
+            "dkdv": 6 * t + 8 * rows}           # q, k, v, dO in; dK, dV out; lse, delta in
+
+
+def method_bytes(w):
+    """Bytes of the method per phase (forward: q,k,v,o,lse; backward: q,k,v,o,dO,dQ,dK,dV,lse,delta)."""
+    s = 2 if w.dtype == "bf16" else 4
+    rows = float(w.tokens) * w.heads
+    return 4 * rows * w.D * s + 4 * rows, 8 * rows * w.D * s + 12 * rows
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ---------------------------------------------------------------------------------------------
+# Clock sampling
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+# Oracle (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------------------------
+
+def oracle_sample(w, h, n_rows, seed=0):
+    """Time the oracle on a bounded sample: forward of n_rows query rows, dQ of n_rows rows and
+    dK/dV of n_rows rows.  Returns (seconds, useful FLOPs of the sample)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    total = w.tokens * w.heads
+    rows = np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.na_fwd(h["q"], h["k"], h["v"], w.kernel, w.dilation, w.scale, rows=rows)
+    oracle.na_bwd(h["q"], h["k"], h["v"], h["dO"], w.kernel, w.dilation, w.scale, qrows=rows, krows=rows)
+    dt = time.perf_counter() - t0
+    f_fwd, f_bwd = useful_flops(w)
+    frac = len(rows) / float(total)
+    return dt, (f_fwd + f_bwd) * frac, len(rows)
+
+
+def calibrate_oracle(w, h, target_s):
+    n = 64
+    dt, _, n = oracle_sample(w, h, n)
+    while dt < 0.5 and n < w.tokens * w.heads:
+        n *= 4
+        dt, _, n = oracle_sample(w, h, n)
+    return max(16, min(int(n * target_s / max(dt, 1e-6)), w.tokens * w.heads))
+
+
+def host_inputs(t):
+    return {k: nain.to_oracle_array(v) for k, v in t.items()}
+
+
+def cpu_baseline(w, t, target_s=15.0):
+    import oracle
+
+    h = host_inputs(t)
+    n = calibrate_oracle(w, h, target_s)
+    dt, flops, n = oracle_sample(w, h, n, seed=1)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle forward of {n} random query rows and backward (dQ of the same {n} rows, "
+                      f"dK/dV of {n} key rows) of {w.name}; useful FLOPs of the sample / wall time"}
+
+
+# ---------------------------------------------------------------------------------------------
+# Device step
+# ---------------------------------------------------------------------------------------------
+
+class Step:
+    """Buffers and launches of one fwd + bwd step on the current stream."""
+
+    def __init__(self, w, t):
+        import neighborhood_attention_fwd_gb300 as na
+
+        self.na = na
+        self.w = w
+        self.t = t
+        q = t["q"]
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        self.delta = torch.empty_like(self.lse)
+        self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+
+    def launch(self, events=None):
+        na, w, t = self.na, self.w, self.t
+        ev = events or {}
+        s = torch.cuda.current_stream()
+
+        def mark(name):
+            if name in ev:
+                ev[name].record(s)
+
+        mark("fwd0")
+        na.na_fwd(t["q"], t["k"], t["v"], self.o, self.lse, w.kernel, w.dilation, w.scale)
+        mark("fwd1")
+        na.na_bwd_delta(self.o, t["dO"], self.delta)
+        mark("delta1")
+        na.na_bwd_dq(t["q"], t["k"], t["v"], t["dO"], self.lse, self.delta, self.dq, w.kernel, w.dilation, w.scale)
+        mark("dq1")
+        na.na_bwd_dkdv(t["q"], t["k"], t["v"], t["dO"], self.lse, self.delta, self.dk, self.dv, w.kernel,
+                       w.dilation, w.scale)
+        mark("dkdv1")
+
+    LAUNCHES_PER_STEP = 4
+
+
+def run_ours(args, w, rank, world, dist):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import neighborhood_attention_fwd_gb300 as na
+
+    na.load()
+    t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
+    step = Step(w, t)
+    tensor_bytes = t["q"].numel() * t["q"].element_size()
+    flush = None
+    if tensor_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    names = ["fwd0", "fwd1", "delta1", "dq1", "dkdv1"]
+    for _ in range(args.warmup):
+        step.launch()
+        if flush is not None:
+            flush.fill_(1.0)
+    st, raw = na.na_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({raw:#x}) after warm-up")
+
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step.launch(evs[i])
+        if flush is not None:
+            flush.fill_(float(i))
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st, raw = na.na_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({raw:#x}) in the timed region")
+
+    per = {k: [] for k in ("fwd", "delta", "dq", "dkdv", "step")}
+    for e in evs:
+        per["fwd"].append(e["fwd0"].elapsed_time(e["fwd1"]))
+        per["delta"].append(e["fwd1"].elapsed_time(e["delta1"]))
+        per["dq"].append(e["delta1"].elapsed_time(e["dq1"]))
+        per["dkdv"].append(e["dq1"].elapsed_time(e["dkdv1"]))
+        per["step"].append(e["fwd0"].elapsed_time(e["dkdv1"]))
+    ms = {k: float(np.mean(v)) for k, v in per.items()}
+    ms_step = ms["step"]
+    if dist is not None:
+        tt = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    f_fwd, f_bwd = useful_flops(w)
+    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+
+    # --- roofline: per kernel, the slower of tile-level MMA FLOPs at the bf16 peak and the
+    # algorithmic bytes at HBM bandwidth
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    ten = peaks["bf16_tflops"] * 1e12
+    kb = kernel_bytes(w)
+    tile_flops = {"fwd": 0.0, "delta": 0.0, "dq": 0.0, "dkdv": 0.0}
+    if w.dtype == "bf16":
+        for which, name in ((0, "fwd"), (1, "dq"), (2, "dkdv")):
+            tile_flops[name] = float(na.na_plan_info(which, w.B, w.spatial, w.heads, w.D, w.kernel,
+                                                     w.dilation)["mma_flops"])
+    kernels = {}
+    for name in ("fwd", "delta", "dq", "dkdv"):
+        t_b = kb[name] / hbm
+        t_f = tile_flops[name] / ten
+        bound = "tensor" if t_f > t_b else "hbm"
+        sec = ms[name] * 1e-3
+        if bound == "tensor":
+            ach, peak, unit = tile_flops[name] / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        else:
+            ach, peak, unit = kb[name] / sec / 1e9, peaks["hbm_gbs"], "GB/s"
+        kernels[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                         "frac": ach / peak, "roof_ms": max(t_b, t_f) * 1e3, "tile_flops": tile_flops[name],
+                         "alg_bytes": kb[name]}
+    dom = max(("fwd", "delta", "dq", "dkdv"), key=lambda k: ms[k])
+    traffic = load_traffic(w.name, dom)
+    roof_step = sum(kernels[k]["roof_ms"] for k in kernels)
+    m_fwd, m_bwd = method_bytes(w)
+    useful_roof_ms = (max(f_fwd / ten, m_fwd / hbm) + max(f_bwd / ten, m_bwd / hbm)) * 1e3
+
+    # --- end to end through the public API with host buffers
+    e2e = run_e2e(args, w, t, step) if not args.no_e2e else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.dtype != "fp32" else "f32",
+        "data": "synthetic (seeded N(0,1) inputs, dO = ones as loss = O.sum())" if w.dO == "ones"
+                else "synthetic (seeded N(0,1) inputs and dO)",
+        "config": {"workload": w.name, "B": w.B, "spatial": list(w.spatial), "heads": w.heads, "D": w.D,
+                   "kernel": list(w.kernel), "dilation": list(w.dilation), "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps (256 MB write)"},
+        "ms": {"fwd": ms["fwd"], "bwd": ms["delta"] + ms["dq"] + ms["dkdv"], "fwd_bwd": ms_step,
+               "per_kernel": {k: ms[k] for k in ("fwd", "delta", "dq", "dkdv")}},
+        "tflops": {"fwd": f_fwd / (ms["fwd"] * 1e-3) / 1e12,
+                   "bwd": f_bwd / ((ms["delta"] + ms["dq"] + ms["dkdv"]) * 1e-3) / 1e12},
+        "roofline": {"bound": kernels[dom]["bound"], "achieved": kernels[dom]["achieved"],
+                     "peak": kernels[dom]["peak"], "unit": kernels[dom]["unit"], "frac": kernels[dom]["frac"],
+                     "traffic": traffic, "kernel": dom, "peak_source": peaks["source"]},
+        "roofline_step": {"tile_roof_ms": roof_step, "frac_tile": roof_step / ms_step,
+                          "useful_roof_ms": useful_roof_ms, "frac_useful": useful_roof_ms / ms_step},
+        "kernels": kernels,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+        "gpu_launches": Step.LAUNCHES_PER_STEP * args.steps,
+        "e2e": e2e,
+    }
+    return line, t
+
+
+def run_e2e(args, w, t, step):
+    """Same metric measured through the public API with host buffers: per step, copy q, k, v, dO
+    from pinned host memory, run forward + backward, copy O, LSE, dQ, dK, dV back."""
+    hs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in t.items()}
+    for k in hs:
+        hs[k].copy_(t[k])
+    outs = [step.o, step.lse, step.dq, step.dk, step.dv]
+    ho = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    dev_in = {k: torch.empty_like(v) for k, v in t.items()}
+    e2e_step = Step(w, dev_in)
+    e2e_step.o, e2e_step.lse, e2e_step.dq, e2e_step.dk, e2e_step.dv = outs[0], outs[1], outs[2], outs[3], outs[4]
+    e2e_step.delta = step.delta
+    steps = max(3, min(args.steps, 10))
+    s = torch.cuda.current_stream()
+
+    def one():
+        for k in dev_in:
+            dev_in[k].copy_(hs[k], non_blocking=True)
+        e2e_step.launch()
+        for d, hh in zip(outs, ho):
+            hh.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        one()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    f_fwd, f_bwd = useful_flops(w)
+    h2d = sum(v.numel() * v.element_size() for v in hs.values())
+    d2h = sum(x.numel() * x.element_size() for x in ho)
+    return {"value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def load_traffic(workload, kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if one exists for it."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    entry = data.get(workload, {}).get(kernel)
+    return None if entry is None else entry.get("dram_bytes_per_launch")
+
+
+def run_reference(args, w, rank):
+    """The oracle as it stands, timed on the host cores: each step is a bounded sample."""
+    import oracle
+
+    t = nain.make_inputs(w, device="cpu")
+    h = host_inputs(t)
+    n = calibrate_oracle(w, h, target_s=2.0)
+    for i in range(args.warmup):
+        oracle_sample(w, h, n, seed=100 + i)
+    times, flops = [], []
+    for i in range(args.steps):
+        dt, fl, n = oracle_sample(w, h, n, seed=i)
+        times.append(dt)
+        flops.append(fl)
+    value = float(np.sum(flops) / np.sum(times) / 1e12)
+    ms = float(np.mean(times) * 1e3)
+    sample = (f"each step: fp64 oracle forward of {n} random query rows and backward (dQ of those rows, dK/dV of "
+              f"{n} key rows) of {w.name}")
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "B": w.B, "spatial": list(w.spatial), "heads": w.heads, "D": w.D,
+                   "kernel": list(w.kernel), "dilation": list(w.dilation), "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=nain.HEADLINE, choices=sorted(nain.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = nain.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w, rank)), flush=True)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    line, t = run_ours(args, w, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w, t, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

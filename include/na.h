@@ -1,0 +1,145 @@
+/*
+ * na.h -- C ABI of libna: multi-dimensional neighborhood attention (NA), forward and backward,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * What is computed.  NATTEN issue #161, "Backward pass is very slow towards much tokens and large
+ * kernels" (the user's benchmark script: na2d/na3d(query, key, value, kernel_size) and the unfused
+ * na*_qk -> softmax -> na*_av chain with a dilation argument) is the source of the operation; it
+ * never writes the window down, so this library fixes the plainest reading:
+ *   per spatial axis of length L, odd kernel size k (r = k/2) and dilation d, query index i is in
+ *   residue class c = i mod d at class index j = i div d; the class has Lc = ceil((L-c)/d) positions;
+ *   the window starts at class index s = clamp(j - r, 0, Lc - k) -- shifted, never truncated, at the
+ *   borders -- and holds the k positions c + d*(s+t), t = 0..k-1.  A query's neighbourhood is the
+ *   Cartesian product of its per-axis windows (every query sees exactly prod(k) keys).
+ *   O_i = sum_j softmax_j(scale * <q_i, k_j>) v_j over that neighbourhood;
+ *   LSE_i = natural-log logsumexp of the scaled logits.
+ * The backward follows the maintainer's fused-kernel profile in the same issue: a ComputeDelta
+ * prologue Delta_i = <dO_i, O_i>, then dQ, dK and dV from the recomputed probabilities.
+ *
+ * Tensor layout (all entry points).  q, k, v, o, dO, dQ, dK, dV are contiguous
+ * [B, L_1, ..., L_ndim, heads, D] arrays of one element type (the layout of NATTEN's fused ops,
+ * [b, (t,) h, w, heads, dim] in the user's script); lse and delta are contiguous fp32
+ * [B, L_1, ..., L_ndim, heads].  Every pointer is a DEVICE pointer owned by the caller; the
+ * library keeps none of them after a call returns.  All work is enqueued on `stream` (a
+ * cudaStream_t passed as void*; NULL is the legacy default stream) and the calls return without
+ * waiting for it.
+ *
+ * Errors.  Arguments are validated before anything is enqueued; on a validation error nothing is
+ * written and no work is enqueued.  No entry point aborts, prints or traps.  Device-side waits
+ * are bounded: a wait that runs out records NA_ERR_TIMEOUT in a per-device status word that
+ * na_device_status() reports.
+ */
+#ifndef NA_H_
+#define NA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NA_BF16 = 0, /* bfloat16 tensors; tcgen05 tensor-core kernels, fp32 accumulation */
+    NA_FP32 = 1  /* float32 tensors; CUDA-core FMA kernels, fp32 throughout */
+} na_dtype;
+
+typedef enum {
+    NA_OK = 0,
+    NA_ERR_INVALID_ARG = 1, /* bad sizes, kernel, dilation, scale or a null pointer */
+    NA_ERR_UNSUPPORTED = 2, /* valid NA problem outside what the kernels implement (see below) */
+    NA_ERR_ALIGNMENT = 3,   /* a tensor pointer is not 16-byte aligned */
+    NA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+    NA_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out (reported by na_device_status) */
+    NA_ERR_WORKSPACE = 6    /* workspace too small, or it could not be allocated */
+} na_status;
+
+/*
+ * Forward.  Writes o (same type as q) and lse (fp32, natural log).
+ *   B >= 1; 1 <= ndim <= 3; spatial[a] >= 1; heads >= 1;
+ *   kernel[a] odd and >= 1; dilation[a] >= 1; spatial[a] / dilation[a] >= kernel[a]
+ *   (every residue class holds at least k positions); scale finite (the workloads use D^-0.5).
+ *   Every tensor pointer 16-byte aligned.
+ * Supported (else NA_ERR_UNSUPPORTED):
+ *   NA_BF16: D in {16, 32, 64}; dilation[a] <= 8; per-axis halos within the TMA box limit.
+ *   NA_FP32: D a multiple of 4, D <= 128.
+ */
+na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int ndim, const int* spatial, int heads, int D,
+                 const int* kernel, const int* dilation, float scale,
+                 na_dtype dtype, void* stream);
+
+/* Bytes of workspace na_bwd needs (the fp32 Delta array, B * prod(spatial) * heads * 4, rounded
+   up to 256).  Returns 0 for invalid sizes. */
+size_t na_bwd_workspace_size(int B, int ndim, const int* spatial, int heads);
+
+/*
+ * Backward = na_bwd_delta + na_bwd_dq + na_bwd_dkdv.  Reads q, k, v, o, dO and the forward's lse;
+ * writes dQ, dK, dV (same type as q).  Each output element is written exactly once (no atomics),
+ * so the result is bitwise deterministic.
+ *   workspace: device memory of at least na_bwd_workspace_size() bytes, or NULL, in which case
+ *   the call allocates it with cudaMallocAsync and frees it with cudaFreeAsync on `stream`.
+ * Argument rules and support are those of na_fwd.
+ */
+na_status na_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dQ, void* dK, void* dV,
+                 int B, int ndim, const int* spatial, int heads, int D,
+                 const int* kernel, const int* dilation, float scale, na_dtype dtype,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Backward step 1 (the maintainer's "ComputeDelta"): delta[row] = sum_c dO[row, c] * o[row, c]
+ * for every (batch, token, head) row, in fp32.  delta: fp32 [B, L.., heads].
+ */
+na_status na_bwd_delta(const void* o, const void* dO, float* delta,
+                       int B, int ndim, const int* spatial, int heads, int D,
+                       na_dtype dtype, void* stream);
+
+/*
+ * Backward step 2: dQ_i = scale * sum_{j in N(i)} P_ij (<dO_i, v_j> - delta_i) k_j, with
+ * P_ij = exp(scale <q_i, k_j> - lse_i).  One pass over query tiles; writes every dQ row once.
+ */
+na_status na_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
+                    const float* lse, const float* delta, void* dQ,
+                    int B, int ndim, const int* spatial, int heads, int D,
+                    const int* kernel, const int* dilation, float scale,
+                    na_dtype dtype, void* stream);
+
+/*
+ * Backward step 3: dV_j = sum_{i : j in N(i)} P_ij dO_i and
+ * dK_j = scale * sum_{i : j in N(i)} P_ij (<dO_i, v_j> - delta_i) q_i.  One pass over key tiles,
+ * each walking the queries whose windows hold its keys (the inverse neighbourhood); every dK/dV
+ * row is written once, with no atomics.
+ */
+na_status na_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                      const float* lse, const float* delta, void* dK, void* dV,
+                      int B, int ndim, const int* spatial, int heads, int D,
+                      const int* kernel, const int* dilation, float scale,
+                      na_dtype dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.  Returns
+ * NA_ERR_TIMEOUT if a kernel gave up on a bounded wait since the last call, NA_ERR_CUDA if the
+ * stream reports an error, else NA_OK.  If raw is non-NULL it receives the raw status word
+ * (0x5000 | wait site) for diagnostics.
+ */
+na_status na_device_status(void* stream, uint32_t* raw);
+
+/* Static description of a status code. */
+const char* na_strerror(na_status status);
+
+/*
+ * Tile plan the bf16 kernels would use for this problem, for benchmarking and roofline
+ * accounting.  which: 0 = forward, 1 = dQ, 2 = dK/dV.  out[16] receives
+ *   {T1, T2, T3, H1, H2, H3, G1, G2, G3, NC, chunks_per_tile_max, tiles, mma_flops_per_tile_hi,
+ *    mma_flops_per_tile_lo, tmem_cols, smem_bytes}
+ * (axes embedded as 3D, outermost first; mma flops split into two 32-bit halves).
+ */
+na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads, int D,
+                       const int* kernel, const int* dilation, int64_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NA_H_ */

@@ -1,0 +1,218 @@
+"""libna: GB300-native multi-dimensional neighborhood attention (NA), forward and backward.
+
+A thin ctypes binding over the C ABI in include/na.h: every function takes torch tensors that
+already live on the GPU, checks shapes, and passes raw device pointers, sizes and the current CUDA
+stream to the library.  All arithmetic runs in the library's CUDA kernels (tcgen05 tensor-core
+kernels for bf16, CUDA-core FMA kernels for fp32); there is no fallback of any kind, and a missing
+library raises.
+
+Tensors are contiguous [B, L_1, .., L_n, heads, D] (n = 1..3); lse/delta are fp32 [B, L.., heads].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "NAError", "load", "na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv",
+    "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
+]
+
+NA_BF16, NA_FP32 = 0, 1
+_STATUS = {0: "NA_OK", 1: "NA_ERR_INVALID_ARG", 2: "NA_ERR_UNSUPPORTED", 3: "NA_ERR_ALIGNMENT",
+           4: "NA_ERR_CUDA", 5: "NA_ERR_TIMEOUT", 6: "NA_ERR_WORKSPACE"}
+
+_lib = None
+
+
+class NAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_STATUS.get(status, status)} ({na_strerror(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Load libna.so (built by neighborhood_attention_fwd_gb300.build.build()); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libna.so not found at {path}: run neighborhood_attention_fwd_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    IP = ctypes.POINTER(ctypes.c_int)
+    geo = [I, I, IP, I, I]                   # B, ndim, spatial, heads, D
+    kd = [IP, IP, F]                         # kernel, dilation, scale
+    lib.na_fwd.argtypes = [P, P, P, P, P] + geo + kd + [I, P]
+    lib.na_bwd.argtypes = [P, P, P, P, P, P, P, P, P] + geo + kd + [I, P, ctypes.c_size_t, P]
+    lib.na_bwd_delta.argtypes = [P, P, P] + geo + [I, P]
+    lib.na_bwd_dq.argtypes = [P, P, P, P, P, P, P] + geo + kd + [I, P]
+    lib.na_bwd_dkdv.argtypes = [P, P, P, P, P, P, P, P] + geo + kd + [I, P]
+    lib.na_bwd_workspace_size.argtypes = [I, I, IP, I]
+    lib.na_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.na_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.na_strerror.argtypes = [I]
+    lib.na_strerror.restype = ctypes.c_char_p
+    lib.na_plan_info.argtypes = [I, I, I, IP, I, I, IP, IP, ctypes.POINTER(ctypes.c_int64)]
+    for f in ("na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv", "na_device_status", "na_plan_info"):
+        getattr(lib, f).restype = I
+    _lib = lib
+    return lib
+
+
+def na_strerror(status: int) -> str:
+    return load().na_strerror(int(status)).decode()
+
+
+def _ints(vals):
+    vals = [int(x) for x in vals]
+    return (ctypes.c_int * len(vals))(*vals)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return NA_BF16
+    if t.dtype == torch.float32:
+        return NA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _geometry(q: torch.Tensor):
+    if q.dim() < 4 or q.dim() > 6:
+        raise ValueError("expected [B, L_1..L_n, heads, D] with n in 1..3")
+    B = q.shape[0]
+    spatial = tuple(int(s) for s in q.shape[1:-2])
+    return B, len(spatial), spatial, int(q.shape[-2]), int(q.shape[-1])
+
+
+def _check(t: torch.Tensor, shape, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name}: expected {tuple(shape)} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ok(status: int, what: str):
+    if status != 0:
+        raise NAError(status, what)
+
+
+def _kd(ndim, kernel, dilation):
+    kernel = (kernel,) * ndim if isinstance(kernel, int) else tuple(kernel)
+    dilation = (1,) * ndim if dilation is None else ((dilation,) * ndim if isinstance(dilation, int) else tuple(dilation))
+    if len(kernel) != ndim or len(dilation) != ndim:
+        raise ValueError("kernel and dilation need one entry per spatial axis")
+    return kernel, dilation
+
+
+def na_fwd(q, k, v, o, lse, kernel, dilation=None, scale=None, stream=None):
+    """O = NA(q, k, v) and the natural-log LSE, written into o and lse."""
+    B, ndim, spatial, heads, D = _geometry(q)
+    for name, t in (("k", k), ("v", v), ("o", o)):
+        _check(t, q.shape, q.dtype, name)
+    _check(q, q.shape, q.dtype, "q")
+    _check(lse, q.shape[:-1], torch.float32, "lse")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = load().na_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       B, ndim, _ints(spatial), heads, D, _ints(kernel), _ints(dilation), scale,
+                       _dtype_code(q), _stream(stream))
+    _ok(st, "na_fwd")
+
+
+def na_bwd_workspace_size(B, spatial, heads) -> int:
+    return int(load().na_bwd_workspace_size(int(B), len(spatial), _ints(spatial), int(heads)))
+
+
+def na_bwd(q, k, v, o, dO, lse, dQ, dK, dV, kernel, dilation=None, scale=None, workspace=None, stream=None):
+    """dQ, dK, dV of NA for upstream gradient dO (Delta prologue + dQ pass + dK/dV pass)."""
+    B, ndim, spatial, heads, D = _geometry(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dO", dO), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _check(t, q.shape, q.dtype, name)
+    _check(lse, q.shape[:-1], torch.float32, "lse")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    scale = D ** -0.5 if scale is None else float(scale)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = load().na_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                       dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), B, ndim, _ints(spatial), heads, D,
+                       _ints(kernel), _ints(dilation), scale, _dtype_code(q), ws_ptr, ws_bytes, _stream(stream))
+    _ok(st, "na_bwd")
+
+
+def na_bwd_delta(o, dO, delta, stream=None):
+    """delta = <dO, O> per row (fp32)."""
+    B, ndim, spatial, heads, D = _geometry(o)
+    _check(dO, o.shape, o.dtype, "dO")
+    _check(delta, o.shape[:-1], torch.float32, "delta")
+    st = load().na_bwd_delta(o.data_ptr(), dO.data_ptr(), delta.data_ptr(), B, ndim, _ints(spatial), heads, D,
+                             _dtype_code(o), _stream(stream))
+    _ok(st, "na_bwd_delta")
+
+
+def na_bwd_dq(q, k, v, dO, lse, delta, dQ, kernel, dilation=None, scale=None, stream=None):
+    B, ndim, spatial, heads, D = _geometry(q)
+    for name, t in (("k", k), ("v", v), ("dO", dO), ("dQ", dQ)):
+        _check(t, q.shape, q.dtype, name)
+    _check(lse, q.shape[:-1], torch.float32, "lse")
+    _check(delta, q.shape[:-1], torch.float32, "delta")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = load().na_bwd_dq(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(), delta.data_ptr(),
+                          dQ.data_ptr(), B, ndim, _ints(spatial), heads, D, _ints(kernel), _ints(dilation), scale,
+                          _dtype_code(q), _stream(stream))
+    _ok(st, "na_bwd_dq")
+
+
+def na_bwd_dkdv(q, k, v, dO, lse, delta, dK, dV, kernel, dilation=None, scale=None, stream=None):
+    B, ndim, spatial, heads, D = _geometry(q)
+    for name, t in (("k", k), ("v", v), ("dO", dO), ("dK", dK), ("dV", dV)):
+        _check(t, q.shape, q.dtype, name)
+    _check(lse, q.shape[:-1], torch.float32, "lse")
+    _check(delta, q.shape[:-1], torch.float32, "delta")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = load().na_bwd_dkdv(q.data_ptr(), k.data_ptr(), v.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+                            delta.data_ptr(), dK.data_ptr(), dV.data_ptr(), B, ndim, _ints(spatial), heads, D,
+                            _ints(kernel), _ints(dilation), scale, _dtype_code(q), _stream(stream))
+    _ok(st, "na_bwd_dkdv")
+
+
+def na_device_status(stream=None):
+    """Synchronise the stream and return (status, raw status word); clears the word."""
+    raw = ctypes.c_uint32(0)
+    st = load().na_device_status(_stream(stream), ctypes.byref(raw))
+    return int(st), int(raw.value)
+
+
+PLAN_FIELDS = ("T1", "T2", "T3", "H1", "H2", "H3", "G1", "G2", "G3", "NC", "chunks_max", "ctas", "mma_flops",
+               "tmem_cols", "smem_bytes", "chunks_total")
+
+
+def na_plan_info(which: int, B, spatial, heads, D, kernel, dilation=None) -> dict:
+    """Tile plan of the bf16 kernel `which` (0 forward, 1 dQ, 2 dK/dV) for this problem."""
+    ndim = len(spatial)
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    out = (ctypes.c_int64 * 16)()
+    st = load().na_plan_info(int(which), int(B), ndim, _ints(spatial), int(heads), int(D), _ints(kernel),
+                             _ints(dilation), out)
+    _ok(st, "na_plan_info")
+    return dict(zip(PLAN_FIELDS, [int(x) for x in out]))

@@ -1,0 +1,555 @@
+// na_api.cu -- the C ABI of libna (include/na.h): argument validation, embedding of 1/2/3-D
+// problems as 3 axes, the static tile planner of the tensor-core kernels, TMA tensor-map encoding,
+// the per-device status word and the launches.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/na.h"
+#include "na_internal.h"
+
+namespace na {
+uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D);
+}
+
+namespace {
+
+using na::Geom;
+using na::TilePlan;
+
+// Per-device status word written by kernels whose bounded waits ran out.
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+na_status status_ptr(unsigned** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return NA_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<unsigned*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return NA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+na_status get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return NA_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return NA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return NA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Validate sizes and embed the problem as 3 axes (outermost first).
+na_status make_geom(int B, int ndim, const int* spatial, int heads, int D, const int* kernel, const int* dilation,
+                    Geom& g) {
+    if (ndim < 1 || ndim > 3 || !spatial || !kernel || !dilation || B < 1 || heads < 1 || D < 1)
+        return NA_ERR_INVALID_ARG;
+    g.B = B;
+    g.heads = heads;
+    g.D = D;
+    const int off = 3 - ndim;
+    for (int a = 0; a < 3; ++a) {
+        g.L[a] = 1;
+        g.k[a] = 1;
+        g.d[a] = 1;
+    }
+    long long tokens = 1;
+    for (int a = 0; a < ndim; ++a) {
+        const int L = spatial[a], k = kernel[a], d = dilation[a];
+        if (L < 1 || k < 1 || (k % 2) == 0 || d < 1 || L / d < k) return NA_ERR_INVALID_ARG;
+        g.L[off + a] = L;
+        g.k[off + a] = k;
+        g.d[off + a] = d;
+        tokens *= L;
+    }
+    const long long elems = tokens * B * heads * static_cast<long long>(D);
+    if (tokens > (1LL << 31) || elems > (1LL << 40)) return NA_ERR_UNSUPPORTED;
+    return NA_OK;
+}
+
+long long tokens_of(const Geom& g) { return static_cast<long long>(g.L[0]) * g.L[1] * g.L[2]; }
+
+// ---------------------------------------------------------------------------------------------
+// Tile planner of the tensor-core kernels
+// ---------------------------------------------------------------------------------------------
+
+struct PlanKey {
+    int which, D, B, heads, L[3], k[3], d[3];
+    bool operator<(const PlanKey& o) const {
+        return std::tie(which, D, B, heads, L[0], L[1], L[2], k[0], k[1], k[2], d[0], d[1], d[2]) <
+               std::tie(o.which, o.D, o.B, o.heads, o.L[0], o.L[1], o.L[2], o.k[0], o.k[1], o.k[2], o.d[0], o.d[1],
+                        o.d[2]);
+    }
+};
+
+std::map<PlanKey, TilePlan> g_plans;
+
+// Chunks a CTA whose tile starts at class index t0 actually processes along one outer axis, as the
+// kernels compute it (window or inverse-window range, halo box clamped into the class).
+int chunks_along(int which, int t0, int T, int Lc, int k, int H, int G, int nchk) {
+    const int last = std::min(t0 + T, Lc) - 1;
+    int lo, hi;
+    auto ws = [&](int j) { return std::max(0, std::min(j - k / 2, Lc - k)); };
+    if (which != 2) {
+        lo = ws(t0);
+        hi = ws(last) + k - 1;
+    } else {
+        lo = t0 < k ? 0 : t0 - k / 2;
+        hi = last >= Lc - k ? Lc - 1 : last + k / 2;
+    }
+    const int h0 = std::min(lo, std::max(0, Lc - H));
+    return std::min(nchk, ceil_div(hi - h0 + 1, G));
+}
+
+na_status plan_tc(int which, const Geom& g, TilePlan& out) {
+    const PlanKey key{which, g.D, g.B, g.heads, {g.L[0], g.L[1], g.L[2]}, {g.k[0], g.k[1], g.k[2]},
+                      {g.d[0], g.d[1], g.d[2]}};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            out = it->second;
+            return NA_OK;
+        }
+    }
+    const int D = g.D;
+    int tmem_cols, ncmax;
+    if (which == 0) {
+        tmem_cols = 128;
+        ncmax = 128 - D;
+    } else if (which == 1) {
+        tmem_cols = 256;
+        ncmax = (256 - D) / 2;
+    } else {
+        tmem_cols = 256;
+        ncmax = (256 - 2 * D) / 2;
+    }
+    ncmax = std::min(256, ncmax) / 16 * 16;
+    int Lcm[3];
+    for (int a = 0; a < 3; ++a) Lcm[a] = ceil_div(g.L[a], g.d[a]);
+    const int n_score = which == 0 ? 1 : 2, n_update = which == 2 ? 2 : 1;
+
+    bool found = false;
+    double best = 0;
+    TilePlan bp{};
+    for (int T2 = 8; T2 <= 128; T2 *= 2)
+        for (int T1 = 1; T1 * T2 <= 128; T1 *= 2) {
+            const int T0 = 128 / (T1 * T2);
+            const int T[3] = {T0, T1, T2};
+            bool skip = false;
+            for (int a = 0; a < 3; ++a)
+                if (T[a] * g.d[a] > 256) skip = true;  // TMA box limit (rows past an axis end are just idle)
+            if (skip) continue;
+            int Hx[3];
+            for (int a = 0; a < 3; ++a) {
+                const int extra = which == 2 ? g.k[a] / 2 : 0;
+                Hx[a] = std::min(T[a] + g.k[a] - 1 + extra, Lcm[a]);
+            }
+            // warp block (32 consecutive rows, innermost axis fastest) and its union of windows
+            const int W2 = std::min(T2, 32), W1 = std::min(T1, 32 / W2), W0 = 32 / (W2 * W1);
+            const int W[3] = {W0, W1, W2};
+            int U[3];
+            for (int a = 0; a < 3; ++a) U[a] = std::min(W[a] + g.k[a] - 1 + (which == 2 ? g.k[a] / 2 : 0), Hx[a]);
+            for (int h2pass = 0; h2pass < 2; ++h2pass) {
+                const int H2 = h2pass == 0 ? (Hx[2] + 7) / 8 * 8 : (Hx[2] + 15) / 16 * 16;
+                if (h2pass == 1 && H2 == (Hx[2] + 7) / 8 * 8) continue;
+                if (H2 * g.d[2] > 256) continue;
+                const int ucols = 8 * std::min(H2 / 8, ceil_div(U[2], 8) + 1);
+                const double logits_row = static_cast<double>(U[0]) * U[1] * ucols;
+                for (int G1 = 1; G1 <= Hx[1]; ++G1)
+                    for (int G0 = 1; G0 <= Hx[0]; ++G0) {
+                        const int NC = G0 * G1 * H2;
+                        if (NC > ncmax || NC % 16 != 0) continue;
+                        if (G0 * g.d[0] > 256 || G1 * g.d[1] > 256) continue;
+                        if (G0 > 1 && G1 != Hx[1]) continue;  // chunks are slabs of whole axis-1 rows or part of one
+                        const int n0 = ceil_div(Hx[0], G0), n1 = ceil_div(Hx[1], G1);
+                        const double C = static_cast<double>(n0) * n1;
+                        const double mma = C * (n_score + n_update) * 2.0 * 128 * NC * D / 8192.0;
+                        const double soft = logits_row * (which == 0 ? 10.0 : 12.0);
+                        const double zero = C * NC / 8.0 * (which == 2 ? 2 : 1);
+                        const double tile_cost = soft + 0.5 * mma + zero + 300.0 * C;
+                        double tiles = 1;
+                        for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
+                        const double cost = tile_cost * tiles;
+                        if (!found || cost < best) {
+                            found = true;
+                            best = cost;
+                            bp = TilePlan{};
+                            for (int a = 0; a < 3; ++a) {
+                                bp.T[a] = T[a];
+                                bp.ntile[a] = ceil_div(Lcm[a], T[a]);
+                            }
+                            bp.H[0] = Hx[0];
+                            bp.H[1] = Hx[1];
+                            bp.H[2] = H2;
+                            bp.G[0] = G0;
+                            bp.G[1] = G1;
+                            bp.G[2] = H2;
+                            bp.NC = NC;
+                            bp.nchk[0] = n0;
+                            bp.nchk[1] = n1;
+                        }
+                    }
+            }
+        }
+    if (!found) return NA_ERR_UNSUPPORTED;
+    bp.tmem_cols = tmem_cols;
+    // Shared memory: the layout, padded so that at most 512 / tmem_cols CTAs share an SM (their
+    // TMEM allocations then never wait on each other).
+    int smem = static_cast<int>(na::tc_smem_bytes(which, bp, D));
+    const int max_ctas = 512 / tmem_cols;
+    const int floor_bytes = (228 * 1024) / (max_ctas + 1) - 1024 + 1;
+    if (smem < floor_bytes) smem = floor_bytes;
+    if (smem > 227 * 1024) return NA_ERR_UNSUPPORTED;
+    bp.smem_bytes = smem;
+    long long ctas = static_cast<long long>(g.B) * g.heads;
+    for (int a = 0; a < 3; ++a) ctas *= static_cast<long long>(bp.ntile[a]) * g.d[a];
+    if (ctas > 0x7fffffffLL) return NA_ERR_UNSUPPORTED;
+    bp.ctas = ctas;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_plans[key] = bp;
+    }
+    out = bp;
+    return NA_OK;
+}
+
+// Tensor map over a [B, L0, L1, L2, heads, D] bf16 tensor whose box is `e` class positions per axis
+// (element stride = dilation) and D channels of one head.
+na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int e[3]) {
+    const cuuint64_t es = 2;
+    const cuuint64_t hd = static_cast<cuuint64_t>(g.heads) * g.D;
+    cuuint64_t dims[5] = {hd, static_cast<cuuint64_t>(g.L[2]), static_cast<cuuint64_t>(g.L[1]),
+                          static_cast<cuuint64_t>(g.L[0]), static_cast<cuuint64_t>(g.B)};
+    cuuint64_t strides[4] = {hd * es, hd * es * g.L[2], hd * es * g.L[2] * g.L[1], hd * es * g.L[2] * g.L[1] * g.L[0]};
+    cuuint32_t box[5] = {static_cast<cuuint32_t>(g.D), static_cast<cuuint32_t>(e[2] * g.d[2]),
+                         static_cast<cuuint32_t>(e[1] * g.d[1]), static_cast<cuuint32_t>(e[0] * g.d[0]), 1};
+    cuuint32_t estr[5] = {1, static_cast<cuuint32_t>(g.d[2]), static_cast<cuuint32_t>(g.d[1]),
+                          static_cast<cuuint32_t>(g.d[0]), 1};
+    for (int i = 0; i < 5; ++i)
+        if (box[i] < 1 || box[i] > 256 || estr[i] > 8) return NA_ERR_UNSUPPORTED;
+    const int rowb = g.D * 2;
+    const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                              : (rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NA_OK : NA_ERR_CUDA;
+}
+
+na_status tc_common(int which, const Geom& g, float scale, na::TcParams& p) {
+    if (g.D != 16 && g.D != 32 && g.D != 64) return NA_ERR_UNSUPPORTED;
+    for (int a = 0; a < 3; ++a)
+        if (g.d[a] > 8) return NA_ERR_UNSUPPORTED;
+    std::memset(&p, 0, sizeof p);
+    na_status st = plan_tc(which, g, p.plan);
+    if (st != NA_OK) return st;
+    if ((st = get_encoder()) != NA_OK) return st;
+    for (int a = 0; a < 3; ++a) {
+        p.L[a] = g.L[a];
+        p.k[a] = g.k[a];
+        p.d[a] = g.d[a];
+    }
+    p.B = g.B;
+    p.heads = g.heads;
+    p.D = g.D;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.44269504088896340736f;
+    return status_ptr(&p.err);
+}
+
+na_status cuda_status(int e) { return e == 0 ? NA_OK : NA_ERR_CUDA; }
+
+na_status check_ptrs(std::initializer_list<const void*> ps) {
+    for (const void* p : ps)
+        if (!p) return NA_ERR_INVALID_ARG;
+    for (const void* p : ps)
+        if (!aligned16(p)) return NA_ERR_ALIGNMENT;
+    return NA_OK;
+}
+
+na::FmaParams fma_params(const Geom& g, float scale) {
+    na::FmaParams p{};
+    for (int a = 0; a < 3; ++a) {
+        p.L[a] = g.L[a];
+        p.k[a] = g.k[a];
+        p.d[a] = g.d[a];
+    }
+    p.B = g.B;
+    p.heads = g.heads;
+    p.D = g.D;
+    p.N = tokens_of(g);
+    p.scale = scale;
+    return p;
+}
+
+na_status check_dtype(na_dtype dt, const Geom& g) {
+    if (dt == NA_FP32) return (g.D == 16 || g.D == 32 || g.D == 64 || g.D == 128) ? NA_OK : NA_ERR_UNSUPPORTED;
+    if (dt == NA_BF16) return NA_OK;
+    return NA_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int ndim, const int* spatial,
+                 int heads, int D, const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream) {
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if ((st = check_ptrs({q, k, v, o, lse})) != NA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == NA_FP32) {
+        na::FmaParams p = fma_params(g, scale);
+        p.q = q;
+        p.key = k;
+        p.value = v;
+        p.out0 = o;
+        p.out1 = lse;
+        return cuda_status(na::launch_fwd_fma(p, s));
+    }
+    na::TcParams p;
+    if ((st = tc_common(0, g, scale, p)) != NA_OK) return st;
+    const TilePlan& pl = p.plan;
+    const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
+    if ((st = encode_map(&p.tm[0], q, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], k, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], v, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[3], o, g, pl.T)) != NA_OK) return st;
+    p.lse_out = lse;
+    return cuda_status(na::launch_fwd_tc(p, s));
+}
+
+size_t na_bwd_workspace_size(int B, int ndim, const int* spatial, int heads) {
+    if (ndim < 1 || ndim > 3 || !spatial || B < 1 || heads < 1) return 0;
+    long long n = static_cast<long long>(B) * heads;
+    for (int a = 0; a < ndim; ++a) {
+        if (spatial[a] < 1) return 0;
+        n *= spatial[a];
+    }
+    return static_cast<size_t>((n * 4 + 255) / 256 * 256);
+}
+
+na_status na_bwd_delta(const void* o, const void* dO, float* delta, int B, int ndim, const int* spatial, int heads,
+                       int D, na_dtype dtype, void* stream) {
+    const int ones[3] = {1, 1, 1};
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, ones, ones, g);
+    if (st != NA_OK) return st;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if (dtype == NA_BF16 && (D % 8 != 0 || D > 256)) return NA_ERR_UNSUPPORTED;
+    if ((st = check_ptrs({o, dO, delta})) != NA_OK) return st;
+    na::FmaParams p = fma_params(g, 1.f);
+    p.o = o;
+    p.dO = dO;
+    p.out0 = delta;
+    return cuda_status(na::launch_delta(p, dtype == NA_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+na_status na_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* delta,
+                    void* dQ, int B, int ndim, const int* spatial, int heads, int D, const int* kernel,
+                    const int* dilation, float scale, na_dtype dtype, void* stream) {
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if ((st = check_ptrs({q, k, v, dO, lse, delta, dQ})) != NA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == NA_FP32) {
+        na::FmaParams p = fma_params(g, scale);
+        p.q = q;
+        p.key = k;
+        p.value = v;
+        p.dO = dO;
+        p.lse = lse;
+        p.delta = delta;
+        p.out0 = dQ;
+        return cuda_status(na::launch_dq_fma(p, s));
+    }
+    na::TcParams p;
+    if ((st = tc_common(1, g, scale, p)) != NA_OK) return st;
+    const TilePlan& pl = p.plan;
+    const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
+    if ((st = encode_map(&p.tm[0], q, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], dO, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], k, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[3], v, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[4], dQ, g, pl.T)) != NA_OK) return st;
+    p.lse = lse;
+    p.delta = delta;
+    return cuda_status(na::launch_dq_tc(p, s));
+}
+
+na_status na_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                      const float* delta, void* dK, void* dV, int B, int ndim, const int* spatial, int heads, int D,
+                      const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream) {
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if ((st = check_ptrs({q, k, v, dO, lse, delta, dK, dV})) != NA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (dtype == NA_FP32) {
+        na::FmaParams p = fma_params(g, scale);
+        p.q = q;
+        p.key = k;
+        p.value = v;
+        p.dO = dO;
+        p.lse = lse;
+        p.delta = delta;
+        p.out0 = dK;
+        p.out1 = dV;
+        return cuda_status(na::launch_dkdv_fma(p, s));
+    }
+    na::TcParams p;
+    if ((st = tc_common(2, g, scale, p)) != NA_OK) return st;
+    const TilePlan& pl = p.plan;
+    const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
+    if ((st = encode_map(&p.tm[0], k, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], v, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], q, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[3], dO, g, chunk)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[4], dK, g, pl.T)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[5], dV, g, pl.T)) != NA_OK) return st;
+    p.lse = lse;
+    p.delta = delta;
+    return cuda_status(na::launch_dkdv_tc(p, s));
+}
+
+na_status na_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse, void* dQ,
+                 void* dK, void* dV, int B, int ndim, const int* spatial, int heads, int D, const int* kernel,
+                 const int* dilation, float scale, na_dtype dtype, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if ((st = check_ptrs({q, k, v, o, dO, lse, dQ, dK, dV})) != NA_OK) return st;
+    if (dtype == NA_BF16) {  // reject unsupported problems before anything is enqueued
+        na::TcParams probe;
+        if ((st = tc_common(1, g, scale, probe)) != NA_OK) return st;
+        if ((st = tc_common(2, g, scale, probe)) != NA_OK) return st;
+    }
+    const size_t need = na_bwd_workspace_size(B, ndim, spatial, heads);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need) return NA_ERR_WORKSPACE;
+        if (!aligned16(ws)) return NA_ERR_ALIGNMENT;
+    } else {
+        if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return NA_ERR_WORKSPACE;
+        owned = true;
+    }
+    float* delta = static_cast<float*>(ws);
+    st = na_bwd_delta(o, dO, delta, B, ndim, spatial, heads, D, dtype, stream);
+    if (st == NA_OK)
+        st = na_bwd_dq(q, k, v, dO, lse, delta, dQ, B, ndim, spatial, heads, D, kernel, dilation, scale, dtype, stream);
+    if (st == NA_OK)
+        st = na_bwd_dkdv(q, k, v, dO, lse, delta, dK, dV, B, ndim, spatial, heads, D, kernel, dilation, scale, dtype,
+                         stream);
+    if (owned && cudaFreeAsync(ws, s) != cudaSuccess && st == NA_OK) st = NA_ERR_CUDA;
+    return st;
+}
+
+na_status na_device_status(void* stream, uint32_t* raw) {
+    unsigned* ptr = nullptr;
+    na_status st = status_ptr(&ptr);
+    if (st != NA_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return NA_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, ptr, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return NA_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(ptr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return NA_ERR_CUDA;
+    }
+    if (raw) *raw = word;
+    return word ? NA_ERR_TIMEOUT : NA_OK;
+}
+
+const char* na_strerror(na_status s) {
+    switch (s) {
+        case NA_OK: return "success";
+        case NA_ERR_INVALID_ARG: return "invalid argument";
+        case NA_ERR_UNSUPPORTED: return "unsupported problem for this dtype";
+        case NA_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+        case NA_ERR_CUDA: return "CUDA error";
+        case NA_ERR_TIMEOUT: return "a device-side wait timed out";
+        case NA_ERR_WORKSPACE: return "workspace too small or not allocatable";
+        default: return "unknown status";
+    }
+}
+
+na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads, int D, const int* kernel,
+                       const int* dilation, int64_t* out) {
+    if (!out || which < 0 || which > 2) return NA_ERR_INVALID_ARG;
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    if (D != 16 && D != 32 && D != 64) return NA_ERR_UNSUPPORTED;
+    TilePlan pl;
+    if ((st = plan_tc(which, g, pl)) != NA_OK) return st;
+    // chunks summed over every CTA (depends on the tile position along the two outer axes and class)
+    long long total_chunks = 0;
+    for (int c0 = 0; c0 < g.d[0]; ++c0)
+        for (int c1 = 0; c1 < g.d[1]; ++c1) {
+            const int Lc0 = (g.L[0] - c0 + g.d[0] - 1) / g.d[0], Lc1 = (g.L[1] - c1 + g.d[1] - 1) / g.d[1];
+            long long n0 = 0, n1 = 0;
+            for (int t = 0; t * pl.T[0] < Lc0; ++t)
+                n0 += chunks_along(which, t * pl.T[0], pl.T[0], Lc0, g.k[0], pl.H[0], pl.G[0], pl.nchk[0]);
+            for (int t = 0; t * pl.T[1] < Lc1; ++t)
+                n1 += chunks_along(which, t * pl.T[1], pl.T[1], Lc1, g.k[1], pl.H[1], pl.G[1], pl.nchk[1]);
+            long long inner = 0;  // tiles along axis 2 for every class of axis 2
+            for (int c2 = 0; c2 < g.d[2]; ++c2) inner += ceil_div((g.L[2] - c2 + g.d[2] - 1) / g.d[2], pl.T[2]);
+            total_chunks += n0 * n1 * inner;
+        }
+    total_chunks *= static_cast<long long>(g.B) * g.heads;
+    const int n_mma = which == 0 ? 2 : (which == 1 ? 3 : 4);
+    out[0] = pl.T[0];
+    out[1] = pl.T[1];
+    out[2] = pl.T[2];
+    out[3] = pl.H[0];
+    out[4] = pl.H[1];
+    out[5] = pl.H[2];
+    out[6] = pl.G[0];
+    out[7] = pl.G[1];
+    out[8] = pl.G[2];
+    out[9] = pl.NC;
+    out[10] = static_cast<int64_t>(pl.nchk[0]) * pl.nchk[1];
+    out[11] = pl.ctas;
+    out[12] = total_chunks * n_mma * 2LL * 128 * pl.NC * D;  // MMA FLOPs issued by all CTAs
+    out[13] = pl.tmem_cols;
+    out[14] = pl.smem_bytes;
+    out[15] = total_chunks;
+    return NA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// na_internal.h -- structures shared by the host API and the kernels of libna (not installed).
+//
+// Problems of 1, 2 or 3 spatial axes are embedded as 3 axes, outermost first, with leading
+// axes of length 1, kernel 1 and dilation 1.  All tile geometry is in *class coordinates*: along
+// an axis with dilation d, residue class c holds the positions c, c+d, c+2d, ... and a tile or
+// halo is a run of consecutive class indices.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace na {
+
+constexpr int kRows = 128;          // query (or key) rows per CTA tile = tcgen05 M
+constexpr int kSoftmaxWarps = 4;    // one warp per 32-lane TMEM sub-partition
+constexpr int kThreads = 160;       // 4 softmax/epilogue warps + 1 producer (TMA + MMA) warp
+constexpr int kSlots = 2;           // K/V (or Q/dO) chunk ring depth
+
+struct Geom {
+    int B, heads, D;
+    int L[3], k[3], d[3];
+};
+
+// Static tile plan of one tensor-core kernel for one problem.
+struct TilePlan {
+    int T[3];        // CTA tile extents (class coordinates), T0*T1*T2 == 128
+    int H[3];        // halo box extents: keys (fwd, dQ) or queries (dK/dV) a tile may need
+    int G[3];        // chunk box extents; G[2] == H[2]
+    int NC;          // rows of one chunk = G0*G1*G2 (multiple of 16, <= 256)
+    int nchk[2];     // chunks along axes 0 and 1 that cover the halo box
+    int ntile[3];    // tiles per axis and residue class: ceil(ceil(L/d) / T)
+    int tmem_cols;   // TMEM columns allocated per CTA (power of two)
+    int smem_bytes;  // dynamic shared memory per CTA (includes alignment slack)
+    int64_t ctas;    // grid size
+};
+
+// Kernel parameters of the tensor-core kernels (passed as __grid_constant__).
+// Tensor-map roles per kernel:
+//   fwd : tm[0] q tile, tm[1] k chunk, tm[2] v chunk, tm[3] o tile (store)
+//   dq  : tm[0] q tile, tm[1] dO tile, tm[2] k chunk, tm[3] v chunk, tm[4] dQ tile (store)
+//   dkdv: tm[0] k tile, tm[1] v tile, tm[2] q chunk, tm[3] dO chunk, tm[4] dK tile, tm[5] dV tile
+struct TcParams {
+    CUtensorMap tm[6];
+    TilePlan plan;
+    int L[3], k[3], d[3];
+    int B, heads, D;
+    float scale;        // softmax scale (applied to q.k)
+    float scale_log2;   // scale * log2(e)
+    float* lse_out;     // fwd: [B, L.., heads] natural-log LSE
+    const float* lse;   // bwd: forward LSE
+    const float* delta; // bwd: Delta = <dO, O>
+    unsigned* err;      // device status word
+};
+
+// Parameters of the CUDA-core kernels (fp32 path and the Delta prologue).
+struct FmaParams {
+    const void* q;
+    const void* key;
+    const void* value;
+    const void* o;
+    const void* dO;
+    const float* lse;
+    const float* delta;
+    void* out0;         // fwd: o      dq: dQ   dkdv: dK   delta: delta (float*)
+    void* out1;         // fwd: lse    dkdv: dV
+    int L[3], k[3], d[3];
+    int B, heads, D;
+    int64_t N;          // tokens per batch entry
+    float scale;
+};
+
+// Launchers (defined next to their kernels).  Return a cudaError_t as int.
+int launch_fwd_tc(const TcParams& p, cudaStream_t stream);
+int launch_dq_tc(const TcParams& p, cudaStream_t stream);
+int launch_dkdv_tc(const TcParams& p, cudaStream_t stream);
+int launch_fwd_fma(const FmaParams& p, cudaStream_t stream);
+int launch_dq_fma(const FmaParams& p, cudaStream_t stream);
+int launch_dkdv_fma(const FmaParams& p, cudaStream_t stream);
+int launch_delta(const FmaParams& p, bool bf16, cudaStream_t stream);
+
+// Kernel attributes that depend on the plan (dynamic smem opt-in); called before the launch.
+int prepare_tc_kernel(int which, int D, int smem_bytes);
+
+}  // namespace na

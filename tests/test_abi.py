@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI (CPU only): the library loads, exports every entry point that
+include/na.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import neighborhood_attention_fwd_gb300 as na
+from neighborhood_attention_fwd_gb300 import build as nabuild
+from neighborhood_attention_fwd_gb300 import inputs as nain
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    nabuild.build()
+    return na.load()
+
+
+def declared_entry_points():
+    text = open(os.path.join(ROOT, "include", "na.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:na_status|size_t|const char\*)\s+(na_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for required in ("na_fwd", "na_bwd", "na_bwd_workspace_size", "na_strerror", "na_bwd_delta", "na_bwd_dq",
+                     "na_bwd_dkdv", "na_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_entry_points():
+        assert hasattr(lib, name), name
+
+
+def test_strerror(lib):
+    for code in range(7):
+        assert na.na_strerror(code)
+    assert na.na_strerror(99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    assert na.na_bwd_workspace_size(1, (1024, 1024), 8) == 1024 * 1024 * 8 * 4
+    assert na.na_bwd_workspace_size(2, (3, 5, 7), 3) == (2 * 105 * 3 * 4 + 255) // 256 * 256
+    assert lib.na_bwd_workspace_size(0, 1, (ctypes.c_int * 1)(5), 1) == 0
+
+
+def _fwd(lib, spatial, kernel, dilation, heads=2, D=32, B=1, scale=0.1, ptr=16, dtype=0):
+    n = len(spatial)
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    p = ctypes.c_void_p(ptr) if ptr is not None else None
+    return lib.na_fwd(p, p, p, p, p, B, n, I(spatial), heads, D, I(kernel), I(dilation), ctypes.c_float(scale),
+                      dtype, None)
+
+
+def test_invalid_arguments_are_rejected_before_any_launch(lib):
+    assert _fwd(lib, (16, 16), (4, 5), (1, 1)) == 1            # even kernel
+    assert _fwd(lib, (16, 16), (5, 5), (1, 4)) == 1            # class of 4 positions < 5
+    assert _fwd(lib, (16, 16), (5, 5), (1, 0)) == 1            # dilation 0
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), B=0) == 1
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), heads=0) == 1
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), scale=float("nan")) == 1
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), ptr=None) == 1  # null pointers
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), ptr=8) == 3     # misaligned
+    assert _fwd(lib, (16, 16), (5, 5), (1, 1), dtype=7) == 1   # unknown dtype
+    assert _fwd(lib, (4, 4, 4, 4), (1, 1, 1, 1), (1, 1, 1, 1)) == 1  # ndim 4
+
+
+def test_unsupported_problems(lib):
+    assert _fwd(lib, (64, 64), (5, 5), (1, 1), D=48) == 2            # bf16 head dim
+    assert _fwd(lib, (64, 64), (5, 5), (1, 1), D=24, dtype=1) == 2   # fp32 head dim
+    assert _fwd(lib, (128, 128), (5, 5), (1, 9)) == 2                # dilation beyond the TMA element stride
+
+
+@pytest.mark.parametrize("name", [n for n in nain.WORKLOADS if nain.WORKLOADS[n].dtype == "bf16"])
+def test_plans_cover_the_workloads(lib, name):
+    w = nain.WORKLOADS[name]
+    for which in range(3):
+        plan = na.na_plan_info(which, w.B, w.spatial, w.heads, w.D, w.kernel, w.dilation)
+        assert plan["T1"] * plan["T2"] * plan["T3"] == 128
+        assert plan["NC"] % 16 == 0 and 16 <= plan["NC"] <= 256
+        assert plan["G3"] == plan["H3"] and plan["H3"] % 8 == 0
+        assert plan["smem_bytes"] <= 227 * 1024
+        # every CTA's TMEM fits next to the others an SM can hold
+        assert plan["tmem_cols"] in (128, 256)
+        assert plan["mma_flops"] > 0 and plan["chunks_total"] >= plan["ctas"] // 2
+
+
+def test_plan_for_one_dimensional_dilated_problem(lib):
+    plan = na.na_plan_info(0, 1, (300,), 1, 16, (13,), (3,))
+    assert plan["T3"] * 3 <= 256

@@ -1,0 +1,98 @@
+"""GPU parity: the CUDA library against the fp64 oracle, through the C ABI.
+
+Small problems are compared element by element on every output; the full-size workloads (the
+shapes the benchmark times, launched the same way) are compared on sampled rows that the oracle
+computes one by one, plus finiteness of every output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from neighborhood_attention_fwd_gb300 import inputs as nain
+from na_testlib import check_full, check_sampled, host, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # dtype, spatial, heads, D, kernel, dilation, B
+    ("fp32", (16, 16), 2, 16, (5, 5), (1, 1), 1),          # the small fp32 workload
+    ("fp32", (37,), 3, 32, (7,), (2,), 2),
+    ("fp32", (9, 11, 10), 2, 16, (3, 5, 3), (2, 1, 3), 1),
+    ("fp32", (12, 13), 1, 64, (5, 3), (1, 4), 1),
+    ("fp32", (7, 9), 2, 128, (7, 9), (1, 1), 1),            # kernel == extent: full attention
+    ("bf16", (40, 37), 3, 32, (5, 7), (1, 1), 2),
+    ("bf16", (33, 45), 2, 32, (9, 9), (1, 1), 1),
+    ("bf16", (200,), 2, 32, (7,), (1,), 2),
+    ("bf16", (300,), 1, 16, (13,), (3,), 1),
+    ("bf16", (6, 20, 19), 2, 32, (3, 5, 5), (1, 1, 1), 1),
+    ("bf16", (10, 18, 21), 1, 64, (5, 7, 7), (1, 1, 1), 1),
+    ("bf16", (41, 38), 2, 32, (13, 13), (2, 2), 1),
+    ("bf16", (23, 29), 2, 16, (3, 5), (3, 2), 2),           # classes of unequal length
+    ("bf16", (17, 16), 1, 64, (17, 15), (1, 1), 1),         # kernel == extent along axis 1
+    ("bf16", (8, 30, 30), 1, 32, (1, 9, 1), (1, 2, 1), 1),  # kernel 1 on some axes
+    ("bf16", (5, 9, 33), 2, 32, (5, 9, 3), (1, 1, 8), 1),
+]
+
+
+def _ids(c):
+    return f"{c[0]}-{'x'.join(map(str, c[1]))}-h{c[2]}-D{c[3]}-k{'x'.join(map(str, c[4]))}-d{'x'.join(map(str, c[5]))}-B{c[6]}"
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[_ids(c) for c in SMALL])
+def test_small_full_parity(case, cuda_lib):
+    dtype, spatial, heads, D, kernel, dilation, B = case
+    w = nain.small_workload(dtype, spatial, heads, D, kernel, dilation, B=B, seed=11)
+    t = nain.make_inputs(w, device="cpu")
+    gpu = run_gpu(w, {k: v.cuda() for k, v in t.items()})
+    check_full(w, gpu, host(t))
+
+
+def test_split_backward_matches_fused_entry_point(cuda_lib):
+    w = nain.small_workload("bf16", (30, 26), 2, 32, (7, 5), (1, 2), B=1, seed=3)
+    t = {k: v.cuda() for k, v in nain.make_inputs(w, device="cpu").items()}
+    a = run_gpu(w, t)
+    b = run_gpu(w, t, split_bwd=True)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_backward_is_deterministic(cuda_lib):
+    w = nain.small_workload("bf16", (40, 40), 2, 32, (9, 9), (1, 1), B=1, seed=4)
+    t = {k: v.cuda() for k, v in nain.make_inputs(w, device="cpu").items()}
+    a = run_gpu(w, t)
+    b = run_gpu(w, t)
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_delta_matches_rowwise_dot(cuda_lib):
+    import neighborhood_attention_fwd_gb300 as na
+
+    for dtype in (torch.bfloat16, torch.float32):
+        g = torch.Generator().manual_seed(5)
+        o = torch.randn(2, 9, 7, 3, 32, generator=g).to(dtype)
+        dO = torch.randn(2, 9, 7, 3, 32, generator=g).to(dtype)
+        delta = torch.empty(2, 9, 7, 3, dtype=torch.float32, device="cuda")
+        na.na_bwd_delta(o.cuda(), dO.cuda(), delta)
+        ref = (o.double() * dO.double()).sum(-1)
+        tol = 1e-5 if dtype == torch.float32 else 1e-4
+        assert (delta.cpu().double() - ref).abs().max() <= tol * ref.abs().max()
+
+
+FULL = [name for name in nain.WORKLOADS if nain.WORKLOADS[name].dtype == "bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_parity(name, cuda_lib):
+    w = nain.WORKLOADS[name]
+    t = nain.make_inputs(w, device="cuda")
+    gpu = run_gpu(w, t)
+    h = host(t)
+    check_sampled(w, gpu, h, n=256)
+
+
+def test_full_size_fp32_workload(cuda_lib):
+    w = nain.WORKLOADS["2d_fp32_16x16_k5"]
+    t = nain.make_inputs(w, device="cpu")
+    gpu = run_gpu(w, {k: v.cuda() for k, v in t.items()})
+    check_full(w, gpu, host(t))
