@@ -61,6 +61,18 @@ def method_bytes(w):
     return 4 * rows * w.D * s + 4 * rows, 8 * rows * w.D * s + 12 * rows
 
 
+def arithmetic_intensity(w, fused=True, elem_bytes=None):
+    """Forward FLOP per byte: q, k, v read and o written once; the unfused chain also writes the
+    attention weights once (QK op) and reads them once (AV op)."""
+    s = elem_bytes or (2 if w.dtype == "bf16" else 4)
+    rows = float(w.tokens) * w.heads
+    flops = 4.0 * rows * w.keys_per_query * w.D
+    nbytes = 4.0 * rows * w.D * s
+    if not fused:
+        nbytes += 2.0 * rows * w.keys_per_query * s
+    return flops / nbytes
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -181,6 +193,20 @@ def cpu_baseline(w, t, target_s=15.0):
 # Device step
 # ---------------------------------------------------------------------------------------------
 
+def ranks_max(x: float, dist, device) -> float:
+    """The largest value of x over all ranks (the slowest rank sets the step time)."""
+    if dist is None:
+        return float(x)
+    tt = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_value(world: int, flops_per_rank_step: float, ms_step: float) -> float:
+    """Whole-job useful TFLOP/s: every rank processes its own workload instance per step."""
+    return world * flops_per_rank_step / (ms_step * 1e-3) / 1e12
+
+
 class Step:
     """Buffers and launches of one fwd + bwd step on the current stream."""
 
@@ -270,14 +296,10 @@ def run_ours(args, w, rank, world, dist):
         per["dkdv"].append(e["dq1"].elapsed_time(e["dkdv1"]))
         per["step"].append(e["fwd0"].elapsed_time(e["dkdv1"]))
     ms = {k: float(np.mean(v)) for k, v in per.items()}
-    ms_step = ms["step"]
-    if dist is not None:
-        tt = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = ranks_max(ms["step"], dist, dev)
 
     f_fwd, f_bwd = useful_flops(w)
-    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    value = job_value(world, f_fwd + f_bwd, ms_step)
 
     # --- roofline: per kernel, the slower of tile-level MMA FLOPs at the bf16 peak and the
     # algorithmic bytes at HBM bandwidth
