@@ -164,7 +164,9 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
             if (skip) continue;
             int Hx[3];
             for (int a = 0; a < 3; ++a) {
-                const int extra = which == 2 ? g.k[a] / 2 : 0;
+                // dK/dV: a key near a border is seen by up to k/2 extra queries on that side, and a
+                // tile of keys can touch both borders of a short axis.
+                const int extra = which == 2 ? 2 * (g.k[a] / 2) : 0;
                 Hx[a] = std::min(T[a] + g.k[a] - 1 + extra, Lcm[a]);
             }
             // warp block (32 consecutive rows, innermost axis fastest) and its union of windows

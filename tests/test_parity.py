@@ -31,6 +31,8 @@ SMALL = [
     ("bf16", (17, 16), 1, 64, (17, 15), (1, 1), 1),         # kernel == extent along axis 1
     ("bf16", (8, 30, 30), 1, 32, (1, 9, 1), (1, 2, 1), 1),  # kernel 1 on some axes
     ("bf16", (5, 9, 33), 2, 32, (5, 9, 3), (1, 1, 8), 1),
+    ("bf16", (16, 8), 1, 32, (1, 1), (1, 1), 1),            # k = 1: O = V, dQ = dK = 0
+    ("bf16", (6, 5, 70), 1, 32, (3, 5, 1), (2, 1, 1), 3),   # short axes: windows touch both borders
 ]
 
 
