@@ -99,16 +99,17 @@ def check_sampled(w, gpu, h, n=256, want_bwd=True, seed=0):
     tol = TOL[w.dtype]
     rows = sample_rows(w, n, seed)
     D = w.D
-    flat = lambda t: to64(t).reshape(-1, D)
+    idx = torch.as_tensor(rows, device=gpu["o"].device)
+    pick = lambda t: to64(t.reshape(-1, D)[idx])          # gather on the device, then copy
     o, lse = oracle.na_fwd(h["q"], h["k"], h["v"], w.kernel, w.dilation, w.scale, rows=rows)
-    rel = {"o": compare("O", flat(gpu["o"])[rows], o, tol),
-           "lse": compare("LSE", to64(gpu["lse"]).reshape(-1)[rows], lse, tol)}
+    rel = {"o": compare("O", pick(gpu["o"]), o, tol),
+           "lse": compare("LSE", to64(gpu["lse"].reshape(-1)[idx]), lse, tol)}
     if want_bwd:
         dq, dk, dv = oracle.na_bwd(h["q"], h["k"], h["v"], h["dO"], w.kernel, w.dilation, w.scale,
                                    qrows=rows, krows=rows)
-        rel["dq"] = compare("dQ", flat(gpu["dq"])[rows], dq, tol, scale_ref=dv)
-        rel["dk"] = compare("dK", flat(gpu["dk"])[rows], dk, tol, scale_ref=dv)
-        rel["dv"] = compare("dV", flat(gpu["dv"])[rows], dv, tol)
+        rel["dq"] = compare("dQ", pick(gpu["dq"]), dq, tol, scale_ref=dv)
+        rel["dk"] = compare("dK", pick(gpu["dk"]), dk, tol, scale_ref=dv)
+        rel["dv"] = compare("dV", pick(gpu["dv"]), dv, tol)
     for key in ("o", "dq", "dk", "dv"):
         if key in gpu:
             assert torch.isfinite(gpu[key]).all(), f"{key} has non-finite values"
