@@ -88,6 +88,35 @@ na_status na_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward without any allocation.  The source pages have no counterpart for this entry point; it
+ * exists for callers that cannot allocate device memory while they run: a host framework that has
+ * handed out all device memory up front under a fixed budget, or a latency-critical loop where an
+ * allocation may block, fail under memory pressure, or is simply forbidden by the caller's rules.
+ * Such callers cannot pass workspace = NULL to na_bwd (that allocates with cudaMallocAsync), and
+ * may have no spare buffer of na_bwd_workspace_size() bytes to lend either.
+ *
+ * It computes exactly what na_bwd computes, with the same arguments minus the workspace, and calls
+ * no cudaMalloc, cudaFree or other allocating routine.  The Delta scratch is a fixed array of
+ * NA_NOALLOC_MAX_ROWS floats (32 MiB) that the library reserves in device memory on every GPU
+ * where it is loaded, for the life of the process.
+ *   - Limit: B * prod(spatial) * heads must be <= NA_NOALLOC_MAX_ROWS; larger problems return
+ *     NA_ERR_WORKSPACE before anything is enqueued (use na_bwd for them).
+ *   - Set-up: the first call on each device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current).  Make that first call before any stream
+ *     capture on the device.
+ *   - Sharing: every call on a device uses the same array, which keeps the last call's contents.
+ *     Each call overwrites every row it reads before reading it, so nothing needs clearing, but
+ *     two calls whose work overlaps on the GPU (e.g. on different streams) race on the array:
+ *     order them on one stream or with events.
+ */
+#define NA_NOALLOC_MAX_ROWS (8 * 1024 * 1024)
+na_status na_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dQ, void* dK, void* dV,
+                         int B, int ndim, const int* spatial, int heads, int D,
+                         const int* kernel, const int* dilation, float scale, na_dtype dtype,
+                         void* stream);
+
+/*
  * Backward step 1 (the maintainer's "ComputeDelta"): delta[row] = sum_c dO[row, c] * o[row, c]
  * for every (batch, token, head) row, in fp32.  delta: fp32 [B, L.., heads].
  */

@@ -30,6 +30,27 @@ constexpr int kMaxDevices = 64;
 unsigned* g_status_ptr[kMaxDevices] = {};
 std::mutex g_mu;
 
+// Fixed Delta scratch for na_bwd_noalloc: NA_NOALLOC_MAX_ROWS fp32 values (32 MiB), reserved on every
+// device that loads this library for as long as the process lives.  Host code must not use the
+// symbol as a device address; the address is looked up per device with cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_delta[NA_NOALLOC_MAX_ROWS];
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_delta on the current device (looked up on the first call per device).
+na_status noalloc_scratch(float** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NA_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        float* p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_delta) != cudaSuccess || !p)
+            return NA_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return NA_OK;
+}
+
 na_status status_ptr(unsigned** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NA_ERR_CUDA;
@@ -479,6 +500,37 @@ na_status na_bwd(const void* q, const void* k, const void* v, const void* o, con
         st = na_bwd_dkdv(q, k, v, dO, lse, delta, dK, dV, B, ndim, spatial, heads, D, kernel, dilation, scale, dtype,
                          stream);
     if (owned && cudaFreeAsync(ws, s) != cudaSuccess && st == NA_OK) st = NA_ERR_CUDA;
+    return st;
+}
+
+na_status na_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dQ, void* dK, void* dV, int B, int ndim, const int* spatial,
+                         int heads, int D, const int* kernel, const int* dilation, float scale, na_dtype dtype,
+                         void* stream) {
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
+    if (st != NA_OK) return st;
+    // Size limit first, before any CUDA call: the Delta rows must fit the static scratch.
+    const long long rows = tokens_of(g) * g.B * g.heads;
+    if (rows > static_cast<long long>(NA_NOALLOC_MAX_ROWS)) return NA_ERR_WORKSPACE;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if ((st = check_dtype(dtype, g)) != NA_OK) return st;
+    if ((st = check_ptrs({q, k, v, o, dO, lse, dQ, dK, dV})) != NA_OK) return st;
+    if (dtype == NA_BF16) {
+        na::TcParams probe;
+        if ((st = tc_common(1, g, scale, probe)) != NA_OK) return st;
+        if ((st = tc_common(2, g, scale, probe)) != NA_OK) return st;
+    }
+    float* delta = nullptr;
+    if ((st = noalloc_scratch(&delta)) != NA_OK) return st;
+    // Every row of delta is rewritten by the Delta step before dQ and dK/dV read it, so the
+    // previous call's contents never leak into this one and nothing has to be cleared.
+    st = na_bwd_delta(o, dO, delta, B, ndim, spatial, heads, D, dtype, stream);
+    if (st == NA_OK)
+        st = na_bwd_dq(q, k, v, dO, lse, delta, dQ, B, ndim, spatial, heads, D, kernel, dilation, scale, dtype, stream);
+    if (st == NA_OK)
+        st = na_bwd_dkdv(q, k, v, dO, lse, delta, dK, dV, B, ndim, spatial, heads, D, kernel, dilation, scale, dtype,
+                         stream);
     return st;
 }
 
