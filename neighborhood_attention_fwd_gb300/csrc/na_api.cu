@@ -16,6 +16,8 @@
 
 namespace na {
 uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D);
+int tc_tmem_cols(int which);
+int tc_max_nc(int which, int D);
 }
 
 namespace {
@@ -144,6 +146,30 @@ int chunks_along(int which, int t0, int T, int Lc, int k, int H, int G, int nchk
     return std::min(nchk, ceil_div(hi - h0 + 1, G));
 }
 
+// Largest halo extent (class positions) any tile of T positions needs along an axis, over every
+// residue class and tile position: the window range [s(first), s(last) + k) for the forward and
+// dQ, the inverse range [i_lo(first), i_hi(last)] for dK/dV (a key near a border is seen by up
+// to k/2 extra queries on that side, and a tile can touch both borders of a short axis).
+int max_halo(int which, int T, int L, int k, int d) {
+    int best = 1;
+    for (int c = 0; c < d && c < L; ++c) {
+        const int Lc = (L - c + d - 1) / d;
+        for (int t0 = 0; t0 < Lc; t0 += T) {
+            const int last = std::min(t0 + T, Lc) - 1;
+            int lo, hi;
+            if (which != 2) {
+                lo = std::max(0, std::min(t0 - k / 2, Lc - k));
+                hi = std::max(0, std::min(last - k / 2, Lc - k)) + k - 1;
+            } else {
+                lo = t0 < k ? 0 : t0 - k / 2;
+                hi = last >= Lc - k ? Lc - 1 : last + k / 2;
+            }
+            best = std::max(best, hi - lo + 1);
+        }
+    }
+    return best;
+}
+
 na_status plan_tc(int which, const Geom& g, TilePlan& out) {
     const PlanKey key{which, g.D, g.B, g.heads, {g.L[0], g.L[1], g.L[2]}, {g.k[0], g.k[1], g.k[2]},
                       {g.d[0], g.d[1], g.d[2]}};
@@ -156,18 +182,8 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
         }
     }
     const int D = g.D;
-    int tmem_cols, ncmax;
-    if (which == 0) {
-        tmem_cols = 128;
-        ncmax = 128 - D;
-    } else if (which == 1) {
-        tmem_cols = 256;
-        ncmax = (256 - D) / 2;
-    } else {
-        tmem_cols = 256;
-        ncmax = (256 - 2 * D) / 2;
-    }
-    ncmax = std::min(256, ncmax) / 16 * 16;
+    const int tmem_cols = na::tc_tmem_cols(which);
+    const int ncmax = na::tc_max_nc(which, D);
     int Lcm[3];
     for (int a = 0; a < 3; ++a) Lcm[a] = ceil_div(g.L[a], g.d[a]);
     const int n_score = which == 0 ? 1 : 2, n_update = which == 2 ? 2 : 1;
@@ -184,37 +200,33 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
                 if (T[a] * g.d[a] > 256) skip = true;  // TMA box limit (rows past an axis end are just idle)
             if (skip) continue;
             int Hx[3];
-            for (int a = 0; a < 3; ++a) {
-                // dK/dV: a key near a border is seen by up to k/2 extra queries on that side, and a
-                // tile of keys can touch both borders of a short axis.
-                const int extra = which == 2 ? 2 * (g.k[a] / 2) : 0;
-                Hx[a] = std::min(T[a] + g.k[a] - 1 + extra, Lcm[a]);
-            }
+            for (int a = 0; a < 3; ++a) Hx[a] = max_halo(which, T[a], g.L[a], g.k[a], g.d[a]);
             // warp block (32 consecutive rows, innermost axis fastest) and its union of windows
             const int W2 = std::min(T2, 32), W1 = std::min(T1, 32 / W2), W0 = 32 / (W2 * W1);
             const int W[3] = {W0, W1, W2};
             int U[3];
             for (int a = 0; a < 3; ++a) U[a] = std::min(W[a] + g.k[a] - 1 + (which == 2 ? g.k[a] / 2 : 0), Hx[a]);
-            for (int h2pass = 0; h2pass < 2; ++h2pass) {
-                const int H2 = h2pass == 0 ? (Hx[2] + 7) / 8 * 8 : (Hx[2] + 15) / 16 * 16;
-                if (h2pass == 1 && H2 == (Hx[2] + 7) / 8 * 8) continue;
-                if (H2 * g.d[2] > 256) continue;
-                const int ucols = 8 * std::min(H2 / 8, ceil_div(U[2], 8) + 1);
-                const double logits_row = static_cast<double>(U[0]) * U[1] * ucols;
+            double tiles = 1;
+            for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
+            for (int NB = 1; NB <= 4; ++NB) {
+                const int G2 = 8 * NB;
+                if (G2 > (Hx[2] + 7) / 8 * 8 || G2 * g.d[2] > 256) continue;
+                const int n2 = ceil_div(Hx[2], G2);
+                // softmax work per row: the warp union's segments times its 8-column blocks
+                const double logits_row = static_cast<double>(U[0]) * U[1] * 8.0 * (ceil_div(U[2], 8) + (n2 > 1 ? 1 : 0));
                 for (int G1 = 1; G1 <= Hx[1]; ++G1)
                     for (int G0 = 1; G0 <= Hx[0]; ++G0) {
-                        const int NC = G0 * G1 * H2;
+                        const int NC = G0 * G1 * G2;
                         if (NC > ncmax || NC % 16 != 0) continue;
                         if (G0 * g.d[0] > 256 || G1 * g.d[1] > 256) continue;
-                        if (G0 > 1 && G1 != Hx[1]) continue;  // chunks are slabs of whole axis-1 rows or part of one
+                        if (G0 > 1 && G1 != Hx[1]) continue;  // chunks: slabs of whole axis-1 rows or part of one
+                        if (G0 * G1 > 1 && G2 != 8 * NB) continue;
                         const int n0 = ceil_div(Hx[0], G0), n1 = ceil_div(Hx[1], G1);
-                        const double C = static_cast<double>(n0) * n1;
+                        const double C = static_cast<double>(n0) * n1 * n2;
                         const double mma = C * (n_score + n_update) * 2.0 * 128 * NC * D / 8192.0;
-                        const double soft = logits_row * (which == 0 ? 10.0 : 12.0);
-                        const double zero = C * NC / 8.0 * (which == 2 ? 2 : 1);
-                        const double tile_cost = soft + 0.5 * mma + zero + 300.0 * C;
-                        double tiles = 1;
-                        for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
+                        const double soft = logits_row * (which == 0 ? 4.0 : 5.0);
+                        const double block_overhead = C * (NC / 8) * 6.0;
+                        const double tile_cost = std::max(soft + block_overhead, 0.6 * mma) + 150.0 * C;
                         const double cost = tile_cost * tiles;
                         if (!found || cost < best) {
                             found = true;
@@ -223,29 +235,32 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
                             for (int a = 0; a < 3; ++a) {
                                 bp.T[a] = T[a];
                                 bp.ntile[a] = ceil_div(Lcm[a], T[a]);
+                                bp.H[a] = Hx[a];
                             }
-                            bp.H[0] = Hx[0];
-                            bp.H[1] = Hx[1];
-                            bp.H[2] = H2;
                             bp.G[0] = G0;
                             bp.G[1] = G1;
-                            bp.G[2] = H2;
+                            bp.G[2] = G2;
+                            bp.NB = NB;
                             bp.NC = NC;
                             bp.nchk[0] = n0;
                             bp.nchk[1] = n1;
+                            bp.nchk[2] = n2;
                         }
                     }
             }
         }
     if (!found) return NA_ERR_UNSUPPORTED;
     bp.tmem_cols = tmem_cols;
-    // Shared memory: the layout, padded so that at most 512 / tmem_cols CTAs share an SM (their
-    // TMEM allocations then never wait on each other).
-    int smem = static_cast<int>(na::tc_smem_bytes(which, bp, D));
-    const int max_ctas = 512 / tmem_cols;
-    const int floor_bytes = (228 * 1024) / (max_ctas + 1) - 1024 + 1;
+    // Shared memory: the layout, padded so that no more than 512 / tmem_cols CTAs fit on an SM
+    // (their TMEM allocations then never wait on each other), and checked so that that many do fit.
+    const int need = static_cast<int>(na::tc_smem_bytes(which, bp, D));
+    int per_sm = 512 / tmem_cols;
+    while (per_sm > 1 && per_sm * (need + 1024) > 228 * 1024) --per_sm;
+    int smem = need;
+    const int floor_bytes = (228 * 1024) / (per_sm + 1) - 1024 + 1;
     if (smem < floor_bytes) smem = floor_bytes;
     if (smem > 227 * 1024) return NA_ERR_UNSUPPORTED;
+    bp.per_sm = per_sm;
     bp.smem_bytes = smem;
     long long ctas = static_cast<long long>(g.B) * g.heads;
     for (int a = 0; a < 3; ++a) ctas *= static_cast<long long>(bp.ntile[a]) * g.d[a];
@@ -299,7 +314,12 @@ na_status tc_common(int which, const Geom& g, float scale, na::TcParams& p) {
     p.heads = g.heads;
     p.D = g.D;
     p.scale = scale;
-    p.scale_log2 = scale * 1.44269504088896340736f;
+    // a negative scale is folded into the S product (negated A operand); a zero scale becomes a
+    // tiny positive one (uniform weights up to ~1e-28 relative) so that masked scores stay -inf
+    p.neg = scale < 0.f ? 1u : 0u;
+    p.scale_log2 = std::max(std::fabs(scale), 1e-30f) * 1.44269504088896340736f;
+    const int rad[8] = {g.heads, p.plan.ntile[2], p.plan.ntile[1], p.plan.ntile[0], g.d[2], g.d[1], g.d[0], g.B};
+    for (int i = 0; i < 8; ++i) p.rad[i] = static_cast<uint32_t>(rad[i]);
     return status_ptr(&p.err);
 }
 
@@ -581,9 +601,13 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
                 n0 += chunks_along(which, t * pl.T[0], pl.T[0], Lc0, g.k[0], pl.H[0], pl.G[0], pl.nchk[0]);
             for (int t = 0; t * pl.T[1] < Lc1; ++t)
                 n1 += chunks_along(which, t * pl.T[1], pl.T[1], Lc1, g.k[1], pl.H[1], pl.G[1], pl.nchk[1]);
-            long long inner = 0;  // tiles along axis 2 for every class of axis 2
-            for (int c2 = 0; c2 < g.d[2]; ++c2) inner += ceil_div((g.L[2] - c2 + g.d[2] - 1) / g.d[2], pl.T[2]);
-            total_chunks += n0 * n1 * inner;
+            long long n2 = 0;  // chunks along axis 2 summed over its tiles and classes
+            for (int c2 = 0; c2 < g.d[2]; ++c2) {
+                const int Lc2 = (g.L[2] - c2 + g.d[2] - 1) / g.d[2];
+                for (int t = 0; t * pl.T[2] < Lc2; ++t)
+                    n2 += chunks_along(which, t * pl.T[2], pl.T[2], Lc2, g.k[2], pl.H[2], pl.G[2], pl.nchk[2]);
+            }
+            total_chunks += n0 * n1 * n2;
         }
     total_chunks *= static_cast<long long>(g.B) * g.heads;
     const int n_mma = which == 0 ? 2 : (which == 1 ? 3 : 4);
@@ -597,7 +621,7 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
     out[7] = pl.G[1];
     out[8] = pl.G[2];
     out[9] = pl.NC;
-    out[10] = static_cast<int64_t>(pl.nchk[0]) * pl.nchk[1];
+    out[10] = static_cast<int64_t>(pl.nchk[0]) * pl.nchk[1] * pl.nchk[2];
     out[11] = pl.ctas;
     out[12] = total_chunks * n_mma * 2LL * 128 * pl.NC * D;  // MMA FLOPs issued by all CTAs
     out[13] = pl.tmem_cols;

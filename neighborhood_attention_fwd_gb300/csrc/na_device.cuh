@@ -16,7 +16,7 @@ namespace dev {
 
 // Wait sites recorded in the status word (0x5000 | site) when a bounded wait runs out.
 enum WaitSite : unsigned {
-    kSiteQ = 1, kSiteKV = 2, kSiteS = 3, kSiteP = 4, kSitePV = 5, kSiteEmpty = 6, kSiteFinal = 7,
+    kSiteQ = 1, kSiteKV = 2, kSiteS = 3, kSiteP = 4, kSitePV = 5, kSiteEmpty = 6, kSiteFinal = 7, kSiteSt = 8,
 };
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -58,31 +58,33 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Test the phase with the given parity; if it is not complete the thread sleeps in hardware until
+// it completes or `suspend_ns` elapses (so waiting warps do not take issue slots from working ones).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
 
+constexpr uint32_t kSuspendNs = 100000;  // 0.1 ms per sleep; the status word is polled between sleeps
+
 // Wait for the phase with the given parity to complete.  Gives up (returns false, records the
 // site in the status word) after kWaitLimitNs, or as soon as another CTA has recorded an error.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     const unsigned long long t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (ld_volatile(err) != 0u) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                record_error(err, site);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+        if (ld_volatile(err) != 0u) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            record_error(err, site);
+            return false;
         }
     }
 }
@@ -121,6 +123,11 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Wait until every committed bulk store of this thread has finished reading its shared memory.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -221,6 +228,15 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&r)[8], uint32_t (&s)[8]
     asm volatile("tcgen05.wait::ld.sync.aligned;"
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                    "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]), "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7])
+                 :
+                 : "memory");
+}
+
+// Wait for this thread's outstanding tcgen05.ld; follow it with reg_fence8 on every register set
+// that a load wrote, so that no use of those registers moves above the wait.
+__device__ __forceinline__ void tmem_ld_wait_all() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void reg_fence8(uint32_t (&r)[8]) {
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
                  :
                  : "memory");
 }

@@ -11,11 +11,6 @@
 
 namespace na {
 
-constexpr int kRows = 128;          // query (or key) rows per CTA tile = tcgen05 M
-constexpr int kSoftmaxWarps = 4;    // one warp per 32-lane TMEM sub-partition
-constexpr int kThreads = 160;       // 4 softmax/epilogue warps + 1 producer (TMA + MMA) warp
-constexpr int kSlots = 2;           // K/V (or Q/dO) chunk ring depth
-
 struct Geom {
     int B, heads, D;
     int L[3], k[3], d[3];
@@ -23,15 +18,18 @@ struct Geom {
 
 // Static tile plan of one tensor-core kernel for one problem.
 struct TilePlan {
-    int T[3];        // CTA tile extents (class coordinates), T0*T1*T2 == 128
-    int H[3];        // halo box extents: keys (fwd, dQ) or queries (dK/dV) a tile may need
-    int G[3];        // chunk box extents; G[2] == H[2]
-    int NC;          // rows of one chunk = G0*G1*G2 (multiple of 16, <= 256)
-    int nchk[2];     // chunks along axes 0 and 1 that cover the halo box
+    int T[3];        // tile extents (class coordinates), T0*T1*T2 == 128, powers of two
+    int H[3];        // halo box extents: keys (fwd, dQ) or queries (dK/dV) a tile may need;
+                     // H[a] == nchk[a] * G[a] along every axis
+    int G[3];        // chunk box extents; G[2] == 8 * NB
+    int NB;          // 8-column blocks per chunk segment (1..4)
+    int NC;          // rows of one chunk = G0*G1*G2 (multiple of 16, <= 112)
+    int nchk[3];     // chunks along each axis that cover the halo box
     int ntile[3];    // tiles per axis and residue class: ceil(ceil(L/d) / T)
     int tmem_cols;   // TMEM columns allocated per CTA (power of two)
+    int per_sm;      // persistent CTAs per SM (the grid is per_sm x SM count, at most `ctas`)
     int smem_bytes;  // dynamic shared memory per CTA (includes alignment slack)
-    int64_t ctas;    // grid size
+    int64_t ctas;    // tiles (linearised: head fastest, then tile along axes 2,1,0, class 2,1,0, batch)
 };
 
 // Kernel parameters of the tensor-core kernels (passed as __grid_constant__).
@@ -45,7 +43,10 @@ struct TcParams {
     int L[3], k[3], d[3];
     int B, heads, D;
     float scale;        // softmax scale (applied to q.k)
-    float scale_log2;   // scale * log2(e)
+    float scale_log2;   // max(|scale|, tiny) * log2(e); a negative scale negates A of the S product
+    uint32_t neg;       // 1 when scale < 0
+    uint32_t rad[8];    // mixed radix of the tile index: heads, ntile2, ntile1, ntile0, d2, d1, d0, B
+    uint32_t step[8];   // the grid size written in that radix (persistent CTAs step by it)
     float* lse_out;     // fwd: [B, L.., heads] natural-log LSE
     const float* lse;   // bwd: forward LSE
     const float* delta; // bwd: Delta = <dO, O>

@@ -35,15 +35,30 @@ def inv_hi(j, Lc, k):
     return Lc - 1 if j >= Lc - k else j + k // 2
 
 
+def range_bits(lo, hi, width=32):
+    lo, hi = max(0, min(width, lo)), max(0, min(width, hi))
+    return ((1 << hi) - 1) & ~((1 << lo) - 1) if hi > lo else 0
+
+
+def segment_bits(G0, G1, y0, z0, ylo, yhi, zlo, zhi):
+    zb = range_bits(zlo - z0, zhi - z0) & range_bits(0, G1)
+    bits = 0
+    for y in range(max(ylo, y0), min(yhi, y0 + G0)):
+        bits |= zb << ((y - y0) * G1)
+    return bits
+
+
 def replay(which, L, k, d, plan):
     """Yield (row_global_coords, key_or_query_global_coords) pairs the kernel marks live."""
     T = (plan["T1"], plan["T2"], plan["T3"])
     H = (plan["H1"], plan["H2"], plan["H3"])
     G = (plan["G1"], plan["G2"], plan["G3"])
     NC = plan["NC"]
+    NB = G[2] // 8
+    assert G[2] % 8 == 0 and 1 <= NB <= 4
     Lcm = [-(-L[a] // d[a]) for a in range(3)]
     ntile = [-(-Lcm[a] // T[a]) for a in range(3)]
-    nchk = [-(-H[0] // G[0]), -(-H[1] // G[1])]
+    nchk = [-(-H[a] // G[a]) for a in range(3)]
     pairs = []
     for cls in itertools.product(*[range(x) for x in d]):
         Lc = [(L[a] - cls[a] + d[a] - 1) // d[a] for a in range(3)]
@@ -51,7 +66,7 @@ def replay(which, L, k, d, plan):
             t0 = [t[a] * T[a] for a in range(3)]
             if any(t0[a] >= Lc[a] for a in range(3)):
                 continue
-            h0, need = [0] * 3, [0] * 3
+            h0, nc = [0] * 3, [0] * 3
             for a in range(3):
                 last = min(t0[a] + T[a], Lc[a]) - 1
                 if which != 2:
@@ -59,10 +74,8 @@ def replay(which, L, k, d, plan):
                 else:
                     lo, hi = inv_lo(t0[a], k[a]), inv_hi(last, Lc[a], k[a])
                 h0[a] = min(lo, max(0, Lc[a] - H[a]))
-                need[a] = hi - h0[a] + 1
-                assert need[a] <= H[a], "halo box too small"
-            ncy = min(nchk[0], -(-need[0] // G[0]))
-            ncz = min(nchk[1], -(-need[1] // G[1]))
+                assert hi - h0[a] + 1 <= H[a], "halo box too small"
+                nc[a] = min(nchk[a], (hi - h0[a] + G[a]) // G[a])
             rows = []
             for row in range(128):
                 tq = (row // (T[2] * T[1]), (row // T[2]) % T[1], row % T[2])
@@ -87,29 +100,41 @@ def replay(which, L, k, d, plan):
                     continue
                 ulo = [min(r[2][a] for r in live) for a in range(3)]
                 uhi = [max(r[2][a] + r[3][a] for r in live) for a in range(3)]
-                blo, bhi = max(0, ulo[2]) >> 3, min(H[2], uhi[2] + 7) >> 3
-                for ci in range(ncy * ncz):
-                    y0, z0 = (ci // ncz) * G[0], (ci % ncz) * G[1]
-                    ya, yb = max(ulo[0], y0), min(uhi[0], y0 + G[0])
-                    za, zb = max(ulo[1], z0), min(uhi[1], z0 + G[1])
-                    for y in range(ya, yb):
-                        for z in range(za, zb):
-                            seg = ((y - y0) * G[1] + (z - z0)) * H[2]
-                            for bb in range(blo, bhi):
-                                assert seg + bb * 8 + 8 <= NC, "TMEM/P column outside the chunk"
-                                for valid, j, lo, ln in lanes:
-                                    if not (0 <= y - lo[0] < ln[0] and 0 <= z - lo[1] < ln[1]):
+                for ci in range(nc[0] * nc[1] * nc[2]):
+                    cx, r = ci % nc[2], ci // nc[2]
+                    cz, cy = r % nc[1], r // nc[1]
+                    y0, z0, x0 = cy * G[0], cz * G[1], cx * G[2]
+                    useg = segment_bits(G[0], G[1], y0, z0, ulo[0], uhi[0], ulo[1], uhi[1])
+                    xa, xb = ulo[2] - x0, uhi[2] - x0
+                    ublk = range_bits(xa >> 3, (xb + 7) >> 3) & ((1 << NB) - 1) if xb > xa else 0
+                    act = 0
+                    for s_ in range(16):
+                        if (useg >> s_) & 1:
+                            act |= ublk << (s_ * NB)
+                    for valid, j, lo, ln in lanes:
+                        is_live = all(x > 0 for x in ln)
+                        rowseg = segment_bits(G[0], G[1], y0, z0, lo[0], lo[0] + ln[0], lo[1], lo[1] + ln[1]) if is_live else 0
+                        m8 = 0
+                        for bb in range(NB):
+                            m8 |= range_bits(lo[2] - x0 - 8 * bb, lo[2] + ln[2] - x0 - 8 * bb, 8) << (8 * bb)
+                        for i in range(NC // 8):
+                            if not (act >> i) & 1:
+                                continue
+                            assert 8 * i + 8 <= NC, "TMEM/P column outside the chunk"
+                            seg, bb = i // NB, i % NB
+                            if not (rowseg >> seg) & 1:
+                                continue
+                            byte = (m8 >> (8 * bb)) & 0xFF
+                            y, z = y0 + seg // G[1], z0 + seg % G[1]
+                            for e in range(8):
+                                if (byte >> e) & 1:
+                                    assert valid or which == 0
+                                    if not valid:
                                         continue
-                                    for e in range(8):
-                                        x = 8 * bb + e
-                                        if lo[2] <= x < lo[2] + ln[2]:
-                                            assert valid or which == 0
-                                            if not valid:
-                                                continue
-                                            other = [h0[0] + y, h0[1] + z, h0[2] + x]
-                                            rg = tuple(cls[a] + d[a] * j[a] for a in range(3))
-                                            og = tuple(cls[a] + d[a] * other[a] for a in range(3))
-                                            pairs.append((rg, og))
+                                    other = [h0[0] + y, h0[1] + z, h0[2] + x0 + 8 * bb + e]
+                                    rg = tuple(cls[a] + d[a] * j[a] for a in range(3))
+                                    og = tuple(cls[a] + d[a] * other[a] for a in range(3))
+                                    pairs.append((rg, og))
     return pairs
 
 
