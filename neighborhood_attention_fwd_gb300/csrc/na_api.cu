@@ -170,6 +170,65 @@ int max_halo(int which, int T, int L, int k, int d) {
     return best;
 }
 
+// Modelled cycles of one interior tile (every row's window unclamped) under a candidate plan.
+// The softmax term replays what the kernels do: per chunk each warp (32 consecutive rows) reads
+// the run of 16-column groups that holds its rows' windows (forward: one warp per row quarter;
+// backward: two warps share a quarter's groups).  Chunks of a tile overlap on the tensor core and
+// the copy engine, so the tile costs the largest of softmax, MMA and chunk-copy time.
+double tile_cost(int which, const Geom& g, const TilePlan& pl, int n_mma, int per_sm) {
+    int ulo[4][3], uhi[4][3];
+    for (int w = 0; w < 4; ++w)
+        for (int a = 0; a < 3; ++a) {
+            ulo[w][a] = 1 << 30;
+            uhi[w][a] = -(1 << 30);
+        }
+    for (int row = 0; row < 128; ++row) {
+        const int tq[3] = {row / (pl.T[1] * pl.T[2]), (row / pl.T[2]) % pl.T[1], row % pl.T[2]};
+        for (int a = 0; a < 3; ++a) {
+            const int len = 2 * (g.k[a] / 2) + 1;  // window or inverse window of an interior row
+            ulo[row / 32][a] = std::min(ulo[row / 32][a], tq[a]);
+            uhi[row / 32][a] = std::max(uhi[row / 32][a], tq[a] + len);
+        }
+    }
+    int nc[3];
+    for (int a = 0; a < 3; ++a) nc[a] = std::min(pl.nchk[a], ceil_div(pl.T[a] + 2 * (g.k[a] / 2), pl.G[a]));
+    double soft = 0;
+    const int C = nc[0] * nc[1] * nc[2];
+    for (int c0 = 0; c0 < nc[0]; ++c0)
+        for (int c1 = 0; c1 < nc[1]; ++c1)
+            for (int c2 = 0; c2 < nc[2]; ++c2) {
+                const int o[3] = {c0 * pl.G[0], c1 * pl.G[1], c2 * pl.G[2]};
+                int mx = 0, sum = 0;
+                for (int w = 0; w < 4; ++w) {
+                    int lo[3], hi[3];
+                    bool empty = false;
+                    for (int a = 0; a < 3; ++a) {
+                        lo[a] = std::max(ulo[w][a] - o[a], 0);
+                        hi[a] = std::min(uhi[w][a] - o[a], pl.G[a]);
+                        if (lo[a] >= hi[a]) empty = true;
+                    }
+                    int n = 0;
+                    if (!empty) {
+                        const int clo = (lo[0] * pl.G[1] + lo[1]) * pl.G[2] + lo[2];
+                        const int chi = ((hi[0] - 1) * pl.G[1] + hi[1] - 1) * pl.G[2] + hi[2];
+                        n = (chi + 15) / 16 - clo / 16;
+                    }
+                    mx = std::max(mx, n);
+                    sum += n;
+                }
+                soft += 0.5 * mx + 0.125 * sum;
+            }
+    const double per_group = which == 0 ? 150.0 : 90.0;  // cycles per 16-column group and warp
+    const double soft_cyc = soft * per_group + 300.0 * C;
+    int nbias = 0;
+    for (int a = 0; a < 3; ++a) nbias += pl.H[a] > 1 ? ceil_div(pl.G[a], 16) : 0;
+    const double mma_cyc = C * (n_mma * 2.0 * 128 * pl.NC * g.D + nbias * 2.0 * 128 * pl.NC * 16) / 6144.0;
+    const double copy_cyc = C * 4.0 * pl.NC * g.D / 40.0;
+    double t = std::max(soft_cyc, std::max(mma_cyc, copy_cyc)) + 300.0;
+    if (which == 0 && per_sm < 2) t *= 1.7;  // the forward relies on two CTAs per SM to hide latency
+    return t;
+}
+
 na_status plan_tc(int which, const Geom& g, TilePlan& out) {
     const PlanKey key{which, g.D, g.B, g.heads, {g.L[0], g.L[1], g.L[2]}, {g.k[0], g.k[1], g.k[2]},
                       {g.d[0], g.d[1], g.d[2]}};
@@ -196,55 +255,41 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
             const int T0 = 128 / (T1 * T2);
             const int T[3] = {T0, T1, T2};
             bool skip = false;
-            for (int a = 0; a < 3; ++a)
-                if (T[a] * g.d[a] > 256) skip = true;  // TMA box limit (rows past an axis end are just idle)
+            for (int a = 0; a < 3; ++a) {
+                if (T[a] * g.d[a] > 256) skip = true;        // TMA box limit (rows past an axis end are just idle)
+            }
             if (skip) continue;
             int Hx[3];
             for (int a = 0; a < 3; ++a) Hx[a] = max_halo(which, T[a], g.L[a], g.k[a], g.d[a]);
-            // warp block (32 consecutive rows, innermost axis fastest) and its union of windows
-            const int W2 = std::min(T2, 32), W1 = std::min(T1, 32 / W2), W0 = 32 / (W2 * W1);
-            const int W[3] = {W0, W1, W2};
-            int U[3];
-            for (int a = 0; a < 3; ++a) U[a] = std::min(W[a] + g.k[a] - 1 + (which == 2 ? g.k[a] / 2 : 0), Hx[a]);
             double tiles = 1;
             for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
-            for (int NB = 1; NB <= 4; ++NB) {
-                const int G2 = 8 * NB;
+            const int gmax0 = Hx[0] > 1 ? std::min(Hx[0], 32) : 1, gmax1 = Hx[1] > 1 ? std::min(Hx[1], 32) : 1;
+            for (int G2 = 8; G2 <= 32; G2 += 8) {
                 if (G2 > (Hx[2] + 7) / 8 * 8 || G2 * g.d[2] > 256) continue;
-                const int n2 = ceil_div(Hx[2], G2);
-                // softmax work per row: the warp union's segments times its 8-column blocks
-                const double logits_row = static_cast<double>(U[0]) * U[1] * 8.0 * (ceil_div(U[2], 8) + (n2 > 1 ? 1 : 0));
-                for (int G1 = 1; G1 <= Hx[1]; ++G1)
-                    for (int G0 = 1; G0 <= Hx[0]; ++G0) {
+                for (int G1 = 1; G1 <= gmax1; ++G1)
+                    for (int G0 = 1; G0 <= gmax0; ++G0) {
                         const int NC = G0 * G1 * G2;
                         if (NC > ncmax || NC % 16 != 0) continue;
                         if (G0 * g.d[0] > 256 || G1 * g.d[1] > 256) continue;
-                        if (G0 > 1 && G1 != Hx[1]) continue;  // chunks: slabs of whole axis-1 rows or part of one
-                        if (G0 * G1 > 1 && G2 != 8 * NB) continue;
-                        const int n0 = ceil_div(Hx[0], G0), n1 = ceil_div(Hx[1], G1);
-                        const double C = static_cast<double>(n0) * n1 * n2;
-                        const double mma = C * (n_score + n_update) * 2.0 * 128 * NC * D / 8192.0;
-                        const double soft = logits_row * (which == 0 ? 4.0 : 5.0);
-                        const double block_overhead = C * (NC / 8) * 6.0;
-                        const double tile_cost = std::max(soft + block_overhead, 0.6 * mma) + 150.0 * C;
-                        const double cost = tile_cost * tiles;
+                        TilePlan cand{};
+                        const int G[3] = {G0, G1, G2};
+                        for (int a = 0; a < 3; ++a) {
+                            cand.T[a] = T[a];
+                            cand.ntile[a] = ceil_div(Lcm[a], T[a]);
+                            cand.H[a] = Hx[a];
+                            cand.G[a] = G[a];
+                            cand.nchk[a] = ceil_div(Hx[a], G[a]);
+                        }
+                        cand.NC = NC;
+                        const int need = static_cast<int>(na::tc_smem_bytes(which, cand, D));
+                        if (need > 227 * 1024) continue;
+                        const int per_sm = std::max(1, std::min(512 / tmem_cols, (228 * 1024) / (need + 1024)));
+                        const double cost =
+                            tile_cost(which, g, cand, n_score + n_update, per_sm) * tiles;
                         if (!found || cost < best) {
                             found = true;
                             best = cost;
-                            bp = TilePlan{};
-                            for (int a = 0; a < 3; ++a) {
-                                bp.T[a] = T[a];
-                                bp.ntile[a] = ceil_div(Lcm[a], T[a]);
-                                bp.H[a] = Hx[a];
-                            }
-                            bp.G[0] = G0;
-                            bp.G[1] = G1;
-                            bp.G[2] = G2;
-                            bp.NB = NB;
-                            bp.NC = NC;
-                            bp.nchk[0] = n0;
-                            bp.nchk[1] = n1;
-                            bp.nchk[2] = n2;
+                            bp = cand;
                         }
                     }
             }
@@ -383,7 +428,7 @@ na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if ((st = encode_map(&p.tm[0], q, g, pl.T)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[1], k, g, chunk)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[2], v, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[3], o, g, pl.T)) != NA_OK) return st;
+    p.out0 = static_cast<__nv_bfloat16*>(o);
     p.lse_out = lse;
     return cuda_status(na::launch_fwd_tc(p, s));
 }
@@ -443,7 +488,7 @@ na_status na_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     if ((st = encode_map(&p.tm[1], dO, g, pl.T)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[2], k, g, chunk)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[3], v, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[4], dQ, g, pl.T)) != NA_OK) return st;
+    p.out0 = static_cast<__nv_bfloat16*>(dQ);
     p.lse = lse;
     p.delta = delta;
     return cuda_status(na::launch_dq_tc(p, s));
@@ -479,8 +524,8 @@ na_status na_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
     if ((st = encode_map(&p.tm[1], v, g, pl.T)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[2], q, g, chunk)) != NA_OK) return st;
     if ((st = encode_map(&p.tm[3], dO, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[4], dK, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[5], dV, g, pl.T)) != NA_OK) return st;
+    p.out0 = static_cast<__nv_bfloat16*>(dK);
+    p.out1 = static_cast<__nv_bfloat16*>(dV);
     p.lse = lse;
     p.delta = delta;
     return cuda_status(na::launch_dkdv_tc(p, s));

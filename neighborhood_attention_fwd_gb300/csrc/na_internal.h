@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 namespace na {
 
@@ -21,8 +22,7 @@ struct TilePlan {
     int T[3];        // tile extents (class coordinates), T0*T1*T2 == 128, powers of two
     int H[3];        // halo box extents: keys (fwd, dQ) or queries (dK/dV) a tile may need;
                      // H[a] == nchk[a] * G[a] along every axis
-    int G[3];        // chunk box extents; G[2] == 8 * NB
-    int NB;          // 8-column blocks per chunk segment (1..4)
+    int G[3];        // chunk box extents; G[2] a multiple of 8; G[a] <= 32 along masked axes
     int NC;          // rows of one chunk = G0*G1*G2 (multiple of 16, <= 112)
     int nchk[3];     // chunks along each axis that cover the halo box
     int ntile[3];    // tiles per axis and residue class: ceil(ceil(L/d) / T)
@@ -34,11 +34,12 @@ struct TilePlan {
 
 // Kernel parameters of the tensor-core kernels (passed as __grid_constant__).
 // Tensor-map roles per kernel:
-//   fwd : tm[0] q tile, tm[1] k chunk, tm[2] v chunk, tm[3] o tile (store)
-//   dq  : tm[0] q tile, tm[1] dO tile, tm[2] k chunk, tm[3] v chunk, tm[4] dQ tile (store)
-//   dkdv: tm[0] k tile, tm[1] v tile, tm[2] q chunk, tm[3] dO chunk, tm[4] dK tile, tm[5] dV tile
+//   fwd : tm[0] q tile, tm[1] k chunk, tm[2] v chunk
+//   dq  : tm[0] q tile, tm[1] dO tile, tm[2] k chunk, tm[3] v chunk
+//   dkdv: tm[0] k tile, tm[1] v tile, tm[2] q chunk, tm[3] dO chunk
+// Outputs are written with plain 16-byte stores, one row per thread.
 struct TcParams {
-    CUtensorMap tm[6];
+    CUtensorMap tm[4];
     TilePlan plan;
     int L[3], k[3], d[3];
     int B, heads, D;
@@ -47,6 +48,8 @@ struct TcParams {
     uint32_t neg;       // 1 when scale < 0
     uint32_t rad[8];    // mixed radix of the tile index: heads, ntile2, ntile1, ntile0, d2, d1, d0, B
     uint32_t step[8];   // the grid size written in that radix (persistent CTAs step by it)
+    __nv_bfloat16* out0; // fwd: O; dQ: dQ; dK/dV: dK  ([B, L.., heads, D])
+    __nv_bfloat16* out1; // dK/dV: dV
     float* lse_out;     // fwd: [B, L.., heads] natural-log LSE
     const float* lse;   // bwd: forward LSE
     const float* delta; // bwd: Delta = <dO, O>

@@ -12,17 +12,22 @@
 //   * the keys (or queries) any row of the tile can touch form a box, the halo; TMA stages it in
 //     chunks (boxes of the halo with element stride = dilation), so nothing outside it is read;
 //   * S = Q K^T and the products with P run on tcgen05 (bf16 in, fp32 accumulators in TMEM);
-//   * a chunk is G0 x G1 segments of NB 8-column blocks; each softmax warp owns 32 TMEM lanes
-//     (32 rows) and touches only the blocks that hold a key of at least one of its rows; the
-//     exact per-row window is applied from bit masks (one bit per segment, one byte per block
-//     column), so the predication costs a few integer ops per 8 logits.
+//   * the window mask costs the softmax nothing: it is one more tensor-core product per chunk
+//     and axis, S += A_bias B_bias^T, where B_bias holds the one-hot local coordinate of every
+//     chunk column and A_bias, per row, 0 inside the row's window and -2^100 outside.  A_bias
+//     depends on the tile only through its position relative to the borders, so it is built once
+//     and rebuilt only along the axes whose border situation changes;
+//   * each softmax warp owns 32 TMEM lanes (32 rows) and reads, per chunk, only the contiguous run
+//     of 16-column groups that holds the keys of its rows' windows; the rest of its P rows is zero.
 //
 // Pipeline (persistent CTAs, each looping over tiles):
-//   producer warp : TMA of the tile tensors (2-slot ring) and of halo chunks (kStages-slot ring)
-//   MMA warp      : per chunk the "score" products into a double-buffered TMEM accumulator, then
-//                   the previous chunk's "update" products into a double-buffered tile accumulator
+//   producer warp : TMA of the tile tensors (2-slot ring) and of halo chunks (stage ring); the
+//                   window-bias operand when a tile's border situation differs from the last one
+//   MMA warp      : per chunk the "score" products (and the bias products) into a double-buffered
+//                   TMEM accumulator, then the previous chunk's "update" products into a
+//                   double-buffered tile accumulator
 //   softmax warps : per chunk read scores from TMEM, write P (or dS) to a double-buffered smem
-//                   operand; per tile read the accumulator and store it with TMA.
+//                   operand; per tile read the accumulator and store it.
 // Every mbarrier wait is bounded (see na_device.cuh); a wait that gives up records the site in the
 // status word and the CTA stops issuing work.
 #include <cmath>
@@ -38,30 +43,54 @@ namespace {
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
-constexpr int kStages = 3;                  // halo chunk ring depth
-constexpr int kMaxBlocks = 14;              // 8-column blocks per chunk (NC <= 112)
+constexpr int kMaxStages = 3;
 
+__host__ __device__ constexpr int stages_of(int D) { return D <= 32 ? 3 : 2; }  // halo chunk ring depth
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
 __host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2); }
 
-// Most 8-column blocks one forward chunk can hold for head dim D (TMEM: 2 * NC + 2 * D <= 256).
-__host__ __device__ constexpr int fwd_max_blocks(int D) {
-    return ((256 - 2 * D) / 2) / 8 < 12 ? ((256 - 2 * D) / 2) / 8 : 12;
-}
-
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// Window-bias operands.  Along every axis whose halo is longer than one position, a chunk column's
+// local coordinate (< G[a] <= 32) is one-hot encoded in nbg[a] 16-column groups of the constant
+// operand B; the per-tile operand A holds, for every row, chunk index along the axis and group,
+// 0 where the coordinate is inside the row's window and -2^100 elsewhere.  Both are K-major
+// 16-column blocks with 32-byte swizzle: A groups of 128 rows (4 KB), B groups of NC rows.
+struct BiasGeom {
+    int nbg[3];    // groups per chunk along each axis (0: the axis needs no mask)
+    int abase[3];  // first A group of each axis (A group = abase + chunk index * nbg + group)
+    int bbase[3];  // first B group of each axis
+    int na, nb;    // A groups, B groups
+};
+
+__host__ __device__ inline BiasGeom bias_geom(const TilePlan& pl) {
+    BiasGeom b{};
+    for (int a = 0; a < 3; ++a) {
+        b.nbg[a] = pl.H[a] > 1 ? (pl.G[a] + 15) / 16 : 0;
+        b.abase[a] = b.na;
+        b.bbase[a] = b.nb;
+        b.na += pl.nchk[a] * b.nbg[a];
+        b.nb += b.nbg[a];
+    }
+    return b;
+}
+
+constexpr uint32_t kBf16One = 0x3F80u;    // 1.0
+constexpr uint32_t kBf16Neg = 0xF180u;    // -2^100
+constexpr float kMaskedBelow = -1.0e29f;  // a chunk maximum below this means "no live key"
+
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-//   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [kStages] x {K, V};  P[2];           staging {O}
-//   which 1 (dQ)  : tile ring [2] x {Q, dO}; chunk ring [kStages] x {K, V};  dS[2];          staging {dQ}
-//   which 2 (dKdV): tile ring [2] x {K, V};  chunk ring [kStages] x {Q, dO}; P^T[2], dS^T[2]; staging {dK, dV}
-//                   plus per chunk slot the LSE (log2 units) and Delta of its queries.
+//   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [S] x {K, V};  P[2]
+//   which 1 (dQ)  : tile ring [2] x {Q, dO}; chunk ring [S] x {K, V};  dS[2]
+//   which 2 (dKdV): tile ring [2] x {K, V};  chunk ring [S] x {Q, dO}; P^T[2], dS^T[2];
+//                   per chunk slot the -LSE (log2 units) and Delta of the chunk's queries
+//   all: window-bias operands A (per tile) and B (constant).
 struct TcLayout {
     uint32_t tile0, tile_slot, tile_t;     // tile ring: tile0 + slot * tile_slot + tensor * tile_t
     uint32_t chunk0, chunk_slot, chunk_t;  // chunk ring
     uint32_t p0, p_buf, p_op;              // P / dS operands
-    uint32_t aux0, aux_slot;               // dK/dV per-column LSE (log2) and Delta
-    uint32_t stage0, stage_t;              // epilogue staging
+    uint32_t abias, bbias, bgroup;         // window-bias operands; bgroup = bytes of one B group
+    uint32_t aux0, aux_slot;               // dK/dV: per chunk slot -LSE (log2) and Delta
     uint32_t bars, total;
     __host__ __device__ uint32_t tile(uint32_t slot, uint32_t t) const { return tile0 + slot * tile_slot + t * tile_t; }
     __host__ __device__ uint32_t chunk(uint32_t slot, uint32_t t) const {
@@ -69,15 +98,14 @@ struct TcLayout {
     }
     __host__ __device__ uint32_t p(uint32_t buf, uint32_t op) const { return p0 + buf * p_buf + op * p_op; }
     __host__ __device__ uint32_t aux(uint32_t slot) const { return aux0 + slot * aux_slot; }
-    __host__ __device__ uint32_t stage(uint32_t t) const { return stage0 + t * stage_t; }
 };
 
 __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int D) {
     const uint32_t tile = align_up(128u * D * 2u, 1024);
     const uint32_t chunk = align_up(static_cast<uint32_t>(pl.NC) * D * 2u, 1024);
     const uint32_t pbytes = static_cast<uint32_t>((pl.NC + 31) / 32) * 8192u;
-    const uint32_t ntile = which == 0 ? 1 : 2, nop = which == 2 ? 2 : 1, nstage = which == 2 ? 2 : 1;
-    const uint32_t auxb = which == 2 ? align_up(2u * 4u * static_cast<uint32_t>(pl.NC), 1024) : 0u;
+    const uint32_t ntile = which == 0 ? 1 : 2, nop = which == 2 ? 2 : 1;
+    const BiasGeom bg = bias_geom(pl);
     TcLayout L{};
     uint32_t o = 0;
     L.tile0 = o;
@@ -87,17 +115,19 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     L.chunk0 = o;
     L.chunk_t = chunk;
     L.chunk_slot = 2 * chunk;
-    o += kStages * L.chunk_slot;
+    o += stages_of(D) * L.chunk_slot;
     L.p0 = o;
     L.p_op = pbytes;
     L.p_buf = nop * pbytes;
     o += 2 * L.p_buf;
+    L.abias = o;
+    o += static_cast<uint32_t>(bg.na) * 4096u;
+    L.bbias = o;
+    L.bgroup = static_cast<uint32_t>(pl.NC) * 32u;
+    o += align_up(static_cast<uint32_t>(bg.nb) * L.bgroup, 1024);
     L.aux0 = o;
-    L.aux_slot = auxb;
-    o += kStages * auxb;
-    L.stage0 = o;
-    L.stage_t = tile;
-    o += nstage * tile;
+    L.aux_slot = which == 2 ? align_up(8u * static_cast<uint32_t>(pl.NC), 128) : 0u;
+    o += align_up(stages_of(D) * L.aux_slot, 1024);
     L.bars = o;
     o += 512;
     L.total = o;
@@ -106,9 +136,9 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
 
 // mbarrier indices
 enum Bar {
-    kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kStages, kSFull = 4 + 2 * kStages,
+    kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kMaxStages, kSFull = 4 + 2 * kMaxStages,
     kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + 2, kOFull = kPEmpty + 2, kOEmpty = kOFull + 2,
-    kStFree = kOEmpty + 2, kStFull = kStFree + 1, kFin = kStFull + 1, kNumBars = kFin + 1
+    kFin = kOEmpty + 2, kNumBars = kFin + 1
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -203,17 +233,25 @@ __device__ __forceinline__ bool next_tile(const TcParams& p, int which, TileIter
     return false;
 }
 
-// Chunk ci's origin in halo coordinates (chunk grid order: axis 0 slowest, axis 2 fastest).
-__device__ __forceinline__ void chunk_origin(const TilePlan& pl, const Cta& c, int ci, int& y0, int& z0, int& x0) {
-    const int cx = ci % c.nc[2], r = ci / c.nc[2];
-    const int cz = r % c.nc[1], cy = r / c.nc[1];
-    y0 = cy * pl.G[0];
-    z0 = cz * pl.G[1];
-    x0 = cx * pl.G[2];
+// Border situation of a tile along one axis: 0 when every row is inside the class, every row's
+// window (or inverse window) is the unclamped one and the halo starts at the window of the tile's
+// first row -- then the rows' ranges relative to the halo are the same for every such tile --
+// otherwise a code of (t0, Lc), which fixes them.
+__device__ __forceinline__ uint64_t axis_sig(int which, int t0, int T, int Lc, int k, int H) {
+    const int r = k >> 1;
+    bool in = t0 + T <= Lc && t0 - r <= Lc - H;
+    if (which != 2) {
+        in = in && t0 >= r && t0 + T - 1 <= Lc - 1 - r;
+    } else {
+        in = in && t0 >= k && t0 + T - 1 < Lc - k;
+    }
+    return in ? 0ull : ((static_cast<uint64_t>(static_cast<uint32_t>(Lc)) << 32) | static_cast<uint32_t>(t0 + 1));
 }
 
 // Per-row geometry: for each axis the halo-coordinate range [lo, lo + len) of keys (fwd, dQ: the
-// query's window) or queries (dK/dV: the queries whose windows hold the key) of this row.
+// query's window) or queries (dK/dV: the queries whose windows hold the key) of this row.  For dQ
+// and dK/dV a row past the end of an axis has len = 0 along that axis (its P row is zero); the
+// range along an axis depends on that axis alone.
 struct RowGeom {
     int lo[3], len[3];
     bool valid;
@@ -231,7 +269,8 @@ __device__ __forceinline__ RowGeom row_geom(const TcParams& p, int which, const 
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
         const int j = c.t0[a] + tq[a];
-        if (j >= c.Lc[a]) g.valid = false;
+        const bool in = j < c.Lc[a];
+        if (!in) g.valid = false;
         const int jc = min(j, c.Lc[a] - 1);
         if (which != 2) {
             g.lo[a] = win_start(jc, c.Lc[a], p.k[a]) - c.h0[a];
@@ -240,11 +279,8 @@ __device__ __forceinline__ RowGeom row_geom(const TcParams& p, int which, const 
             g.lo[a] = inv_lo(jc, p.k[a]) - c.h0[a];
             g.len[a] = inv_hi(jc, c.Lc[a], p.k[a]) - inv_lo(jc, p.k[a]) + 1;
         }
+        if (!in && which != 0) g.len[a] = 0;
         tok = tok * p.L[a] + (c.cls[a] + p.d[a] * jc);
-    }
-    if (!g.valid && which != 0) {
-#pragma unroll
-        for (int a = 0; a < 3; ++a) g.len[a] = 0;  // no keys: the P row is all zero
     }
     g.token = tok;
     return g;
@@ -275,65 +311,68 @@ __device__ __forceinline__ uint32_t range_bits32(int lo, int hi) {
     return up_hi & ~up_lo;
 }
 
-// Segment bits of a chunk (segment s = (y - y0) * G1 + (z - z0)) whose (y, z) lies in
-// [ylo, yhi) x [zlo, zhi).
-__device__ __forceinline__ uint32_t segment_bits(const TilePlan& pl, int y0, int z0, int ylo, int yhi, int zlo,
-                                                 int zhi) {
-    const uint32_t zb = range_bits32(zlo - z0, zhi - z0) & range_bits32(0, pl.G[1]);
-    uint32_t bits = 0;
-    for (int y = max(ylo, y0); y < min(yhi, y0 + pl.G[0]); ++y) bits |= zb << ((y - y0) * pl.G[1]);
-    return bits;
-}
-
-// Per-chunk masks.  act: bit i = block i of the chunk intersects the warp union (warp-uniform).
-// rowseg: bit s = segment s lies inside this row's window along axes 0 and 1.
-// m8: byte bb = this row's live columns of block bb (block columns 8bb .. 8bb+7 of a segment).
-struct ChunkMasks {
-    uint32_t act, rowseg, m8;
-};
-
-// Chunk cursor: origin (halo coordinates) of the current chunk, stepped in chunk-grid order
-// (axis 0 slowest, axis 2 fastest) without divisions.
+// Chunk cursor: chunk indices along each axis and the chunk origin in halo coordinates, stepped in
+// chunk-grid order (axis 0 slowest, axis 2 fastest) without divisions.
 struct ChunkCursor {
-    int y0, z0, x0;
+    int ix[3];
+    int o[3];
 };
+__device__ __forceinline__ ChunkCursor cursor_begin() { return ChunkCursor{{0, 0, 0}, {0, 0, 0}}; }
 __device__ __forceinline__ void cursor_next(const TilePlan& pl, const Cta& c, ChunkCursor& k) {
-    k.x0 += pl.G[2];
-    if (k.x0 >= c.nc[2] * pl.G[2]) {
-        k.x0 = 0;
-        k.z0 += pl.G[1];
-        if (k.z0 >= c.nc[1] * pl.G[1]) {
-            k.z0 = 0;
-            k.y0 += pl.G[0];
+    ++k.ix[2];
+    k.o[2] += pl.G[2];
+    if (k.ix[2] >= c.nc[2]) {
+        k.ix[2] = 0;
+        k.o[2] = 0;
+        ++k.ix[1];
+        k.o[1] += pl.G[1];
+        if (k.ix[1] >= c.nc[1]) {
+            k.ix[1] = 0;
+            k.o[1] = 0;
+            ++k.ix[0];
+            k.o[0] += pl.G[0];
         }
     }
 }
 
-template <int NB>
-__device__ __forceinline__ ChunkMasks chunk_masks(const TilePlan& pl, const ChunkCursor& k, const WarpUnion& u,
-                                                  const RowGeom& g, bool live) {
-    constexpr int kSeg = (kMaxBlocks + NB - 1) / NB;
-    ChunkMasks m;
-    const uint32_t useg = segment_bits(pl, k.y0, k.z0, u.lo[0], u.hi[0], u.lo[1], u.hi[1]);
-    // blocks of a segment that intersect the warp's column union
-    const int xa = u.lo[2] - k.x0, xb = u.hi[2] - k.x0;
-    const uint32_t ublk = xb > xa ? range_bits32(xa >> 3, (xb + 7) >> 3) & ((1u << NB) - 1u) : 0u;
-    m.act = 0;
+// The run of 16-column groups [glo, glo + n) of a chunk that holds every key (column) inside the
+// union of a warp's windows.  Chunk column = (y * G1 + z) * G2 + x for local coordinates (y, z, x).
+__device__ __forceinline__ void chunk_range(const TilePlan& pl, const ChunkCursor& k, const WarpUnion& u, int& glo,
+                                            int& n) {
+    int lo[3], hi[3];
+    bool empty = false;
 #pragma unroll
-    for (int s = 0; s < kSeg; ++s) m.act |= ((useg >> s) & 1u) ? (ublk << (s * NB)) : 0u;
-    m.rowseg = live ? segment_bits(pl, k.y0, k.z0, g.lo[0], g.lo[0] + g.len[0], g.lo[1], g.lo[1] + g.len[1]) : 0u;
-    m.m8 = 0;
-#pragma unroll
-    for (int bb = 0; bb < NB; ++bb)
-        m.m8 |= range_bits8(g.lo[2] - k.x0 - 8 * bb, g.lo[2] + g.len[2] - k.x0 - 8 * bb) << (8 * bb);
-    return m;
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = max(u.lo[a] - k.o[a], 0);
+        hi[a] = min(u.hi[a] - k.o[a], pl.G[a]);
+        if (lo[a] >= hi[a]) empty = true;
+    }
+    if (empty) {
+        glo = 0;
+        n = 0;
+        return;
+    }
+    const int clo = (lo[0] * pl.G[1] + lo[1]) * pl.G[2] + lo[2];
+    const int chi = ((hi[0] - 1) * pl.G[1] + hi[1] - 1) * pl.G[2] + hi[2];
+    glo = clo >> 4;
+    n = ((chi + 15) >> 4) - glo;
 }
 
-// Live-column byte of block i (runtime) of the chunk for this row.
-template <int NB>
-__device__ __forceinline__ uint32_t block_live(const ChunkMasks& m, int i) {
-    const int seg = i / NB, bb = i - seg * NB;
-    return ((m.rowseg >> seg) & 1u) ? (m.m8 >> (8 * bb)) & 0xffu : 0u;
+// bf16 pair for bits (2w, 2w+1) of `bits`: `v` where the bit is set, 0 elsewhere.
+__device__ __forceinline__ uint32_t bf16_pair(uint32_t bits, int w, uint32_t v) {
+    const uint32_t two = (bits >> (2 * w)) & 3u;
+    return ((two & 1u) | ((two & 2u) << 15)) * v;
+}
+
+// Row r of a K-major 16-column bf16 block with 32-byte swizzle (32-byte rows, base 256-byte
+// aligned): element t = `v` where bit t of `bits` is set, 0 elsewhere.
+__device__ __forceinline__ void st_row32(uint32_t blk, int r, uint32_t bits, uint32_t v) {
+    const uint32_t row = blk + static_cast<uint32_t>(r) * 32u;
+    const uint32_t sw = (static_cast<uint32_t>(r) >> 2) & 1u;
+    st_shared_v4(row + (sw << 4), bf16_pair(bits, 0, v), bf16_pair(bits, 1, v), bf16_pair(bits, 2, v),
+                 bf16_pair(bits, 3, v));
+    st_shared_v4(row + ((sw ^ 1u) << 4), bf16_pair(bits, 4, v), bf16_pair(bits, 5, v), bf16_pair(bits, 6, v),
+                 bf16_pair(bits, 7, v));
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
@@ -382,34 +421,158 @@ __device__ __forceinline__ uint32_t bf16x2_of(uint64_t r) {
     return pack_bf16x2(a, b);
 }
 
-// Scores of one block with the masked columns replaced by -inf.
-__device__ __forceinline__ void mask_block(uint32_t (&v)[8], uint32_t live) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-        if (!(live & (1u << e))) v[e] = 0xff800000u;  // -inf
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 32 lanes x 16 consecutive columns of 32 bits (one row per lane), and the register fence that
+// keeps uses of them below the tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // ---------------------------------------------------------------------------------------------
-// Producer warp: TMA of tile tensors and halo chunks; for dK/dV also the per-column LSE / Delta.
+// Window-bias operands (built by the producer warp)
 // ---------------------------------------------------------------------------------------------
 
-template <int D>
-__device__ void producer_loop(const TcParams& p, int which, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
+// Constant operand B: per chunk column its local coordinate along each masked axis, one-hot.
+__device__ void build_bias_b(const TilePlan& pl, const BiasGeom& bg, uint32_t bbias, uint32_t bgroup, int lane) {
+    for (int key = lane; key < pl.NC; key += 32) {
+        const int loc[3] = {key / (pl.G[2] * pl.G[1]), (key / pl.G[2]) % pl.G[1], key % pl.G[2]};
+        for (int a = 0; a < 3; ++a)
+            for (int q = 0; q < bg.nbg[a]; ++q) {
+                const int t = loc[a] - 16 * q;
+                const uint32_t bits = (t >= 0 && t < 16) ? (1u << t) : 0u;
+                st_row32(bbias + static_cast<uint32_t>(bg.bbase[a] + q) * bgroup, key, bits, kBf16One);
+            }
+    }
+}
+
+// Per-tile operand A along the axes in `axes`: for each row, chunk index and group, -2^100 at the
+// coordinates outside the row's range along that axis.
+__device__ void build_bias_a(const TcParams& p, int which, const Cta& c, const BiasGeom& bg, uint32_t abias,
+                             int lane, uint32_t axes) {
+    const TilePlan& pl = p.plan;
+    for (int q = 0; q < 4; ++q) {
+        const int r = lane + 32 * q;
+        const RowGeom rg = row_geom(p, which, c, r);
+        for (int a = 0; a < 3; ++a) {
+            if (!((axes >> a) & 1u)) continue;
+            for (int ch = 0; ch < pl.nchk[a]; ++ch)
+                for (int qq = 0; qq < bg.nbg[a]; ++qq) {
+                    const int o = ch * pl.G[a] + 16 * qq;
+                    const uint32_t nv = ~range_bits32(rg.lo[a] - o, rg.lo[a] + rg.len[a] - o);
+                    const uint32_t grp = static_cast<uint32_t>(bg.abase[a] + ch * bg.nbg[a] + qq);
+                    st_row32(abias + grp * 4096u, r, nv, kBf16Neg);
+                }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Producer warp: TMA of tile tensors and halo chunks; the window-bias operands; for dK/dV also the
+// per-column LSE / Delta of each chunk.
+// ---------------------------------------------------------------------------------------------
+
+// dK/dV: -LSE (log2 units) and Delta of the chunk columns lane + 32 i (-inf / 0 outside the class).
+struct AuxFetch {
+    int loc[4][3];
+    float l[4], dl[4];
+};
+
+__device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const ChunkCursor& k, AuxFetch& f,
+                                          int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int col = lane + 32 * i;
+        float lv = -INFINITY, dv = 0.f;
+        if (col < p.plan.NC) {
+            const int j0 = c.h0[0] + k.o[0] + f.loc[i][0], j1 = c.h0[1] + k.o[1] + f.loc[i][1],
+                      j2 = c.h0[2] + k.o[2] + f.loc[i][2];
+            if (j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) {
+                const long long tok =
+                    ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * j0)) * p.L[1] +
+                     (c.cls[1] + p.d[1] * j1)) * p.L[2] + (c.cls[2] + p.d[2] * j2);
+                lv = -__ldg(p.lse + tok * p.heads + c.h) * kLog2e;
+                dv = __ldg(p.delta + tok * p.heads + c.h);
+            }
+        }
+        f.l[i] = lv;
+        f.dl[i] = dv;
+    }
+}
+
+template <int D, int WHICH>
+__device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
+    constexpr int kS = stages_of(D);
+    constexpr int ntile = WHICH == 0 ? 1 : 2;
+    constexpr int tmCk = WHICH == 0 ? 1 : 2, tmCv = WHICH == 0 ? 2 : 3;
     const int lane = threadIdx.x & 31;
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
+    const BiasGeom bg = bias_geom(pl);
     const uint32_t tile_bytes = 128u * D * 2u, chunk_bytes = static_cast<uint32_t>(pl.NC) * D * 2u;
-    const int ntile = which == 0 ? 1 : 2;
-    const int tmCk = which == 0 ? 1 : 2, tmCv = which == 0 ? 2 : 3;
+    const uint32_t abias = smem_u32(smem + lay.abias);
+
+    build_bias_b(pl, bg, smem_u32(smem + lay.bbias), lay.bgroup, lane);
+    fence_proxy_async_smem();
+    uint32_t built = 0;  // axes whose part of A holds the geometry of sig[]
+    uint64_t sig[3] = {0, 0, 0};
+    AuxFetch f;
+    if (WHICH == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = lane + 32 * i;
+            f.loc[i][0] = col / (pl.G[2] * pl.G[1]);
+            f.loc[i][1] = (col / pl.G[2]) % pl.G[1];
+            f.loc[i][2] = col % pl.G[2];
+        }
+    }
+
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && next_tile(p, which, it, started, c)) {
+    while (ok && next_tile(p, WHICH, it, started, c)) {
         const uint32_t qs = j & 1;
         if (j >= 2) ok = warp_wait(&bars[kQEmpty + qs], ((j >> 1) - 1) & 1, err, kSiteQ);
         if (!ok) break;
+        // the bias operand A: rebuilt along the axes whose border situation changed, once every
+        // score product of the previous tile (its last reader) is done
+        uint32_t stale = 0;
+        uint64_t ns[3];
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            ns[a] = axis_sig(WHICH, c.t0[a], pl.T[a], c.Lc[a], p.k[a], pl.H[a]);
+            if (bg.nbg[a] > 0 && (!((built >> a) & 1u) || ns[a] != sig[a])) stale |= 1u << a;
+        }
+        if (stale) {
+            if (j >= 1) ok = warp_wait(&bars[kQEmpty + (qs ^ 1u)], ((j - 1) >> 1) & 1, err, kSiteQ);
+            if (!ok) break;
+            build_bias_a(p, WHICH, c, bg, abias, lane, stale);
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int a = 0; a < 3; ++a) sig[a] = ns[a];
+            built |= stale;
+        }
+        __syncwarp();
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars[kQFull + qs], ntile * tile_bytes);
             for (int tt = 0; tt < ntile; ++tt)
@@ -417,12 +580,13 @@ __device__ void producer_loop(const TcParams& p, int which, uint8_t* smem, const
                             c.cls[2] + p.d[2] * c.t0[2], c.cls[1] + p.d[1] * c.t0[1], c.cls[0] + p.d[0] * c.t0[0],
                             c.b);
         }
-        ChunkCursor cur{0, 0, 0};
-        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t s = g % kStages;
-            if (g >= kStages) ok = warp_wait(&bars[kKVEmpty + s], ((g / kStages) - 1) & 1, err, kSiteEmpty);
+        ChunkCursor cur = cursor_begin();
+        if (WHICH == 2) aux_fetch(p, c, cur, f, lane);
+        for (int ci = 0; ci < c.C; ++ci, ++g) {
+            const uint32_t s = g % kS;
+            if (g >= kS) ok = warp_wait(&bars[kKVEmpty + s], ((g / kS) - 1) & 1, err, kSiteEmpty);
             if (!ok) break;
-            const int y0 = c.h0[0] + cur.y0, z0 = c.h0[1] + cur.z0, x0 = c.h0[2] + cur.x0;
+            const int y0 = c.h0[0] + cur.o[0], z0 = c.h0[1] + cur.o[1], x0 = c.h0[2] + cur.o[2];
             if (lane == 0) {
                 mbar_arrive_expect_tx(&bars[kKVFull + s], 2u * chunk_bytes);
                 tma_load_5d(smem + lay.chunk(s, 0), &p.tm[tmCk], &bars[kKVFull + s], c.h * D,
@@ -430,27 +594,22 @@ __device__ void producer_loop(const TcParams& p, int which, uint8_t* smem, const
                 tma_load_5d(smem + lay.chunk(s, 1), &p.tm[tmCv], &bars[kKVFull + s], c.h * D,
                             c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
             }
-            if (which == 2) {
-                // LSE (log2 units) and Delta of the chunk's queries; +inf LSE outside the class
+            if (WHICH == 2) {
                 float* l2 = reinterpret_cast<float*>(smem + lay.aux(s));
                 float* dl = l2 + pl.NC;
-                for (int col = lane; col < pl.NC; col += 32) {
-                    const int x2 = col % pl.G[2], x1 = (col / pl.G[2]) % pl.G[1], xx0 = col / (pl.G[2] * pl.G[1]);
-                    const int j0 = y0 + xx0, j1 = z0 + x1, j2 = x0 + x2;
-                    float lv = INFINITY, dv = 0.f;
-                    if (j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) {
-                        const long long tok =
-                            ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * j0)) * p.L[1] +
-                             (c.cls[1] + p.d[1] * j1)) * p.L[2] + (c.cls[2] + p.d[2] * j2);
-                        lv = __ldg(p.lse + tok * p.heads + c.h) * kLog2e;
-                        dv = __ldg(p.delta + tok * p.heads + c.h);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int col = lane + 32 * i;
+                    if (col < pl.NC) {
+                        l2[col] = f.l[i];
+                        dl[col] = f.dl[i];
                     }
-                    l2[col] = lv;
-                    dl[col] = dv;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kKVFull + s]);
             }
+            cursor_next(pl, c, cur);
+            if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, cur, f, lane);  // the next chunk's, in flight
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKVFull + s]);
         }
         ++j;
     }
@@ -464,6 +623,8 @@ template <int D>
 struct MmaIssuer {
     const TcParams& p;
     uint8_t* smem;
+    const TcLayout& lay;
+    BiasGeom bg;
 
     // D_tmem = A_tile(128 x D) * B_chunk(NC x D)^T, both K-major; A negated when `neg`.
     __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
@@ -474,6 +635,18 @@ struct MmaIssuer {
         for (int kk = 0; kk < D / 16; ++kk)
             umma_bf16(d_tmem, sdesc(a + kk * 32u, 16u, sbo, lay_), sdesc(b + kk * 32u, 16u, sbo, lay_), idesc,
                       kk > 0);
+    }
+    // D_tmem += A_bias(chunk) * B_bias^T along every masked axis: the window mask.
+    __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
+        const uint32_t idesc = idesc_bf16(128, p.plan.NC, false, false);
+        const uint32_t a = smem_u32(smem + lay.abias), b = smem_u32(smem + lay.bbias);
+        for (int ax = 0; ax < 3; ++ax)
+            for (int q = 0; q < bg.nbg[ax]; ++q) {
+                const uint32_t ga = static_cast<uint32_t>(bg.abase[ax] + k.ix[ax] * bg.nbg[ax] + q);
+                const uint32_t gb = static_cast<uint32_t>(bg.bbase[ax] + q);
+                umma_bf16(d_tmem, sdesc(a + ga * 4096u, 16u, 256u, 6u), sdesc(b + gb * lay.bgroup, 16u, 256u, 6u),
+                          idesc, 1u);
+            }
     }
     // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major.
     __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
@@ -504,12 +677,12 @@ struct PendingUpdate {
     bool valid;
 };
 
-template <int D>
-__device__ void mma_loop(const TcParams& p, int which, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
-                         uint32_t tmem) {
+template <int D, int WHICH>
+__device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr int kS = stages_of(D);
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
-    MmaIssuer<D> mi{p, smem};
+    const MmaIssuer<D> mi{p, smem, lay, bias_geom(pl)};
     const bool neg = p.neg != 0;
     TileIter it = tile_iter_begin(p);
     bool started = false;
@@ -523,10 +696,10 @@ __device__ void mma_loop(const TcParams& p, int which, uint8_t* smem, const TcLa
         if (pd.ci == 0 && pd.j >= 2 && !mbar_wait(&bars[kOEmpty + ob], ((pd.j >> 1) - 1) & 1, err, kSitePV))
             return false;
         tc_fence_after();
-        const uint32_t acc = tmem + tm_acc<D>(which, ob);
-        if (which == 0) {
+        const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
+        if (WHICH == 0) {
             mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 1), pd.ci > 0);  // O += P V
-        } else if (which == 1) {
+        } else if (WHICH == 1) {
             mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 0), pd.ci > 0);  // dQ += dS K
         } else {
             mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 1), pd.ci > 0);      // dV += P^T dO
@@ -537,17 +710,19 @@ __device__ void mma_loop(const TcParams& p, int which, uint8_t* smem, const TcLa
         if (pd.ci == pd.C - 1) umma_commit(&bars[kOFull + ob]);
         return true;
     };
-    while (ok && next_tile(p, which, it, started, c)) {
+    while (ok && next_tile(p, WHICH, it, started, c)) {
         const uint32_t qs = j & 1;
         if (!mbar_wait(&bars[kQFull + qs], (j >> 1) & 1, err, kSiteQ)) break;
-        for (int ci = 0; ci < c.C && ok; ++ci, ++g) {
-            const uint32_t s = g % kStages, sb = g & 1;
-            ok = mbar_wait(&bars[kKVFull + s], (g / kStages) & 1, err, kSiteKV);
+        ChunkCursor cur = cursor_begin();
+        for (int ci = 0; ci < c.C && ok; ++ci, ++g, cursor_next(pl, c, cur)) {
+            const uint32_t s = g % kS, sb = g & 1;
+            ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
             if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
             if (!ok) break;
             tc_fence_after();
             mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
-            if (which != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
+            mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
+            if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
             umma_commit(&bars[kSFull + sb]);
             if (ci == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
             if (pend.valid) ok = update(pend);
@@ -562,55 +737,150 @@ __device__ void mma_loop(const TcParams& p, int which, uint8_t* smem, const TcLa
 // Epilogue helpers
 // ---------------------------------------------------------------------------------------------
 
-// Stage columns [c0, c1) of this thread's accumulator row (fp32 at taddr) as bf16 in the tile
-// layout of the tensor map (row-major [128][D], swizzle = row width).
+// Store columns [c0, c1) of this thread's accumulator row (fp32 at taddr), times `mul`, as bf16
+// to dst (the row's first element in global memory).
 template <int D>
-__device__ __forceinline__ void stage_cols(uint32_t taddr, float mul, uint8_t* stage, int row, int c0, int c1) {
-    const uint32_t base = smem_u32(stage), mask = swizzle_mask(D * 2);
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid, int c0, int c1) {
 #pragma unroll
     for (int cc = 0; cc < D; cc += 8) {
         if (cc < c0 || cc >= c1) continue;
         uint32_t r[8];
         tmem_ld8(taddr + cc, r);
         tmem_ld_wait(r);
-        const uint32_t w0 = pack_bf16x2(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul);
-        const uint32_t w1 = pack_bf16x2(__uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
-        const uint32_t w2 = pack_bf16x2(__uint_as_float(r[4]) * mul, __uint_as_float(r[5]) * mul);
-        const uint32_t w3 = pack_bf16x2(__uint_as_float(r[6]) * mul, __uint_as_float(r[7]) * mul);
-        st_shared_v4(base + swz(static_cast<uint32_t>(row) * (D * 2) + cc * 2, mask), w0, w1, w2, w3);
+        if (valid) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul);
+            w.y = pack_bf16x2(__uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
+            w.z = pack_bf16x2(__uint_as_float(r[4]) * mul, __uint_as_float(r[5]) * mul);
+            w.w = pack_bf16x2(__uint_as_float(r[6]) * mul, __uint_as_float(r[7]) * mul);
+            *reinterpret_cast<uint4*>(dst + cc) = w;
+        }
     }
 }
 
-__device__ __forceinline__ void tile_store(const TcParams& p, const Cta& c, int m, uint8_t* stage, int D) {
-    tma_store_5d(&p.tm[m], stage, c.h * D, c.cls[2] + p.d[2] * c.t0[2], c.cls[1] + p.d[1] * c.t0[1],
-                 c.cls[0] + p.d[0] * c.t0[0], c.b);
+// Zero 16-column group gi of this row in a P operand.
+__device__ __forceinline__ void zero_group(uint32_t sP, uint32_t rowbase, uint32_t sw, int gi) {
+    st_shared_v4(sP + p_off(rowbase, sw, 2 * gi), 0u, 0u, 0u, 0u);
+    st_shared_v4(sP + p_off(rowbase, sw, 2 * gi + 1), 0u, 0u, 0u, 0u);
 }
 
 // ---------------------------------------------------------------------------------------------
 // Forward softmax warps (4 warps, 128 rows)
 // ---------------------------------------------------------------------------------------------
 
-// Zero the P groups of the blocks in `mask` (blocks of the chunk no row of this warp needs).
-__device__ __forceinline__ void zero_blocks(uint32_t sP, uint32_t rowbase, uint32_t sw, uint32_t mask) {
-    while (mask) {
-        const int i = __ffs(mask) - 1;
-        mask &= mask - 1;
-        st_shared_v4(sP + p_off(rowbase, sw, i), 0u, 0u, 0u, 0u);
+struct FwdCtx {
+    uint64_t* bars;
+    unsigned* err;
+    uint32_t tS0, tS_step;  // this warp's lanes of score buffer 0, and the offset of buffer 1
+    uint32_t tO;            // this warp's lanes of the tile accumulator
+    uint32_t sP0, sP_step;  // P operand 0, and the offset of operand 1
+    uint32_t rowbase, sw;
+    int ngroups;       // 16-column groups per chunk
+    float sl2;
+    uint64_t sl2x2;
+    int lane;
+};
+
+// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + N).
+template <int D, int N>
+__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4]) {
+    const uint32_t sb = g & 1;
+    uint32_t v[N > 0 ? N : 1][16];
+    const uint32_t tS = x.tS0 + sb * x.tS_step;
+#pragma unroll
+    for (int i = 0; i < N; ++i) tmem_ld16(tS + 16u * (glo + i), v[i]);
+    if (N > 0) {
+        tmem_ld_wait_all();
+#pragma unroll
+        for (int i = 0; i < N; ++i) reg_fence16(v[i]);
     }
+    // the score buffer is free for the product of chunk g + 2
+    tc_fence_before();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kSEmpty + sb]);
+    // chunk row max (masked scores carry the -2^100 window bias), four independent chains
+    float cmax = -INFINITY;
+    if (N > 0) {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                mx[e] = fmax3(mx[e], fmaxf(__uint_as_float(v[i][4 * e]), __uint_as_float(v[i][4 * e + 1])),
+                              fmaxf(__uint_as_float(v[i][4 * e + 2]), __uint_as_float(v[i][4 * e + 3])));
+        cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    }
+    // running max (log2 units; the scale's sign is folded into the S product)
+    const float cm2 = cmax > kMaskedBelow ? cmax * x.sl2 : -INFINITY;  // no live key: -inf
+    const float mnew = fmaxf(m, cm2);
+    const bool rescale = (m != -INFINITY) && (mnew > m + kRescaleThreshold);
+    const float alpha = rescale ? fast_exp2(m - mnew) : 1.f;
+    if (m == -INFINITY || rescale) m = mnew;
+    if (__any_sync(0xffffffffu, rescale)) {
+        // O holds the products of chunks g-1, g-2, ...: wait for the last one
+        if (!warp_wait(&x.bars[kPEmpty + ((g - 1) & 1)], ((g - 1) >> 1) & 1, x.err, kSitePV)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 8) {
+            uint32_t r[8];
+            tmem_ld8(x.tO + cc, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st8(x.tO + cc, r);
+        }
+        tmem_st_wait();
+        const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) lsum[t] = f2_mul(lsum[t], a2);
+    }
+    // P buffer sb is free once the product of chunk g-2 is done
+    if (g >= 2 && !warp_wait(&x.bars[kPEmpty + sb], ((g >> 1) - 1) & 1, x.err, kSitePV)) return false;
+    const uint32_t sP = x.sP0 + sb * x.sP_step;
+    const float nm = m == -INFINITY ? 0.f : -m;  // masked scores are -inf: exp2 gives 0
+    const uint64_t nm2 = f2(nm, nm);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            const uint64_t t = f2_fma(f2(__uint_as_float(v[i][e]), __uint_as_float(v[i][e + 1])), x.sl2x2, nm2);
+            float ta, tb;
+            f2_split(t, ta, tb);
+            const uint64_t pe = f2(fast_exp2(ta), fast_exp2(tb));
+            lsum[(e >> 1) & 3] = f2_add(lsum[(e >> 1) & 3], pe);
+            w[e >> 1] = bf16x2_of(pe);
+        }
+        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i)), w[0], w[1], w[2], w[3]);
+        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i) + 1), w[4], w[5], w[6], w[7]);
+    }
+    for (int gi = 0; gi < x.ngroups; ++gi)
+        if (gi < glo || gi >= glo + N) zero_group(sP, x.rowbase, x.sw, gi);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + sb]);
+    return true;
 }
 
-template <int D, int NB>
+template <int D>
 __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
                                  uint32_t tmem) {
-    constexpr int kMB = fwd_max_blocks(D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, row = warp * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    unsigned* err = p.err;
     const TilePlan& pl = p.plan;
-    const uint32_t all_blocks = (1u << (pl.NC >> 3)) - 1u;
-    const float sl2 = p.scale_log2;
-    const uint64_t sl2x2 = f2(sl2, sl2);
-    const uint32_t rowbase = static_cast<uint32_t>(row) * 64u, sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    FwdCtx x;
+    x.bars = bars;
+    x.err = p.err;
+    x.tS0 = tmem + tm_s(pl, 0) + lane_base;
+    x.tS_step = tm_s(pl, 1) - tm_s(pl, 0);
+    x.sP0 = smem_u32(smem + lay.p(0, 0));
+    x.sP_step = lay.p(1, 0) - lay.p(0, 0);
+    x.rowbase = static_cast<uint32_t>(row) * 64u;
+    x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    x.ngroups = pl.NC >> 4;
+    x.sl2 = p.scale_log2;
+    x.sl2x2 = f2(x.sl2, x.sl2);
+    x.lane = lane;
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -618,165 +888,136 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     bool ok = true;
     while (ok && next_tile(p, 0, it, started, c)) {
         const RowGeom geo = row_geom(p, 0, c, row);
-        const WarpUnion u = warp_union(geo);
-        const bool live = geo.len[0] > 0 && geo.len[1] > 0 && geo.len[2] > 0;
+        const WarpUnion wu = warp_union(geo);
         const uint32_t ob = j & 1;
-        const uint32_t tO = tmem + tm_acc<D>(0, ob);
+        x.tO = tmem + tm_acc<D>(0, ob) + lane_base;
         float m = -INFINITY;
         uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (independent chains)
-        ChunkCursor cur{0, 0, 0};
+        ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t sb = g & 1;
-            const uint32_t tS = tmem + tm_s(pl, sb) + lane_base;
-            const ChunkMasks cm = chunk_masks<NB>(pl, cur, u, geo, live);
-            const uint32_t act = cm.act & all_blocks;
-            ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
+            ok = warp_wait(&bars[kSFull + (g & 1)], (g >> 1) & 1, x.err, kSiteS);
             if (!ok) break;
             tc_fence_after();
-            // the active blocks of the chunk, compacted into registers, one wait
-            uint32_t val[kMB][8];
-            int idx[kMB];
-            const int nact = __popc(act);
-            {
-                uint32_t rem = act;
-#pragma unroll
-                for (int q = 0; q < kMB; ++q) {
-                    idx[q] = rem ? __ffs(rem) - 1 : 0;
-                    if (rem) {
-                        tmem_ld8(tS + 8 * idx[q], val[q]);
-                        rem &= rem - 1;
-                    }
-                }
+            int glo, n;
+            chunk_range(pl, cur, wu, glo, n);
+            switch (n) {
+                case 0: ok = fwd_chunk<D, 0>(x, g, glo, m, lsum); break;
+                case 1: ok = fwd_chunk<D, 1>(x, g, glo, m, lsum); break;
+                case 2: ok = fwd_chunk<D, 2>(x, g, glo, m, lsum); break;
+                case 3: ok = fwd_chunk<D, 3>(x, g, glo, m, lsum); break;
+                case 4: ok = fwd_chunk<D, 4>(x, g, glo, m, lsum); break;
+                case 5: ok = fwd_chunk<D, 5>(x, g, glo, m, lsum); break;
+                default: ok = fwd_chunk<D, 6>(x, g, glo, m, lsum); break;
             }
-            tmem_ld_wait_all();
-            // mask, then the chunk row max with one accumulator per column position
-            float mx[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < kMB; ++q)
-                if (q < nact) {
-                    reg_fence8(val[q]);
-                    mask_block(val[q], block_live<NB>(cm, idx[q]));
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(val[q][e]));
-                }
-            const float cmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            // running max (log2 units; the scale's sign is folded into the S product)
-            const float cm2 = cmax * sl2;  // -inf when no live key
-            const float mnew = fmaxf(m, cm2);
-            const bool rescale = (m != -INFINITY) && (mnew > m + kRescaleThreshold);
-            const float alpha = rescale ? fast_exp2(m - mnew) : 1.f;
-            if (m == -INFINITY || rescale) m = mnew;
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O holds the products of chunks g-1, g-2, ...: wait for the last one
-                ok = warp_wait(&bars[kPEmpty + ((g - 1) & 1)], ((g - 1) >> 1) & 1, err, kSitePV);
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int cc = 0; cc < D; cc += 8) {
-                    uint32_t r[8];
-                    tmem_ld8(tO + lane_base + cc, r);
-                    tmem_ld_wait(r);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st8(tO + lane_base + cc, r);
-                }
-                tmem_st_wait();
-                const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) lsum[t] = f2_mul(lsum[t], a2);
-            }
-            // P buffer sb is free once the product of chunk g-2 is done
-            if (g >= 2) {
-                ok = warp_wait(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSitePV);
-                if (!ok) break;
-            }
-            const uint32_t sP = smem_u32(smem + lay.p(sb, 0));
-            const float nm = m == -INFINITY ? 0.f : -m;  // masked scores are -inf: exp2 gives 0
-            const uint64_t nm2 = f2(nm, nm);
-#pragma unroll
-            for (int q = 0; q < kMB; ++q)
-                if (q < nact) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const uint64_t x =
-                            f2_fma(f2(__uint_as_float(val[q][e]), __uint_as_float(val[q][e + 1])), sl2x2, nm2);
-                        float xa, xb;
-                        f2_split(x, xa, xb);
-                        const uint64_t pe = f2(fast_exp2(xa), fast_exp2(xb));
-                        lsum[e >> 1] = f2_add(lsum[e >> 1], pe);
-                        w[e >> 1] = bf16x2_of(pe);
-                    }
-                    st_shared_v4(sP + p_off(rowbase, sw, idx[q]), w[0], w[1], w[2], w[3]);
-                }
-            zero_blocks(sP, rowbase, sw, all_blocks & ~act);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[kSEmpty + sb]);
-                mbar_arrive(&bars[kPFull + sb]);
-            }
+            if (!ok) break;
         }
         if (!ok) break;
-        // epilogue: O / l -> bf16 -> TMA store; LSE = (m + log2 l) * ln 2
+        // epilogue: O / l -> bf16; LSE = (m + log2 l) * ln 2
         const uint64_t ls = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
         float la, lb;
         f2_split(ls, la, lb);
         const float l = la + lb;
-        ok = warp_wait(&bars[kOFull + ob], (j >> 1) & 1, err, kSitePV);
+        ok = warp_wait(&bars[kOFull + ob], (j >> 1) & 1, x.err, kSitePV);
         if (!ok) break;
         tc_fence_after();
-        // the staging buffer is free once the previous tile's store has read it
-        if (threadIdx.x == 0) {
-            tma_store_wait_read();
-            mbar_arrive(&bars[kStFree]);
-        }
-        ok = warp_wait(&bars[kStFree], j & 1, err, kSiteSt);
-        if (!ok) break;
-        stage_cols<D>(tO + lane_base, 1.f / l, smem + lay.stage(0), row, 0, D);
+        const long long orow = geo.token * p.heads + c.h;
+        store_row<D>(x.tO, 1.f / l, p.out0 + orow * D, geo.valid, 0, D);
         tc_fence_before();
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&bars[kOEmpty + ob]);
-            mbar_arrive(&bars[kStFull]);
-        }
-        if (geo.valid) p.lse_out[geo.token * p.heads + c.h] = (m + __log2f(l)) * kLn2;
-        if (threadIdx.x == 0) {
-            ok = mbar_wait(&bars[kStFull], j & 1, err, kSiteSt);
-            if (ok) {
-                tile_store(p, c, 3, smem + lay.stage(0), D);
-                tma_store_commit();
-            }
-        }
-        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) mbar_arrive(&bars[kOEmpty + ob]);
+        if (geo.valid) p.lse_out[orow] = (m + __log2f(l)) * kLn2;
         ++j;
     }
-    if (threadIdx.x == 0) tma_store_wait_all();
 }
 
 // ---------------------------------------------------------------------------------------------
-// Backward softmax warps (8 warps: two warpgroups split each chunk's active blocks)
+// Backward softmax warps (8 warps: two warpgroups share each chunk's groups, alternating)
 // ---------------------------------------------------------------------------------------------
 
-template <int D, int WHICH, int NB>
+struct BwdCtx {
+    uint32_t tS, tP;     // this warp's lanes of the current score / dP buffers
+    uint32_t sP0, sP1;   // P-side operands of the current buffer (dQ: dS; dK/dV: P^T, dS^T)
+    uint32_t rowbase, sw;
+    const float* l2;     // dK/dV: -LSE (log2 units) of the chunk columns
+    const float* dl;     // dK/dV: Delta of the chunk columns
+    uint64_t nl2, dl2;   // dQ: -LSE (log2 units) and Delta of this row, packed twice
+    uint64_t sl2x2;
+};
+
+// Groups g0 (and g0 + 2 when K == 2) of this warp's rows: P = exp2(S sl2 - LSE2), dS = P (dP - Delta).
+template <int WHICH, int K>
+__device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0) {
+    uint32_t rs[K][16], rp[K][16];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        tmem_ld16(x.tS + 16u * (g0 + 2 * i), rs[i]);
+        tmem_ld16(x.tP + 16u * (g0 + 2 * i), rp[i]);
+    }
+    tmem_ld_wait_all();
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        reg_fence16(rs[i]);
+        reg_fence16(rp[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const int gi = g0 + 2 * i;
+        uint32_t a[8], b[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            uint64_t nlc[2] = {x.nl2, x.nl2}, dlc[2] = {x.dl2, x.dl2};
+            if (WHICH == 2) {
+                const float4 lv = *reinterpret_cast<const float4*>(x.l2 + 16 * gi + e);
+                const float4 dv = *reinterpret_cast<const float4*>(x.dl + 16 * gi + e);
+                nlc[0] = f2(lv.x, lv.y);
+                nlc[1] = f2(lv.z, lv.w);
+                dlc[0] = f2(dv.x, dv.y);
+                dlc[1] = f2(dv.z, dv.w);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ee = e + 2 * h;
+                const uint64_t t =
+                    f2_fma(f2(__uint_as_float(rs[i][ee]), __uint_as_float(rs[i][ee + 1])), x.sl2x2, nlc[h]);
+                float ta, tb;
+                f2_split(t, ta, tb);
+                const uint64_t pe = f2(fast_exp2(ta), fast_exp2(tb));
+                const uint64_t dp = f2(__uint_as_float(rp[i][ee]), __uint_as_float(rp[i][ee + 1]));
+                const uint64_t ds = f2_mul(pe, f2_sub(dp, dlc[h]));
+                b[ee >> 1] = bf16x2_of(ds);
+                if (WHICH == 2) a[ee >> 1] = bf16x2_of(pe);
+            }
+        }
+        const uint32_t o0 = p_off(x.rowbase, x.sw, 2 * gi), o1 = p_off(x.rowbase, x.sw, 2 * gi + 1);
+        if (WHICH == 2) {
+            st_shared_v4(x.sP0 + o0, a[0], a[1], a[2], a[3]);  // P^T
+            st_shared_v4(x.sP0 + o1, a[4], a[5], a[6], a[7]);
+            st_shared_v4(x.sP1 + o0, b[0], b[1], b[2], b[3]);  // dS^T
+            st_shared_v4(x.sP1 + o1, b[4], b[5], b[6], b[7]);
+        } else {
+            st_shared_v4(x.sP0 + o0, b[0], b[1], b[2], b[3]);  // dS
+            st_shared_v4(x.sP0 + o1, b[4], b[5], b[6], b[7]);
+        }
+    }
+}
+
+template <int D, int WHICH>
 __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
                                  uint32_t tmem) {
-    constexpr int kMB = 4;  // blocks per warpgroup held in registers at once (more passes if it has more)
+    constexpr int kS = stages_of(D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
-    const uint32_t all_blocks = (1u << (pl.NC >> 3)) - 1u;
-    const float sl2 = p.scale_log2;
-    const uint64_t sl2x2 = f2(sl2, sl2);
-    const uint32_t rowbase = static_cast<uint32_t>(row) * 64u, sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    const int ngroups = pl.NC >> 4;
+    BwdCtx x;
+    x.rowbase = static_cast<uint32_t>(row) * 64u;
+    x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    x.sl2x2 = f2(p.scale_log2, p.scale_log2);
+    x.l2 = nullptr;
+    x.dl = nullptr;
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -784,143 +1025,70 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     bool ok = true;
     while (ok && next_tile(p, WHICH, it, started, c)) {
         const RowGeom geo = row_geom(p, WHICH, c, row);
-        const WarpUnion u = warp_union(geo);
-        const bool live = geo.len[0] > 0 && geo.len[1] > 0 && geo.len[2] > 0;
+        const WarpUnion wu = warp_union(geo);
         const uint32_t ob = j & 1;
         float lse2 = 0.f, dlt = 0.f;
         if (WHICH == 1 && geo.valid) {
             lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
             dlt = __ldg(p.delta + geo.token * p.heads + c.h);
         }
-        const uint64_t nl2 = f2(-lse2, -lse2), dl2 = f2(dlt, dlt);
-        ChunkCursor cur{0, 0, 0};
+        x.nl2 = f2(-lse2, -lse2);
+        x.dl2 = f2(dlt, dlt);
+        ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t sb = g & 1, s = g % kStages;
-            const uint32_t tS = tmem + tm_s(pl, sb) + lane_base, tP = tmem + tm_dp(pl, sb) + lane_base;
-            const ChunkMasks cm = chunk_masks<NB>(pl, cur, u, geo, live);
-            // active blocks alternate between the two warpgroups; each zeroes its share of the rest
-            uint32_t act = cm.act & all_blocks, mine = 0, rest = 0;
-            {
-                uint32_t r = act;
-                int k = 0;
-                while (r) {
-                    const uint32_t bit = r & (0u - r);
-                    if ((k & 1) == wg) mine |= bit;
-                    r ^= bit;
-                    ++k;
-                }
-                const uint32_t idle = all_blocks & ~act;
-                rest = idle & (wg == 0 ? 0x55555555u : 0xaaaaaaaau);
-            }
+            const uint32_t sb = g & 1, s = g % kS;
             ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
+            if (ok && WHICH == 2) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
             if (ok && g >= 2) ok = warp_wait(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSitePV);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t sP0 = smem_u32(smem + lay.p(sb, 0)), sP1 = smem_u32(smem + lay.p(sb, 1));
-            const float* l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
-            const float* dl = l2 + pl.NC;
-            while (mine) {
-                uint32_t rs[kMB][8], rp[kMB][8];
-                int idx[kMB];
-                const int n = min(__popc(mine), kMB);
-#pragma unroll
-                for (int q = 0; q < kMB; ++q) {
-                    idx[q] = mine ? __ffs(mine) - 1 : 0;
-                    if (q < n) {
-                        tmem_ld8(tS + 8 * idx[q], rs[q]);
-                        tmem_ld8(tP + 8 * idx[q], rp[q]);
-                        mine &= mine - 1;
-                    }
-                }
-                tmem_ld_wait_all();
-#pragma unroll
-                for (int q = 0; q < kMB; ++q)
-                    if (q < n) {
-                        const int i = idx[q];
-                        reg_fence8(rs[q]);
-                        reg_fence8(rp[q]);
-                        mask_block(rs[q], block_live<NB>(cm, i));
-                        uint32_t a[4], b[4];
-#pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            uint64_t nlc = nl2, dlc = dl2;
-                            if (WHICH == 2) {
-                                const float2 lv = *reinterpret_cast<const float2*>(l2 + 8 * i + e);
-                                const float2 dv = *reinterpret_cast<const float2*>(dl + 8 * i + e);
-                                nlc = f2(-lv.x, -lv.y);
-                                dlc = f2(dv.x, dv.y);
-                            }
-                            const uint64_t x =
-                                f2_fma(f2(__uint_as_float(rs[q][e]), __uint_as_float(rs[q][e + 1])), sl2x2, nlc);
-                            float xa, xb;
-                            f2_split(x, xa, xb);
-                            const uint64_t pe = f2(fast_exp2(xa), fast_exp2(xb));
-                            const uint64_t dp = f2(__uint_as_float(rp[q][e]), __uint_as_float(rp[q][e + 1]));
-                            const uint64_t ds = f2_mul(pe, f2_sub(dp, dlc));
-                            b[e >> 1] = bf16x2_of(ds);
-                            if (WHICH == 2) a[e >> 1] = bf16x2_of(pe);
-                        }
-                        const uint32_t off = p_off(rowbase, sw, i);
-                        if (WHICH == 2) {
-                            st_shared_v4(sP0 + off, a[0], a[1], a[2], a[3]);  // P^T
-                            st_shared_v4(sP1 + off, b[0], b[1], b[2], b[3]);  // dS^T
-                        } else {
-                            st_shared_v4(sP0 + off, b[0], b[1], b[2], b[3]);  // dS
-                        }
-                    }
+            x.tS = tmem + tm_s(pl, sb) + lane_base;
+            x.tP = tmem + tm_dp(pl, sb) + lane_base;
+            x.sP0 = smem_u32(smem + lay.p(sb, 0));
+            x.sP1 = smem_u32(smem + lay.p(sb, 1));
+            if (WHICH == 2) {
+                x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
+                x.dl = x.l2 + pl.NC;
             }
-            zero_blocks(sP0, rowbase, sw, rest);
-            if (WHICH == 2) zero_blocks(sP1, rowbase, sw, rest);
-            fence_proxy_async_smem();
+            int glo, n;
+            chunk_range(pl, cur, wu, glo, n);
+            // this warpgroup's groups: glo + wg, glo + wg + 2, ...
+            const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
+            int k = 0;
+            for (; k + 2 <= mine; k += 2) bwd_groups<WHICH, 2>(x, glo + wg + 2 * k);
+            if (k < mine) bwd_groups<WHICH, 1>(x, glo + wg + 2 * k);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[kSEmpty + sb]);
-                mbar_arrive(&bars[kPFull + sb]);
-            }
+            if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
+            // groups outside the run are zero; the warpgroups split them by parity
+            for (int gi = wg; gi < ngroups; gi += 2)
+                if (gi < glo || gi >= glo + n) {
+                    zero_group(x.sP0, x.rowbase, x.sw, gi);
+                    if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, gi);
+                }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kPFull + sb]);
         }
         if (!ok) break;
-        // epilogue: each warpgroup stages half of the D columns of its quarter's rows
+        // epilogue: each warpgroup writes half of the D columns of its quarter's rows
         ok = warp_wait(&bars[kOFull + ob], (j >> 1) & 1, err, kSitePV);
         if (!ok) break;
         tc_fence_after();
-        if (threadIdx.x == 0) {
-            tma_store_wait_read();
-            mbar_arrive(&bars[kStFree]);
-        }
-        ok = warp_wait(&bars[kStFree], j & 1, err, kSiteSt);
-        if (!ok) break;
         const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + lane_base;
+        const long long orow = geo.token * p.heads + c.h;
         const int c0 = wg * (D / 2), c1 = c0 + D / 2;
         if (WHICH == 1) {
-            stage_cols<D>(acc, p.scale, smem + lay.stage(0), row, c0, c1);  // dQ
+            store_row<D>(acc, p.scale, p.out0 + orow * D, geo.valid, c0, c1);  // dQ
         } else {
-            stage_cols<D>(acc, 1.f, smem + lay.stage(1), row, c0, c1);          // dV
-            stage_cols<D>(acc + D, p.scale, smem + lay.stage(0), row, c0, c1);  // dK
+            store_row<D>(acc, 1.f, p.out1 + orow * D, geo.valid, c0, c1);          // dV
+            store_row<D>(acc + D, p.scale, p.out0 + orow * D, geo.valid, c0, c1);  // dK
         }
         tc_fence_before();
-        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&bars[kOEmpty + ob]);
-            mbar_arrive(&bars[kStFull]);
-        }
-        if (threadIdx.x == 0) {
-            ok = mbar_wait(&bars[kStFull], j & 1, err, kSiteSt);
-            if (ok) {
-                if (WHICH == 1) {
-                    tile_store(p, c, 4, smem + lay.stage(0), D);
-                } else {
-                    tile_store(p, c, 4, smem + lay.stage(0), D);  // dK
-                    tile_store(p, c, 5, smem + lay.stage(1), D);  // dV
-                }
-                tma_store_commit();
-            }
-        }
-        ok = __all_sync(0xffffffffu, ok);
+        if (lane == 0) mbar_arrive(&bars[kOEmpty + ob]);
         ++j;
     }
-    if (threadIdx.x == 0) tma_store_wait_all();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -931,7 +1099,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
-template <int WHICH>
+template <int D, int WHICH>
 __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     constexpr uint32_t kSoft = 4 * nwg_of(WHICH);
     for (int i = 0; i < 2; ++i) {
@@ -944,17 +1112,15 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kOFull + i], 1);
         mbar_init(&bars[kOEmpty + i], kSoft);
     }
-    for (int s = 0; s < kStages; ++s) {
-        mbar_init(&bars[kKVFull + s], WHICH == 2 ? 2 : 1);
+    for (int s = 0; s < stages_of(D); ++s) {
+        mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
         mbar_init(&bars[kKVEmpty + s], 1);
     }
-    mbar_init(&bars[kStFree], 1);
-    mbar_init(&bars[kStFull], kSoft);
     mbar_init(&bars[kFin], 1);
     fence_barrier_init();
 }
 
-template <int D, int WHICH, int NB>
+template <int D, int WHICH>
 __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
@@ -968,8 +1134,8 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
 
     if (warp == kSoftWarps) {
         if (lane == 0) {
-            init_barriers<WHICH>(bars);
-            for (int m = 0; m < 6; ++m) tma_prefetch_desc(&p.tm[m]);
+            init_barriers<D, WHICH>(bars);
+            for (int m = 0; m < 4; ++m) tma_prefetch_desc(&p.tm[m]);
         }
         __syncwarp();
     }
@@ -983,14 +1149,14 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     const uint32_t tmem = *tmem_slot;
 
     if (warp == kSoftWarps) {
-        producer_loop<D>(p, WHICH, smem, lay, bars);
+        producer_loop<D, WHICH>(p, smem, lay, bars);
     } else if (warp == kSoftWarps + 1) {
-        if (lane == 0) mma_loop<D>(p, WHICH, smem, lay, bars, tmem);
+        if (lane == 0) mma_loop<D, WHICH>(p, smem, lay, bars, tmem);
         __syncwarp();
     } else if (WHICH == 0) {
-        fwd_softmax_loop<D, NB>(p, smem, lay, bars, tmem);
+        fwd_softmax_loop<D>(p, smem, lay, bars, tmem);
     } else {
-        bwd_softmax_loop<D, WHICH, NB>(p, smem, lay, bars, tmem);
+        bwd_softmax_loop<D, WHICH>(p, smem, lay, bars, tmem);
     }
 
     // teardown: every MMA of this CTA done before TMEM is freed
@@ -1006,10 +1172,10 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     }
 }
 
-template <int D, int WHICH, int NB>
-int launch_tc_nb(const TcParams& p0, cudaStream_t stream) {
+template <int D, int WHICH>
+int launch_tc(const TcParams& p0, cudaStream_t stream) {
     const int smem = p0.plan.smem_bytes;
-    auto kernel = tc_kernel<D, WHICH, NB>;
+    auto kernel = tc_kernel<D, WHICH>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return static_cast<int>(e);
     if (p0.plan.ctas <= 0) return 0;
@@ -1030,17 +1196,6 @@ int launch_tc_nb(const TcParams& p0, cudaStream_t stream) {
     return static_cast<int>(cudaGetLastError());
 }
 
-template <int D, int WHICH>
-int launch_tc(const TcParams& p, cudaStream_t stream) {
-    switch (p.plan.NB) {
-        case 1: return launch_tc_nb<D, WHICH, 1>(p, stream);
-        case 2: return launch_tc_nb<D, WHICH, 2>(p, stream);
-        case 3: return launch_tc_nb<D, WHICH, 3>(p, stream);
-        case 4: return launch_tc_nb<D, WHICH, 4>(p, stream);
-        default: return static_cast<int>(cudaErrorInvalidValue);
-    }
-}
-
 }  // namespace
 
 uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D) { return tc_layout(which, pl, D).total + 1024u; }
@@ -1048,10 +1203,12 @@ uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D) { return tc_layout(
 int tc_tmem_cols(int which) { return which == 0 ? 256 : 512; }
 
 int tc_max_nc(int which, int D) {
-    // double-buffered score accumulators plus double-buffered tile accumulators
+    // double-buffered score accumulators plus double-buffered tile accumulators; the forward keeps
+    // at most 6 groups (96 columns) of scores in registers
     const int cols = tc_tmem_cols(which);
-    const int nc = which == 0 ? 8 * fwd_max_blocks(D) : (which == 1 ? (cols - 2 * D) / 4 : (cols - 4 * D) / 4);
-    return (nc < 8 * kMaxBlocks ? nc : 8 * kMaxBlocks) / 16 * 16;
+    const int nc = which == 0 ? (cols - 2 * D) / 2 : (which == 1 ? (cols - 2 * D) / 4 : (cols - 4 * D) / 4);
+    const int cap = which == 0 ? 96 : 128;
+    return (nc < cap ? nc : cap) / 16 * 16;
 }
 
 int launch_fwd_tc(const TcParams& p, cudaStream_t s) {

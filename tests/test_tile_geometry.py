@@ -1,11 +1,12 @@
 """CPU model of the tensor-core kernels' tile geometry (host logic; no GPU).
 
-The kernels decide, per CTA, which halo box to load, which chunks to process, which halo rows and
-8-column blocks each softmax warp visits (the union of its 32 rows' windows), and an 8-bit mask of
-live keys per block.  This test replays those decisions with the real tile plans (na_plan_info) and
-checks, against the oracle's window function, that every (query, key) pair of the neighbourhood is
-visited exactly once and nothing else is, that every visited column lies inside the chunk, and
-that dK/dV's inverse windows are exactly the queries whose windows hold each key.
+The kernels decide, per CTA, which halo box to load and which chunks to process; the window-bias
+product decides which (row, column) scores of a chunk stay live (one-hot local coordinates against
+per-row window bits, per axis); and each softmax warp reads only the run of 16-column groups that
+holds its rows' windows.  This test replays those decisions with the real tile plans
+(na_plan_info) and checks, against the oracle's window function, that every (query, key) pair of
+the neighbourhood is live in exactly one chunk and read by its warp, and that nothing else is
+live; for dK/dV, that the inverse windows are exactly the queries whose windows hold each key.
 """
 import itertools
 
@@ -35,27 +36,30 @@ def inv_hi(j, Lc, k):
     return Lc - 1 if j >= Lc - k else j + k // 2
 
 
-def range_bits(lo, hi, width=32):
-    lo, hi = max(0, min(width, lo)), max(0, min(width, hi))
-    return ((1 << hi) - 1) & ~((1 << lo) - 1) if hi > lo else 0
-
-
-def segment_bits(G0, G1, y0, z0, ylo, yhi, zlo, zhi):
-    zb = range_bits(zlo - z0, zhi - z0) & range_bits(0, G1)
-    bits = 0
-    for y in range(max(ylo, y0), min(yhi, y0 + G0)):
-        bits |= zb << ((y - y0) * G1)
-    return bits
+def group_run(G, o, ulo, uhi):
+    """The kernels' chunk_range: 16-column groups [glo, glo + n) covering a warp union."""
+    lo = [max(ulo[a] - o[a], 0) for a in range(3)]
+    hi = [min(uhi[a] - o[a], G[a]) for a in range(3)]
+    if any(lo[a] >= hi[a] for a in range(3)):
+        return 0, 0
+    clo = (lo[0] * G[1] + lo[1]) * G[2] + lo[2]
+    chi = ((hi[0] - 1) * G[1] + hi[1] - 1) * G[2] + hi[2]
+    glo = clo >> 4
+    return glo, ((chi + 15) >> 4) - glo
 
 
 def replay(which, L, k, d, plan):
-    """Yield (row_global_coords, key_or_query_global_coords) pairs the kernel marks live."""
+    """Yield (row_global_coords, key_or_query_global_coords) pairs the kernel keeps live."""
     T = (plan["T1"], plan["T2"], plan["T3"])
     H = (plan["H1"], plan["H2"], plan["H3"])
     G = (plan["G1"], plan["G2"], plan["G3"])
     NC = plan["NC"]
-    NB = G[2] // 8
-    assert G[2] % 8 == 0 and 1 <= NB <= 4
+    assert NC == G[0] * G[1] * G[2] and NC % 16 == 0
+    for a in range(3):
+        if H[a] > 1:
+            assert G[a] <= 32, "window-bias operand: at most two 16-column groups per axis"
+    if which == 0:
+        assert NC <= 96, "the forward holds at most 6 groups of scores in registers"
     Lcm = [-(-L[a] // d[a]) for a in range(3)]
     ntile = [-(-Lcm[a] // T[a]) for a in range(3)]
     nchk = [-(-H[a] // G[a]) for a in range(3)]
@@ -81,60 +85,44 @@ def replay(which, L, k, d, plan):
                 tq = (row // (T[2] * T[1]), (row // T[2]) % T[1], row % T[2])
                 j = [t0[a] + tq[a] for a in range(3)]
                 valid = all(j[a] < Lc[a] for a in range(3))
-                jc = [min(j[a], Lc[a] - 1) for a in range(3)]
                 lo, ln = [], []
                 for a in range(3):
+                    jc = min(j[a], Lc[a] - 1)
                     if which != 2:
-                        lo.append(win_start(jc[a], Lc[a], k[a]) - h0[a])
+                        lo.append(win_start(jc, Lc[a], k[a]) - h0[a])
                         ln.append(k[a])
                     else:
-                        lo.append(inv_lo(jc[a], k[a]) - h0[a])
-                        ln.append(inv_hi(jc[a], Lc[a], k[a]) - inv_lo(jc[a], k[a]) + 1)
-                if not valid and which != 0:
-                    ln = [0, 0, 0]
+                        lo.append(inv_lo(jc, k[a]) - h0[a])
+                        ln.append(inv_hi(jc, Lc[a], k[a]) - inv_lo(jc, k[a]) + 1)
+                    if which != 0 and j[a] >= Lc[a]:
+                        ln[a] = 0  # the row's bias part along this axis is all -2^100
                 rows.append((valid, j, lo, ln))
             for w in range(4):
                 lanes = rows[32 * w:32 * w + 32]
-                live = [r for r in lanes if all(x > 0 for x in r[3])]
-                if not live:
-                    continue
-                ulo = [min(r[2][a] for r in live) for a in range(3)]
-                uhi = [max(r[2][a] + r[3][a] for r in live) for a in range(3)]
-                for ci in range(nc[0] * nc[1] * nc[2]):
-                    cx, r = ci % nc[2], ci // nc[2]
-                    cz, cy = r % nc[1], r // nc[1]
-                    y0, z0, x0 = cy * G[0], cz * G[1], cx * G[2]
-                    useg = segment_bits(G[0], G[1], y0, z0, ulo[0], uhi[0], ulo[1], uhi[1])
-                    xa, xb = ulo[2] - x0, uhi[2] - x0
-                    ublk = range_bits(xa >> 3, (xb + 7) >> 3) & ((1 << NB) - 1) if xb > xa else 0
-                    act = 0
-                    for s_ in range(16):
-                        if (useg >> s_) & 1:
-                            act |= ublk << (s_ * NB)
+                live_rows = [r for r in lanes if all(x > 0 for x in r[3])]
+                if live_rows:
+                    ulo = [min(r[2][a] for r in live_rows) for a in range(3)]
+                    uhi = [max(r[2][a] + r[3][a] for r in live_rows) for a in range(3)]
+                else:
+                    ulo, uhi = [1 << 30] * 3, [-(1 << 30)] * 3
+                for ix in itertools.product(range(nc[0]), range(nc[1]), range(nc[2])):
+                    o = [ix[a] * G[a] for a in range(3)]
+                    glo, n = group_run(G, o, ulo, uhi)
+                    assert 16 * (glo + n) <= NC, "group run outside the chunk"
                     for valid, j, lo, ln in lanes:
-                        is_live = all(x > 0 for x in ln)
-                        rowseg = segment_bits(G[0], G[1], y0, z0, lo[0], lo[0] + ln[0], lo[1], lo[1] + ln[1]) if is_live else 0
-                        m8 = 0
-                        for bb in range(NB):
-                            m8 |= range_bits(lo[2] - x0 - 8 * bb, lo[2] + ln[2] - x0 - 8 * bb, 8) << (8 * bb)
-                        for i in range(NC // 8):
-                            if not (act >> i) & 1:
-                                continue
-                            assert 8 * i + 8 <= NC, "TMEM/P column outside the chunk"
-                            seg, bb = i // NB, i % NB
-                            if not (rowseg >> seg) & 1:
-                                continue
-                            byte = (m8 >> (8 * bb)) & 0xFF
-                            y, z = y0 + seg // G[1], z0 + seg % G[1]
-                            for e in range(8):
-                                if (byte >> e) & 1:
-                                    assert valid or which == 0
-                                    if not valid:
-                                        continue
-                                    other = [h0[0] + y, h0[1] + z, h0[2] + x0 + 8 * bb + e]
-                                    rg = tuple(cls[a] + d[a] * j[a] for a in range(3))
-                                    og = tuple(cls[a] + d[a] * other[a] for a in range(3))
-                                    pairs.append((rg, og))
+                        for col in range(NC):
+                            loc = (col // (G[1] * G[2]), (col // G[2]) % G[1], col % G[2])
+                            pos = [o[a] + loc[a] for a in range(3)]
+                            # bias: 0 along every axis (masked axes: inside the row's range)
+                            live = all(lo[a] <= pos[a] < lo[a] + ln[a] if H[a] > 1 else loc[a] == 0
+                                       for a in range(3))
+                            if not live or not valid:
+                                continue  # a row past an axis end is computed but never stored
+                            assert glo * 16 <= col < (glo + n) * 16, "a live score outside the warp's run"
+                            other = [h0[a] + pos[a] for a in range(3)]
+                            rg = tuple(cls[a] + d[a] * j[a] for a in range(3))
+                            og = tuple(cls[a] + d[a] * other[a] for a in range(3))
+                            pairs.append((rg, og))
     return pairs
 
 
