@@ -490,31 +490,28 @@ __device__ void build_bias_a(const TcParams& p, int which, const Cta& c, const B
 // per-column LSE / Delta of each chunk.
 // ---------------------------------------------------------------------------------------------
 
-// dK/dV: -LSE (log2 units) and Delta of the chunk columns lane + 32 i (-inf / 0 outside the class).
+// dK/dV: LSE and Delta of the chunk columns lane + 32 i.  The loads read clamped (always valid)
+// positions and nothing consumes them until the chunk's slot is written, so their latency hides
+// behind the producer's next waits; `in` marks the columns inside the class.
 struct AuxFetch {
     int loc[4][3];
     float l[4], dl[4];
+    uint32_t in;
 };
 
 __device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const ChunkCursor& k, AuxFetch& f,
                                           int lane) {
+    f.in = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int col = lane + 32 * i;
-        float lv = -INFINITY, dv = 0.f;
-        if (col < p.plan.NC) {
-            const int j0 = c.h0[0] + k.o[0] + f.loc[i][0], j1 = c.h0[1] + k.o[1] + f.loc[i][1],
-                      j2 = c.h0[2] + k.o[2] + f.loc[i][2];
-            if (j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) {
-                const long long tok =
-                    ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * j0)) * p.L[1] +
-                     (c.cls[1] + p.d[1] * j1)) * p.L[2] + (c.cls[2] + p.d[2] * j2);
-                lv = -__ldg(p.lse + tok * p.heads + c.h) * kLog2e;
-                dv = __ldg(p.delta + tok * p.heads + c.h);
-            }
-        }
-        f.l[i] = lv;
-        f.dl[i] = dv;
+        const int j0 = c.h0[0] + k.o[0] + f.loc[i][0], j1 = c.h0[1] + k.o[1] + f.loc[i][1],
+                  j2 = c.h0[2] + k.o[2] + f.loc[i][2];
+        if (lane + 32 * i < p.plan.NC && j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) f.in |= 1u << i;
+        const int c0 = min(j0, c.Lc[0] - 1), c1 = min(j1, c.Lc[1] - 1), c2 = min(j2, c.Lc[2] - 1);
+        const long long tok = ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * c0)) * p.L[1] +
+                               (c.cls[1] + p.d[1] * c1)) * p.L[2] + (c.cls[2] + p.d[2] * c2);
+        f.l[i] = __ldg(p.lse + tok * p.heads + c.h);
+        f.dl[i] = __ldg(p.delta + tok * p.heads + c.h);
     }
 }
 
@@ -539,9 +536,10 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int col = lane + 32 * i;
-            f.loc[i][0] = col / (pl.G[2] * pl.G[1]);
-            f.loc[i][1] = (col / pl.G[2]) % pl.G[1];
-            f.loc[i][2] = col % pl.G[2];
+            const int cc = min(col, pl.NC - 1);
+            f.loc[i][0] = cc / (pl.G[2] * pl.G[1]);
+            f.loc[i][1] = (cc / pl.G[2]) % pl.G[1];
+            f.loc[i][2] = cc % pl.G[2];
         }
     }
 
@@ -601,8 +599,9 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
                 for (int i = 0; i < 4; ++i) {
                     const int col = lane + 32 * i;
                     if (col < pl.NC) {
-                        l2[col] = f.l[i];
-                        dl[col] = f.dl[i];
+                        const bool in = (f.in >> i) & 1u;
+                        l2[col] = in ? -f.l[i] * kLog2e : -INFINITY;  // -LSE in log2 units; none outside
+                        dl[col] = in ? f.dl[i] : 0.f;
                     }
                 }
             }
@@ -739,21 +738,24 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
 
 // Store columns [c0, c1) of this thread's accumulator row (fp32 at taddr), times `mul`, as bf16
 // to dst (the row's first element in global memory).
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid, int c0, int c1) {
+template <int NCOL>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, __nv_bfloat16* dst, bool valid) {
+    static_assert(NCOL % 8 == 0 && NCOL <= 64, "row slice of 8..64 columns");
+    uint32_t r[NCOL / 8][8];
 #pragma unroll
-    for (int cc = 0; cc < D; cc += 8) {
-        if (cc < c0 || cc >= c1) continue;
-        uint32_t r[8];
-        tmem_ld8(taddr + cc, r);
-        tmem_ld_wait(r);
-        if (valid) {
+    for (int i = 0; i < NCOL / 8; ++i) tmem_ld8(taddr + 8 * i, r[i]);
+    tmem_ld_wait_all();
+#pragma unroll
+    for (int i = 0; i < NCOL / 8; ++i) reg_fence8(r[i]);
+    if (valid) {
+#pragma unroll
+        for (int i = 0; i < NCOL / 8; ++i) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[0]) * mul, __uint_as_float(r[1]) * mul);
-            w.y = pack_bf16x2(__uint_as_float(r[2]) * mul, __uint_as_float(r[3]) * mul);
-            w.z = pack_bf16x2(__uint_as_float(r[4]) * mul, __uint_as_float(r[5]) * mul);
-            w.w = pack_bf16x2(__uint_as_float(r[6]) * mul, __uint_as_float(r[7]) * mul);
-            *reinterpret_cast<uint4*>(dst + cc) = w;
+            w.x = pack_bf16x2(__uint_as_float(r[i][0]) * mul, __uint_as_float(r[i][1]) * mul);
+            w.y = pack_bf16x2(__uint_as_float(r[i][2]) * mul, __uint_as_float(r[i][3]) * mul);
+            w.z = pack_bf16x2(__uint_as_float(r[i][4]) * mul, __uint_as_float(r[i][5]) * mul);
+            w.w = pack_bf16x2(__uint_as_float(r[i][6]) * mul, __uint_as_float(r[i][7]) * mul);
+            *reinterpret_cast<uint4*>(dst + 8 * i) = w;
         }
     }
 }
@@ -781,9 +783,15 @@ struct FwdCtx {
     int lane;
 };
 
-// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + N).
+// Groups [glo, glo + n) as a bit mask.
+__device__ __forceinline__ uint32_t run_mask(int glo, int n) { return ((1u << n) - 1u) << glo; }
+
+// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + N).  `nz` holds
+// the groups of this warp's rows of P buffer g & 1 that may be nonzero (its last run); groups in
+// nz outside the new run are zeroed, and nz becomes the new run.
 template <int D, int N>
-__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4]) {
+__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4],
+                                          uint32_t& nz) {
     const uint32_t sb = g & 1;
     uint32_t v[N > 0 ? N : 1][16];
     const uint32_t tS = x.tS0 + sb * x.tS_step;
@@ -800,7 +808,9 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     if (x.lane == 0) mbar_arrive(&x.bars[kSEmpty + sb]);
     // chunk row max (masked scores carry the -2^100 window bias), four independent chains
     float cmax = -INFINITY;
-    if (N > 0) {
+    if (N == 0) {
+        // no key of this warp's rows in the chunk: nothing to read, the running max is unchanged
+    } else {
         float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int i = 0; i < N; ++i)
@@ -816,7 +826,7 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     const bool rescale = (m != -INFINITY) && (mnew > m + kRescaleThreshold);
     const float alpha = rescale ? fast_exp2(m - mnew) : 1.f;
     if (m == -INFINITY || rescale) m = mnew;
-    if (__any_sync(0xffffffffu, rescale)) {
+    if (N > 0 && __any_sync(0xffffffffu, rescale)) {
         // O holds the products of chunks g-1, g-2, ...: wait for the last one
         if (!warp_wait(&x.bars[kPEmpty + ((g - 1) & 1)], ((g - 1) >> 1) & 1, x.err, kSitePV)) return false;
         tc_fence_after();
@@ -833,6 +843,13 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
         const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
         for (int t = 0; t < 4; ++t) lsum[t] = f2_mul(lsum[t], a2);
+    }
+    const uint32_t run = N > 0 ? run_mask(glo, N) : 0u, stale = nz & ~run;
+    nz = run;
+    if (N == 0 && stale == 0) {  // nothing to write: this warp's rows of the buffer are already zero
+        __syncwarp();
+        if (x.lane == 0) mbar_arrive(&x.bars[kPFull + sb]);
+        return true;
     }
     // P buffer sb is free once the product of chunk g-2 is done
     if (g >= 2 && !warp_wait(&x.bars[kPEmpty + sb], ((g >> 1) - 1) & 1, x.err, kSitePV)) return false;
@@ -854,8 +871,7 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
         st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i)), w[0], w[1], w[2], w[3]);
         st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i) + 1), w[4], w[5], w[6], w[7]);
     }
-    for (int gi = 0; gi < x.ngroups; ++gi)
-        if (gi < glo || gi >= glo + N) zero_group(sP, x.rowbase, x.sw, gi);
+    for (uint32_t z = stale; z; z &= z - 1) zero_group(sP, x.rowbase, x.sw, __ffs(z) - 1);
     fence_proxy_async_smem();
     __syncwarp();
     if (x.lane == 0) mbar_arrive(&x.bars[kPFull + sb]);
@@ -881,6 +897,7 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2 = p.scale_log2;
     x.sl2x2 = f2(x.sl2, x.sl2);
     x.lane = lane;
+    uint32_t nz0 = run_mask(0, x.ngroups), nz1 = nz0;  // groups of the two P buffers that may be nonzero
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -900,15 +917,17 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             tc_fence_after();
             int glo, n;
             chunk_range(pl, cur, wu, glo, n);
+            uint32_t nz = (g & 1) ? nz1 : nz0;
             switch (n) {
-                case 0: ok = fwd_chunk<D, 0>(x, g, glo, m, lsum); break;
-                case 1: ok = fwd_chunk<D, 1>(x, g, glo, m, lsum); break;
-                case 2: ok = fwd_chunk<D, 2>(x, g, glo, m, lsum); break;
-                case 3: ok = fwd_chunk<D, 3>(x, g, glo, m, lsum); break;
-                case 4: ok = fwd_chunk<D, 4>(x, g, glo, m, lsum); break;
-                case 5: ok = fwd_chunk<D, 5>(x, g, glo, m, lsum); break;
-                default: ok = fwd_chunk<D, 6>(x, g, glo, m, lsum); break;
+                case 0: ok = fwd_chunk<D, 0>(x, g, glo, m, lsum, nz); break;
+                case 1: ok = fwd_chunk<D, 1>(x, g, glo, m, lsum, nz); break;
+                case 2: ok = fwd_chunk<D, 2>(x, g, glo, m, lsum, nz); break;
+                case 3: ok = fwd_chunk<D, 3>(x, g, glo, m, lsum, nz); break;
+                case 4: ok = fwd_chunk<D, 4>(x, g, glo, m, lsum, nz); break;
+                case 5: ok = fwd_chunk<D, 5>(x, g, glo, m, lsum, nz); break;
+                default: ok = fwd_chunk<D, 6>(x, g, glo, m, lsum, nz); break;
             }
+            if (g & 1) nz1 = nz; else nz0 = nz;
             if (!ok) break;
         }
         if (!ok) break;
@@ -921,7 +940,7 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
         if (!ok) break;
         tc_fence_after();
         const long long orow = geo.token * p.heads + c.h;
-        store_row<D>(x.tO, 1.f / l, p.out0 + orow * D, geo.valid, 0, D);
+        store_row<D>(x.tO, 1.f / l, p.out0 + orow * D, geo.valid);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[kOEmpty + ob]);
@@ -1018,6 +1037,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2x2 = f2(p.scale_log2, p.scale_log2);
     x.l2 = nullptr;
     x.dl = nullptr;
+    uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0;  // groups of the quarter's rows that may be nonzero
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -1038,10 +1058,30 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
             const uint32_t sb = g & 1, s = g % kS;
             ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
-            if (ok && WHICH == 2) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
-            if (ok && g >= 2) ok = warp_wait(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSitePV);
             if (!ok) break;
             tc_fence_after();
+            int glo, n;
+            chunk_range(pl, cur, wu, glo, n);
+            // this warpgroup's groups of the run: glo + wg, glo + wg + 2, ...; the groups of the
+            // quarter's last run in this buffer that the new run does not cover are zeroed, split
+            // between the warpgroups by parity
+            const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
+            const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
+            const uint32_t nzq = sb ? nz1 : nz0;
+            const uint32_t stale = nzq & ~run & (wg ? 0xaaaaaaaau : 0x55555555u);
+            if (sb) nz1 = run; else nz0 = run;
+            if (mine == 0 && stale == 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[kSEmpty + sb]);
+                    mbar_arrive(&bars[kPFull + sb]);
+                }
+                continue;
+            }
+            if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
+            if (ok && g >= 2) ok = warp_wait(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSitePV);
+            if (!ok) break;
             x.tS = tmem + tm_s(pl, sb) + lane_base;
             x.tP = tmem + tm_dp(pl, sb) + lane_base;
             x.sP0 = smem_u32(smem + lay.p(sb, 0));
@@ -1050,22 +1090,16 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                 x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
                 x.dl = x.l2 + pl.NC;
             }
-            int glo, n;
-            chunk_range(pl, cur, wu, glo, n);
-            // this warpgroup's groups: glo + wg, glo + wg + 2, ...
-            const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
             int k = 0;
             for (; k + 2 <= mine; k += 2) bwd_groups<WHICH, 2>(x, glo + wg + 2 * k);
             if (k < mine) bwd_groups<WHICH, 1>(x, glo + wg + 2 * k);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
-            // groups outside the run are zero; the warpgroups split them by parity
-            for (int gi = wg; gi < ngroups; gi += 2)
-                if (gi < glo || gi >= glo + n) {
-                    zero_group(x.sP0, x.rowbase, x.sw, gi);
-                    if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, gi);
-                }
+            for (uint32_t z = stale; z; z &= z - 1) {
+                zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
+                if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, __ffs(z) - 1);
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kPFull + sb]);
@@ -1077,12 +1111,12 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
         tc_fence_after();
         const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + lane_base;
         const long long orow = geo.token * p.heads + c.h;
-        const int c0 = wg * (D / 2), c1 = c0 + D / 2;
+        const int c0 = wg * (D / 2);
         if (WHICH == 1) {
-            store_row<D>(acc, p.scale, p.out0 + orow * D, geo.valid, c0, c1);  // dQ
+            store_row<D / 2>(acc + c0, p.scale, p.out0 + orow * D + c0, geo.valid);  // dQ
         } else {
-            store_row<D>(acc, 1.f, p.out1 + orow * D, geo.valid, c0, c1);          // dV
-            store_row<D>(acc + D, p.scale, p.out0 + orow * D, geo.valid, c0, c1);  // dK
+            store_row<D / 2>(acc + c0, 1.f, p.out1 + orow * D + c0, geo.valid);          // dV
+            store_row<D / 2>(acc + D + c0, p.scale, p.out0 + orow * D + c0, geo.valid);  // dK
         }
         tc_fence_before();
         __syncwarp();
