@@ -45,7 +45,12 @@ constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
 constexpr int kMaxStages = 3;
 
-__host__ __device__ constexpr int stages_of(int D) { return D <= 32 ? 3 : 2; }  // halo chunk ring depth
+// Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
+// the copy latency; dQ has the shared memory for a third P buffer (more slack between unevenly
+// loaded softmax warps), the forward (two CTAs per SM) and dK/dV (two P operands) do not.
+__host__ __device__ constexpr int stages_of(int which, int D) { return (void)which, D <= 32 ? 3 : 2; }
+__host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
+constexpr int kMaxPBufs = 3;
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
 __host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2); }
 
@@ -115,11 +120,11 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     L.chunk0 = o;
     L.chunk_t = chunk;
     L.chunk_slot = 2 * chunk;
-    o += stages_of(D) * L.chunk_slot;
+    o += stages_of(which, D) * L.chunk_slot;
     L.p0 = o;
     L.p_op = pbytes;
     L.p_buf = nop * pbytes;
-    o += 2 * L.p_buf;
+    o += pbufs_of(which) * L.p_buf;
     L.abias = o;
     o += static_cast<uint32_t>(bg.na) * 4096u;
     L.bbias = o;
@@ -127,7 +132,7 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     o += align_up(static_cast<uint32_t>(bg.nb) * L.bgroup, 1024);
     L.aux0 = o;
     L.aux_slot = which == 2 ? align_up(8u * static_cast<uint32_t>(pl.NC), 128) : 0u;
-    o += align_up(stages_of(D) * L.aux_slot, 1024);
+    o += align_up(stages_of(which, D) * L.aux_slot, 1024);
     L.bars = o;
     o += 512;
     L.total = o;
@@ -137,7 +142,8 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
 // mbarrier indices
 enum Bar {
     kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kMaxStages, kSFull = 4 + 2 * kMaxStages,
-    kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + 2, kOFull = kPEmpty + 2, kOEmpty = kOFull + 2,
+    kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + kMaxPBufs, kOFull = kPEmpty + kMaxPBufs,
+    kOEmpty = kOFull + 2,
     kFin = kOEmpty + 2, kNumBars = kFin + 1
 };
 
@@ -517,7 +523,7 @@ __device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const
 
 template <int D, int WHICH>
 __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
-    constexpr int kS = stages_of(D);
+    constexpr int kS = stages_of(WHICH, D);
     constexpr int ntile = WHICH == 0 ? 1 : 2;
     constexpr int tmCk = WHICH == 0 ? 1 : 2, tmCv = WHICH == 0 ? 2 : 3;
     const int lane = threadIdx.x & 31;
@@ -673,12 +679,17 @@ __device__ __forceinline__ uint32_t tm_acc(int which, uint32_t b) {
 struct PendingUpdate {
     uint32_t g, s, j;
     int ci, C;
-    bool valid;
 };
 
+// The MMA lane runs two streams: the score products of the next chunk (as soon as its K/V chunk is
+// loaded and its TMEM score buffer has been read by the softmax warps) and the update products of
+// the oldest scored chunk (as soon as its P operand is written).  Neither waits for the other, so
+// one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
+// after kWaitLimitNs without progress the lane records an error and stops.
 template <int D, int WHICH>
 __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
-    constexpr int kS = stages_of(D);
+    constexpr int kS = stages_of(WHICH, D);
+    constexpr uint32_t kPB = pbufs_of(WHICH);
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
     const MmaIssuer<D> mi{p, smem, lay, bias_geom(pl)};
@@ -686,50 +697,78 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
-    uint32_t j = 0, g = 0;
-    PendingUpdate pend{0, 0, 0, 0, 0, false};
-    bool ok = true;
-    auto update = [&](const PendingUpdate& pd) -> bool {
-        const uint32_t pb = pd.g & 1, ob = pd.j & 1;
-        if (!mbar_wait(&bars[kPFull + pb], (pd.g >> 1) & 1, err, kSiteP)) return false;
-        if (pd.ci == 0 && pd.j >= 2 && !mbar_wait(&bars[kOEmpty + ob], ((pd.j >> 1) - 1) & 1, err, kSitePV))
-            return false;
-        tc_fence_after();
-        const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
-        if (WHICH == 0) {
-            mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 1), pd.ci > 0);  // O += P V
-        } else if (WHICH == 1) {
-            mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 0), pd.ci > 0);  // dQ += dS K
-        } else {
-            mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(pd.s, 1), pd.ci > 0);      // dV += P^T dO
-            mi.p_x_chunk(acc + D, lay.p(pb, 1), lay.chunk(pd.s, 0), pd.ci > 0);  // dK += dS^T Q
+    bool have = next_tile(p, WHICH, it, started, c);
+    uint32_t jS = 0, gS = 0;
+    int ciS = 0;
+    bool qready = false;
+    ChunkCursor cur = cursor_begin();
+    PendingUpdate q0{}, q1{}, q2{};  // scored chunks awaiting their update, oldest first
+    int nq = 0;
+    unsigned long long t_last = globaltimer();
+    for (;;) {
+        bool progress = false;
+        if (nq > 0) {
+            const uint32_t pb = q0.g % kPB, ob = q0.j & 1;
+            if (mbar_test(&bars[kPFull + pb], (q0.g / kPB) & 1) &&
+                (q0.ci != 0 || q0.j < 2 || mbar_test(&bars[kOEmpty + ob], ((q0.j >> 1) - 1) & 1))) {
+                tc_fence_after();
+                const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
+                if (WHICH == 0) {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
+                } else if (WHICH == 1) {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 0), q0.ci > 0);  // dQ += dS K
+                } else {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);      // dV += P^T dO
+                    mi.p_x_chunk(acc + D, lay.p(pb, 1), lay.chunk(q0.s, 0), q0.ci > 0);  // dK += dS^T Q
+                }
+                umma_commit(&bars[kPEmpty + pb]);
+                umma_commit(&bars[kKVEmpty + q0.s]);
+                if (q0.ci == q0.C - 1) umma_commit(&bars[kOFull + ob]);
+                q0 = q1;
+                q1 = q2;
+                --nq;
+                progress = true;
+            }
         }
-        umma_commit(&bars[kPEmpty + pb]);
-        umma_commit(&bars[kKVEmpty + pd.s]);
-        if (pd.ci == pd.C - 1) umma_commit(&bars[kOFull + ob]);
-        return true;
-    };
-    while (ok && next_tile(p, WHICH, it, started, c)) {
-        const uint32_t qs = j & 1;
-        if (!mbar_wait(&bars[kQFull + qs], (j >> 1) & 1, err, kSiteQ)) break;
-        ChunkCursor cur = cursor_begin();
-        for (int ci = 0; ci < c.C && ok; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t s = g % kS, sb = g & 1;
-            ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
-            if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
-            if (!ok) break;
-            tc_fence_after();
-            mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
-            mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
-            if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
-            umma_commit(&bars[kSFull + sb]);
-            if (ci == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
-            if (pend.valid) ok = update(pend);
-            pend = PendingUpdate{g, s, j, ci, c.C, true};
+        if (have && nq < 3) {
+            const uint32_t qs = jS & 1, s = gS % kS, sb = gS & 1;
+            if (!qready) qready = mbar_test(&bars[kQFull + qs], (jS >> 1) & 1);
+            if (qready && mbar_test(&bars[kKVFull + s], (gS / kS) & 1) &&
+                (gS < 2 || mbar_test(&bars[kSEmpty + sb], ((gS >> 1) - 1) & 1))) {
+                tc_fence_after();
+                mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
+                mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
+                if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
+                umma_commit(&bars[kSFull + sb]);
+                if (ciS == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
+                const PendingUpdate pu{gS, s, jS, ciS, c.C};
+                if (nq == 0) q0 = pu; else if (nq == 1) q1 = pu; else q2 = pu;
+                ++nq;
+                ++gS;
+                if (++ciS == c.C) {
+                    ciS = 0;
+                    ++jS;
+                    qready = false;
+                    cur = cursor_begin();
+                    have = next_tile(p, WHICH, it, started, c);
+                } else {
+                    cursor_next(pl, c, cur);
+                }
+                progress = true;
+            }
         }
-        ++j;
+        if (!have && nq == 0) break;
+        if (progress) {
+            t_last = globaltimer();
+            continue;
+        }
+        if (ld_volatile(err) != 0u) break;
+        if (globaltimer() - t_last > kWaitLimitNs) {
+            record_error(err, kSiteP);
+            break;
+        }
+        __nanosleep(32);
     }
-    if (ok && pend.valid) update(pend);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -792,7 +831,8 @@ __device__ __forceinline__ uint32_t run_mask(int glo, int n) { return ((1u << n)
 template <int D, int N>
 __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4],
                                           uint32_t& nz) {
-    const uint32_t sb = g & 1;
+    constexpr uint32_t kPB = pbufs_of(0);
+    const uint32_t sb = g & 1, pb = g % kPB;
     uint32_t v[N > 0 ? N : 1][16];
     const uint32_t tS = x.tS0 + sb * x.tS_step;
 #pragma unroll
@@ -828,7 +868,7 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     if (m == -INFINITY || rescale) m = mnew;
     if (N > 0 && __any_sync(0xffffffffu, rescale)) {
         // O holds the products of chunks g-1, g-2, ...: wait for the last one
-        if (!warp_wait(&x.bars[kPEmpty + ((g - 1) & 1)], ((g - 1) >> 1) & 1, x.err, kSitePV)) return false;
+        if (!warp_wait(&x.bars[kPEmpty + (g - 1) % kPB], ((g - 1) / kPB) & 1, x.err, kSitePV)) return false;
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D; cc += 8) {
@@ -848,12 +888,12 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     nz = run;
     if (N == 0 && stale == 0) {  // nothing to write: this warp's rows of the buffer are already zero
         __syncwarp();
-        if (x.lane == 0) mbar_arrive(&x.bars[kPFull + sb]);
+        if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
         return true;
     }
-    // P buffer sb is free once the product of chunk g-2 is done
-    if (g >= 2 && !warp_wait(&x.bars[kPEmpty + sb], ((g >> 1) - 1) & 1, x.err, kSitePV)) return false;
-    const uint32_t sP = x.sP0 + sb * x.sP_step;
+    // P buffer pb is free once the product of chunk g - kPB is done
+    if (g >= kPB && !warp_wait(&x.bars[kPEmpty + pb], ((g / kPB) - 1) & 1, x.err, kSitePV)) return false;
+    const uint32_t sP = x.sP0 + pb * x.sP_step;
     const float nm = m == -INFINITY ? 0.f : -m;  // masked scores are -inf: exp2 gives 0
     const uint64_t nm2 = f2(nm, nm);
 #pragma unroll
@@ -874,7 +914,28 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     for (uint32_t z = stale; z; z &= z - 1) zero_group(sP, x.rowbase, x.sw, __ffs(z) - 1);
     fence_proxy_async_smem();
     __syncwarp();
-    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + sb]);
+    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
+    return true;
+}
+
+// A tile whose rows still have to be written: O / l -> bf16 and LSE = (m + log2 l) * ln 2.
+struct FwdEpilogue {
+    bool live, valid;
+    float m, l;
+    long long orow;  // row index into [B * tokens * heads]
+    uint32_t ob, j;  // accumulator buffer and tile ordinal
+};
+
+template <int D>
+__device__ __forceinline__ bool fwd_epilogue(const TcParams& p, const FwdCtx& x, const FwdEpilogue& e,
+                                             uint32_t tmem_lanes) {
+    if (!warp_wait(&x.bars[kOFull + e.ob], (e.j >> 1) & 1, x.err, kSitePV)) return false;
+    tc_fence_after();
+    store_row<D>(tmem_lanes + tm_acc<D>(0, e.ob), 1.f / e.l, p.out0 + e.orow * D, e.valid);
+    tc_fence_before();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kOEmpty + e.ob]);
+    if (e.valid) p.lse_out[e.orow] = (e.m + __log2f(e.l)) * kLn2;
     return true;
 }
 
@@ -897,7 +958,8 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2 = p.scale_log2;
     x.sl2x2 = f2(x.sl2, x.sl2);
     x.lane = lane;
-    uint32_t nz0 = run_mask(0, x.ngroups), nz1 = nz0;  // groups of the two P buffers that may be nonzero
+    uint32_t nz0 = run_mask(0, x.ngroups), nz1 = nz0, nz2 = nz0;  // groups of the P buffers that may be nonzero
+    FwdEpilogue ep{false, false, 0.f, 0.f, 0, 0, 0};
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -917,36 +979,29 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             tc_fence_after();
             int glo, n;
             chunk_range(pl, cur, wu, glo, n);
-            uint32_t nz = (g & 1) ? nz1 : nz0;
+            const uint32_t pb = g % pbufs_of(0);
+            uint32_t nz = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
             switch (n) {
                 case 0: ok = fwd_chunk<D, 0>(x, g, glo, m, lsum, nz); break;
                 case 1: ok = fwd_chunk<D, 1>(x, g, glo, m, lsum, nz); break;
                 case 2: ok = fwd_chunk<D, 2>(x, g, glo, m, lsum, nz); break;
                 case 3: ok = fwd_chunk<D, 3>(x, g, glo, m, lsum, nz); break;
-                case 4: ok = fwd_chunk<D, 4>(x, g, glo, m, lsum, nz); break;
-                case 5: ok = fwd_chunk<D, 5>(x, g, glo, m, lsum, nz); break;
-                default: ok = fwd_chunk<D, 6>(x, g, glo, m, lsum, nz); break;
+                default: ok = fwd_chunk<D, 4>(x, g, glo, m, lsum, nz); break;
             }
-            if (g & 1) nz1 = nz; else nz0 = nz;
+            if (pb == 0) nz0 = nz; else if (pb == 1) nz1 = nz; else nz2 = nz;
             if (!ok) break;
         }
         if (!ok) break;
-        // epilogue: O / l -> bf16; LSE = (m + log2 l) * ln 2
+        // the previous tile's epilogue, deferred until this tile's chunks are done so that a warp
+        // does not idle at the end of a tile while the slowest warp finishes it
+        if (ep.live && !(ok = fwd_epilogue<D>(p, x, ep, tmem + lane_base))) break;
         const uint64_t ls = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
         float la, lb;
         f2_split(ls, la, lb);
-        const float l = la + lb;
-        ok = warp_wait(&bars[kOFull + ob], (j >> 1) & 1, x.err, kSitePV);
-        if (!ok) break;
-        tc_fence_after();
-        const long long orow = geo.token * p.heads + c.h;
-        store_row<D>(x.tO, 1.f / l, p.out0 + orow * D, geo.valid);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kOEmpty + ob]);
-        if (geo.valid) p.lse_out[orow] = (m + __log2f(l)) * kLn2;
+        ep = FwdEpilogue{true, geo.valid, m, la + lb, geo.token * p.heads + c.h, ob, j};
         ++j;
     }
+    if (ok && ep.live) fwd_epilogue<D>(p, x, ep, tmem + lane_base);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1020,10 +1075,37 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0) {
     }
 }
 
+// A tile whose rows still have to be written; each warpgroup writes half of the D columns of its
+// quarter's rows (dQ, or dV and dK).
+struct BwdEpilogue {
+    bool live, valid;
+    long long orow;
+    uint32_t ob, j;
+};
+
+template <int D, int WHICH>
+__device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, const BwdEpilogue& e,
+                                             uint32_t tmem_lanes, int wg, int lane) {
+    if (!warp_wait(&bars[kOFull + e.ob], (e.j >> 1) & 1, p.err, kSitePV)) return false;
+    tc_fence_after();
+    const uint32_t acc = tmem_lanes + tm_acc<D>(WHICH, e.ob);
+    const int c0 = wg * (D / 2);
+    if (WHICH == 1) {
+        store_row<D / 2>(acc + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dQ
+    } else {
+        store_row<D / 2>(acc + c0, 1.f, p.out1 + e.orow * D + c0, e.valid);          // dV
+        store_row<D / 2>(acc + D + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dK
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kOEmpty + e.ob]);
+    return true;
+}
+
 template <int D, int WHICH>
 __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
                                  uint32_t tmem) {
-    constexpr int kS = stages_of(D);
+    constexpr int kS = stages_of(WHICH, D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
     const int row = wq * 32 + lane;
@@ -1037,7 +1119,8 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2x2 = f2(p.scale_log2, p.scale_log2);
     x.l2 = nullptr;
     x.dl = nullptr;
-    uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0;  // groups of the quarter's rows that may be nonzero
+    uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0, nz2 = nz0;  // groups of the quarter's rows that may be nonzero
+    BwdEpilogue ep{false, false, 0, 0, 0};
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
@@ -1056,7 +1139,8 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
         x.dl2 = f2(dlt, dlt);
         ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t sb = g & 1, s = g % kS;
+            constexpr uint32_t kPB = pbufs_of(WHICH);
+            const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
             ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
             if (!ok) break;
             tc_fence_after();
@@ -1067,25 +1151,25 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             // between the warpgroups by parity
             const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
             const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
-            const uint32_t nzq = sb ? nz1 : nz0;
+            const uint32_t nzq = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
             const uint32_t stale = nzq & ~run & (wg ? 0xaaaaaaaau : 0x55555555u);
-            if (sb) nz1 = run; else nz0 = run;
+            if (pb == 0) nz0 = run; else if (pb == 1) nz1 = run; else nz2 = run;
             if (mine == 0 && stale == 0) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bars[kSEmpty + sb]);
-                    mbar_arrive(&bars[kPFull + sb]);
+                    mbar_arrive(&bars[kPFull + pb]);
                 }
                 continue;
             }
             if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
-            if (ok && g >= 2) ok = warp_wait(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSitePV);
+            if (ok && g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
             if (!ok) break;
             x.tS = tmem + tm_s(pl, sb) + lane_base;
             x.tP = tmem + tm_dp(pl, sb) + lane_base;
-            x.sP0 = smem_u32(smem + lay.p(sb, 0));
-            x.sP1 = smem_u32(smem + lay.p(sb, 1));
+            x.sP0 = smem_u32(smem + lay.p(pb, 0));
+            x.sP1 = smem_u32(smem + lay.p(pb, 1));
             if (WHICH == 2) {
                 x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
                 x.dl = x.l2 + pl.NC;
@@ -1102,27 +1186,15 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kPFull + sb]);
+            if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
         }
         if (!ok) break;
-        // epilogue: each warpgroup writes half of the D columns of its quarter's rows
-        ok = warp_wait(&bars[kOFull + ob], (j >> 1) & 1, err, kSitePV);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + lane_base;
-        const long long orow = geo.token * p.heads + c.h;
-        const int c0 = wg * (D / 2);
-        if (WHICH == 1) {
-            store_row<D / 2>(acc + c0, p.scale, p.out0 + orow * D + c0, geo.valid);  // dQ
-        } else {
-            store_row<D / 2>(acc + c0, 1.f, p.out1 + orow * D + c0, geo.valid);          // dV
-            store_row<D / 2>(acc + D + c0, p.scale, p.out0 + orow * D + c0, geo.valid);  // dK
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[kOEmpty + ob]);
+        // the previous tile's epilogue, deferred until this tile's chunks are done
+        if (ep.live && !(ok = bwd_epilogue<D, WHICH>(p, bars, ep, tmem + lane_base, wg, lane))) break;
+        ep = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
         ++j;
     }
+    if (ok && ep.live) bwd_epilogue<D, WHICH>(p, bars, ep, tmem + lane_base, wg, lane);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1141,12 +1213,14 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kQEmpty + i], 1);
         mbar_init(&bars[kSFull + i], 1);
         mbar_init(&bars[kSEmpty + i], kSoft);
-        mbar_init(&bars[kPFull + i], kSoft);
-        mbar_init(&bars[kPEmpty + i], 1);
         mbar_init(&bars[kOFull + i], 1);
         mbar_init(&bars[kOEmpty + i], kSoft);
     }
-    for (int s = 0; s < stages_of(D); ++s) {
+    for (int i = 0; i < pbufs_of(WHICH); ++i) {
+        mbar_init(&bars[kPFull + i], kSoft);
+        mbar_init(&bars[kPEmpty + i], 1);
+    }
+    for (int s = 0; s < stages_of(WHICH, D); ++s) {
         mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
         mbar_init(&bars[kKVEmpty + s], 1);
     }
@@ -1238,10 +1312,10 @@ int tc_tmem_cols(int which) { return which == 0 ? 256 : 512; }
 
 int tc_max_nc(int which, int D) {
     // double-buffered score accumulators plus double-buffered tile accumulators; the forward keeps
-    // at most 6 groups (96 columns) of scores in registers
+    // at most 4 groups (64 columns) of scores in registers
     const int cols = tc_tmem_cols(which);
     const int nc = which == 0 ? (cols - 2 * D) / 2 : (which == 1 ? (cols - 2 * D) / 4 : (cols - 4 * D) / 4);
-    const int cap = which == 0 ? 96 : 128;
+    const int cap = which == 0 ? 64 : 128;
     return (nc < cap ? nc : cap) / 16 * 16;
 }
 
