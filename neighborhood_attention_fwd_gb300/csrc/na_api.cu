@@ -216,7 +216,7 @@ double tile_cost(int which, const Geom& g, const TilePlan& pl, int n_mma, int pe
                     mx = std::max(mx, n);
                     sum += n;
                 }
-                soft += 0.5 * mx + 0.125 * sum;
+                soft += 0.75 * mx + 0.0625 * sum;  // warps wait for the slowest one within a chunk or two
             }
     const double per_group = which == 0 ? 150.0 : 90.0;  // cycles per 16-column group and warp
     const double soft_cyc = soft * per_group + 300.0 * C;
@@ -264,8 +264,8 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
             double tiles = 1;
             for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
             const int gmax0 = Hx[0] > 1 ? std::min(Hx[0], 32) : 1, gmax1 = Hx[1] > 1 ? std::min(Hx[1], 32) : 1;
-            for (int G2 = 8; G2 <= 32; G2 += 8) {
-                if (G2 > (Hx[2] + 7) / 8 * 8 || G2 * g.d[2] > 256) continue;
+            for (int G2 = 1; G2 <= std::min(Hx[2], 32); ++G2) {
+                if (G2 * g.d[2] > 256) continue;
                 for (int G1 = 1; G1 <= gmax1; ++G1)
                     for (int G0 = 1; G0 <= gmax0; ++G0) {
                         const int NC = G0 * G1 * G2;

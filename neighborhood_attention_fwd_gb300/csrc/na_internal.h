@@ -22,7 +22,7 @@ struct TilePlan {
     int T[3];        // tile extents (class coordinates), T0*T1*T2 == 128, powers of two
     int H[3];        // halo box extents: keys (fwd, dQ) or queries (dK/dV) a tile may need;
                      // H[a] == nchk[a] * G[a] along every axis
-    int G[3];        // chunk box extents; G[2] a multiple of 8; G[a] <= 32 along masked axes
+    int G[3];        // chunk box extents; G[a] <= 32 along masked axes; NC multiple of 16
     int NC;          // rows of one chunk = G0*G1*G2 (multiple of 16, <= 112)
     int nchk[3];     // chunks along each axis that cover the halo box
     int ntile[3];    // tiles per axis and residue class: ceil(ceil(L/d) / T)

@@ -1018,20 +1018,29 @@ struct BwdCtx {
     uint64_t sl2x2;
 };
 
-// Groups g0 (and g0 + 2 when K == 2) of this warp's rows: P = exp2(S sl2 - LSE2), dS = P (dP - Delta).
+// This warp's K (<= 2) groups g0, g0 + 2 of the chunk: their scores and dP values are read, the
+// score buffer is released when these are the warp's last groups of the chunk (so the next chunk's
+// products can start), then P = exp2(S sl2 - LSE2) and dS = P (dP - Delta) are formed and stored.
 template <int WHICH, int K>
-__device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0) {
-    uint32_t rs[K][16], rp[K][16];
+__device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* sempty, bool release, int lane) {
+    uint32_t rs[K > 0 ? K : 1][16], rp[K > 0 ? K : 1][16];
 #pragma unroll
     for (int i = 0; i < K; ++i) {
         tmem_ld16(x.tS + 16u * (g0 + 2 * i), rs[i]);
         tmem_ld16(x.tP + 16u * (g0 + 2 * i), rp[i]);
     }
-    tmem_ld_wait_all();
+    if (K > 0) {
+        tmem_ld_wait_all();
 #pragma unroll
-    for (int i = 0; i < K; ++i) {
-        reg_fence16(rs[i]);
-        reg_fence16(rp[i]);
+        for (int i = 0; i < K; ++i) {
+            reg_fence16(rs[i]);
+            reg_fence16(rp[i]);
+        }
+    }
+    if (release) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty);
     }
 #pragma unroll
     for (int i = 0; i < K; ++i) {
@@ -1174,12 +1183,14 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                 x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
                 x.dl = x.l2 + pl.NC;
             }
-            int k = 0;
-            for (; k + 2 <= mine; k += 2) bwd_groups<WHICH, 2>(x, glo + wg + 2 * k);
-            if (k < mine) bwd_groups<WHICH, 1>(x, glo + wg + 2 * k);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
+            if (mine == 0) bwd_groups<WHICH, 0>(x, glo + wg, &bars[kSEmpty + sb], true, lane);
+            for (int k = 0; k < mine; k += 2) {
+                const bool last = k + 2 >= mine;
+                if (k + 1 < mine)
+                    bwd_groups<WHICH, 2>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+                else
+                    bwd_groups<WHICH, 1>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+            }
             for (uint32_t z = stale; z; z &= z - 1) {
                 zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
                 if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, __ffs(z) - 1);
