@@ -70,6 +70,8 @@ WORKLOADS = {
                  "randn", 1238, "the issue's (8,128,128)/(5,7,7) model shape"),
         Workload("2d_bf16_2048x2048_k13_d2", "bf16", 1, (2048, 2048), 8, 32, (13, 13), (2, 2), "randn",
                  1239, "large dilated 2D stress case"),
+        Workload("2d_bf16_512x512_k9", "bf16", 1, (512, 512), 8, 32, (9, 9), (1, 1), "ones", 1240,
+                 "profiling case: the 2D benchmark's kernels on a quarter of its tokens (inputs > L2)"),
     ]
 }
 
