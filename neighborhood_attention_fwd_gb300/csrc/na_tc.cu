@@ -52,7 +52,12 @@ __host__ __device__ constexpr int stages_of(int which, int D) { return (void)whi
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
 constexpr int kMaxPBufs = 3;
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
-__host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2); }
+// Warps that issue update products: the forward's one MMA warp issues everything; the backward has
+// one issuing warp per update accumulator (dQ; or dV and dK) beside the warp issuing score products.
+// A single lane waits tens of cycles on each tcgen05.mma it issues, so products into independent
+// accumulators are issued by different warps.
+__host__ __device__ constexpr int nupd_of(int which) { return which == 0 ? 0 : (which == 1 ? 1 : 2); }
+__host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2 + nupd_of(which)); }
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -624,44 +629,67 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
 // MMA warp (lane 0): score products per chunk, update products of the previous chunk.
 // ---------------------------------------------------------------------------------------------
 
+// Issues the tensor-core products.  The MMA lane shares its SM sub-partition with softmax warps, so
+// every instruction it spends per MMA counts: descriptors are built once with start address 0 and
+// offset per operand (the start-address field is the low 14 bits of the descriptor and holds
+// address >> 4; shared addresses are below 256 KB), and the instruction descriptors are constant.
 template <int D>
 struct MmaIssuer {
-    const TcParams& p;
-    uint8_t* smem;
-    const TcLayout& lay;
-    BiasGeom bg;
+    uint32_t sbase;                        // shared address of the layout base
+    uint64_t dk, dp, dmn, dbias;           // descriptor bases: K-major rows of D, P atoms, MN-major rows of D, bias blocks
+    uint32_t idesc_s, idesc_sn, idesc_u;   // scores (N = NC), negated scores, updates (N = D)
+    uint32_t nkk;                          // NC / 16
+    uint32_t abias, bbias, bgroup;
+    int nbg[3], abase[3], bbase[3];
+
+    __device__ static __forceinline__ uint64_t at(uint64_t base, uint32_t addr) { return base + (addr >> 4); }
+
+    __device__ void init(const TcParams& p, uint8_t* smem, const TcLayout& lay) {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        sbase = smem_u32(smem);
+        dk = sdesc(0u, 16u, sbo, lay_);
+        dp = sdesc(0u, 16u, 512u, 4u);
+        dmn = sdesc(0u, 16u * rowb, sbo, lay_);
+        dbias = sdesc(0u, 16u, 256u, 6u);
+        idesc_s = idesc_bf16(128, p.plan.NC, false, false);
+        idesc_sn = idesc_s | (1u << 13);
+        idesc_u = idesc_bf16(128, D, false, true);
+        nkk = static_cast<uint32_t>(p.plan.NC) / 16u;
+        abias = sbase + lay.abias;
+        bbias = sbase + lay.bbias;
+        bgroup = lay.bgroup;
+        const BiasGeom bg = bias_geom(p.plan);
+        for (int a = 0; a < 3; ++a) {
+            nbg[a] = bg.nbg[a];
+            abase[a] = bg.abase[a];
+            bbase[a] = bg.bbase[a];
+        }
+    }
 
     // D_tmem = A_tile(128 x D) * B_chunk(NC x D)^T, both K-major; A negated when `neg`.
-    __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_bf16(128, p.plan.NC, false, false) | (neg ? (1u << 13) : 0u);
-        const uint32_t a = smem_u32(smem + a_off), b = smem_u32(smem + b_off);
+    __device__ __forceinline__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
+        const uint32_t a = sbase + a_off, b = sbase + b_off, id = neg ? idesc_sn : idesc_s;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16(d_tmem, sdesc(a + kk * 32u, 16u, sbo, lay_), sdesc(b + kk * 32u, 16u, sbo, lay_), idesc,
-                      kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(d_tmem, at(dk, a + kk * 32u), at(dk, b + kk * 32u), id, kk > 0);
     }
     // D_tmem += A_bias(chunk) * B_bias^T along every masked axis: the window mask.
-    __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
-        const uint32_t idesc = idesc_bf16(128, p.plan.NC, false, false);
-        const uint32_t a = smem_u32(smem + lay.abias), b = smem_u32(smem + lay.bbias);
-        for (int ax = 0; ax < 3; ++ax)
-            for (int q = 0; q < bg.nbg[ax]; ++q) {
-                const uint32_t ga = static_cast<uint32_t>(bg.abase[ax] + k.ix[ax] * bg.nbg[ax] + q);
-                const uint32_t gb = static_cast<uint32_t>(bg.bbase[ax] + q);
-                umma_bf16(d_tmem, sdesc(a + ga * 4096u, 16u, 256u, 6u), sdesc(b + gb * lay.bgroup, 16u, 256u, 6u),
-                          idesc, 1u);
-            }
+    __device__ __forceinline__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
+#pragma unroll
+        for (int ax = 0; ax < 3; ++ax) {
+            if (nbg[ax] == 0) continue;
+            const uint32_t ga = abias + static_cast<uint32_t>(abase[ax] + k.ix[ax] * nbg[ax]) * 4096u;
+            const uint32_t gb = bbias + static_cast<uint32_t>(bbase[ax]) * bgroup;
+            umma_bf16(d_tmem, at(dbias, ga), at(dbias, gb), idesc_s, 1u);
+            if (nbg[ax] > 1) umma_bf16(d_tmem, at(dbias, ga + 4096u), at(dbias, gb + bgroup), idesc_s, 1u);
+        }
     }
     // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major.
-    __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_bf16(128, D, false, true);
-        const uint32_t a = smem_u32(smem + p_off), b = smem_u32(smem + b_off);
-        for (int kk = 0; kk < p.plan.NC / 16; ++kk) {
-            const uint64_t ad = sdesc(a + (kk >> 1) * 8192u + (kk & 1) * 32u, 16u, 512u, 4u);
-            const uint64_t bd = sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_);
-            umma_bf16(d_tmem, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    __device__ __forceinline__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
+        uint32_t a = sbase + p_off, b = sbase + b_off;
+        for (uint32_t kk = 0; kk < nkk; ++kk) {
+            umma_bf16(d_tmem, at(dp, a), at(dmn, b), idesc_u, (accumulate || kk > 0) ? 1u : 0u);
+            a += (kk & 1u) ? 8192u - 32u : 32u;
+            b += 16u * D * 2u;
         }
     }
 };
@@ -692,7 +720,8 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     constexpr uint32_t kPB = pbufs_of(WHICH);
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
-    const MmaIssuer<D> mi{p, smem, lay, bias_geom(pl)};
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
     const bool neg = p.neg != 0;
     TileIter it = tile_iter_begin(p);
     bool started = false;
@@ -768,6 +797,79 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
             break;
         }
         __nanosleep(32);
+    }
+}
+
+// Backward: the score products of every chunk, issued by one lane (S or S^T, the window bias, dP).
+template <int D, int WHICH>
+__device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr uint32_t kS = stages_of(WHICH, D);
+    unsigned* err = p.err;
+    const TilePlan& pl = p.plan;
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
+    const bool neg = p.neg != 0;
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const uint32_t qs = j & 1;
+        if (!mbar_wait(&bars[kQFull + qs], (j >> 1) & 1, err, kSiteQ)) break;
+        ChunkCursor cur = cursor_begin();
+        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+            const uint32_t s = g % kS, sb = g & 1;
+            ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
+            if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            if (!ok) break;
+            tc_fence_after();
+            mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S or S^T
+            mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
+            mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP or dP^T
+            umma_commit(&bars[kSFull + sb]);
+            if (ci == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
+        }
+        ++j;
+    }
+}
+
+// Backward: one update accumulator's products of every chunk, issued by one lane.  `u` selects the
+// product: dQ += dS K (dQ kernel); dV += P^T dO (u = 0) or dK += dS^T Q (u = 1) (dK/dV kernel).
+// Each issuer arrives once on the chunk-slot, P-buffer and accumulator barriers (their counts are
+// the number of issuers).  The chunk slot is also read by the score products, which are complete
+// before the P operand (written after their results were read) exists.
+template <int D, int WHICH>
+__device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem,
+                            int u) {
+    constexpr uint32_t kS = stages_of(WHICH, D);
+    constexpr uint32_t kPB = pbufs_of(WHICH);
+    unsigned* err = p.err;
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    const uint32_t op_p = WHICH == 2 ? static_cast<uint32_t>(u) : 0u;              // P^T or dS^T
+    const uint32_t op_b = WHICH == 1 ? 0u : (u == 0 ? 1u : 0u);                    // K; dO or Q
+    const uint32_t acc_off = WHICH == 2 && u == 1 ? static_cast<uint32_t>(D) : 0u;  // dK beside dV
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const uint32_t ob = j & 1;
+        const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + acc_off;
+        for (int ci = 0; ci < c.C; ++ci, ++g) {
+            const uint32_t s = g % kS, pb = g % kPB;
+            ok = mbar_wait(&bars[kPFull + pb], (g / kPB) & 1, err, kSiteP);
+            if (ok && ci == 0 && j >= 2) ok = mbar_wait(&bars[kOEmpty + ob], ((j >> 1) - 1) & 1, err, kSitePV);
+            if (!ok) break;
+            tc_fence_after();
+            mi.p_x_chunk(acc, lay.p(pb, op_p), lay.chunk(s, op_b), ci > 0);
+            umma_commit(&bars[kPEmpty + pb]);
+            umma_commit(&bars[kKVEmpty + s]);
+            if (ci == c.C - 1) umma_commit(&bars[kOFull + ob]);
+        }
+        ++j;
     }
 }
 
@@ -1224,18 +1326,18 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kQEmpty + i], 1);
         mbar_init(&bars[kSFull + i], 1);
         mbar_init(&bars[kSEmpty + i], kSoft);
-        mbar_init(&bars[kOFull + i], 1);
+        mbar_init(&bars[kOFull + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
         mbar_init(&bars[kOEmpty + i], kSoft);
     }
     for (int i = 0; i < pbufs_of(WHICH); ++i) {
         mbar_init(&bars[kPFull + i], kSoft);
-        mbar_init(&bars[kPEmpty + i], 1);
+        mbar_init(&bars[kPEmpty + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
     for (int s = 0; s < stages_of(WHICH, D); ++s) {
         mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
-        mbar_init(&bars[kKVEmpty + s], 1);
+        mbar_init(&bars[kKVEmpty + s], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
-    mbar_init(&bars[kFin], 1);
+    mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
     fence_barrier_init();
 }
 
@@ -1270,7 +1372,13 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     if (warp == kSoftWarps) {
         producer_loop<D, WHICH>(p, smem, lay, bars);
     } else if (warp == kSoftWarps + 1) {
-        if (lane == 0) mma_loop<D, WHICH>(p, smem, lay, bars, tmem);
+        if (lane == 0) {
+            if (WHICH == 0) mma_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            else score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftWarps + 2) {
+        if (lane == 0) update_loop<D, WHICH>(p, smem, lay, bars, tmem, warp - (kSoftWarps + 2));
         __syncwarp();
     } else if (WHICH == 0) {
         fwd_softmax_loop<D>(p, smem, lay, bars, tmem);
@@ -1278,8 +1386,8 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         bwd_softmax_loop<D, WHICH>(p, smem, lay, bars, tmem);
     }
 
-    // teardown: every MMA of this CTA done before TMEM is freed
-    if (warp == kSoftWarps + 1 && lane == 0) {
+    // teardown: every MMA of this CTA done before TMEM is freed (each issuing lane commits once)
+    if (warp >= kSoftWarps + 1 && lane == 0) {
         umma_commit(&bars[kFin]);
         mbar_wait(&bars[kFin], 0, p.err, kSiteFinal);
     }
