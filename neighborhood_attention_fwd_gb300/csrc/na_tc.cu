@@ -43,12 +43,14 @@ namespace {
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
-constexpr int kMaxStages = 3;
+constexpr int kMaxStages = 4;
 
 // Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
-// the copy latency; dQ has the shared memory for a third P buffer (more slack between unevenly
-// loaded softmax warps), the forward (two CTAs per SM) and dK/dV (two P operands) do not.
-__host__ __device__ constexpr int stages_of(int which, int D) { return (void)which, D <= 32 ? 3 : 2; }
+// the copy latency.  dQ has the shared memory for a fourth chunk stage and a third P buffer (more
+// slack between unevenly loaded softmax warps).  The forward (two CTAs per SM) does not, and dK/dV
+// (two P operands) measured slower with a fourth stage: its per-column LSE/Delta gathers go
+// through L1, which shrinks as shared memory grows.
+__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
 constexpr int kMaxPBufs = 3;
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
@@ -694,6 +696,48 @@ struct MmaIssuer {
     }
 };
 
+// The forward's issuer: descriptors built in each call from the parameters.  (The forward's single
+// MMA lane runs a polling loop; measured on the 2048x2048 / 13x13 problem this form issues faster
+// there than the precomputed-descriptor form the backward issuers use.)
+template <int D>
+struct FwdIssuer {
+    const TcParams& p;
+    uint8_t* smem;
+    const TcLayout& lay;
+    BiasGeom bg;
+
+    __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_bf16(128, p.plan.NC, false, false) | (neg ? (1u << 13) : 0u);
+        const uint32_t a = smem_u32(smem + a_off), b = smem_u32(smem + b_off);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16(d_tmem, sdesc(a + kk * 32u, 16u, sbo, lay_), sdesc(b + kk * 32u, 16u, sbo, lay_), idesc,
+                      kk > 0);
+    }
+    __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
+        const uint32_t idesc = idesc_bf16(128, p.plan.NC, false, false);
+        const uint32_t a = smem_u32(smem + lay.abias), b = smem_u32(smem + lay.bbias);
+        for (int ax = 0; ax < 3; ++ax)
+            for (int q = 0; q < bg.nbg[ax]; ++q) {
+                const uint32_t ga = static_cast<uint32_t>(bg.abase[ax] + k.ix[ax] * bg.nbg[ax] + q);
+                const uint32_t gb = static_cast<uint32_t>(bg.bbase[ax] + q);
+                umma_bf16(d_tmem, sdesc(a + ga * 4096u, 16u, 256u, 6u), sdesc(b + gb * lay.bgroup, 16u, 256u, 6u),
+                          idesc, 1u);
+            }
+    }
+    __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_bf16(128, D, false, true);
+        const uint32_t a = smem_u32(smem + p_off), b = smem_u32(smem + b_off);
+        for (int kk = 0; kk < p.plan.NC / 16; ++kk) {
+            const uint64_t ad = sdesc(a + (kk >> 1) * 8192u + (kk & 1) * 32u, 16u, 512u, 4u);
+            const uint64_t bd = sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_);
+            umma_bf16(d_tmem, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        }
+    }
+};
+
 // TMEM column bases.  fwd (256 columns): S[b] at b*NC, O[b] at 256 - (2 - b) * D.
 // dQ (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dQ[b] at 512 - (2 - b) * D.
 // dKdV (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dV[b] at 512 - (4 - 2b) * D, dK[b] = dV[b] + D.
@@ -720,8 +764,7 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     constexpr uint32_t kPB = pbufs_of(WHICH);
     unsigned* err = p.err;
     const TilePlan& pl = p.plan;
-    MmaIssuer<D> mi;
-    mi.init(p, smem, lay);
+    const FwdIssuer<D> mi{p, smem, lay, bias_geom(pl)};
     const bool neg = p.neg != 0;
     TileIter it = tile_iter_begin(p);
     bool started = false;
