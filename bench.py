@@ -13,6 +13,7 @@ Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead (b
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -45,7 +46,7 @@ def useful_flops(w):
 
 def kernel_bytes(w):
     """Algorithmic bytes each kernel must move (read inputs once, write outputs once)."""
-    s = 2 if w.dtype == "bf16" else 4
+    s = 2 if w.dtype in ("bf16", "fp16") else 4
     rows = float(w.tokens) * w.heads
     t = rows * w.D * s
     return {"fwd": 4 * t + 4 * rows,            # q, k, v in; o out; lse out
@@ -56,7 +57,7 @@ def kernel_bytes(w):
 
 def method_bytes(w):
     """Bytes of the method per phase (forward: q,k,v,o,lse; backward: q,k,v,o,dO,dQ,dK,dV,lse,delta)."""
-    s = 2 if w.dtype == "bf16" else 4
+    s = 2 if w.dtype in ("bf16", "fp16") else 4
     rows = float(w.tokens) * w.heads
     return 4 * rows * w.D * s + 4 * rows, 8 * rows * w.D * s + 12 * rows
 
@@ -64,7 +65,7 @@ def method_bytes(w):
 def arithmetic_intensity(w, fused=True, elem_bytes=None):
     """Forward FLOP per byte: q, k, v read and o written once; the unfused chain also writes the
     attention weights once (QK op) and reads them once (AV op)."""
-    s = elem_bytes or (2 if w.dtype == "bf16" else 4)
+    s = elem_bytes or (2 if w.dtype in ("bf16", "fp16") else 4)
     rows = float(w.tokens) * w.heads
     flops = 4.0 * rows * w.keys_per_query * w.D
     nbytes = 4.0 * rows * w.D * s
@@ -308,7 +309,7 @@ def run_ours(args, w, rank, world, dist):
     ten = peaks["bf16_tflops"] * 1e12
     kb = kernel_bytes(w)
     tile_flops = {"fwd": 0.0, "delta": 0.0, "dq": 0.0, "dkdv": 0.0}
-    if w.dtype == "bf16":
+    if w.dtype in ("bf16", "fp16"):
         for which, name in ((0, "fwd"), (1, "dq"), (2, "dkdv")):
             tile_flops[name] = float(na.na_plan_info(which, w.B, w.spatial, w.heads, w.D, w.kernel,
                                                      w.dilation)["mma_flops"])
@@ -452,6 +453,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
+                    help="run a bf16 workload's shapes with fp16 tensors instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -459,6 +462,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = nain.WORKLOADS[args.workload]
+    if args.dtype and args.dtype != w.dtype:
+        if w.dtype != "bf16":
+            ap.error("--dtype applies to the bf16 workloads")
+        w = dataclasses.replace(w, name=w.name.replace("bf16", args.dtype), dtype=args.dtype)
 
     if args.impl == "reference":
         if rank == 0:

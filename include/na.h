@@ -41,7 +41,10 @@ extern "C" {
 
 typedef enum {
     NA_BF16 = 0, /* bfloat16 tensors; tcgen05 tensor-core kernels, fp32 accumulation */
-    NA_FP32 = 1  /* float32 tensors; CUDA-core FMA kernels, fp32 throughout */
+    NA_FP32 = 1, /* float32 tensors; CUDA-core FMA kernels, fp32 throughout */
+    NA_FP16 = 2  /* float16 tensors; the same tensor-core kernels as NA_BF16 with fp16 operands (P and
+                    dS are rounded to fp16), fp32 accumulation.  The kernels mask keys outside a
+                    window with a -65504 bias, so |scale * q.k| must stay below 3.2e4. */
 } na_dtype;
 
 typedef enum {
@@ -61,8 +64,8 @@ typedef enum {
  *   (every residue class holds at least k positions); scale finite (the workloads use D^-0.5).
  *   Every tensor pointer 16-byte aligned.
  * Supported (else NA_ERR_UNSUPPORTED):
- *   NA_BF16: D in {16, 32, 64}; dilation[a] <= 8; per-axis halos within the TMA box limit.
- *   NA_FP32: D a multiple of 4, D <= 128.
+ *   NA_BF16, NA_FP16: D in {16, 32, 64}; dilation[a] <= 8; per-axis halos within the TMA box limit.
+ *   NA_FP32: D in {16, 32, 64, 128}.
  */
 na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int ndim, const int* spatial, int heads, int D,

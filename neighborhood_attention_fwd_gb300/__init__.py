@@ -22,7 +22,7 @@ __all__ = [
     "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
 ]
 
-NA_BF16, NA_FP32 = 0, 1
+NA_BF16, NA_FP32, NA_FP16 = 0, 1, 2
 _STATUS = {0: "NA_OK", 1: "NA_ERR_INVALID_ARG", 2: "NA_ERR_UNSUPPORTED", 3: "NA_ERR_ALIGNMENT",
            4: "NA_ERR_CUDA", 5: "NA_ERR_TIMEOUT", 6: "NA_ERR_WORKSPACE"}
 
@@ -83,7 +83,9 @@ def _dtype_code(t: torch.Tensor) -> int:
         return NA_BF16
     if t.dtype == torch.float32:
         return NA_FP32
-    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+    if t.dtype == torch.float16:
+        return NA_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16, float16 or float32")
 
 
 def _geometry(q: torch.Tensor):

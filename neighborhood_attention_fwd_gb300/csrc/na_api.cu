@@ -321,7 +321,7 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
 
 // Tensor map over a [B, L0, L1, L2, heads, D] bf16 tensor whose box is `e` class positions per axis
 // (element stride = dilation) and D channels of one head.
-na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int e[3]) {
+na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int e[3], bool f16) {
     const cuuint64_t es = 2;
     const cuuint64_t hd = static_cast<cuuint64_t>(g.heads) * g.D;
     cuuint64_t dims[5] = {hd, static_cast<cuuint64_t>(g.L[2]), static_cast<cuuint64_t>(g.L[1]),
@@ -336,7 +336,7 @@ na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int 
     const int rowb = g.D * 2;
     const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                               : (rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+    const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? NA_OK : NA_ERR_CUDA;
@@ -395,7 +395,7 @@ na::FmaParams fma_params(const Geom& g, float scale) {
 
 na_status check_dtype(na_dtype dt, const Geom& g) {
     if (dt == NA_FP32) return (g.D == 16 || g.D == 32 || g.D == 64 || g.D == 128) ? NA_OK : NA_ERR_UNSUPPORTED;
-    if (dt == NA_BF16) return NA_OK;
+    if (dt == NA_BF16 || dt == NA_FP16) return NA_OK;
     return NA_ERR_INVALID_ARG;
 }
 
@@ -423,12 +423,13 @@ na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     }
     na::TcParams p;
     if ((st = tc_common(0, g, scale, p)) != NA_OK) return st;
+    p.f16 = dtype == NA_FP16 ? 1u : 0u;
     const TilePlan& pl = p.plan;
     const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
-    if ((st = encode_map(&p.tm[0], q, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[1], k, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[2], v, g, chunk)) != NA_OK) return st;
-    p.out0 = static_cast<__nv_bfloat16*>(o);
+    if ((st = encode_map(&p.tm[0], q, g, pl.T, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], k, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], v, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    p.out0 = static_cast<uint16_t*>(o);
     p.lse_out = lse;
     return cuda_status(na::launch_fwd_tc(p, s));
 }
@@ -450,13 +451,13 @@ na_status na_bwd_delta(const void* o, const void* dO, float* delta, int B, int n
     na_status st = make_geom(B, ndim, spatial, heads, D, ones, ones, g);
     if (st != NA_OK) return st;
     if ((st = check_dtype(dtype, g)) != NA_OK) return st;
-    if (dtype == NA_BF16 && (D % 8 != 0 || D > 256)) return NA_ERR_UNSUPPORTED;
+    if (dtype != NA_FP32 && (D % 8 != 0 || D > 256)) return NA_ERR_UNSUPPORTED;
     if ((st = check_ptrs({o, dO, delta})) != NA_OK) return st;
     na::FmaParams p = fma_params(g, 1.f);
     p.o = o;
     p.dO = dO;
     p.out0 = delta;
-    return cuda_status(na::launch_delta(p, dtype == NA_BF16, static_cast<cudaStream_t>(stream)));
+    return cuda_status(na::launch_delta(p, dtype == NA_BF16 ? 0 : (dtype == NA_FP16 ? 2 : 1), static_cast<cudaStream_t>(stream)));
 }
 
 na_status na_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse, const float* delta,
@@ -482,13 +483,14 @@ na_status na_bwd_dq(const void* q, const void* k, const void* v, const void* dO,
     }
     na::TcParams p;
     if ((st = tc_common(1, g, scale, p)) != NA_OK) return st;
+    p.f16 = dtype == NA_FP16 ? 1u : 0u;
     const TilePlan& pl = p.plan;
     const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
-    if ((st = encode_map(&p.tm[0], q, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[1], dO, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[2], k, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[3], v, g, chunk)) != NA_OK) return st;
-    p.out0 = static_cast<__nv_bfloat16*>(dQ);
+    if ((st = encode_map(&p.tm[0], q, g, pl.T, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], dO, g, pl.T, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], k, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[3], v, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    p.out0 = static_cast<uint16_t*>(dQ);
     p.lse = lse;
     p.delta = delta;
     return cuda_status(na::launch_dq_tc(p, s));
@@ -518,14 +520,15 @@ na_status na_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
     }
     na::TcParams p;
     if ((st = tc_common(2, g, scale, p)) != NA_OK) return st;
+    p.f16 = dtype == NA_FP16 ? 1u : 0u;
     const TilePlan& pl = p.plan;
     const int chunk[3] = {pl.G[0], pl.G[1], pl.G[2]};
-    if ((st = encode_map(&p.tm[0], k, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[1], v, g, pl.T)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[2], q, g, chunk)) != NA_OK) return st;
-    if ((st = encode_map(&p.tm[3], dO, g, chunk)) != NA_OK) return st;
-    p.out0 = static_cast<__nv_bfloat16*>(dK);
-    p.out1 = static_cast<__nv_bfloat16*>(dV);
+    if ((st = encode_map(&p.tm[0], k, g, pl.T, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[1], v, g, pl.T, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[2], q, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    if ((st = encode_map(&p.tm[3], dO, g, chunk, p.f16 != 0)) != NA_OK) return st;
+    p.out0 = static_cast<uint16_t*>(dK);
+    p.out1 = static_cast<uint16_t*>(dV);
     p.lse = lse;
     p.delta = delta;
     return cuda_status(na::launch_dkdv_tc(p, s));
@@ -541,7 +544,7 @@ na_status na_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
     if ((st = check_dtype(dtype, g)) != NA_OK) return st;
     if ((st = check_ptrs({q, k, v, o, dO, lse, dQ, dK, dV})) != NA_OK) return st;
-    if (dtype == NA_BF16) {  // reject unsupported problems before anything is enqueued
+    if (dtype != NA_FP32) {  // reject unsupported problems before anything is enqueued
         na::TcParams probe;
         if ((st = tc_common(1, g, scale, probe)) != NA_OK) return st;
         if ((st = tc_common(2, g, scale, probe)) != NA_OK) return st;
@@ -581,7 +584,7 @@ na_status na_bwd_noalloc(const void* q, const void* k, const void* v, const void
     if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
     if ((st = check_dtype(dtype, g)) != NA_OK) return st;
     if ((st = check_ptrs({q, k, v, o, dO, lse, dQ, dK, dV})) != NA_OK) return st;
-    if (dtype == NA_BF16) {
+    if (dtype != NA_FP32) {
         na::TcParams probe;
         if ((st = tc_common(1, g, scale, probe)) != NA_OK) return st;
         if ((st = tc_common(2, g, scale, probe)) != NA_OK) return st;

@@ -9,6 +9,8 @@
 // overlap instead of tiling through shared memory.
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "na_device.cuh"
 #include "na_internal.h"
 
@@ -290,21 +292,25 @@ int launch_dkdv_fma(const FmaParams& p, cudaStream_t s) {
     }
 }
 
-int launch_delta(const FmaParams& p, bool bf16, cudaStream_t s) {
+int launch_delta(const FmaParams& p, int elem, cudaStream_t s) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
     if (rows == 0) return 0;
-    const int per = bf16 ? 8 : 4;
+    const int per = elem == 1 ? 4 : 8;  // elements per 16-byte load
     const int G = p.D / per;
     const long long rows_per_block = (256 / 32) * (32 / G);
     long long blocks = (rows + rows_per_block - 1) / rows_per_block;
     if (blocks > 152LL * 16) blocks = 152LL * 16;  // grid-stride: 16 resident blocks per SM
-    if (bf16)
-        delta_kernel<__nv_bfloat16><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s>>>(
-            static_cast<const __nv_bfloat16*>(p.o), static_cast<const __nv_bfloat16*>(p.dO),
-            static_cast<float*>(p.out0), rows, p.D);
+    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
+    if (elem == 0)
+        delta_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(p.o),
+                                                           static_cast<const __nv_bfloat16*>(p.dO),
+                                                           static_cast<float*>(p.out0), rows, p.D);
+    else if (elem == 2)
+        delta_kernel<__half><<<grid, block, 0, s>>>(static_cast<const __half*>(p.o), static_cast<const __half*>(p.dO),
+                                                    static_cast<float*>(p.out0), rows, p.D);
     else
-        delta_kernel<float><<<dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s>>>(
-            static_cast<const float*>(p.o), static_cast<const float*>(p.dO), static_cast<float*>(p.out0), rows, p.D);
+        delta_kernel<float><<<grid, block, 0, s>>>(static_cast<const float*>(p.o), static_cast<const float*>(p.dO),
+                                                   static_cast<float*>(p.out0), rows, p.D);
     return static_cast<int>(cudaGetLastError());
 }
 

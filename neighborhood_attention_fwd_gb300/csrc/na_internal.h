@@ -48,8 +48,9 @@ struct TcParams {
     uint32_t neg;       // 1 when scale < 0
     uint32_t rad[8];    // mixed radix of the tile index: heads, ntile2, ntile1, ntile0, d2, d1, d0, B
     uint32_t step[8];   // the grid size written in that radix (persistent CTAs step by it)
-    __nv_bfloat16* out0; // fwd: O; dQ: dQ; dK/dV: dK  ([B, L.., heads, D])
-    __nv_bfloat16* out1; // dK/dV: dV
+    uint16_t* out0;     // fwd: O; dQ: dQ; dK/dV: dK  ([B, L.., heads, D], 2-byte elements)
+    uint16_t* out1;     // dK/dV: dV
+    uint32_t f16;       // element type of every tensor of D channels: 0 bf16, 1 fp16
     float* lse_out;     // fwd: [B, L.., heads] natural-log LSE
     const float* lse;   // bwd: forward LSE
     const float* delta; // bwd: Delta = <dO, O>
@@ -75,12 +76,15 @@ struct FmaParams {
 
 // Launchers (defined next to their kernels).  Return a cudaError_t as int.
 int launch_fwd_tc(const TcParams& p, cudaStream_t stream);
+int launch_fwd_tc_f16(const TcParams& p, cudaStream_t stream);
+int launch_dq_tc_f16(const TcParams& p, cudaStream_t stream);
+int launch_dkdv_tc_f16(const TcParams& p, cudaStream_t stream);
 int launch_dq_tc(const TcParams& p, cudaStream_t stream);
 int launch_dkdv_tc(const TcParams& p, cudaStream_t stream);
 int launch_fwd_fma(const FmaParams& p, cudaStream_t stream);
 int launch_dq_fma(const FmaParams& p, cudaStream_t stream);
 int launch_dkdv_fma(const FmaParams& p, cudaStream_t stream);
-int launch_delta(const FmaParams& p, bool bf16, cudaStream_t stream);
+int launch_delta(const FmaParams& p, int elem, cudaStream_t stream);  // elem: 0 bf16, 1 fp32, 2 fp16
 
 // Kernel attributes that depend on the plan (dynamic smem opt-in); called before the launch.
 int prepare_tc_kernel(int which, int D, int smem_bytes);

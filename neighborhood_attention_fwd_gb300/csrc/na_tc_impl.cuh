@@ -1,0 +1,1496 @@
+// na_tc_impl.cuh -- tensor-core (tcgen05 / TMEM / TMA) kernels of libna for bf16 or fp16 tensors on
+// sm_103a: the query-tile forward, the dQ pass over query tiles and the atomic-free dK/dV pass over
+// key tiles.  Included by na_tc.cu (bf16 instantiations) and na_tc_f16.cu (fp16 instantiations).
+//
+// The operation is neighborhood attention as read from NATTEN issue #161 ("Backward pass is very
+// slow towards much tokens and large kernels"): each query attends a per-axis window of k keys of
+// its residue class (dilation d), shifted at the borders, and the Cartesian product over axes.
+// The maintainer's explanation there -- tiled kernels gain their speed by skipping key tiles that
+// are fully masked, and pay for the partially masked ones with software predication in 2D/3D --
+// is the cost this design attacks:
+//   * a tile is 128 rows (a box of queries, or keys) of one (batch, head, residue class);
+//   * the keys (or queries) any row of the tile can touch form a box, the halo; TMA stages it in
+//     chunks (boxes of the halo with element stride = dilation), so nothing outside it is read;
+//   * S = Q K^T and the products with P run on tcgen05 (bf16 in, fp32 accumulators in TMEM);
+//   * the window mask costs the softmax nothing: it is one more tensor-core product per chunk
+//     and axis, S += A_bias B_bias^T, where B_bias holds the one-hot local coordinate of every
+//     chunk column and A_bias, per row, 0 inside the row's window and -2^100 outside.  A_bias
+//     depends on the tile only through its position relative to the borders, so it is built once
+//     and rebuilt only along the axes whose border situation changes;
+//   * each softmax warp owns 32 TMEM lanes (32 rows) and reads, per chunk, only the contiguous run
+//     of 16-column groups that holds the keys of its rows' windows; the rest of its P rows is zero.
+//
+// Pipeline (persistent CTAs, each looping over tiles):
+//   producer warp : TMA of the tile tensors (2-slot ring) and of halo chunks (stage ring); the
+//                   window-bias operand when a tile's border situation differs from the last one
+//   MMA warp      : per chunk the "score" products (and the bias products) into a double-buffered
+//                   TMEM accumulator, then the previous chunk's "update" products into a
+//                   double-buffered tile accumulator
+//   softmax warps : per chunk read scores from TMEM, write P (or dS) to a double-buffered smem
+//                   operand; per tile read the accumulator and store it.
+// Every mbarrier wait is bounded (see na_device.cuh); a wait that gives up records the site in the
+// status word and the CTA stops issuing work.
+#pragma once
+#include <cmath>
+#include <cuda_fp16.h>
+
+#include "na_device.cuh"
+#include "na_internal.h"
+
+namespace na {
+using namespace dev;
+
+namespace {
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
+constexpr int kMaxStages = 4;
+
+// Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
+// the copy latency.  dQ has the shared memory for a fourth chunk stage and a third P buffer (more
+// slack between unevenly loaded softmax warps).  The forward (two CTAs per SM) does not, and dK/dV
+// (two P operands) measured slower with a fourth stage: its per-column LSE/Delta gathers go
+// through L1, which shrinks as shared memory grows.
+__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
+__host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
+constexpr int kMaxPBufs = 3;
+__host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
+// Warps that issue update products: the forward's one MMA warp issues everything; the backward has
+// one issuing warp per update accumulator (dQ; or dV and dK) beside the warp issuing score products.
+// A single lane waits tens of cycles on each tcgen05.mma it issues, so products into independent
+// accumulators are issued by different warps.
+__host__ __device__ constexpr int nupd_of(int which) { return which == 0 ? 0 : (which == 1 ? 1 : 2); }
+__host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2 + nupd_of(which)); }
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Window-bias operands.  Along every axis whose halo is longer than one position, a chunk column's
+// local coordinate (< G[a] <= 32) is one-hot encoded in nbg[a] 16-column groups of the constant
+// operand B; the per-tile operand A holds, for every row, chunk index along the axis and group,
+// 0 where the coordinate is inside the row's window and -2^100 elsewhere.  Both are K-major
+// 16-column blocks with 32-byte swizzle: A groups of 128 rows (4 KB), B groups of NC rows.
+struct BiasGeom {
+    int nbg[3];    // groups per chunk along each axis (0: the axis needs no mask)
+    int abase[3];  // first A group of each axis (A group = abase + chunk index * nbg + group)
+    int bbase[3];  // first B group of each axis
+    int na, nb;    // A groups, B groups
+};
+
+__host__ __device__ inline BiasGeom bias_geom(const TilePlan& pl) {
+    BiasGeom b{};
+    for (int a = 0; a < 3; ++a) {
+        b.nbg[a] = pl.H[a] > 1 ? (pl.G[a] + 15) / 16 : 0;
+        b.abase[a] = b.na;
+        b.bbase[a] = b.nb;
+        b.na += pl.nchk[a] * b.nbg[a];
+        b.nb += b.nbg[a];
+    }
+    return b;
+}
+
+// Element types: bf16 or fp16 operands (the same 2-byte layouts), fp32 accumulation.  The window
+// bias needs 1.0 and a large finite negative value in the operand type.
+__host__ __device__ constexpr uint32_t elem_one(bool f16) { return f16 ? 0x3C00u : 0x3F80u; }  // 1.0
+__host__ __device__ constexpr uint32_t elem_neg(bool f16) { return f16 ? 0xFBFFu : 0xF180u; }  // -65504 / -2^100
+// A chunk maximum below this means "no live key": masked scores are at most the bias plus the
+// largest live |score|, so fp16 operands support |scale q.k| < 3.2e4.
+template <bool F16>
+__host__ __device__ constexpr float masked_below() { return F16 ? -3.2e4f : -1.0e29f; }
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+//   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [S] x {K, V};  P[2]
+//   which 1 (dQ)  : tile ring [2] x {Q, dO}; chunk ring [S] x {K, V};  dS[2]
+//   which 2 (dKdV): tile ring [2] x {K, V};  chunk ring [S] x {Q, dO}; P^T[2], dS^T[2];
+//                   per chunk slot the -LSE (log2 units) and Delta of the chunk's queries
+//   all: window-bias operands A (per tile) and B (constant).
+struct TcLayout {
+    uint32_t tile0, tile_slot, tile_t;     // tile ring: tile0 + slot * tile_slot + tensor * tile_t
+    uint32_t chunk0, chunk_slot, chunk_t;  // chunk ring
+    uint32_t p0, p_buf, p_op;              // P / dS operands
+    uint32_t abias, bbias, bgroup;         // window-bias operands; bgroup = bytes of one B group
+    uint32_t aux0, aux_slot;               // dK/dV: per chunk slot -LSE (log2) and Delta
+    uint32_t bars, total;
+    __host__ __device__ uint32_t tile(uint32_t slot, uint32_t t) const { return tile0 + slot * tile_slot + t * tile_t; }
+    __host__ __device__ uint32_t chunk(uint32_t slot, uint32_t t) const {
+        return chunk0 + slot * chunk_slot + t * chunk_t;
+    }
+    __host__ __device__ uint32_t p(uint32_t buf, uint32_t op) const { return p0 + buf * p_buf + op * p_op; }
+    __host__ __device__ uint32_t aux(uint32_t slot) const { return aux0 + slot * aux_slot; }
+};
+
+__host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int D) {
+    const uint32_t tile = align_up(128u * D * 2u, 1024);
+    const uint32_t chunk = align_up(static_cast<uint32_t>(pl.NC) * D * 2u, 1024);
+    const uint32_t pbytes = static_cast<uint32_t>((pl.NC + 31) / 32) * 8192u;
+    const uint32_t ntile = which == 0 ? 1 : 2, nop = which == 2 ? 2 : 1;
+    const BiasGeom bg = bias_geom(pl);
+    TcLayout L{};
+    uint32_t o = 0;
+    L.tile0 = o;
+    L.tile_t = tile;
+    L.tile_slot = ntile * tile;
+    o += 2 * L.tile_slot;
+    L.chunk0 = o;
+    L.chunk_t = chunk;
+    L.chunk_slot = 2 * chunk;
+    o += stages_of(which, D) * L.chunk_slot;
+    L.p0 = o;
+    L.p_op = pbytes;
+    L.p_buf = nop * pbytes;
+    o += pbufs_of(which) * L.p_buf;
+    L.abias = o;
+    o += static_cast<uint32_t>(bg.na) * 4096u;
+    L.bbias = o;
+    L.bgroup = static_cast<uint32_t>(pl.NC) * 32u;
+    o += align_up(static_cast<uint32_t>(bg.nb) * L.bgroup, 1024);
+    L.aux0 = o;
+    L.aux_slot = which == 2 ? align_up(8u * static_cast<uint32_t>(pl.NC), 128) : 0u;
+    o += align_up(stages_of(which, D) * L.aux_slot, 1024);
+    L.bars = o;
+    o += 512;
+    L.total = o;
+    return L;
+}
+
+// mbarrier indices
+enum Bar {
+    kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kMaxStages, kSFull = 4 + 2 * kMaxStages,
+    kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + kMaxPBufs, kOFull = kPEmpty + kMaxPBufs,
+    kOEmpty = kOFull + 2,
+    kFin = kOEmpty + 2, kNumBars = kFin + 1
+};
+
+// ---------------------------------------------------------------------------------------------
+// Tile stream and tile geometry
+// ---------------------------------------------------------------------------------------------
+
+// Position in the mixed-radix tile index (digits: head, tile2, tile1, tile0, class2, class1,
+// class0, batch).  A persistent CTA starts at blockIdx.x and steps by the grid size, adding the
+// grid size's digits with carries instead of dividing.
+struct TileIter {
+    uint32_t dig[8];
+    uint32_t lin;
+};
+
+__device__ __forceinline__ TileIter tile_iter_begin(const TcParams& p) {
+    TileIter it;
+    uint32_t x = blockIdx.x;
+    it.lin = x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        it.dig[i] = x % p.rad[i];
+        x /= p.rad[i];
+    }
+    return it;
+}
+
+__device__ __forceinline__ void tile_iter_next(const TcParams& p, TileIter& it) {
+    uint32_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t v = it.dig[i] + p.step[i] + carry;
+        carry = v >= p.rad[i] ? 1u : 0u;
+        it.dig[i] = carry ? v - p.rad[i] : v;
+    }
+    it.lin += gridDim.x;
+}
+
+// Per-tile decode of (head, tile, residue class, batch) and the halo it needs.
+struct Cta {
+    int h, b;
+    int cls[3], Lc[3], t0[3], h0[3];
+    int nc[3], C;  // chunks actually needed along each axis, and in total
+};
+
+__device__ __forceinline__ int inv_lo(int j, int k) { return j < k ? 0 : j - (k >> 1); }
+__device__ __forceinline__ int inv_hi(int j, int Lc, int k) { return j >= Lc - k ? Lc - 1 : j + (k >> 1); }
+
+__device__ __forceinline__ bool decode_tile(const TcParams& p, int which, const TileIter& it, Cta& c) {
+    const TilePlan& pl = p.plan;
+    c.h = static_cast<int>(it.dig[0]);
+    c.cls[2] = static_cast<int>(it.dig[4]);
+    c.cls[1] = static_cast<int>(it.dig[5]);
+    c.cls[0] = static_cast<int>(it.dig[6]);
+    c.b = static_cast<int>(it.dig[7]);
+    const int t[3] = {static_cast<int>(it.dig[3]), static_cast<int>(it.dig[2]), static_cast<int>(it.dig[1])};
+    bool any = true;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        c.Lc[a] = class_len(p.L[a], p.d[a], c.cls[a]);
+        c.t0[a] = t[a] * pl.T[a];
+        if (c.t0[a] >= c.Lc[a]) any = false;
+    }
+    if (!any) return false;
+    c.C = 1;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const int last = min(c.t0[a] + pl.T[a], c.Lc[a]) - 1;
+        int lo, hi;
+        if (which != 2) {
+            lo = win_start(c.t0[a], c.Lc[a], p.k[a]);
+            hi = win_start(last, c.Lc[a], p.k[a]) + p.k[a] - 1;
+        } else {
+            lo = inv_lo(c.t0[a], p.k[a]);
+            hi = inv_hi(last, c.Lc[a], p.k[a]);
+        }
+        c.h0[a] = min(lo, max(0, c.Lc[a] - pl.H[a]));
+        c.nc[a] = min(pl.nchk[a], (hi - c.h0[a] + pl.G[a]) / pl.G[a]);
+        c.C *= c.nc[a];
+    }
+    return true;
+}
+
+// Next non-empty tile of this persistent CTA.  `started` is false before the first call.
+__device__ __forceinline__ bool next_tile(const TcParams& p, int which, TileIter& it, bool& started, Cta& c) {
+    const uint32_t n = static_cast<uint32_t>(p.plan.ctas);
+    if (started) tile_iter_next(p, it);
+    started = true;
+    while (it.lin < n) {
+        if (decode_tile(p, which, it, c)) return true;
+        tile_iter_next(p, it);
+    }
+    return false;
+}
+
+// Border situation of a tile along one axis: 0 when every row is inside the class, every row's
+// window (or inverse window) is the unclamped one and the halo starts at the window of the tile's
+// first row -- then the rows' ranges relative to the halo are the same for every such tile --
+// otherwise a code of (t0, Lc), which fixes them.
+__device__ __forceinline__ uint64_t axis_sig(int which, int t0, int T, int Lc, int k, int H) {
+    const int r = k >> 1;
+    bool in = t0 + T <= Lc && t0 - r <= Lc - H;
+    if (which != 2) {
+        in = in && t0 >= r && t0 + T - 1 <= Lc - 1 - r;
+    } else {
+        in = in && t0 >= k && t0 + T - 1 < Lc - k;
+    }
+    return in ? 0ull : ((static_cast<uint64_t>(static_cast<uint32_t>(Lc)) << 32) | static_cast<uint32_t>(t0 + 1));
+}
+
+// Per-row geometry: for each axis the halo-coordinate range [lo, lo + len) of keys (fwd, dQ: the
+// query's window) or queries (dK/dV: the queries whose windows hold the key) of this row.  For dQ
+// and dK/dV a row past the end of an axis has len = 0 along that axis (its P row is zero); the
+// range along an axis depends on that axis alone.
+struct RowGeom {
+    int lo[3], len[3];
+    bool valid;
+    long long token;  // flat token index (b * N + spatial), valid rows only
+};
+
+__device__ __forceinline__ RowGeom row_geom(const TcParams& p, int which, const Cta& c, int row) {
+    const TilePlan& pl = p.plan;
+    RowGeom g;
+    // tile extents are powers of two
+    const int s2 = __ffs(pl.T[2]) - 1, s1 = __ffs(pl.T[1]) - 1;
+    const int tq[3] = {row >> (s2 + s1), (row >> s2) & (pl.T[1] - 1), row & (pl.T[2] - 1)};
+    g.valid = true;
+    long long tok = c.b;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        const int j = c.t0[a] + tq[a];
+        const bool in = j < c.Lc[a];
+        if (!in) g.valid = false;
+        const int jc = min(j, c.Lc[a] - 1);
+        if (which != 2) {
+            g.lo[a] = win_start(jc, c.Lc[a], p.k[a]) - c.h0[a];
+            g.len[a] = p.k[a];
+        } else {
+            g.lo[a] = inv_lo(jc, p.k[a]) - c.h0[a];
+            g.len[a] = inv_hi(jc, c.Lc[a], p.k[a]) - inv_lo(jc, p.k[a]) + 1;
+        }
+        if (!in && which != 0) g.len[a] = 0;
+        tok = tok * p.L[a] + (c.cls[a] + p.d[a] * jc);
+    }
+    g.token = tok;
+    return g;
+}
+
+// Warp union of the rows' ranges along each axis (empty when no row of the warp is live).
+struct WarpUnion {
+    int lo[3], hi[3];
+};
+
+__device__ __forceinline__ WarpUnion warp_union(const RowGeom& g) {
+    WarpUnion u;
+    const bool live = g.len[0] > 0 && g.len[1] > 0 && g.len[2] > 0;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        u.lo[a] = warp_min(live ? g.lo[a] : 0x3fffffff);
+        u.hi[a] = warp_max(live ? g.lo[a] + g.len[a] : -0x3fffffff);
+    }
+    return u;
+}
+
+// Bits [lo, hi) of a 32-bit word, lo and hi clamped to [0, 32].
+__device__ __forceinline__ uint32_t range_bits32(int lo, int hi) {
+    lo = max(0, min(32, lo));
+    hi = max(0, min(32, hi));
+    const uint32_t up_hi = hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u);
+    const uint32_t up_lo = lo >= 32 ? 0xffffffffu : ((1u << lo) - 1u);
+    return up_hi & ~up_lo;
+}
+
+// Chunk cursor: chunk indices along each axis and the chunk origin in halo coordinates, stepped in
+// chunk-grid order (axis 0 slowest, axis 2 fastest) without divisions.
+struct ChunkCursor {
+    int ix[3];
+    int o[3];
+};
+__device__ __forceinline__ ChunkCursor cursor_begin() { return ChunkCursor{{0, 0, 0}, {0, 0, 0}}; }
+__device__ __forceinline__ void cursor_next(const TilePlan& pl, const Cta& c, ChunkCursor& k) {
+    ++k.ix[2];
+    k.o[2] += pl.G[2];
+    if (k.ix[2] >= c.nc[2]) {
+        k.ix[2] = 0;
+        k.o[2] = 0;
+        ++k.ix[1];
+        k.o[1] += pl.G[1];
+        if (k.ix[1] >= c.nc[1]) {
+            k.ix[1] = 0;
+            k.o[1] = 0;
+            ++k.ix[0];
+            k.o[0] += pl.G[0];
+        }
+    }
+}
+
+// The run of 16-column groups [glo, glo + n) of a chunk that holds every key (column) inside the
+// union of a warp's windows.  Chunk column = (y * G1 + z) * G2 + x for local coordinates (y, z, x).
+__device__ __forceinline__ void chunk_range(const TilePlan& pl, const ChunkCursor& k, const WarpUnion& u, int& glo,
+                                            int& n) {
+    int lo[3], hi[3];
+    bool empty = false;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = max(u.lo[a] - k.o[a], 0);
+        hi[a] = min(u.hi[a] - k.o[a], pl.G[a]);
+        if (lo[a] >= hi[a]) empty = true;
+    }
+    if (empty) {
+        glo = 0;
+        n = 0;
+        return;
+    }
+    const int clo = (lo[0] * pl.G[1] + lo[1]) * pl.G[2] + lo[2];
+    const int chi = ((hi[0] - 1) * pl.G[1] + hi[1] - 1) * pl.G[2] + hi[2];
+    glo = clo >> 4;
+    n = ((chi + 15) >> 4) - glo;
+}
+
+// bf16 pair for bits (2w, 2w+1) of `bits`: `v` where the bit is set, 0 elsewhere.
+__device__ __forceinline__ uint32_t bf16_pair(uint32_t bits, int w, uint32_t v) {
+    const uint32_t two = (bits >> (2 * w)) & 3u;
+    return ((two & 1u) | ((two & 2u) << 15)) * v;
+}
+
+// Row r of a K-major 16-column bf16 block with 32-byte swizzle (32-byte rows, base 256-byte
+// aligned): element t = `v` where bit t of `bits` is set, 0 elsewhere.
+__device__ __forceinline__ void st_row32(uint32_t blk, int r, uint32_t bits, uint32_t v) {
+    const uint32_t row = blk + static_cast<uint32_t>(r) * 32u;
+    const uint32_t sw = (static_cast<uint32_t>(r) >> 2) & 1u;
+    st_shared_v4(row + (sw << 4), bf16_pair(bits, 0, v), bf16_pair(bits, 1, v), bf16_pair(bits, 2, v),
+                 bf16_pair(bits, 3, v));
+    st_shared_v4(row + ((sw ^ 1u) << 4), bf16_pair(bits, 4, v), bf16_pair(bits, 5, v), bf16_pair(bits, 6, v),
+                 bf16_pair(bits, 7, v));
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
+    const bool ok = mbar_wait(bar, parity, err, site);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Byte offset of block i (columns 8i .. 8i+7) of this row in a K-major operand stored as 32-column
+// atoms (128 rows x 64 B, 64-byte swizzle): rowbase = row * 64, sw = (row >> 1) & 3.
+__device__ __forceinline__ uint32_t p_off(uint32_t rowbase, uint32_t sw, int i) {
+    return static_cast<uint32_t>(i >> 2) * 8192u + rowbase + (((static_cast<uint32_t>(i) & 3u) ^ sw) << 4);
+}
+
+// Packed fp32x2 arithmetic (one instruction for two values).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// Two fp32 values rounded to the operand type, packed (first value in the low half).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        return pack_bf16x2(lo, hi);
+    }
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t x2_of(uint64_t r) {
+    float a, b;
+    f2_split(r, a, b);
+    return pack2<F16>(a, b);
+}
+
+// Instruction descriptor of kind::f16 with fp32 D and bf16 (f16 = false) or fp16 A and B.
+__device__ __forceinline__ uint32_t idesc_mma(int M, int N, bool a_mn, bool b_mn, bool f16) {
+    const uint32_t d = idesc_bf16(M, N, a_mn, b_mn);
+    return f16 ? (d & ~((7u << 7) | (7u << 10))) : d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 32 lanes x 16 consecutive columns of 32 bits (one row per lane), and the register fence that
+// keeps uses of them below the tcgen05.wait::ld.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15])
+                 :
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Window-bias operands (built by the producer warp)
+// ---------------------------------------------------------------------------------------------
+
+// Constant operand B: per chunk column its local coordinate along each masked axis, one-hot.
+__device__ void build_bias_b(const TilePlan& pl, const BiasGeom& bg, uint32_t bbias, uint32_t bgroup, int lane,
+                             bool f16) {
+    for (int key = lane; key < pl.NC; key += 32) {
+        const int loc[3] = {key / (pl.G[2] * pl.G[1]), (key / pl.G[2]) % pl.G[1], key % pl.G[2]};
+        for (int a = 0; a < 3; ++a)
+            for (int q = 0; q < bg.nbg[a]; ++q) {
+                const int t = loc[a] - 16 * q;
+                const uint32_t bits = (t >= 0 && t < 16) ? (1u << t) : 0u;
+                st_row32(bbias + static_cast<uint32_t>(bg.bbase[a] + q) * bgroup, key, bits, elem_one(f16));
+            }
+    }
+}
+
+// Per-tile operand A along the axes in `axes`: for each row, chunk index and group, -2^100 at the
+// coordinates outside the row's range along that axis.
+__device__ void build_bias_a(const TcParams& p, int which, const Cta& c, const BiasGeom& bg, uint32_t abias,
+                             int lane, uint32_t axes) {
+    const uint32_t neg = elem_neg(p.f16 != 0);
+    const TilePlan& pl = p.plan;
+    for (int q = 0; q < 4; ++q) {
+        const int r = lane + 32 * q;
+        const RowGeom rg = row_geom(p, which, c, r);
+        for (int a = 0; a < 3; ++a) {
+            if (!((axes >> a) & 1u)) continue;
+            for (int ch = 0; ch < pl.nchk[a]; ++ch)
+                for (int qq = 0; qq < bg.nbg[a]; ++qq) {
+                    const int o = ch * pl.G[a] + 16 * qq;
+                    const uint32_t nv = ~range_bits32(rg.lo[a] - o, rg.lo[a] + rg.len[a] - o);
+                    const uint32_t grp = static_cast<uint32_t>(bg.abase[a] + ch * bg.nbg[a] + qq);
+                    st_row32(abias + grp * 4096u, r, nv, neg);
+                }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Producer warp: TMA of tile tensors and halo chunks; the window-bias operands; for dK/dV also the
+// per-column LSE / Delta of each chunk.
+// ---------------------------------------------------------------------------------------------
+
+// dK/dV: LSE and Delta of the chunk columns lane + 32 i.  The loads read clamped (always valid)
+// positions and nothing consumes them until the chunk's slot is written, so their latency hides
+// behind the producer's next waits; `in` marks the columns inside the class.
+struct AuxFetch {
+    int loc[4][3];
+    float l[4], dl[4];
+    uint32_t in;
+};
+
+__device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const ChunkCursor& k, AuxFetch& f,
+                                          int lane) {
+    f.in = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j0 = c.h0[0] + k.o[0] + f.loc[i][0], j1 = c.h0[1] + k.o[1] + f.loc[i][1],
+                  j2 = c.h0[2] + k.o[2] + f.loc[i][2];
+        if (lane + 32 * i < p.plan.NC && j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) f.in |= 1u << i;
+        const int c0 = min(j0, c.Lc[0] - 1), c1 = min(j1, c.Lc[1] - 1), c2 = min(j2, c.Lc[2] - 1);
+        const long long tok = ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * c0)) * p.L[1] +
+                               (c.cls[1] + p.d[1] * c1)) * p.L[2] + (c.cls[2] + p.d[2] * c2);
+        f.l[i] = __ldg(p.lse + tok * p.heads + c.h);
+        f.dl[i] = __ldg(p.delta + tok * p.heads + c.h);
+    }
+}
+
+template <int D, int WHICH>
+__device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
+    constexpr int kS = stages_of(WHICH, D);
+    constexpr int ntile = WHICH == 0 ? 1 : 2;
+    constexpr int tmCk = WHICH == 0 ? 1 : 2, tmCv = WHICH == 0 ? 2 : 3;
+    const int lane = threadIdx.x & 31;
+    unsigned* err = p.err;
+    const TilePlan& pl = p.plan;
+    const BiasGeom bg = bias_geom(pl);
+    const uint32_t tile_bytes = 128u * D * 2u, chunk_bytes = static_cast<uint32_t>(pl.NC) * D * 2u;
+    const uint32_t abias = smem_u32(smem + lay.abias);
+
+    build_bias_b(pl, bg, smem_u32(smem + lay.bbias), lay.bgroup, lane, p.f16 != 0);
+    fence_proxy_async_smem();
+    uint32_t built = 0;  // axes whose part of A holds the geometry of sig[]
+    uint64_t sig[3] = {0, 0, 0};
+    AuxFetch f;
+    if (WHICH == 2) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int col = lane + 32 * i;
+            const int cc = min(col, pl.NC - 1);
+            f.loc[i][0] = cc / (pl.G[2] * pl.G[1]);
+            f.loc[i][1] = (cc / pl.G[2]) % pl.G[1];
+            f.loc[i][2] = cc % pl.G[2];
+        }
+    }
+
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const uint32_t qs = j & 1;
+        if (j >= 2) ok = warp_wait(&bars[kQEmpty + qs], ((j >> 1) - 1) & 1, err, kSiteQ);
+        if (!ok) break;
+        // the bias operand A: rebuilt along the axes whose border situation changed, once every
+        // score product of the previous tile (its last reader) is done
+        uint32_t stale = 0;
+        uint64_t ns[3];
+#pragma unroll
+        for (int a = 0; a < 3; ++a) {
+            ns[a] = axis_sig(WHICH, c.t0[a], pl.T[a], c.Lc[a], p.k[a], pl.H[a]);
+            if (bg.nbg[a] > 0 && (!((built >> a) & 1u) || ns[a] != sig[a])) stale |= 1u << a;
+        }
+        if (stale) {
+            if (j >= 1) ok = warp_wait(&bars[kQEmpty + (qs ^ 1u)], ((j - 1) >> 1) & 1, err, kSiteQ);
+            if (!ok) break;
+            build_bias_a(p, WHICH, c, bg, abias, lane, stale);
+            fence_proxy_async_smem();
+#pragma unroll
+            for (int a = 0; a < 3; ++a) sig[a] = ns[a];
+            built |= stale;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[kQFull + qs], ntile * tile_bytes);
+            for (int tt = 0; tt < ntile; ++tt)
+                tma_load_5d(smem + lay.tile(qs, tt), &p.tm[tt], &bars[kQFull + qs], c.h * D,
+                            c.cls[2] + p.d[2] * c.t0[2], c.cls[1] + p.d[1] * c.t0[1], c.cls[0] + p.d[0] * c.t0[0],
+                            c.b);
+        }
+        ChunkCursor cur = cursor_begin();
+        if (WHICH == 2) aux_fetch(p, c, cur, f, lane);
+        for (int ci = 0; ci < c.C; ++ci, ++g) {
+            const uint32_t s = g % kS;
+            if (g >= kS) ok = warp_wait(&bars[kKVEmpty + s], ((g / kS) - 1) & 1, err, kSiteEmpty);
+            if (!ok) break;
+            const int y0 = c.h0[0] + cur.o[0], z0 = c.h0[1] + cur.o[1], x0 = c.h0[2] + cur.o[2];
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[kKVFull + s], 2u * chunk_bytes);
+                tma_load_5d(smem + lay.chunk(s, 0), &p.tm[tmCk], &bars[kKVFull + s], c.h * D,
+                            c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
+                tma_load_5d(smem + lay.chunk(s, 1), &p.tm[tmCv], &bars[kKVFull + s], c.h * D,
+                            c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
+            }
+            if (WHICH == 2) {
+                float* l2 = reinterpret_cast<float*>(smem + lay.aux(s));
+                float* dl = l2 + pl.NC;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int col = lane + 32 * i;
+                    if (col < pl.NC) {
+                        const bool in = (f.in >> i) & 1u;
+                        l2[col] = in ? -f.l[i] * kLog2e : -INFINITY;  // -LSE in log2 units; none outside
+                        dl[col] = in ? f.dl[i] : 0.f;
+                    }
+                }
+            }
+            cursor_next(pl, c, cur);
+            if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, cur, f, lane);  // the next chunk's, in flight
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKVFull + s]);
+        }
+        ++j;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// MMA warp (lane 0): score products per chunk, update products of the previous chunk.
+// ---------------------------------------------------------------------------------------------
+
+// Issues the tensor-core products.  The MMA lane shares its SM sub-partition with softmax warps, so
+// every instruction it spends per MMA counts: descriptors are built once with start address 0 and
+// offset per operand (the start-address field is the low 14 bits of the descriptor and holds
+// address >> 4; shared addresses are below 256 KB), and the instruction descriptors are constant.
+template <int D>
+struct MmaIssuer {
+    uint32_t sbase;                        // shared address of the layout base
+    uint64_t dk, dp, dmn, dbias;           // descriptor bases: K-major rows of D, P atoms, MN-major rows of D, bias blocks
+    uint32_t idesc_s, idesc_sn, idesc_u;   // scores (N = NC), negated scores, updates (N = D)
+    uint32_t nkk;                          // NC / 16
+    uint32_t abias, bbias, bgroup;
+    int nbg[3], abase[3], bbase[3];
+
+    __device__ static __forceinline__ uint64_t at(uint64_t base, uint32_t addr) { return base + (addr >> 4); }
+
+    __device__ void init(const TcParams& p, uint8_t* smem, const TcLayout& lay) {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        sbase = smem_u32(smem);
+        dk = sdesc(0u, 16u, sbo, lay_);
+        dp = sdesc(0u, 16u, 512u, 4u);
+        dmn = sdesc(0u, 16u * rowb, sbo, lay_);
+        dbias = sdesc(0u, 16u, 256u, 6u);
+        idesc_s = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0);
+        idesc_sn = idesc_s | (1u << 13);
+        idesc_u = idesc_mma(128, D, false, true, p.f16 != 0);
+        nkk = static_cast<uint32_t>(p.plan.NC) / 16u;
+        abias = sbase + lay.abias;
+        bbias = sbase + lay.bbias;
+        bgroup = lay.bgroup;
+        const BiasGeom bg = bias_geom(p.plan);
+        for (int a = 0; a < 3; ++a) {
+            nbg[a] = bg.nbg[a];
+            abase[a] = bg.abase[a];
+            bbase[a] = bg.bbase[a];
+        }
+    }
+
+    // D_tmem = A_tile(128 x D) * B_chunk(NC x D)^T, both K-major; A negated when `neg`.
+    __device__ __forceinline__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
+        const uint32_t a = sbase + a_off, b = sbase + b_off, id = neg ? idesc_sn : idesc_s;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(d_tmem, at(dk, a + kk * 32u), at(dk, b + kk * 32u), id, kk > 0);
+    }
+    // D_tmem += A_bias(chunk) * B_bias^T along every masked axis: the window mask.
+    __device__ __forceinline__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
+#pragma unroll
+        for (int ax = 0; ax < 3; ++ax) {
+            if (nbg[ax] == 0) continue;
+            const uint32_t ga = abias + static_cast<uint32_t>(abase[ax] + k.ix[ax] * nbg[ax]) * 4096u;
+            const uint32_t gb = bbias + static_cast<uint32_t>(bbase[ax]) * bgroup;
+            umma_bf16(d_tmem, at(dbias, ga), at(dbias, gb), idesc_s, 1u);
+            if (nbg[ax] > 1) umma_bf16(d_tmem, at(dbias, ga + 4096u), at(dbias, gb + bgroup), idesc_s, 1u);
+        }
+    }
+    // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major.
+    __device__ __forceinline__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
+        uint32_t a = sbase + p_off, b = sbase + b_off;
+        for (uint32_t kk = 0; kk < nkk; ++kk) {
+            umma_bf16(d_tmem, at(dp, a), at(dmn, b), idesc_u, (accumulate || kk > 0) ? 1u : 0u);
+            a += (kk & 1u) ? 8192u - 32u : 32u;
+            b += 16u * D * 2u;
+        }
+    }
+};
+
+// The forward's issuer: descriptors built in each call from the parameters.  (The forward's single
+// MMA lane runs a polling loop; measured on the 2048x2048 / 13x13 problem this form issues faster
+// there than the precomputed-descriptor form the backward issuers use.)
+template <int D>
+struct FwdIssuer {
+    const TcParams& p;
+    uint8_t* smem;
+    const TcLayout& lay;
+    BiasGeom bg;
+
+    __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0) | (neg ? (1u << 13) : 0u);
+        const uint32_t a = smem_u32(smem + a_off), b = smem_u32(smem + b_off);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16(d_tmem, sdesc(a + kk * 32u, 16u, sbo, lay_), sdesc(b + kk * 32u, 16u, sbo, lay_), idesc,
+                      kk > 0);
+    }
+    __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
+        const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0);
+        const uint32_t a = smem_u32(smem + lay.abias), b = smem_u32(smem + lay.bbias);
+        for (int ax = 0; ax < 3; ++ax)
+            for (int q = 0; q < bg.nbg[ax]; ++q) {
+                const uint32_t ga = static_cast<uint32_t>(bg.abase[ax] + k.ix[ax] * bg.nbg[ax] + q);
+                const uint32_t gb = static_cast<uint32_t>(bg.bbase[ax] + q);
+                umma_bf16(d_tmem, sdesc(a + ga * 4096u, 16u, 256u, 6u), sdesc(b + gb * lay.bgroup, 16u, 256u, 6u),
+                          idesc, 1u);
+            }
+    }
+    __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_mma(128, D, false, true, p.f16 != 0);
+        const uint32_t a = smem_u32(smem + p_off), b = smem_u32(smem + b_off);
+        for (int kk = 0; kk < p.plan.NC / 16; ++kk) {
+            const uint64_t ad = sdesc(a + (kk >> 1) * 8192u + (kk & 1) * 32u, 16u, 512u, 4u);
+            const uint64_t bd = sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_);
+            umma_bf16(d_tmem, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        }
+    }
+};
+
+// TMEM column bases.  fwd (256 columns): S[b] at b*NC, O[b] at 256 - (2 - b) * D.
+// dQ (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dQ[b] at 512 - (2 - b) * D.
+// dKdV (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dV[b] at 512 - (4 - 2b) * D, dK[b] = dV[b] + D.
+__device__ __forceinline__ uint32_t tm_s(const TilePlan& pl, uint32_t b) { return b * pl.NC; }
+__device__ __forceinline__ uint32_t tm_dp(const TilePlan& pl, uint32_t b) { return (2 + b) * pl.NC; }
+template <int D>
+__device__ __forceinline__ uint32_t tm_acc(int which, uint32_t b) {
+    return which == 0 ? 256u - (2u - b) * D : (which == 1 ? 512u - (2u - b) * D : 512u - (4u - 2u * b) * D);
+}
+
+struct PendingUpdate {
+    uint32_t g, s, j;
+    int ci, C;
+};
+
+// The MMA lane runs two streams: the score products of the next chunk (as soon as its K/V chunk is
+// loaded and its TMEM score buffer has been read by the softmax warps) and the update products of
+// the oldest scored chunk (as soon as its P operand is written).  Neither waits for the other, so
+// one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
+// after kWaitLimitNs without progress the lane records an error and stops.
+template <int D, int WHICH>
+__device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr int kS = stages_of(WHICH, D);
+    constexpr uint32_t kPB = pbufs_of(WHICH);
+    unsigned* err = p.err;
+    const TilePlan& pl = p.plan;
+    const FwdIssuer<D> mi{p, smem, lay, bias_geom(pl)};
+    const bool neg = p.neg != 0;
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    bool have = next_tile(p, WHICH, it, started, c);
+    uint32_t jS = 0, gS = 0;
+    int ciS = 0;
+    bool qready = false;
+    ChunkCursor cur = cursor_begin();
+    PendingUpdate q0{}, q1{}, q2{};  // scored chunks awaiting their update, oldest first
+    int nq = 0;
+    unsigned long long t_last = globaltimer();
+    for (;;) {
+        bool progress = false;
+        if (nq > 0) {
+            const uint32_t pb = q0.g % kPB, ob = q0.j & 1;
+            if (mbar_test(&bars[kPFull + pb], (q0.g / kPB) & 1) &&
+                (q0.ci != 0 || q0.j < 2 || mbar_test(&bars[kOEmpty + ob], ((q0.j >> 1) - 1) & 1))) {
+                tc_fence_after();
+                const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
+                if (WHICH == 0) {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
+                } else if (WHICH == 1) {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 0), q0.ci > 0);  // dQ += dS K
+                } else {
+                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);      // dV += P^T dO
+                    mi.p_x_chunk(acc + D, lay.p(pb, 1), lay.chunk(q0.s, 0), q0.ci > 0);  // dK += dS^T Q
+                }
+                umma_commit(&bars[kPEmpty + pb]);
+                umma_commit(&bars[kKVEmpty + q0.s]);
+                if (q0.ci == q0.C - 1) umma_commit(&bars[kOFull + ob]);
+                q0 = q1;
+                q1 = q2;
+                --nq;
+                progress = true;
+            }
+        }
+        if (have && nq < 3) {
+            const uint32_t qs = jS & 1, s = gS % kS, sb = gS & 1;
+            if (!qready) qready = mbar_test(&bars[kQFull + qs], (jS >> 1) & 1);
+            if (qready && mbar_test(&bars[kKVFull + s], (gS / kS) & 1) &&
+                (gS < 2 || mbar_test(&bars[kSEmpty + sb], ((gS >> 1) - 1) & 1))) {
+                tc_fence_after();
+                mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
+                mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
+                if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
+                umma_commit(&bars[kSFull + sb]);
+                if (ciS == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
+                const PendingUpdate pu{gS, s, jS, ciS, c.C};
+                if (nq == 0) q0 = pu; else if (nq == 1) q1 = pu; else q2 = pu;
+                ++nq;
+                ++gS;
+                if (++ciS == c.C) {
+                    ciS = 0;
+                    ++jS;
+                    qready = false;
+                    cur = cursor_begin();
+                    have = next_tile(p, WHICH, it, started, c);
+                } else {
+                    cursor_next(pl, c, cur);
+                }
+                progress = true;
+            }
+        }
+        if (!have && nq == 0) break;
+        if (progress) {
+            t_last = globaltimer();
+            continue;
+        }
+        if (ld_volatile(err) != 0u) break;
+        if (globaltimer() - t_last > kWaitLimitNs) {
+            record_error(err, kSiteP);
+            break;
+        }
+        __nanosleep(32);
+    }
+}
+
+// Backward: the score products of every chunk, issued by one lane (S or S^T, the window bias, dP).
+template <int D, int WHICH>
+__device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr uint32_t kS = stages_of(WHICH, D);
+    unsigned* err = p.err;
+    const TilePlan& pl = p.plan;
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
+    const bool neg = p.neg != 0;
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const uint32_t qs = j & 1;
+        if (!mbar_wait(&bars[kQFull + qs], (j >> 1) & 1, err, kSiteQ)) break;
+        ChunkCursor cur = cursor_begin();
+        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+            const uint32_t s = g % kS, sb = g & 1;
+            ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
+            if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            if (!ok) break;
+            tc_fence_after();
+            mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S or S^T
+            mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
+            mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP or dP^T
+            umma_commit(&bars[kSFull + sb]);
+            if (ci == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
+        }
+        ++j;
+    }
+}
+
+// Backward: one update accumulator's products of every chunk, issued by one lane.  `u` selects the
+// product: dQ += dS K (dQ kernel); dV += P^T dO (u = 0) or dK += dS^T Q (u = 1) (dK/dV kernel).
+// Each issuer arrives once on the chunk-slot, P-buffer and accumulator barriers (their counts are
+// the number of issuers).  The chunk slot is also read by the score products, which are complete
+// before the P operand (written after their results were read) exists.
+template <int D, int WHICH>
+__device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem,
+                            int u) {
+    constexpr uint32_t kS = stages_of(WHICH, D);
+    constexpr uint32_t kPB = pbufs_of(WHICH);
+    unsigned* err = p.err;
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    const uint32_t op_p = WHICH == 2 ? static_cast<uint32_t>(u) : 0u;              // P^T or dS^T
+    const uint32_t op_b = WHICH == 1 ? 0u : (u == 0 ? 1u : 0u);                    // K; dO or Q
+    const uint32_t acc_off = WHICH == 2 && u == 1 ? static_cast<uint32_t>(D) : 0u;  // dK beside dV
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const uint32_t ob = j & 1;
+        const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + acc_off;
+        for (int ci = 0; ci < c.C; ++ci, ++g) {
+            const uint32_t s = g % kS, pb = g % kPB;
+            ok = mbar_wait(&bars[kPFull + pb], (g / kPB) & 1, err, kSiteP);
+            if (ok && ci == 0 && j >= 2) ok = mbar_wait(&bars[kOEmpty + ob], ((j >> 1) - 1) & 1, err, kSitePV);
+            if (!ok) break;
+            tc_fence_after();
+            mi.p_x_chunk(acc, lay.p(pb, op_p), lay.chunk(s, op_b), ci > 0);
+            umma_commit(&bars[kPEmpty + pb]);
+            umma_commit(&bars[kKVEmpty + s]);
+            if (ci == c.C - 1) umma_commit(&bars[kOFull + ob]);
+        }
+        ++j;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Epilogue helpers
+// ---------------------------------------------------------------------------------------------
+
+// Store columns [c0, c1) of this thread's accumulator row (fp32 at taddr), times `mul`, as bf16
+// to dst (the row's first element in global memory).
+template <int NCOL, bool F16>
+__device__ __forceinline__ void store_row(uint32_t taddr, float mul, uint16_t* dst, bool valid) {
+    static_assert(NCOL % 8 == 0 && NCOL <= 64, "row slice of 8..64 columns");
+    uint32_t r[NCOL / 8][8];
+#pragma unroll
+    for (int i = 0; i < NCOL / 8; ++i) tmem_ld8(taddr + 8 * i, r[i]);
+    tmem_ld_wait_all();
+#pragma unroll
+    for (int i = 0; i < NCOL / 8; ++i) reg_fence8(r[i]);
+    if (valid) {
+#pragma unroll
+        for (int i = 0; i < NCOL / 8; ++i) {
+            uint4 w;
+            w.x = pack2<F16>(__uint_as_float(r[i][0]) * mul, __uint_as_float(r[i][1]) * mul);
+            w.y = pack2<F16>(__uint_as_float(r[i][2]) * mul, __uint_as_float(r[i][3]) * mul);
+            w.z = pack2<F16>(__uint_as_float(r[i][4]) * mul, __uint_as_float(r[i][5]) * mul);
+            w.w = pack2<F16>(__uint_as_float(r[i][6]) * mul, __uint_as_float(r[i][7]) * mul);
+            *reinterpret_cast<uint4*>(dst + 8 * i) = w;
+        }
+    }
+}
+
+// Zero 16-column group gi of this row in a P operand.
+__device__ __forceinline__ void zero_group(uint32_t sP, uint32_t rowbase, uint32_t sw, int gi) {
+    st_shared_v4(sP + p_off(rowbase, sw, 2 * gi), 0u, 0u, 0u, 0u);
+    st_shared_v4(sP + p_off(rowbase, sw, 2 * gi + 1), 0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Forward softmax warps (4 warps, 128 rows)
+// ---------------------------------------------------------------------------------------------
+
+struct FwdCtx {
+    uint64_t* bars;
+    unsigned* err;
+    uint32_t tS0, tS_step;  // this warp's lanes of score buffer 0, and the offset of buffer 1
+    uint32_t tO;            // this warp's lanes of the tile accumulator
+    uint32_t sP0, sP_step;  // P operand 0, and the offset of operand 1
+    uint32_t rowbase, sw;
+    int ngroups;       // 16-column groups per chunk
+    float sl2;
+    uint64_t sl2x2;
+    int lane;
+};
+
+// Groups [glo, glo + n) as a bit mask.
+__device__ __forceinline__ uint32_t run_mask(int glo, int n) { return ((1u << n) - 1u) << glo; }
+
+// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + N).  `nz` holds
+// the groups of this warp's rows of P buffer g & 1 that may be nonzero (its last run); groups in
+// nz outside the new run are zeroed, and nz becomes the new run.
+template <int D, int N, bool F16>
+__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4],
+                                          uint32_t& nz) {
+    constexpr uint32_t kPB = pbufs_of(0);
+    const uint32_t sb = g & 1, pb = g % kPB;
+    uint32_t v[N > 0 ? N : 1][16];
+    const uint32_t tS = x.tS0 + sb * x.tS_step;
+#pragma unroll
+    for (int i = 0; i < N; ++i) tmem_ld16(tS + 16u * (glo + i), v[i]);
+    if (N > 0) {
+        tmem_ld_wait_all();
+#pragma unroll
+        for (int i = 0; i < N; ++i) reg_fence16(v[i]);
+    }
+    // the score buffer is free for the product of chunk g + 2
+    tc_fence_before();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kSEmpty + sb]);
+    // chunk row max (masked scores carry the -2^100 window bias), four independent chains
+    float cmax = -INFINITY;
+    if (N == 0) {
+        // no key of this warp's rows in the chunk: nothing to read, the running max is unchanged
+    } else {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                mx[e] = fmax3(mx[e], fmaxf(__uint_as_float(v[i][4 * e]), __uint_as_float(v[i][4 * e + 1])),
+                              fmaxf(__uint_as_float(v[i][4 * e + 2]), __uint_as_float(v[i][4 * e + 3])));
+        cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    }
+    // running max (log2 units; the scale's sign is folded into the S product)
+    const float cm2 = cmax > masked_below<F16>() ? cmax * x.sl2 : -INFINITY;  // no live key: -inf
+    const float mnew = fmaxf(m, cm2);
+    const bool rescale = (m != -INFINITY) && (mnew > m + kRescaleThreshold);
+    const float alpha = rescale ? fast_exp2(m - mnew) : 1.f;
+    if (m == -INFINITY || rescale) m = mnew;
+    if (N > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O holds the products of chunks g-1, g-2, ...: wait for the last one
+        if (!warp_wait(&x.bars[kPEmpty + (g - 1) % kPB], ((g - 1) / kPB) & 1, x.err, kSitePV)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 8) {
+            uint32_t r[8];
+            tmem_ld8(x.tO + cc, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st8(x.tO + cc, r);
+        }
+        tmem_st_wait();
+        const uint64_t a2 = f2(alpha, alpha);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) lsum[t] = f2_mul(lsum[t], a2);
+    }
+    const uint32_t run = N > 0 ? run_mask(glo, N) : 0u, stale = nz & ~run;
+    nz = run;
+    if (N == 0 && stale == 0) {  // nothing to write: this warp's rows of the buffer are already zero
+        __syncwarp();
+        if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
+        return true;
+    }
+    // P buffer pb is free once the product of chunk g - kPB is done
+    if (g >= kPB && !warp_wait(&x.bars[kPEmpty + pb], ((g / kPB) - 1) & 1, x.err, kSitePV)) return false;
+    const uint32_t sP = x.sP0 + pb * x.sP_step;
+    const float nm = m == -INFINITY ? 0.f : -m;  // masked scores are -inf: exp2 gives 0
+    const uint64_t nm2 = f2(nm, nm);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            const uint64_t t = f2_fma(f2(__uint_as_float(v[i][e]), __uint_as_float(v[i][e + 1])), x.sl2x2, nm2);
+            float ta, tb;
+            f2_split(t, ta, tb);
+            const uint64_t pe = f2(fast_exp2(ta), fast_exp2(tb));
+            lsum[(e >> 1) & 3] = f2_add(lsum[(e >> 1) & 3], pe);
+            w[e >> 1] = x2_of<F16>(pe);
+        }
+        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i)), w[0], w[1], w[2], w[3]);
+        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i) + 1), w[4], w[5], w[6], w[7]);
+    }
+    for (uint32_t z = stale; z; z &= z - 1) zero_group(sP, x.rowbase, x.sw, __ffs(z) - 1);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
+    return true;
+}
+
+// A tile whose rows still have to be written: O / l -> bf16 and LSE = (m + log2 l) * ln 2.
+struct FwdEpilogue {
+    bool live, valid;
+    float m, l;
+    long long orow;  // row index into [B * tokens * heads]
+    uint32_t ob, j;  // accumulator buffer and tile ordinal
+};
+
+template <int D, bool F16>
+__device__ __forceinline__ bool fwd_epilogue(const TcParams& p, const FwdCtx& x, const FwdEpilogue& e,
+                                             uint32_t tmem_lanes) {
+    if (!warp_wait(&x.bars[kOFull + e.ob], (e.j >> 1) & 1, x.err, kSitePV)) return false;
+    tc_fence_after();
+    store_row<D, F16>(tmem_lanes + tm_acc<D>(0, e.ob), 1.f / e.l, p.out0 + e.orow * D, e.valid);
+    tc_fence_before();
+    __syncwarp();
+    if (x.lane == 0) mbar_arrive(&x.bars[kOEmpty + e.ob]);
+    if (e.valid) p.lse_out[e.orow] = (e.m + __log2f(e.l)) * kLn2;
+    return true;
+}
+
+template <int D, bool F16>
+__device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
+                                 uint32_t tmem) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, row = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const TilePlan& pl = p.plan;
+    FwdCtx x;
+    x.bars = bars;
+    x.err = p.err;
+    x.tS0 = tmem + tm_s(pl, 0) + lane_base;
+    x.tS_step = tm_s(pl, 1) - tm_s(pl, 0);
+    x.sP0 = smem_u32(smem + lay.p(0, 0));
+    x.sP_step = lay.p(1, 0) - lay.p(0, 0);
+    x.rowbase = static_cast<uint32_t>(row) * 64u;
+    x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    x.ngroups = pl.NC >> 4;
+    x.sl2 = p.scale_log2;
+    x.sl2x2 = f2(x.sl2, x.sl2);
+    x.lane = lane;
+    uint32_t nz0 = run_mask(0, x.ngroups), nz1 = nz0, nz2 = nz0;  // groups of the P buffers that may be nonzero
+    FwdEpilogue ep{false, false, 0.f, 0.f, 0, 0, 0};
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && next_tile(p, 0, it, started, c)) {
+        const RowGeom geo = row_geom(p, 0, c, row);
+        const WarpUnion wu = warp_union(geo);
+        const uint32_t ob = j & 1;
+        x.tO = tmem + tm_acc<D>(0, ob) + lane_base;
+        float m = -INFINITY;
+        uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (independent chains)
+        ChunkCursor cur = cursor_begin();
+        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+            ok = warp_wait(&bars[kSFull + (g & 1)], (g >> 1) & 1, x.err, kSiteS);
+            if (!ok) break;
+            tc_fence_after();
+            int glo, n;
+            chunk_range(pl, cur, wu, glo, n);
+            const uint32_t pb = g % pbufs_of(0);
+            uint32_t nz = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
+            switch (n) {
+                case 0: ok = fwd_chunk<D, 0, F16>(x, g, glo, m, lsum, nz); break;
+                case 1: ok = fwd_chunk<D, 1, F16>(x, g, glo, m, lsum, nz); break;
+                case 2: ok = fwd_chunk<D, 2, F16>(x, g, glo, m, lsum, nz); break;
+                case 3: ok = fwd_chunk<D, 3, F16>(x, g, glo, m, lsum, nz); break;
+                default: ok = fwd_chunk<D, 4, F16>(x, g, glo, m, lsum, nz); break;
+            }
+            if (pb == 0) nz0 = nz; else if (pb == 1) nz1 = nz; else nz2 = nz;
+            if (!ok) break;
+        }
+        if (!ok) break;
+        // the previous tile's epilogue, deferred until this tile's chunks are done so that a warp
+        // does not idle at the end of a tile while the slowest warp finishes it
+        if (ep.live && !(ok = fwd_epilogue<D, F16>(p, x, ep, tmem + lane_base))) break;
+        const uint64_t ls = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
+        float la, lb;
+        f2_split(ls, la, lb);
+        ep = FwdEpilogue{true, geo.valid, m, la + lb, geo.token * p.heads + c.h, ob, j};
+        ++j;
+    }
+    if (ok && ep.live) fwd_epilogue<D, F16>(p, x, ep, tmem + lane_base);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Backward softmax warps (8 warps: two warpgroups share each chunk's groups, alternating)
+// ---------------------------------------------------------------------------------------------
+
+struct BwdCtx {
+    uint32_t tS, tP;     // this warp's lanes of the current score / dP buffers
+    uint32_t sP0, sP1;   // P-side operands of the current buffer (dQ: dS; dK/dV: P^T, dS^T)
+    uint32_t rowbase, sw;
+    const float* l2;     // dK/dV: -LSE (log2 units) of the chunk columns
+    const float* dl;     // dK/dV: Delta of the chunk columns
+    uint64_t nl2, dl2;   // dQ: -LSE (log2 units) and Delta of this row, packed twice
+    uint64_t sl2x2;
+};
+
+// This warp's K (<= 2) groups g0, g0 + 2 of the chunk: their scores and dP values are read, the
+// score buffer is released when these are the warp's last groups of the chunk (so the next chunk's
+// products can start), then P = exp2(S sl2 - LSE2) and dS = P (dP - Delta) are formed and stored.
+template <int WHICH, int K, bool F16>
+__device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* sempty, bool release, int lane) {
+    uint32_t rs[K > 0 ? K : 1][16], rp[K > 0 ? K : 1][16];
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        tmem_ld16(x.tS + 16u * (g0 + 2 * i), rs[i]);
+        tmem_ld16(x.tP + 16u * (g0 + 2 * i), rp[i]);
+    }
+    if (K > 0) {
+        tmem_ld_wait_all();
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+            reg_fence16(rs[i]);
+            reg_fence16(rp[i]);
+        }
+    }
+    if (release) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty);
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+        const int gi = g0 + 2 * i;
+        uint32_t a[8], b[8];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            uint64_t nlc[2] = {x.nl2, x.nl2}, dlc[2] = {x.dl2, x.dl2};
+            if (WHICH == 2) {
+                const float4 lv = *reinterpret_cast<const float4*>(x.l2 + 16 * gi + e);
+                const float4 dv = *reinterpret_cast<const float4*>(x.dl + 16 * gi + e);
+                nlc[0] = f2(lv.x, lv.y);
+                nlc[1] = f2(lv.z, lv.w);
+                dlc[0] = f2(dv.x, dv.y);
+                dlc[1] = f2(dv.z, dv.w);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ee = e + 2 * h;
+                const uint64_t t =
+                    f2_fma(f2(__uint_as_float(rs[i][ee]), __uint_as_float(rs[i][ee + 1])), x.sl2x2, nlc[h]);
+                float ta, tb;
+                f2_split(t, ta, tb);
+                const uint64_t pe = f2(fast_exp2(ta), fast_exp2(tb));
+                const uint64_t dp = f2(__uint_as_float(rp[i][ee]), __uint_as_float(rp[i][ee + 1]));
+                const uint64_t ds = f2_mul(pe, f2_sub(dp, dlc[h]));
+                b[ee >> 1] = x2_of<F16>(ds);
+                if (WHICH == 2) a[ee >> 1] = x2_of<F16>(pe);
+            }
+        }
+        const uint32_t o0 = p_off(x.rowbase, x.sw, 2 * gi), o1 = p_off(x.rowbase, x.sw, 2 * gi + 1);
+        if (WHICH == 2) {
+            st_shared_v4(x.sP0 + o0, a[0], a[1], a[2], a[3]);  // P^T
+            st_shared_v4(x.sP0 + o1, a[4], a[5], a[6], a[7]);
+            st_shared_v4(x.sP1 + o0, b[0], b[1], b[2], b[3]);  // dS^T
+            st_shared_v4(x.sP1 + o1, b[4], b[5], b[6], b[7]);
+        } else {
+            st_shared_v4(x.sP0 + o0, b[0], b[1], b[2], b[3]);  // dS
+            st_shared_v4(x.sP0 + o1, b[4], b[5], b[6], b[7]);
+        }
+    }
+}
+
+// A tile whose rows still have to be written; each warpgroup writes half of the D columns of its
+// quarter's rows (dQ, or dV and dK).
+struct BwdEpilogue {
+    bool live, valid;
+    long long orow;
+    uint32_t ob, j;
+};
+
+template <int D, int WHICH, bool F16>
+__device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, const BwdEpilogue& e,
+                                             uint32_t tmem_lanes, int wg, int lane) {
+    if (!warp_wait(&bars[kOFull + e.ob], (e.j >> 1) & 1, p.err, kSitePV)) return false;
+    tc_fence_after();
+    const uint32_t acc = tmem_lanes + tm_acc<D>(WHICH, e.ob);
+    const int c0 = wg * (D / 2);
+    if (WHICH == 1) {
+        store_row<D / 2, F16>(acc + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dQ
+    } else {
+        store_row<D / 2, F16>(acc + c0, 1.f, p.out1 + e.orow * D + c0, e.valid);          // dV
+        store_row<D / 2, F16>(acc + D + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dK
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars[kOEmpty + e.ob]);
+    return true;
+}
+
+template <int D, int WHICH, bool F16>
+__device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
+                                 uint32_t tmem) {
+    constexpr int kS = stages_of(WHICH, D);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
+    const int row = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    unsigned* err = p.err;
+    const TilePlan& pl = p.plan;
+    const int ngroups = pl.NC >> 4;
+    BwdCtx x;
+    x.rowbase = static_cast<uint32_t>(row) * 64u;
+    x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
+    x.sl2x2 = f2(p.scale_log2, p.scale_log2);
+    x.l2 = nullptr;
+    x.dl = nullptr;
+    uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0, nz2 = nz0;  // groups of the quarter's rows that may be nonzero
+    BwdEpilogue ep{false, false, 0, 0, 0};
+    TileIter it = tile_iter_begin(p);
+    bool started = false;
+    Cta c;
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && next_tile(p, WHICH, it, started, c)) {
+        const RowGeom geo = row_geom(p, WHICH, c, row);
+        const WarpUnion wu = warp_union(geo);
+        const uint32_t ob = j & 1;
+        float lse2 = 0.f, dlt = 0.f;
+        if (WHICH == 1 && geo.valid) {
+            lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
+            dlt = __ldg(p.delta + geo.token * p.heads + c.h);
+        }
+        x.nl2 = f2(-lse2, -lse2);
+        x.dl2 = f2(dlt, dlt);
+        ChunkCursor cur = cursor_begin();
+        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+            constexpr uint32_t kPB = pbufs_of(WHICH);
+            const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
+            ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
+            if (!ok) break;
+            tc_fence_after();
+            int glo, n;
+            chunk_range(pl, cur, wu, glo, n);
+            // this warpgroup's groups of the run: glo + wg, glo + wg + 2, ...; the groups of the
+            // quarter's last run in this buffer that the new run does not cover are zeroed, split
+            // between the warpgroups by parity
+            const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
+            const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
+            const uint32_t nzq = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
+            const uint32_t stale = nzq & ~run & (wg ? 0xaaaaaaaau : 0x55555555u);
+            if (pb == 0) nz0 = run; else if (pb == 1) nz1 = run; else nz2 = run;
+            if (mine == 0 && stale == 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bars[kSEmpty + sb]);
+                    mbar_arrive(&bars[kPFull + pb]);
+                }
+                continue;
+            }
+            if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
+            if (ok && g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
+            if (!ok) break;
+            x.tS = tmem + tm_s(pl, sb) + lane_base;
+            x.tP = tmem + tm_dp(pl, sb) + lane_base;
+            x.sP0 = smem_u32(smem + lay.p(pb, 0));
+            x.sP1 = smem_u32(smem + lay.p(pb, 1));
+            if (WHICH == 2) {
+                x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
+                x.dl = x.l2 + pl.NC;
+            }
+            if (mine == 0) bwd_groups<WHICH, 0, F16>(x, glo + wg, &bars[kSEmpty + sb], true, lane);
+            for (int k = 0; k < mine; k += 2) {
+                const bool last = k + 2 >= mine;
+                if (k + 1 < mine)
+                    bwd_groups<WHICH, 2, F16>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+                else
+                    bwd_groups<WHICH, 1, F16>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+            }
+            for (uint32_t z = stale; z; z &= z - 1) {
+                zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
+                if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, __ffs(z) - 1);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
+        }
+        if (!ok) break;
+        // the previous tile's epilogue, deferred until this tile's chunks are done
+        if (ep.live && !(ok = bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane))) break;
+        ep = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
+        ++j;
+    }
+    if (ok && ep.live) bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Kernels
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, int WHICH>
+__device__ __forceinline__ void init_barriers(uint64_t* bars) {
+    constexpr uint32_t kSoft = 4 * nwg_of(WHICH);
+    for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars[kQFull + i], 1);
+        mbar_init(&bars[kQEmpty + i], 1);
+        mbar_init(&bars[kSFull + i], 1);
+        mbar_init(&bars[kSEmpty + i], kSoft);
+        mbar_init(&bars[kOFull + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
+        mbar_init(&bars[kOEmpty + i], kSoft);
+    }
+    for (int i = 0; i < pbufs_of(WHICH); ++i) {
+        mbar_init(&bars[kPFull + i], kSoft);
+        mbar_init(&bars[kPEmpty + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
+    }
+    for (int s = 0; s < stages_of(WHICH, D); ++s) {
+        mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
+        mbar_init(&bars[kKVEmpty + s], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
+    }
+    mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
+    fence_barrier_init();
+}
+
+template <int D, int WHICH, bool F16>
+__global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = aligned_smem(smem_raw);
+    const TilePlan& pl = p.plan;
+    const TcLayout lay = tc_layout(WHICH, pl, D);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+    constexpr int kSoftWarps = 4 * nwg_of(WHICH);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t tmem_cols = WHICH == 0 ? 256u : 512u;
+
+    if (warp == kSoftWarps) {
+        if (lane == 0) {
+            init_barriers<D, WHICH>(bars);
+            for (int m = 0; m < 4; ++m) tma_prefetch_desc(&p.tm[m]);
+        }
+        __syncwarp();
+    }
+    if (warp == kSoftWarps + 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kSoftWarps) {
+        producer_loop<D, WHICH>(p, smem, lay, bars);
+    } else if (warp == kSoftWarps + 1) {
+        if (lane == 0) {
+            if (WHICH == 0) mma_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            else score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+        }
+        __syncwarp();
+    } else if (warp >= kSoftWarps + 2) {
+        if (lane == 0) update_loop<D, WHICH>(p, smem, lay, bars, tmem, warp - (kSoftWarps + 2));
+        __syncwarp();
+    } else if (WHICH == 0) {
+        fwd_softmax_loop<D, F16>(p, smem, lay, bars, tmem);
+    } else {
+        bwd_softmax_loop<D, WHICH, F16>(p, smem, lay, bars, tmem);
+    }
+
+    // teardown: every MMA of this CTA done before TMEM is freed (each issuing lane commits once)
+    if (warp >= kSoftWarps + 1 && lane == 0) {
+        umma_commit(&bars[kFin]);
+        mbar_wait(&bars[kFin], 0, p.err, kSiteFinal);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kSoftWarps + 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+template <int D, int WHICH, bool F16>
+int launch_tc(const TcParams& p0, cudaStream_t stream) {
+    const int smem = p0.plan.smem_bytes;
+    auto kernel = tc_kernel<D, WHICH, F16>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return static_cast<int>(e);
+    if (p0.plan.ctas <= 0) return 0;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return static_cast<int>(e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return static_cast<int>(e);
+    const long long per_sm = p0.plan.per_sm;
+    const long long grid = p0.plan.ctas < per_sm * sms ? p0.plan.ctas : per_sm * sms;
+    // the grid size written in the tile index's mixed radix
+    TcParams p = p0;
+    uint32_t x = static_cast<uint32_t>(grid);
+    for (int i = 0; i < 8; ++i) {
+        p.step[i] = x % p.rad[i];
+        x /= p.rad[i];
+    }
+    kernel<<<dim3(static_cast<unsigned>(grid)), dim3(threads_of(WHICH)), smem, stream>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace na

@@ -9,7 +9,7 @@ a 9x9 kernel and 3D 16x256x256 with a (3,5,5) kernel, loss = output.sum() so dO 
 oracle finishes in well under a second, and a large dilated 2D stress case.
 
 Recipe: q, k, v and (when not ones) dO are drawn in that order, iid N(0, 1) in float32 from a
-torch.Generator seeded with ``seed``, then rounded to bfloat16 for bf16 workloads.
+torch.Generator seeded with ``seed``, then rounded to bfloat16 (fp16) for bf16 (fp16) workloads.
 """
 from __future__ import annotations
 
@@ -22,7 +22,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    dtype: str                 # "bf16" or "fp32"
+    dtype: str                 # "bf16", "fp16" or "fp32"
     B: int
     spatial: tuple
     heads: int
@@ -54,7 +54,7 @@ class Workload:
         return int(np.prod(self.kernel))
 
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        return {"bf16": torch.bfloat16, "fp16": torch.float16}.get(self.dtype, torch.float32)
 
 
 WORKLOADS = {
@@ -100,10 +100,13 @@ def small_workload(dtype: str, spatial, heads, D, kernel, dilation, B=1, dO="ran
 
 
 def to_oracle_array(t: torch.Tensor) -> np.ndarray:
-    """Host copy in the form the oracle reads: float32 values, or bfloat16 bit patterns as uint16."""
+    """Host copy in the form the oracle reads: float32 values, bfloat16 bit patterns as uint16, or
+    float16 values widened to float64 (exact: every float16 is a float64)."""
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float16:
+        return t.numpy().astype(np.float64)
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(f"unsupported dtype {t.dtype}")
