@@ -73,3 +73,72 @@ def test_pins_reject_mutant(tmp_path, name):
     with oracle.library(lib):
         failed = pin_results()
     assert failed, f"no pin caught the planted mistake {name}"
+
+
+# ---------------------------------------------------------------------------------------------
+# The unfused operations' oracle (oracle/unfused.py): mutants are compiled from edited source text
+# into a fresh module object, and test_oracle_unfused.py's pins run against it.
+# ---------------------------------------------------------------------------------------------
+
+import types
+
+import oracle.unfused as unfused
+import test_oracle_unfused as unpins
+
+UNFUSED_SRC = os.path.join(os.path.dirname(oracle.__file__), "unfused.py")
+
+UNFUSED_MUTANTS = {
+    "inverse_offset_order": ("offsets = (offsets[:, None] * self.kernel[a] + ti[None, :]).ravel()",
+                             "offsets = (offsets[:, None] + ti[None, :] * (self.K // self.kernel[a] if a == 0 else 1)).ravel()"),
+    "dk_missing_scale": ("dk = scale * _scatter", "dk = _scatter"),
+    "softmax_bwd_sign": ("return y * (dy - (y * dy).sum(axis=-1, keepdims=True))",
+                         "return y * (dy + (y * dy).sum(axis=-1, keepdims=True))"),
+    "window_offsets_reversed": ("idx = idx + (tab[x[:, a]] * self.strides[a]).reshape(shape)",
+                                "idx = idx + (tab[x[:, a]][:, ::-1] * self.strides[a]).reshape(shape)"),
+    "dv_scatters_dO_with_dattn": ("dv = _scatter(af, gf, g, rows, B, N, heads)",
+                                  "dv = _scatter(af, vf, g, rows, B, N, heads)"),
+    "qk_missing_scale_on_rows": ("return scale * np.einsum(\"rc,rtc->rt\"", "return np.einsum(\"rc,rtc->rt\""),
+}
+
+
+def unfused_mutant(name):
+    old, new = UNFUSED_MUTANTS[name]
+    src = open(UNFUSED_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mod = types.ModuleType(f"oracle._unfused_mutant_{name}")
+    mod.__package__ = "oracle"
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def unfused_pin_results(mod):
+    failed = []
+    checks = {"softmax_fd": unpins.test_softmax_bwd_matches_finite_differences,
+              "inverse_lists": unpins.test_inverse_lists_cover_every_pair_once,
+              "offset_order": lambda: unpins.test_offset_order_from_index_coded_keys((7, 9), (3, 5), (2, 1))}
+    for i, case in enumerate(pins.CASES):
+        checks[f"chain_fwd_{i}"] = lambda c=case: unpins.test_chain_forward_equals_fused_oracle(*c)
+        checks[f"chain_bwd_{i}"] = lambda c=case: unpins.test_chain_backward_equals_fused_oracle(*c)
+        checks[f"adjoint_{i}"] = lambda c=case: unpins.test_adjoint_identities(*c)
+    for i in (2, 4, 6, 7):
+        checks[f"rows_{i}"] = lambda c=pins.CASES[i]: unpins.test_sampled_rows_match_full(*c)
+    saved = unpins.un
+    unpins.un = mod
+    try:
+        for name, fn in checks.items():
+            try:
+                fn()
+            except (AssertionError, ValueError, IndexError):
+                failed.append(name)
+    finally:
+        unpins.un = saved
+    return failed
+
+
+def test_unfused_pins_pass_on_the_real_oracle():
+    assert unfused_pin_results(unfused) == []
+
+
+@pytest.mark.parametrize("name", sorted(UNFUSED_MUTANTS))
+def test_unfused_pins_reject_mutant(name):
+    assert unfused_pin_results(unfused_mutant(name)), f"no pin caught the planted mistake {name}"
