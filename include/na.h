@@ -161,14 +161,60 @@ na_status na_device_status(void* stream, uint32_t* raw);
 const char* na_strerror(na_status status);
 
 /*
- * Tile plan the bf16 kernels would use for this problem, for benchmarking and roofline
- * accounting.  which: 0 = forward, 1 = dQ, 2 = dK/dV.  out[16] receives
- *   {T1, T2, T3, H1, H2, H3, G1, G2, G3, NC, chunks_per_tile_max, tiles, mma_flops_per_tile_hi,
- *    mma_flops_per_tile_lo, tmem_cols, smem_bytes}
- * (axes embedded as 3D, outermost first; mma flops split into two 32-bit halves).
+ * Tile plan the tensor-core kernels (bf16 and fp16) would use for this problem, for benchmarking
+ * and roofline accounting.  which: 0 = forward, 1 = dQ, 2 = dK/dV.  out[16] receives
+ *   {T1, T2, T3, H1, H2, H3, G1, G2, G3, NC, chunks_per_tile_max, ctas, mma_flops,
+ *    tmem_cols, smem_bytes, chunks_total}
+ * (axes embedded as 3D, outermost first; mma_flops = the attention products' FLOPs that all
+ * tiles issue, without the window-bias products; ctas = persistent grid size;
+ * chunks_total = chunks over all tiles).
  */
 na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads, int D,
                        const int* kernel, const int* dilation, int64_t* out);
+
+
+/*
+ * Unfused operations.  NATTEN issue #161 ("Backward pass is very slow towards much tokens and large
+ * kernels") times the chain na2d_qk -> softmax -> na2d_av beside the fused op, and the maintainer's
+ * profile there lists its kernels (attention logits, AV, their gradients QGRAD, KGRAD, AGRAD, VGRAD,
+ * softmax forward and backward).  These entry points compute that chain on CUDA cores.
+ *
+ * Attention weights attn: [B, L.., heads, K] in the dtype of q, K = kernel[0] * ... * kernel[ndim-1];
+ * the weight of window offset (t_0, .., t_{n-1}) (t_a < kernel[a], first axis outermost) sits at
+ * t = (t_0 * kernel[1] + t_1) * kernel[2] + ... and belongs to the key at position
+ * c + dilation[a] * (s_a + t_a) along each axis (c, s_a: the query's residue class and window start).
+ * Tensors of D channels: [B, L.., heads, D] as for na_fwd.  Every pointer caller-owned device
+ * memory, 16-byte aligned; arithmetic in fp32.  Supported: NA_FP32, NA_BF16, NA_FP16 with
+ * D in {16, 32, 64, 128} (else NA_ERR_UNSUPPORTED); sizes are validated as for na_fwd.
+ */
+
+/* attn = scale * q . k over each query's window (the logits). */
+na_status na_qk(const void* q, const void* k, void* attn, int B, int ndim, const int* spatial, int heads, int D,
+                const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream);
+
+/* o = sum over each query's window of attn * v. */
+na_status na_av(const void* attn, const void* v, void* o, int B, int ndim, const int* spatial, int heads, int D,
+                const int* kernel, const int* dilation, na_dtype dtype, void* stream);
+
+/* y = softmax(x) over the K weights of every (batch, token, head) row; y may be x. */
+na_status na_softmax(const void* x, void* y, int B, int ndim, const int* spatial, int heads, const int* kernel,
+                     na_dtype dtype, void* stream);
+
+/* dx = y * (dy - sum_t y dy), the softmax's gradient given its output y; dx may be dy. */
+na_status na_softmax_bwd(const void* y, const void* dy, void* dx, int B, int ndim, const int* spatial, int heads,
+                         const int* kernel, na_dtype dtype, void* stream);
+
+/* Gradients of na_qk given dattn (the logits' gradient): dq = scale * sum_t dattn k over the query's
+ * window; dk = scale * sum over the queries whose windows hold the key of dattn q (no atomics). */
+na_status na_qk_bwd(const void* dattn, const void* q, const void* k, void* dq, void* dk, int B, int ndim,
+                    const int* spatial, int heads, int D, const int* kernel, const int* dilation, float scale,
+                    na_dtype dtype, void* stream);
+
+/* Gradients of na_av given dO: dattn = dO . v over the query's window; dv = sum over the queries
+ * whose windows hold the key of attn dO (no atomics). */
+na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn, void* dv, int B, int ndim,
+                    const int* spatial, int heads, int D, const int* kernel, const int* dilation, na_dtype dtype,
+                    void* stream);
 
 #ifdef __cplusplus
 }

@@ -7,6 +7,8 @@ kernels for bf16, CUDA-core FMA kernels for fp32); there is no fallback of any k
 library raises.
 
 Tensors are contiguous [B, L_1, .., L_n, heads, D] (n = 1..3); lse/delta are fp32 [B, L.., heads].
+The unfused operations (na_qk, na_softmax, na_av and their gradients) keep the attention weights
+as [B, L.., heads, K], K = the product of the kernel sizes, window offsets first axis outermost.
 """
 from __future__ import annotations
 
@@ -20,6 +22,7 @@ from . import build as _build
 __all__ = [
     "NAError", "load", "na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv",
     "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
+    "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd",
 ]
 
 NA_BF16, NA_FP32, NA_FP16 = 0, 1, 2
@@ -63,7 +66,15 @@ def load(path: str | None = None):
     lib.na_strerror.argtypes = [I]
     lib.na_strerror.restype = ctypes.c_char_p
     lib.na_plan_info.argtypes = [I, I, I, IP, I, I, IP, IP, ctypes.POINTER(ctypes.c_int64)]
-    for f in ("na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv", "na_device_status", "na_plan_info"):
+    geo_nd = [I, I, IP, I]                   # B, ndim, spatial, heads
+    lib.na_qk.argtypes = [P, P, P] + geo + kd + [I, P]
+    lib.na_av.argtypes = [P, P, P] + geo + [IP, IP, I, P]
+    lib.na_softmax.argtypes = [P, P] + geo_nd + [IP, I, P]
+    lib.na_softmax_bwd.argtypes = [P, P, P] + geo_nd + [IP, I, P]
+    lib.na_qk_bwd.argtypes = [P, P, P, P, P] + geo + kd + [I, P]
+    lib.na_av_bwd.argtypes = [P, P, P, P, P] + geo + [IP, IP, I, P]
+    for f in ("na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv", "na_device_status", "na_plan_info",
+              "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -218,3 +229,101 @@ def na_plan_info(which: int, B, spatial, heads, D, kernel, dilation=None) -> dic
                              _ints(dilation), out)
     _ok(st, "na_plan_info")
     return dict(zip(PLAN_FIELDS, [int(x) for x in out]))
+
+
+# ---------------------------------------------------------------------------------------------
+# Unfused operations: logits, window softmax, weighted sum, and their gradients
+# ---------------------------------------------------------------------------------------------
+
+def _window_size(kernel) -> int:
+    n = 1
+    for x in kernel:
+        n *= int(x)
+    return n
+
+
+def _attn_geometry(attn: torch.Tensor, kernel):
+    """B, ndim, spatial, heads of an attention-weight tensor [B, L.., heads, K]."""
+    if attn.dim() < 4 or attn.dim() > 6:
+        raise ValueError("expected attention weights [B, L_1..L_n, heads, K] with n in 1..3")
+    ndim = attn.dim() - 3
+    kernel = (kernel,) * ndim if isinstance(kernel, int) else tuple(kernel)
+    if len(kernel) != ndim:
+        raise ValueError("kernel needs one entry per spatial axis")
+    if int(attn.shape[-1]) != _window_size(kernel):
+        raise ValueError(f"last axis of the attention weights must be {_window_size(kernel)}")
+    return int(attn.shape[0]), ndim, tuple(int(s) for s in attn.shape[1:-2]), int(attn.shape[-2]), kernel
+
+
+def na_qk(q, k, attn, kernel, dilation=None, scale=None, stream=None):
+    """attn = scale * q . k over each query's window."""
+    B, ndim, spatial, heads, D = _geometry(q)
+    _check(k, q.shape, q.dtype, "k")
+    _check(q, q.shape, q.dtype, "q")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    _check(attn, tuple(q.shape[:-1]) + (_window_size(kernel),), q.dtype, "attn")
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = load().na_qk(q.data_ptr(), k.data_ptr(), attn.data_ptr(), B, ndim, _ints(spatial), heads, D,
+                      _ints(kernel), _ints(dilation), scale, _dtype_code(q), _stream(stream))
+    _ok(st, "na_qk")
+
+
+def na_av(attn, v, o, kernel, dilation=None, stream=None):
+    """o = sum over each query's window of attn * v."""
+    B, ndim, spatial, heads, D = _geometry(v)
+    _check(v, v.shape, v.dtype, "v")
+    _check(o, v.shape, v.dtype, "o")
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    _check(attn, tuple(v.shape[:-1]) + (_window_size(kernel),), v.dtype, "attn")
+    st = load().na_av(attn.data_ptr(), v.data_ptr(), o.data_ptr(), B, ndim, _ints(spatial), heads, D,
+                      _ints(kernel), _ints(dilation), _dtype_code(v), _stream(stream))
+    _ok(st, "na_av")
+
+
+def na_softmax(x, y, kernel, stream=None):
+    """y = softmax of x over each row's K window weights (y may be x)."""
+    B, ndim, spatial, heads, kernel = _attn_geometry(x, kernel)
+    _check(x, x.shape, x.dtype, "x")
+    _check(y, x.shape, x.dtype, "y")
+    st = load().na_softmax(x.data_ptr(), y.data_ptr(), B, ndim, _ints(spatial), heads, _ints(kernel),
+                           _dtype_code(x), _stream(stream))
+    _ok(st, "na_softmax")
+
+
+def na_softmax_bwd(y, dy, dx, kernel, stream=None):
+    """dx = y * (dy - sum_t y dy), the gradient of the window softmax given its output y."""
+    B, ndim, spatial, heads, kernel = _attn_geometry(y, kernel)
+    for name, t in (("y", y), ("dy", dy), ("dx", dx)):
+        _check(t, y.shape, y.dtype, name)
+    st = load().na_softmax_bwd(y.data_ptr(), dy.data_ptr(), dx.data_ptr(), B, ndim, _ints(spatial), heads,
+                               _ints(kernel), _dtype_code(y), _stream(stream))
+    _ok(st, "na_softmax_bwd")
+
+
+def na_qk_bwd(dattn, q, k, dq, dk, kernel, dilation=None, scale=None, stream=None):
+    """dq, dk of na_qk given the logits' gradient dattn."""
+    B, ndim, spatial, heads, D = _geometry(q)
+    for name, t in (("q", q), ("k", k), ("dq", dq), ("dk", dk)):
+        _check(t, q.shape, q.dtype, name)
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    _check(dattn, tuple(q.shape[:-1]) + (_window_size(kernel),), q.dtype, "dattn")
+    scale = D ** -0.5 if scale is None else float(scale)
+    st = load().na_qk_bwd(dattn.data_ptr(), q.data_ptr(), k.data_ptr(), dq.data_ptr(), dk.data_ptr(), B, ndim,
+                          _ints(spatial), heads, D, _ints(kernel), _ints(dilation), scale, _dtype_code(q),
+                          _stream(stream))
+    _ok(st, "na_qk_bwd")
+
+
+def na_av_bwd(dO, attn, v, dattn, dv, kernel, dilation=None, stream=None):
+    """dattn, dv of na_av given the output's gradient dO."""
+    B, ndim, spatial, heads, D = _geometry(v)
+    for name, t in (("dO", dO), ("v", v), ("dv", dv)):
+        _check(t, v.shape, v.dtype, name)
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    K = _window_size(kernel)
+    _check(attn, tuple(v.shape[:-1]) + (K,), v.dtype, "attn")
+    _check(dattn, tuple(v.shape[:-1]) + (K,), v.dtype, "dattn")
+    st = load().na_av_bwd(dO.data_ptr(), attn.data_ptr(), v.data_ptr(), dattn.data_ptr(), dv.data_ptr(), B, ndim,
+                          _ints(spatial), heads, D, _ints(kernel), _ints(dilation), _dtype_code(v),
+                          _stream(stream))
+    _ok(st, "na_av_bwd")

@@ -399,6 +399,33 @@ na_status check_dtype(na_dtype dt, const Geom& g) {
     return NA_ERR_INVALID_ARG;
 }
 
+
+// Validation and parameters shared by the unfused operations.
+int elem_of(na_dtype dt) { return dt == NA_BF16 ? 0 : (dt == NA_FP16 ? 2 : 1); }
+
+na_status unfused_params(int B, int ndim, const int* spatial, int heads, int D, const int* kernel,
+                         const int* dilation, float scale, na_dtype dtype, bool need_d, na::UnfParams& p) {
+    int ones[3] = {1, 1, 1};
+    Geom g;
+    na_status st = make_geom(B, ndim, spatial, heads, need_d ? D : 16, kernel, dilation ? dilation : ones, g);
+    if (st != NA_OK) return st;
+    if (!std::isfinite(scale)) return NA_ERR_INVALID_ARG;
+    if (dtype != NA_BF16 && dtype != NA_FP16 && dtype != NA_FP32) return NA_ERR_INVALID_ARG;
+    if (need_d && D != 16 && D != 32 && D != 64 && D != 128) return NA_ERR_UNSUPPORTED;
+    std::memset(&p, 0, sizeof p);
+    p.K = 1;
+    for (int a = 0; a < 3; ++a) {
+        p.L[a] = g.L[a];
+        p.k[a] = g.k[a];
+        p.d[a] = g.d[a];
+        p.K *= g.k[a];
+    }
+    p.heads = heads;
+    p.D = D;
+    p.rows = tokens_of(g) * B * heads;
+    p.scale = scale;
+    return NA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -676,6 +703,92 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
     out[14] = pl.smem_bytes;
     out[15] = total_chunks;
     return NA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Unfused operations
+// ---------------------------------------------------------------------------------------------
+
+na_status na_qk(const void* q, const void* k, void* attn, int B, int ndim, const int* spatial, int heads, int D,
+                const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, D, kernel, dilation, scale, dtype, true, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({q, k, attn})) != NA_OK) return st;
+    p.a = q;
+    p.b = k;
+    p.out0 = attn;
+    return cuda_status(na::launch_unfused_qk(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+na_status na_av(const void* attn, const void* v, void* o, int B, int ndim, const int* spatial, int heads, int D,
+                const int* kernel, const int* dilation, na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, D, kernel, dilation, 1.f, dtype, true, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({attn, v, o})) != NA_OK) return st;
+    p.a = attn;
+    p.b = v;
+    p.out0 = o;
+    return cuda_status(na::launch_unfused_av(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
+na_status na_softmax(const void* x, void* y, int B, int ndim, const int* spatial, int heads, const int* kernel,
+                     na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, 0, kernel, nullptr, 1.f, dtype, false, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({x, y})) != NA_OK) return st;
+    p.a = x;
+    p.out0 = y;
+    return cuda_status(na::launch_unfused_softmax(p, elem_of(dtype), false, static_cast<cudaStream_t>(stream)));
+}
+
+na_status na_softmax_bwd(const void* y, const void* dy, void* dx, int B, int ndim, const int* spatial, int heads,
+                         const int* kernel, na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, 0, kernel, nullptr, 1.f, dtype, false, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({y, dy, dx})) != NA_OK) return st;
+    p.a = y;
+    p.b = dy;
+    p.out0 = dx;
+    return cuda_status(na::launch_unfused_softmax(p, elem_of(dtype), true, static_cast<cudaStream_t>(stream)));
+}
+
+na_status na_qk_bwd(const void* dattn, const void* q, const void* k, void* dq, void* dk, int B, int ndim,
+                    const int* spatial, int heads, int D, const int* kernel, const int* dilation, float scale,
+                    na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, D, kernel, dilation, scale, dtype, true, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({dattn, q, k, dq, dk})) != NA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.a = dattn;
+    p.b = k;
+    p.out0 = dq;
+    if ((st = cuda_status(na::launch_unfused_gather(p, elem_of(dtype), s))) != NA_OK) return st;
+    p.b = q;
+    p.out0 = dk;
+    return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
+}
+
+na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn, void* dv, int B, int ndim,
+                    const int* spatial, int heads, int D, const int* kernel, const int* dilation, na_dtype dtype,
+                    void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, D, kernel, dilation, 1.f, dtype, true, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({dO, attn, v, dattn, dv})) != NA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.a = dO;
+    p.b = v;
+    p.out0 = dattn;
+    if ((st = cuda_status(na::launch_unfused_dattn(p, elem_of(dtype), s))) != NA_OK) return st;
+    p.a = attn;
+    p.b = dO;
+    p.out0 = dv;
+    return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
 }
 
 }  // extern "C"

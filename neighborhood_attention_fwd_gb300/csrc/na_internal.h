@@ -74,6 +74,18 @@ struct FmaParams {
     float scale;
 };
 
+// Parameters of the unfused operations (na_unfused.cu).  Rows are (batch, token, head) triples;
+// K = k0 k1 k2 attention weights per row.
+struct UnfParams {
+    const void* a;      // qk: q      av: attn   gather: dattn  scatter: dattn/attn  dattn: dO  softmax: x / y
+    const void* b;      // qk: k      av: v      gather: k      scatter: q / dO      dattn: v   softmax bwd: dy
+    void* out0;         // qk: attn   av: o      gather: dq     scatter: dk / dv     dattn: dattn  softmax: y / dx
+    int L[3], k[3], d[3];
+    int heads, D, K;
+    long long rows;     // B * tokens * heads
+    float scale;        // qk: scale; gather, scatter: the factor of the sum (scale, or 1)
+};
+
 // Launchers (defined next to their kernels).  Return a cudaError_t as int.
 int launch_fwd_tc(const TcParams& p, cudaStream_t stream);
 int launch_fwd_tc_f16(const TcParams& p, cudaStream_t stream);
@@ -85,6 +97,13 @@ int launch_fwd_fma(const FmaParams& p, cudaStream_t stream);
 int launch_dq_fma(const FmaParams& p, cudaStream_t stream);
 int launch_dkdv_fma(const FmaParams& p, cudaStream_t stream);
 int launch_delta(const FmaParams& p, int elem, cudaStream_t stream);  // elem: 0 bf16, 1 fp32, 2 fp16
+// elem: 0 bf16, 1 fp32, 2 fp16
+int launch_unfused_qk(const UnfParams& p, int elem, cudaStream_t stream);
+int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t stream);
+int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t stream);
+int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t stream);
+int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t stream);
+int launch_unfused_softmax(const UnfParams& p, int elem, bool bwd, cudaStream_t stream);
 
 // Kernel attributes that depend on the plan (dynamic smem opt-in); called before the launch.
 int prepare_tc_kernel(int which, int D, int smem_bytes);

@@ -93,6 +93,20 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None):
     return out
 
 
+def make_weights(w: Workload, kind: str = "randn", device="cpu", seed: int = 0):
+    """A seeded tensor shaped like the unfused operations' attention weights [B, L.., heads, K] in
+    w's dtype: iid N(0, 1) ("randn": logits, gradients) or U(0, 1) ("uniform": probability-like
+    weights), drawn in float32 and rounded."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (w.B, *w.spatial, w.heads, w.keys_per_query)
+    if kind == "uniform":
+        x = torch.rand(shape, generator=gen, dtype=torch.float32, device=device)
+    else:
+        x = torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+    return x.to(w.torch_dtype())
+
+
 def small_workload(dtype: str, spatial, heads, D, kernel, dilation, B=1, dO="randn", seed=7) -> Workload:
     """An ad-hoc workload (parity sweeps)."""
     return Workload(f"adhoc_{dtype}_{'x'.join(map(str, spatial))}", dtype, B, tuple(spatial), heads, D,

@@ -27,7 +27,8 @@ def declared_entry_points():
 def test_header_declares_the_boundary():
     names = declared_entry_points()
     for required in ("na_fwd", "na_bwd", "na_bwd_workspace_size", "na_strerror", "na_bwd_delta", "na_bwd_dq",
-                     "na_bwd_dkdv", "na_device_status"):
+                     "na_bwd_dkdv", "na_device_status", "na_qk", "na_av", "na_softmax", "na_softmax_bwd",
+                     "na_qk_bwd", "na_av_bwd"):
         assert required in names
 
 
@@ -73,6 +74,32 @@ def test_unsupported_problems(lib):
     assert _fwd(lib, (64, 64), (5, 5), (1, 1), D=48) == 2            # bf16 head dim
     assert _fwd(lib, (64, 64), (5, 5), (1, 1), D=24, dtype=1) == 2   # fp32 head dim
     assert _fwd(lib, (128, 128), (5, 5), (1, 9)) == 2                # dilation beyond the TMA element stride
+
+
+def test_unfused_entry_points_reject_bad_arguments(lib):
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    P = lambda x: ctypes.c_void_p(x) if x is not None else None
+    f = ctypes.c_float
+
+    def qk(ptr=16, kernel=(5, 5), D=32, dtype=0, scale=0.1):
+        return lib.na_qk(P(ptr), P(ptr), P(ptr), 1, 2, I((16, 16)), 2, D, I(kernel), I((1, 1)), f(scale), dtype, None)
+
+    # only argument forms that fail validation are passed: a valid call would launch a kernel
+    assert qk(ptr=None) == 1
+    assert qk(ptr=8) == 3
+    assert qk(kernel=(4, 5)) == 1
+    assert qk(D=48) == 2
+    assert qk(dtype=7) == 1
+    assert qk(scale=float("inf")) == 1
+    assert lib.na_av(None, P(16), P(16), 1, 2, I((16, 16)), 2, 32, I((5, 5)), I((1, 1)), 0, None) == 1
+    assert lib.na_av(P(16), P(16), P(16), 1, 2, I((16, 16)), 2, 24, I((5, 5)), I((1, 1)), 0, None) == 2
+    assert lib.na_softmax(P(16), None, 1, 2, I((16, 16)), 2, I((5, 5)), 0, None) == 1
+    assert lib.na_softmax(P(16), P(16), 1, 2, I((16, 16)), 2, I((5, 6)), 0, None) == 1
+    assert lib.na_softmax_bwd(P(16), P(16), P(8), 1, 2, I((16, 16)), 2, I((5, 5)), 0, None) == 3
+    assert lib.na_qk_bwd(P(16), P(16), P(16), P(16), None, 1, 2, I((16, 16)), 2, 32, I((5, 5)), I((1, 1)), f(0.1), 0,
+                         None) == 1
+    assert lib.na_av_bwd(P(16), P(16), P(16), P(16), P(16), 1, 2, I((16, 16)), 2, 32, I((5, 5)), I((1, 4)), 0,
+                         None) == 1   # class of 4 positions < 5
 
 
 @pytest.mark.parametrize("name", [n for n in nain.WORKLOADS if nain.WORKLOADS[n].dtype == "bf16"])

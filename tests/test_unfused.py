@@ -1,0 +1,190 @@
+"""GPU parity of the unfused operations (logits, window softmax, weighted sum and their gradients)
+against the fp64 oracle, through the C ABI.
+
+Each operation is compared on its own, on seeded inputs of its own (the attention-weight inputs are
+drawn by the input generator, never taken from another kernel's output), element by element at
+small sizes.  The chains qk -> softmax -> av and their gradients are also compared with the fused
+oracle's forward and backward, at small sizes in full and at the 2D benchmark shape on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.unfused as un
+from neighborhood_attention_fwd_gb300 import inputs as nain
+from na_testlib import TOL, compare, host, sample_rows, to64
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # dtype, spatial, heads, D, kernel, dilation, B
+    ("fp32", (37,), 2, 16, (7,), (3,), 2),
+    ("fp32", (6, 9, 10), 2, 128, (3, 3, 3), (2, 1, 1), 1),
+    ("fp32", (16, 16), 2, 16, (5, 5), (1, 1), 1),
+    ("bf16", (13, 18), 2, 32, (5, 7), (1, 2), 2),
+    ("bf16", (6, 9, 10), 1, 64, (3, 5, 5), (1, 1, 2), 1),
+    ("bf16", (20, 24), 3, 128, (9, 9), (1, 1), 1),
+    ("bf16", (23, 29), 2, 16, (3, 5), (3, 2), 1),            # classes of unequal length
+    ("fp16", (13, 18), 2, 32, (5, 7), (1, 2), 1),
+    ("fp16", (5, 7, 9), 2, 16, (5, 7, 9), (1, 1, 1), 1),      # kernel == extent: full attention
+    ("fp16", (16, 8), 1, 64, (1, 1), (1, 1), 1),              # k = 1
+]
+
+
+def _ids(c):
+    return f"{c[0]}-{'x'.join(map(str, c[1]))}-h{c[2]}-D{c[3]}-k{'x'.join(map(str, c[4]))}-d{'x'.join(map(str, c[5]))}-B{c[6]}"
+
+
+def f32(t):
+    """Host float32 copy (exact for fp32, bf16 and fp16 values) in the form the unfused oracle reads."""
+    return t.detach().to("cpu", torch.float32).numpy()
+
+
+def setup(case, seed=17):
+    dtype, spatial, heads, D, kernel, dilation, B = case
+    w = nain.small_workload(dtype, spatial, heads, D, kernel, dilation, B=B, seed=seed)
+    t = nain.make_inputs(w, device="cpu")
+    wt = {"logits": nain.make_weights(w, "randn", seed=seed + 1),
+          "probs": nain.make_weights(w, "uniform", seed=seed + 2),
+          "grad": nain.make_weights(w, "randn", seed=seed + 3)}
+    return w, t, wt
+
+
+def status_ok(na):
+    st, raw = na.na_device_status()
+    assert st == 0, f"device status {st} raw {raw:#x}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_each_operation_matches_the_oracle(case, cuda_lib):
+    na = cuda_lib
+    w, t, wt = setup(case)
+    tol = TOL[w.dtype]
+    dev = {k: v.cuda() for k, v in t.items()}
+    wd = {k: v.cuda() for k, v in wt.items()}
+    h = {k: f32(v) for k, v in t.items()}
+    hw = {k: f32(v) for k, v in wt.items()}
+    kern, dil, scale = w.kernel, w.dilation, w.scale
+
+    attn = torch.empty_like(wd["logits"])
+    na.na_qk(dev["q"], dev["k"], attn, kern, dil, scale)
+    o = torch.empty_like(dev["q"])
+    na.na_av(wd["probs"], dev["v"], o, kern, dil)
+    y = torch.empty_like(wd["logits"])
+    na.na_softmax(wd["logits"], y, kern)
+    dx = torch.empty_like(wd["logits"])
+    na.na_softmax_bwd(wd["probs"], wd["grad"], dx, kern)
+    dq, dk = torch.empty_like(dev["q"]), torch.empty_like(dev["q"])
+    na.na_qk_bwd(wd["grad"], dev["q"], dev["k"], dq, dk, kern, dil, scale)
+    dattn, dv = torch.empty_like(wd["logits"]), torch.empty_like(dev["q"])
+    na.na_av_bwd(dev["dO"], wd["probs"], dev["v"], dattn, dv, kern, dil)
+    status_ok(na)
+
+    compare("attn", to64(attn), un.qk(h["q"], h["k"], kern, dil, scale), tol)
+    compare("o", to64(o), un.av(hw["probs"], h["v"], kern, dil), tol)
+    compare("softmax", to64(y), un.softmax(hw["logits"]), tol)
+    compare("softmax_bwd", to64(dx), un.softmax_bwd(hw["probs"], hw["grad"]), tol)
+    rq, rk = un.qk_bwd(hw["grad"], h["q"], h["k"], kern, dil, scale)
+    compare("dq", to64(dq), rq, tol)
+    compare("dk", to64(dk), rk, tol)
+    ra, rv = un.av_bwd(h["dO"], hw["probs"], h["v"], kern, dil)
+    compare("dattn", to64(dattn), ra, tol)
+    compare("dv", to64(dv), rv, tol)
+
+
+def run_chain(na, w, dev):
+    """qk -> softmax -> av, then the chained gradients, all on the device."""
+    kern, dil, scale = w.kernel, w.dilation, w.scale
+    q, k, v, dO = dev["q"], dev["k"], dev["v"], dev["dO"]
+    K = w.keys_per_query
+    attn = torch.empty(q.shape[:-1] + (K,), dtype=q.dtype, device=q.device)
+    na.na_qk(q, k, attn, kern, dil, scale)
+    na.na_softmax(attn, attn, kern)                          # in place
+    o = torch.empty_like(q)
+    na.na_av(attn, v, o, kern, dil)
+    dattn, dv = torch.empty_like(attn), torch.empty_like(v)
+    na.na_av_bwd(dO, attn, v, dattn, dv, kern, dil)
+    na.na_softmax_bwd(attn, dattn, dattn, kern)              # in place over the incoming gradient
+    dq, dk = torch.empty_like(q), torch.empty_like(k)
+    na.na_qk_bwd(dattn, q, k, dq, dk, kern, dil, scale)
+    status_ok(na)
+    return {"o": o, "dq": dq, "dk": dk, "dv": dv}
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_chain_matches_the_fused_oracle(case, cuda_lib):
+    w, t, _ = setup(case, seed=29)
+    tol = TOL[w.dtype]
+    got = run_chain(cuda_lib, w, {k: v.cuda() for k, v in t.items()})
+    hh = host(t)
+    o, _ = oracle.na_fwd(hh["q"], hh["k"], hh["v"], w.kernel, w.dilation, w.scale)
+    dq, dk, dv = oracle.na_bwd(hh["q"], hh["k"], hh["v"], hh["dO"], w.kernel, w.dilation, w.scale)
+    compare("O", to64(got["o"]), o, tol)
+    compare("dQ", to64(got["dq"]), dq, tol, scale_ref=dv)
+    compare("dK", to64(got["dk"]), dk, tol, scale_ref=dv)
+    compare("dV", to64(got["dv"]), dv, tol)
+
+
+def test_operations_are_deterministic(cuda_lib):
+    na = cuda_lib
+    w, t, _ = setup(("bf16", (30, 26), 2, 32, (7, 5), (1, 2), 1), seed=3)
+    dev = {k: v.cuda() for k, v in t.items()}
+    a = run_chain(na, w, dev)
+    b = run_chain(na, w, dev)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
+
+
+@pytest.mark.slow
+def test_full_size_chain_sampled(cuda_lib):
+    """The 2D benchmark shape (1024x1024, 8 heads of dim 32, 9x9, bf16): each operation on sampled rows
+    against the unfused oracle, and the chain's outputs against the fused oracle."""
+    na = cuda_lib
+    w = nain.WORKLOADS["2d_bf16_1024x1024_k9"]
+    t = nain.make_inputs(w, device="cuda")
+    tol = TOL[w.dtype]
+    got = run_chain(na, w, t)
+    rows = sample_rows(w, 96, seed=5)
+    idx = torch.as_tensor(rows, device="cuda")
+    pick = lambda x: to64(x.reshape(-1, x.shape[-1])[idx])
+    hh = host({k: v for k, v in t.items()})
+    o, _ = oracle.na_fwd(hh["q"], hh["k"], hh["v"], w.kernel, w.dilation, w.scale, rows=rows)
+    dq, dk, dv = oracle.na_bwd(hh["q"], hh["k"], hh["v"], hh["dO"], w.kernel, w.dilation, w.scale,
+                               qrows=rows, krows=rows)
+    compare("O", pick(got["o"]), o, tol)
+    compare("dQ", pick(got["dq"]), dq, tol, scale_ref=dv)
+    compare("dK", pick(got["dk"]), dk, tol, scale_ref=dv)
+    compare("dV", pick(got["dv"]), dv, tol)
+    for key, x in got.items():
+        assert torch.isfinite(x).all(), key
+
+    # each operation on its own, on seeded weights of the full shape
+    h = {k: f32(v) for k, v in t.items()}
+    probs = nain.make_weights(w, "uniform", device="cuda", seed=77)
+    grad = nain.make_weights(w, "randn", device="cuda", seed=78)
+    hp, hg = f32(probs), f32(grad)
+    kern, dil, scale = w.kernel, w.dilation, w.scale
+    attn = torch.empty_like(grad)
+    na.na_qk(t["q"], t["k"], attn, kern, dil, scale)
+    o2 = torch.empty_like(t["q"])
+    na.na_av(probs, t["v"], o2, kern, dil)
+    y = torch.empty_like(grad)
+    na.na_softmax(grad, y, kern)
+    dx = torch.empty_like(grad)
+    na.na_softmax_bwd(probs, grad, dx, kern)
+    dq2, dk2 = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    na.na_qk_bwd(grad, t["q"], t["k"], dq2, dk2, kern, dil, scale)
+    dattn, dv2 = torch.empty_like(grad), torch.empty_like(t["q"])
+    na.na_av_bwd(t["dO"], probs, t["v"], dattn, dv2, kern, dil)
+    status_ok(na)
+    compare("attn", pick(attn), un.qk(h["q"], h["k"], kern, dil, scale, rows), tol)
+    compare("o", pick(o2), un.av(hp, h["v"], kern, dil, rows), tol)
+    compare("softmax", pick(y), un.softmax(hg, rows), tol)
+    compare("softmax_bwd", pick(dx), un.softmax_bwd(hp, hg, rows), tol)
+    rq, rk = un.qk_bwd(hg, h["q"], h["k"], kern, dil, scale, rows)
+    compare("dq", pick(dq2), rq, tol)
+    compare("dk", pick(dk2), rk, tol)
+    ra, rv = un.av_bwd(h["dO"], hp, h["v"], kern, dil, rows)
+    compare("dattn", pick(dattn), ra, tol)
+    compare("dv", pick(dv2), rv, tol)
