@@ -97,9 +97,17 @@ class Geometry:
 
 
 def _split(x):
-    """View [B, L.., heads, C] as [B, N, heads, C] float64."""
-    x = np.asarray(x, dtype=np.float64)
+    """View [B, L.., heads, C] as [B, N, heads, C].  float32 inputs stay float32 here (exact for
+    bf16 and fp16 values, and half the host memory at full size); every operand is widened to
+    float64 by _f64 once gathered, before any arithmetic."""
+    x = np.asarray(x)
+    if x.dtype not in (np.float32, np.float64):
+        raise TypeError(f"unsupported input dtype {x.dtype}: pass float32 or float64")
     return x.reshape(x.shape[0], -1, x.shape[-2], x.shape[-1])
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
 
 
 def _rows_of(rows, B, N, heads):
@@ -114,11 +122,11 @@ def qk(q, k, kernel, dilation, scale, rows=None):
     g = Geometry(q.shape[1:-2], kernel, dilation)
     if rows is None:
         nb = g.neighbours(np.arange(N))                       # [N, K]
-        out = scale * np.einsum("bnhc,bnthc->bnht", qf, kf[:, nb])
+        out = scale * np.einsum("bnhc,bnthc->bnht", _f64(qf), _f64(kf[:, nb]))
         return out.reshape(tuple(q.shape[:-1]) + (g.K,))
     b, tok, h = _rows_of(rows, B, N, heads)
     nb = g.neighbours(tok)
-    return scale * np.einsum("rc,rtc->rt", qf[b, tok, h], kf[b[:, None], nb, h[:, None]])
+    return scale * np.einsum("rc,rtc->rt", _f64(qf[b, tok, h]), _f64(kf[b[:, None], nb, h[:, None]]))
 
 
 def av(attn, v, kernel, dilation, rows=None):
@@ -129,29 +137,30 @@ def av(attn, v, kernel, dilation, rows=None):
     g = Geometry(v.shape[1:-2], kernel, dilation)
     if rows is None:
         nb = g.neighbours(np.arange(N))
-        out = np.einsum("bnht,bnthc->bnhc", af, vf[:, nb])
+        out = np.einsum("bnht,bnthc->bnhc", _f64(af), _f64(vf[:, nb]))
         return out.reshape(v.shape)
     b, tok, h = _rows_of(rows, B, N, heads)
     nb = g.neighbours(tok)
-    return np.einsum("rt,rtc->rc", af[b, tok, h], vf[b[:, None], nb, h[:, None]])
+    return np.einsum("rt,rtc->rc", _f64(af[b, tok, h]), _f64(vf[b[:, None], nb, h[:, None]]))
 
 
 def softmax(x, rows=None):
     """Softmax over the last axis (the window's K weights)."""
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x)
     if rows is not None:
         x = x.reshape(-1, x.shape[-1])[np.asarray(rows, dtype=np.int64).ravel()]
+    x = _f64(x)
     e = np.exp(x - x.max(axis=-1, keepdims=True))
     return e / e.sum(axis=-1, keepdims=True)
 
 
 def softmax_bwd(y, dy, rows=None):
     """Gradient of the window softmax given its output y and the output's gradient dy."""
-    y = np.asarray(y, dtype=np.float64)
-    dy = np.asarray(dy, dtype=np.float64)
+    y, dy = np.asarray(y), np.asarray(dy)
     if rows is not None:
         r = np.asarray(rows, dtype=np.int64).ravel()
         y, dy = y.reshape(-1, y.shape[-1])[r], dy.reshape(-1, dy.shape[-1])[r]
+    y, dy = _f64(y), _f64(dy)
     return y * (dy - (y * dy).sum(axis=-1, keepdims=True))
 
 
@@ -159,10 +168,10 @@ def _gather(w, src, g, rows, B, N, heads):
     """sum_t w[i, t] src_{n(i, t)} for every row (rows=None) or the sampled rows."""
     if rows is None:
         nb = g.neighbours(np.arange(N))
-        return np.einsum("bnht,bnthc->bnhc", w, src[:, nb])
+        return np.einsum("bnht,bnthc->bnhc", _f64(w), _f64(src[:, nb]))
     b, tok, h = _rows_of(rows, B, N, heads)
     nb = g.neighbours(tok)
-    return np.einsum("rt,rtc->rc", w[b, tok, h], src[b[:, None], nb, h[:, None]])
+    return np.einsum("rt,rtc->rc", _f64(w[b, tok, h]), _f64(src[b[:, None], nb, h[:, None]]))
 
 
 def _scatter(w, src, g, rows, B, N, heads):
@@ -171,16 +180,16 @@ def _scatter(w, src, g, rows, B, N, heads):
     D = src.shape[-1]
     if rows is None:
         nb = g.neighbours(np.arange(N))                       # [N, K]
-        out = np.zeros_like(src)
+        out = np.zeros(src.shape, dtype=np.float64)
         for t in range(g.K):
-            contrib = w[:, :, :, t, None] * src               # [B, N, heads, D]
+            contrib = _f64(w[:, :, :, t, None]) * _f64(src)   # [B, N, heads, D]
             np.add.at(out, (slice(None), nb[:, t]), contrib)
         return out
     b, tok, h = _rows_of(rows, B, N, heads)
     out = np.zeros((b.size, D), dtype=np.float64)
     for r in range(b.size):
         qs, ts = g.inverse(int(tok[r]))
-        out[r] = np.einsum("n,nc->c", w[b[r], qs, h[r], ts], src[b[r], qs, h[r]])
+        out[r] = np.einsum("n,nc->c", _f64(w[b[r], qs, h[r], ts]), _f64(src[b[r], qs, h[r]]))
     return out
 
 
@@ -203,11 +212,11 @@ def av_bwd(dO, attn, v, kernel, dilation, rows=None):
     g = Geometry(v.shape[1:-2], kernel, dilation)
     if rows is None:
         nb = g.neighbours(np.arange(N))
-        dattn = np.einsum("bnhc,bnthc->bnht", gf, vf[:, nb]).reshape(tuple(v.shape[:-1]) + (g.K,))
+        dattn = np.einsum("bnhc,bnthc->bnht", _f64(gf), _f64(vf[:, nb])).reshape(tuple(v.shape[:-1]) + (g.K,))
     else:
         b, tok, h = _rows_of(rows, B, N, heads)
         nb = g.neighbours(tok)
-        dattn = np.einsum("rc,rtc->rt", gf[b, tok, h], vf[b[:, None], nb, h[:, None]])
+        dattn = np.einsum("rc,rtc->rt", _f64(gf[b, tok, h]), _f64(vf[b[:, None], nb, h[:, None]]))
     dv = _scatter(af, gf, g, rows, B, N, heads)
     if rows is None:
         dv = dv.reshape(v.shape)
