@@ -8,6 +8,10 @@ is very slow towards much tokens and large kernels", the user's benchmark script
 so dO = 1).  Useful FLOPs follow the maintainer's arithmetic-intensity count in that thread:
 4*N*K*D*heads forward (QK^T and PV) and 10*N*K*D*heads backward.
 
+--path unfused times the unfused chain instead (logits, window softmax, weighted sum, and their
+gradients through na_qk, na_softmax, na_av, na_av_bwd, na_softmax_bwd, na_qk_bwd): the same outputs
+(O, dQ, dK, dV) and the same useful FLOPs, with the attention weights going through HBM.
+
 Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead (bounded samples).
 """
 from __future__ import annotations
@@ -60,6 +64,30 @@ def method_bytes(w):
     s = 2 if w.dtype in ("bf16", "fp16") else 4
     rows = float(w.tokens) * w.heads
     return 4 * rows * w.D * s + 4 * rows, 8 * rows * w.D * s + 12 * rows
+
+
+def fp32_fma_tflops(sm_mhz=None):
+    """CUDA-core fp32 FMA peak: 152 SMs x 128 FP32 lanes x 2 FLOP per FMA x the SM clock (the clock
+    sampled under load, else the 2070 MHz maximum)."""
+    return 152 * 128 * 2 * (sm_mhz or 2070.0) * 1e6 / 1e12
+
+
+UNFUSED_CALLS = ("qk", "softmax", "av", "av_bwd", "softmax_bwd", "qk_bwd")
+
+
+def unfused_call_work(w):
+    """Algorithmic bytes (inputs read once, outputs written once) and FLOPs of each unfused call.
+    R = rows (tokens x heads); weights are R x K elements."""
+    s = 2 if w.dtype in ("bf16", "fp16") else 4
+    R = float(w.tokens) * w.heads
+    RD, RK = R * w.D * s, R * w.keys_per_query * s
+    prod = 2.0 * R * w.keys_per_query * w.D
+    return {"qk": (2 * RD + RK, prod),                 # q, k -> attn
+            "softmax": (2 * RK, 0.0),                  # attn -> attn
+            "av": (2 * RD + RK, prod),                 # attn, v -> o
+            "av_bwd": (3 * RD + 2 * RK, 2 * prod),     # dO, attn, v -> dattn, dv
+            "softmax_bwd": (3 * RK, 0.0),              # y, dy -> dx
+            "qk_bwd": (4 * RD + RK, 2 * prod)}         # dattn, q, k -> dq, dk
 
 
 def arithmetic_intensity(w, fused=True, elem_bytes=None):
@@ -246,6 +274,141 @@ class Step:
     LAUNCHES_PER_STEP = 4
 
 
+class UnfusedStep:
+    """Buffers and launches of one fwd + bwd step through the unfused operations."""
+
+    def __init__(self, w, t):
+        import neighborhood_attention_fwd_gb300 as na
+
+        self.na = na
+        self.w = w
+        self.t = t
+        q = t["q"]
+        self.attn = torch.empty(q.shape[:-1] + (w.keys_per_query,), dtype=q.dtype, device=q.device)
+        self.dattn = torch.empty_like(self.attn)
+        self.o = torch.empty_like(q)
+        self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+
+    def launch(self, events=None):
+        na, w, t = self.na, self.w, self.t
+        ev = events or {}
+        s = torch.cuda.current_stream()
+
+        def mark(name):
+            if name in ev:
+                ev[name].record(s)
+
+        mark("start")
+        na.na_qk(t["q"], t["k"], self.attn, w.kernel, w.dilation, w.scale)
+        mark("qk")
+        na.na_softmax(self.attn, self.attn, w.kernel)
+        mark("softmax")
+        na.na_av(self.attn, t["v"], self.o, w.kernel, w.dilation)
+        mark("av")
+        na.na_av_bwd(t["dO"], self.attn, t["v"], self.dattn, self.dv, w.kernel, w.dilation)
+        mark("av_bwd")
+        na.na_softmax_bwd(self.attn, self.dattn, self.dattn, w.kernel)
+        mark("softmax_bwd")
+        na.na_qk_bwd(self.dattn, t["q"], t["k"], self.dq, self.dk, w.kernel, w.dilation, w.scale)
+        mark("qk_bwd")
+
+    LAUNCHES_PER_STEP = 8   # av_bwd and qk_bwd launch two kernels each
+
+
+def run_unfused(args, w, rank, world, dist):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import neighborhood_attention_fwd_gb300 as na
+
+    na.load()
+    t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
+    step = UnfusedStep(w, t)
+    tensor_bytes = t["q"].numel() * t["q"].element_size()
+    flush = None
+    if tensor_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    names = ("start",) + UNFUSED_CALLS
+    for _ in range(args.warmup):
+        step.launch()
+        if flush is not None:
+            flush.fill_(1.0)
+    st, raw = na.na_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({raw:#x}) after warm-up")
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        step.launch(evs[i])
+        if flush is not None:
+            flush.fill_(float(i))
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    st, raw = na.na_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({raw:#x}) in the timed region")
+
+    ms = {}
+    for a, b in zip(names[:-1], names[1:]):
+        ms[b] = float(np.mean([e[a].elapsed_time(e[b]) for e in evs]))
+    ms_step_local = float(np.mean([e["start"].elapsed_time(e[names[-1]]) for e in evs]))
+    ms_step = ranks_max(ms_step_local, dist, dev)
+    f_fwd, f_bwd = useful_flops(w)
+    value = job_value(world, f_fwd + f_bwd, ms_step)
+
+    peaks = load_peaks()
+    hbm = peaks["hbm_gbs"] * 1e9
+    alu_tflops = fp32_fma_tflops(clk.get("sm_mhz"))
+    work = unfused_call_work(w)
+    calls = {}
+    for name in UNFUSED_CALLS:
+        nbytes, flops = work[name]
+        t_b, t_f = nbytes / hbm, flops / (alu_tflops * 1e12)
+        sec = ms[name] * 1e-3
+        if t_f > t_b:
+            ach, peak, unit, bound = flops / sec / 1e12, alu_tflops, "TFLOP/s", "alu"
+        else:
+            ach, peak, unit, bound = nbytes / sec / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+        calls[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+                       "frac": ach / peak, "roof_ms": max(t_b, t_f) * 1e3, "alg_bytes": nbytes, "flops": flops}
+    dom = max(UNFUSED_CALLS, key=lambda k: ms[k])
+    roof_step = sum(c["roof_ms"] for c in calls.values())
+    e2e = run_e2e(args, w, t, step, UnfusedStep) if not args.no_e2e else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.dtype != "fp32" else "f32",
+        "data": "synthetic (seeded N(0,1) inputs, dO = ones as loss = O.sum())" if w.dO == "ones"
+                else "synthetic (seeded N(0,1) inputs and dO)",
+        "config": {"workload": w.name, "path": "unfused", "B": w.B, "spatial": list(w.spatial), "heads": w.heads,
+                   "D": w.D, "kernel": list(w.kernel), "dilation": list(w.dilation),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps (256 MB write)"},
+        "ms": {"fwd": ms["qk"] + ms["softmax"] + ms["av"],
+               "bwd": ms["av_bwd"] + ms["softmax_bwd"] + ms["qk_bwd"], "fwd_bwd": ms_step, "per_call": ms},
+        "roofline": {"bound": calls[dom]["bound"], "achieved": calls[dom]["achieved"], "peak": calls[dom]["peak"],
+                     "unit": calls[dom]["unit"], "frac": calls[dom]["frac"],
+                     "traffic": load_traffic(w.name + ":unfused", dom), "kernel": dom,
+                     "peak_source": "fp32 FMA peak from unit counts and the sampled clock" if calls[dom]["bound"] == "alu"
+                                    else peaks["source"]},
+        "roofline_step": {"roof_ms": roof_step, "frac": roof_step / ms_step},
+        "calls": calls,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+        "gpu_launches": UnfusedStep.LAUNCHES_PER_STEP * args.steps,
+        "e2e": e2e,
+    }
+    return line, t
+
+
 def run_ours(args, w, rank, world, dist):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
@@ -362,18 +525,24 @@ def run_ours(args, w, rank, world, dist):
     return line, t
 
 
-def run_e2e(args, w, t, step):
+def run_e2e(args, w, t, step, step_cls=None):
     """Same metric measured through the public API with host buffers: per step, copy q, k, v, dO
-    from pinned host memory, run forward + backward, copy O, LSE, dQ, dK, dV back."""
+    from pinned host memory, run forward + backward, copy the outputs (O, LSE when the path has it,
+    dQ, dK, dV) back."""
+    step_cls = step_cls or Step
     hs = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in t.items()}
     for k in hs:
         hs[k].copy_(t[k])
-    outs = [step.o, step.lse, step.dq, step.dk, step.dv]
+    out_names = [n for n in ("o", "lse", "dq", "dk", "dv") if hasattr(step, n)]
+    outs = [getattr(step, n) for n in out_names]
     ho = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
     dev_in = {k: torch.empty_like(v) for k, v in t.items()}
-    e2e_step = Step(w, dev_in)
-    e2e_step.o, e2e_step.lse, e2e_step.dq, e2e_step.dk, e2e_step.dv = outs[0], outs[1], outs[2], outs[3], outs[4]
-    e2e_step.delta = step.delta
+    e2e_step = step_cls(w, dev_in)
+    for n, x in zip(out_names, outs):      # reuse the timed step's output buffers
+        setattr(e2e_step, n, x)
+    for n in ("delta", "attn", "dattn"):   # and its scratch
+        if hasattr(step, n):
+            setattr(e2e_step, n, getattr(step, n))
     steps = max(3, min(args.steps, 10))
     s = torch.cuda.current_stream()
 
@@ -453,8 +622,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
-                    help="run a bf16 workload's shapes with fp16 tensors instead")
+    ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
+                    help="the fused kernels (default) or the unfused chain of separate operations")
+    ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default=None,
+                    help="run a bf16 workload's shapes with fp16 or fp32 tensors instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -479,7 +650,7 @@ def main():
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         tdist.init_process_group("nccl")
         dist = tdist
-    line, t = run_ours(args, w, rank, world, dist)
+    line, t = (run_unfused if args.path == "unfused" else run_ours)(args, w, rank, world, dist)
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, t, args.cpu_seconds)

@@ -4,10 +4,17 @@
 //
 // NATTEN issue #161 ("Backward pass is very slow towards much tokens and large kernels") benchmarks
 // this chain -- na2d_qk, softmax, na2d_av and their backward kernels QGRAD, KGRAD, AGRAD, VGRAD --
-// against the fused operation, and its maintainer notes that in fp32 the unfused chain can match the
-// fused one because both are memory-bound.  These kernels keep one thread per row (a query row, or a
-// key row for the gradients that gather over inverse windows) and let L1/L2 absorb the window
-// overlap.
+// against the fused operation; its maintainer expects the unfused chain to hold its own in fp32,
+// where both are limited by memory rather than arithmetic.
+//
+// Lane layout.  A [.., heads, D] row is D * s bytes, i.e. CPH = D * s / 16 chunks of 16 bytes, and
+// each row gets CPH consecutive lanes, one per chunk: consecutive lanes read consecutive 16-byte
+// chunks of q (and of any neighbour row, as neighbouring rows of the same offset sit next to each
+// other), so every row load of a warp is coalesced.  A dot product over D is then an in-register
+// sum of the lane's chunk plus a butterfly over the row's CPH lanes.  The weights of a warp's rows
+// ([rows, K], contiguous in memory) pass through a per-warp shared-memory stage of 128 offsets at a
+// time, so they are read and written with consecutive lanes on consecutive elements; the stage's
+// row stride is an odd number of 32-bit words, so the rows' lanes hit distinct banks.
 //
 // Attention weights are [B, L.., heads, K] with K = k0 k1 k2; window offset t = (t0 k1 + t1) k2 + t2
 // (axis 0 outermost) selects key c + d (s + t_a) along each axis a, s the window start.  Every tensor
@@ -25,70 +32,109 @@ using namespace dev;
 
 namespace {
 
+constexpr int kThreads = 256;   // 8 warps per block
+constexpr int kKC = 128;        // window offsets staged per warp and pass
+
+// 16-byte chunks: EPC elements widened to fp32 and back (round to nearest even).
 template <typename T>
-__device__ __forceinline__ float to_f(T v) {
-    return static_cast<float>(v);
-}
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int EPC = 4;
+    __device__ static void unpack(const uint4& u, float (&f)[4]) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+    __device__ static uint4 pack(const float (&f)[4]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+    }
+    __device__ static float get(float v) { return v; }
+    __device__ static float put(float v) { return v; }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int EPC = 8;
+    // a bf16 is the upper half of the fp32 with the same bits
+    __device__ static void two(uint32_t w, float& lo, float& hi) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ static void unpack(const uint4& u, float (&f)[8]) {
+        two(u.x, f[0], f[1]);
+        two(u.y, f[2], f[3]);
+        two(u.z, f[4], f[5]);
+        two(u.w, f[6], f[7]);
+    }
+    __device__ static uint32_t pair(float lo, float hi) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __device__ static uint4 pack(const float (&f)[8]) {
+        return make_uint4(pair(f[0], f[1]), pair(f[2], f[3]), pair(f[4], f[5]), pair(f[6], f[7]));
+    }
+    __device__ static float get(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __nv_bfloat16 put(float v) { return __float2bfloat16_rn(v); }
+};
+
+template <>
+struct Elem<__half> {
+    static constexpr int EPC = 8;
+    __device__ static void two(uint32_t w, float& lo, float& hi) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        lo = f.x;
+        hi = f.y;
+    }
+    __device__ static void unpack(const uint4& u, float (&f)[8]) {
+        two(u.x, f[0], f[1]);
+        two(u.y, f[2], f[3]);
+        two(u.z, f[4], f[5]);
+        two(u.w, f[6], f[7]);
+    }
+    __device__ static uint32_t pair(float lo, float hi) {
+        const __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t*>(&h);
+    }
+    __device__ static uint4 pack(const float (&f)[8]) {
+        return make_uint4(pair(f[0], f[1]), pair(f[2], f[3]), pair(f[4], f[5]), pair(f[6], f[7]));
+    }
+    __device__ static float get(__half v) { return __half2float(v); }
+    __device__ static __half put(float v) { return __float2half_rn(v); }
+};
+
 template <typename T>
-__device__ __forceinline__ T from_f(float v);
-template <>
-__device__ __forceinline__ float from_f<float>(float v) {
-    return v;
-}
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
-template <>
-__device__ __forceinline__ __half from_f<__half>(float v) {
-    return __float2half_rn(v);
+__device__ __forceinline__ uint4 ld16(const T* p) {
+    return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
-// D elements of a row, widened to fp32 (16-byte loads).
+// Lane layout of the row-parallel kernels (see the file comment).
 template <typename T, int D>
-__device__ __forceinline__ void load_row(const T* base, long long row, float (&v)[D]) {
-    constexpr int kPer = 16 / sizeof(T);
-    const uint4* src = reinterpret_cast<const uint4*>(base + row * D);
-#pragma unroll
-    for (int i = 0; i < D / kPer; ++i) {
-        const uint4 u = __ldg(src + i);
-        const T* e = reinterpret_cast<const T*>(&u);
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) v[i * kPer + j] = to_f(e[j]);
+struct Lanes {
+    static constexpr int EPC = Elem<T>::EPC;
+    static constexpr int CPH = D / EPC;            // lanes per row
+    static constexpr int RPW = 32 / CPH;           // rows per warp
+    static constexpr int SP = kKC + 4 / sizeof(T); // stage row stride (elements): an odd number of words
+    static constexpr size_t kStageBytes = size_t(kThreads / 32) * RPW * SP * sizeof(T);
+    static_assert(D % EPC == 0 && 32 % CPH == 0, "unsupported head dim");
+
+    int lane, c, rl, nrows;
+    long long row0, row;   // first row of the warp; this lane's row (lanes past the end repeat the last)
+
+    // Returns false for a warp with no rows (the whole warp leaves together).
+    __device__ bool init(long long rows) {
+        lane = threadIdx.x & 31;
+        c = lane % CPH;
+        rl = lane / CPH;
+        row0 = (static_cast<long long>(blockIdx.x) * kThreads + (threadIdx.x & ~31)) / CPH;
+        if (row0 >= rows) return false;
+        nrows = static_cast<int>(min(static_cast<long long>(RPW), rows - row0));
+        row = row0 + min(rl, nrows - 1);
+        return true;
     }
-}
-
-template <typename T, int D>
-__device__ __forceinline__ float dot_row(const float (&a)[D], const T* base, long long row) {
-    float v[D];
-    load_row<T, D>(base, row, v);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc = fmaf(a[c], v[c], acc);
-    return acc;
-}
-
-template <typename T, int D>
-__device__ __forceinline__ void axpy_row(float (&acc)[D], float s, const T* base, long long row) {
-    float v[D];
-    load_row<T, D>(base, row, v);
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = fmaf(s, v[c], acc[c]);
-}
-
-template <typename T, int D>
-__device__ __forceinline__ void store_row(T* base, long long row, const float (&v)[D], float mul) {
-    constexpr int kPer = 16 / sizeof(T);
-    uint4* dst = reinterpret_cast<uint4*>(base + row * D);
-#pragma unroll
-    for (int i = 0; i < D / kPer; ++i) {
-        uint4 u;
-        T* e = reinterpret_cast<T*>(&u);
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) e[j] = from_f<T>(v[i * kPer + j] * mul);
-        dst[i] = u;
-    }
-}
+};
 
 // Row decode and window geometry (embedded 3D, outermost axis first).
 struct Row {
@@ -108,215 +154,366 @@ __device__ __forceinline__ Row decode(const UnfParams& p, long long row) {
     return r;
 }
 
-__device__ __forceinline__ long long row_at(const UnfParams& p, long long b, const int (&x)[3], int h) {
-    return (((b * p.L[0] + x[0]) * p.L[1] + x[1]) * p.L[2] + x[2]) * p.heads + h;
-}
-
 // First neighbour (spatial index) of spatial index i along axis a.
 __device__ __forceinline__ int first_nb(const UnfParams& p, int a, int i) {
     const int d = p.d[a], c = i % d, j = i / d;
     return c + d * win_start(j, class_len(p.L[a], d, c), p.k[a]);
 }
 
-// Queries whose windows hold key index x along axis a: class indices [lo, hi] of x's class.
-__device__ __forceinline__ void inverse_range(const UnfParams& p, int a, int x, int& lo, int& hi) {
-    const int d = p.d[a], c = x % d, j = x / d, Lc = class_len(p.L[a], d, c), k = p.k[a];
-    lo = j < k ? 0 : j - (k >> 1);
-    hi = j >= Lc - k ? Lc - 1 : j + (k >> 1);
-}
-
-// attn[row, t] = scale q_row . k_(t-th neighbour)
-template <typename T, int D>
-__global__ void __launch_bounds__(128) qk_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
-    const T* q = static_cast<const T*>(p.a);
-    const T* k = static_cast<const T*>(p.b);
-    T* attn = static_cast<T*>(p.out0) + row * p.K;
-    const Row r = decode(p, row);
+// A row's window, walked one key line (fixed t0, t1) at a time: the line's first key row and the
+// row step between consecutive keys of the line (offset order t = (t0 k1 + t1) k2 + t2).
+struct Window {
     int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float qv[D];
-    load_row<T, D>(q, row, qv);
-    int t = 0, x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
-        for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2, ++t) {
-                x[2] = f[2] + p.d[2] * t2;
-                attn[t] = from_f<T>(p.scale * dot_row<T, D>(qv, k, row_at(p, r.b, x, r.h)));
-            }
-        }
+    long long b;
+    int h;
+    long long step;   // rows between keys t2 and t2 + 1
+
+    __device__ void start(const UnfParams& p, const Row& r) {
+        b = r.b;
+        h = r.h;
+        for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
+        step = static_cast<long long>(p.d[2]) * p.heads;
+    }
+    __device__ long long line_row(const UnfParams& p, int t0, int t1) const {
+        const long long tok = ((b * p.L[0] + f[0] + p.d[0] * t0) * p.L[1] + f[1] + p.d[1] * t1) * p.L[2] + f[2];
+        return tok * p.heads + h;
+    }
+};
+
+// Keys per group in the row-parallel kernels: their loads are issued together, and the dot
+// kernel reduces a group's partial sums across the row's lanes with a reduce-scatter.
+template <int CPH>
+struct Group {
+    static constexpr int G = CPH < 8 ? CPH : 8;
+};
+
+// Stage <-> global copies of a warp's weight rows [row0, row0 + nrows) x [tc, tc + clen).
+template <typename T, int SP>
+__device__ __forceinline__ void stage_store(T* out, const T* stage, long long row0, int nrows, int K, int tc,
+                                            int clen, int lane) {
+    for (int idx = lane; idx < nrows * clen; idx += 32) {
+        const int rr = idx / clen, j = idx - rr * clen;
+        out[(row0 + rr) * K + tc + j] = stage[rr * SP + j];
     }
 }
 
-// o_row = sum_t attn[row, t] v_(t-th neighbour)
-template <typename T, int D>
-__global__ void __launch_bounds__(128) av_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
-    const T* attn = static_cast<const T*>(p.a) + row * p.K;
-    const T* v = static_cast<const T*>(p.b);
-    const Row r = decode(p, row);
-    int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float acc[D];
+template <typename T, int SP>
+__device__ __forceinline__ void stage_load(T* stage, const T* in, long long row0, int nrows, int K, int tc, int clen,
+                                           int lane) {
+    for (int idx = lane; idx < nrows * clen; idx += 32) {
+        const int rr = idx / clen, j = idx - rr * clen;
+        stage[rr * SP + j] = in[(row0 + rr) * K + tc + j];
+    }
+}
+
+// Reduce-scatter of G partial sums over the row's lanes: afterwards s[0] holds, on lane c, the full
+// sum (over all CPH lanes) of entry c % G.  Each round halves the entries a lane keeps: the lane
+// whose bit m is set keeps the upper half and sends the lower half to its partner, which keeps
+// the lower half.
+template <int G, int CPH>
+__device__ __forceinline__ void reduce_scatter(float (&s)[G], int c) {
 #pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.f;
-    int t = 0, x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
+    for (int m = G / 2; m >= 1; m >>= 1) {
+        const bool upper = (c & m) != 0;
+#pragma unroll
+        for (int j = 0; j < m; ++j) {
+            const float send = upper ? s[j] : s[j + m];
+            const float keep = upper ? s[j + m] : s[j];
+            s[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+#pragma unroll
+    for (int m = G; m < CPH; m <<= 1) s[0] += __shfl_xor_sync(0xffffffffu, s[0], m);
+}
+
+// out[row, t] = scale * a_row . b_(t-th neighbour of row)
+// Logits (a = q, b = k, scale) and the weights' gradient of AV (a = dO, b = v, scale 1).
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    using Ln = Lanes<T, D>;
+    constexpr int EPC = Ln::EPC, CPH = Ln::CPH, SP = Ln::SP, G = Group<CPH>::G;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Ln ln;
+    if (!ln.init(p.rows)) return;
+    T* stage = reinterpret_cast<T*>(smem_raw) + (threadIdx.x >> 5) * Ln::RPW * SP;
+    const T* A = static_cast<const T*>(p.a);
+    const T* Bm = static_cast<const T*>(p.b) + ln.c * EPC;
+    T* out = static_cast<T*>(p.out0);
+
+    float af[EPC];
+    E::unpack(ld16(A + ln.row * D + ln.c * EPC), af);
+    Window win;
+    win.start(p, decode(p, ln.row));
+    const long long kstep = win.step * D;
+    int t = 0, tc = 0;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2, ++t) {
-                x[2] = f[2] + p.d[2] * t2;
-                axpy_row<T, D>(acc, to_f(attn[t]), v, row_at(p, r.b, x, r.h));
+            const T* kp = Bm + win.line_row(p, t0, t1) * D;
+            for (int t2 = 0; t2 < p.k[2]; t2 += G) {
+                const int n = min(G, p.k[2] - t2);
+                if (t + G > tc + kKC) {   // the stage is full: write it out
+                    __syncwarp();
+                    stage_store<T, SP>(out, stage, ln.row0, ln.nrows, p.K, tc, t - tc, ln.lane);
+                    __syncwarp();
+                    tc = t;
+                }
+                uint4 u[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) u[g] = g < n ? ld16(kp + (t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
+                float sg[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float bf[EPC];
+                    E::unpack(u[g], bf);
+                    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPC; e += 2) {
+                        s0 = fmaf(af[e], bf[e], s0);
+                        s1 = fmaf(af[e + 1], bf[e + 1], s1);
+                    }
+                    sg[g] = s0 + s1;
+                }
+                reduce_scatter<G, CPH>(sg, ln.c);
+                const int g = ln.c % G;
+                if (ln.c < G && g < n) stage[ln.rl * SP + (t - tc + g)] = E::put(sg[0] * p.scale);
+                t += n;
+            }
+        }
+    __syncwarp();
+    stage_store<T, SP>(out, stage, ln.row0, ln.nrows, p.K, tc, t - tc, ln.lane);
+}
+
+// out_row = scale * sum_t w[row, t] src_(t-th neighbour of row)
+// AV (w = attn, src = v, scale 1) and dQ of the logits (w = dattn, src = k, scale).
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) wsum_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    using Ln = Lanes<T, D>;
+    constexpr int EPC = Ln::EPC, CPH = Ln::CPH, SP = Ln::SP, G = Group<CPH>::G;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Ln ln;
+    if (!ln.init(p.rows)) return;
+    T* stage = reinterpret_cast<T*>(smem_raw) + (threadIdx.x >> 5) * Ln::RPW * SP;
+    const T* W = static_cast<const T*>(p.a);
+    const T* S = static_cast<const T*>(p.b) + ln.c * EPC;
+
+    float acc[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
+    Window win;
+    win.start(p, decode(p, ln.row));
+    const long long kstep = win.step * D;
+    int t = 0, tc = -kKC;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
+        for (int t1 = 0; t1 < p.k[1]; ++t1) {
+            const T* kp = S + win.line_row(p, t0, t1) * D;
+            for (int t2 = 0; t2 < p.k[2]; t2 += G) {
+                const int n = min(G, p.k[2] - t2);
+                if (t + G > tc + kKC) {   // stage the next weights
+                    tc = t;
+                    __syncwarp();
+                    stage_load<T, SP>(stage, W, ln.row0, ln.nrows, p.K, tc, min(kKC, p.K - tc), ln.lane);
+                    __syncwarp();
+                }
+                uint4 u[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) u[g] = g < n ? ld16(kp + (t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float w = g < n ? E::get(stage[ln.rl * SP + (t - tc + g)]) : 0.f;
+                    float sf[EPC];
+                    E::unpack(u[g], sf);
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w, sf[e], acc[e]);
+                }
+                t += n;
+            }
+        }
+    if (ln.rl < ln.nrows) {
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) acc[e] *= p.scale;
+        *reinterpret_cast<uint4*>(static_cast<T*>(p.out0) + ln.row * D + ln.c * EPC) = E::pack(acc);
+    }
+}
+
+// Gather over a key's inverse window: out_j = scale * sum over queries i whose window holds j of
+// w[i, t(i, j)] src_i, t(i, j) the offset of j in i's window.  dK (w = dattn, src = q, scale) and
+// dV (w = attn, src = dO, scale 1); no atomics, every key row is written once.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    using Ln = Lanes<T, D>;
+    constexpr int EPC = Ln::EPC, G = Group<Ln::CPH>::G < 4 ? 4 : Group<Ln::CPH>::G;
+    Ln ln;
+    if (!ln.init(p.rows)) return;
+    if (ln.rl >= ln.nrows) return;   // no warp-wide operation follows
+    const T* W = static_cast<const T*>(p.a);
+    const T* S = static_cast<const T*>(p.b) + ln.c * EPC;
+    const Row r = decode(p, ln.row);
+    // per axis: the key's class, class index, class length and the class indices of its queries
+    int cl[3], jk[3], Lc[3], lo[3], hi[3];
+    for (int a = 0; a < 3; ++a) {
+        const int d = p.d[a], k = p.k[a];
+        cl[a] = r.x[a] % d;
+        jk[a] = r.x[a] / d;
+        Lc[a] = class_len(p.L[a], d, cl[a]);
+        lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
+        hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
+    }
+    const long long qstep = static_cast<long long>(p.d[2]) * p.heads;
+    float acc[EPC];
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
+    for (int i0 = lo[0]; i0 <= hi[0]; ++i0) {
+        const int ta0 = jk[0] - win_start(i0, Lc[0], p.k[0]);
+        for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
+            const int ta01 = ta0 * p.k[1] + jk[1] - win_start(i1, Lc[1], p.k[1]);
+            const long long q0 =
+                ((r.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] + cl[2];
+            const long long qrow0 = q0 * p.heads + r.h;   // query row of class index 0 along axis 2
+            for (int i2 = lo[2]; i2 <= hi[2]; i2 += G) {
+                const int n = min(G, hi[2] - i2 + 1);
+                float w[G];
+                uint4 u[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (g < n) {
+                        const int ii = i2 + g;
+                        const long long qi = qrow0 + ii * qstep;
+                        const int t = ta01 * p.k[2] + jk[2] - win_start(ii, Lc[2], p.k[2]);
+                        w[g] = E::get(W[qi * p.K + t]);
+                        u[g] = ld16(S + qi * D);
+                    } else {
+                        w[g] = 0.f;
+                        u[g] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float sf[EPC];
+                    E::unpack(u[g], sf);
+#pragma unroll
+                    for (int e = 0; e < EPC; ++e) acc[e] = fmaf(w[g], sf[e], acc[e]);
+                }
             }
         }
     }
-    store_row<T, D>(static_cast<T*>(p.out0), row, acc, 1.f);
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) acc[e] *= p.scale;
+    *reinterpret_cast<uint4*>(static_cast<T*>(p.out0) + ln.row * D + ln.c * EPC) = E::pack(acc);
 }
 
-// y = softmax(x) over each row of K weights (x and y may be the same tensor).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+__device__ __forceinline__ float warp_maxf(float v) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// Rows of up to kRegK weights are held in registers (kRegK / 32 per lane) and read once; longer
+// rows are read again for each pass.
+constexpr int kRegK = 128;
+
+// y = softmax(x) over each row of K weights, one warp per row (x and y may be the same tensor: every
+// read of the row happens before its first write).
 template <typename T>
-__global__ void __launch_bounds__(128) softmax_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
+__global__ void __launch_bounds__(kThreads) softmax_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    constexpr int NV = kRegK / 32;
+    const long long row = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    if (row >= p.rows) return;   // warp-uniform
+    const int lane = threadIdx.x & 31;
     const T* x = static_cast<const T*>(p.a) + row * p.K;
     T* y = static_cast<T*>(p.out0) + row * p.K;
+    if (p.K <= kRegK) {
+        float v[NV];
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int t = lane + 32 * i;
+            v[i] = t < p.K ? E::get(x[t]) : -INFINITY;
+            m = fmaxf(m, v[i]);
+        }
+        m = warp_maxf(m);
+        float l = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            v[i] = lane + 32 * i < p.K ? expf(v[i] - m) : 0.f;
+            l += v[i];
+        }
+        const float inv = 1.f / warp_sum(l);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (lane + 32 * i < p.K) y[lane + 32 * i] = E::put(v[i] * inv);
+        return;
+    }
     float m = -INFINITY;
-    for (int t = 0; t < p.K; ++t) m = fmaxf(m, to_f(x[t]));
+    for (int t = lane; t < p.K; t += 32) m = fmaxf(m, E::get(x[t]));
+    m = warp_maxf(m);
     float l = 0.f;
-    for (int t = 0; t < p.K; ++t) l += expf(to_f(x[t]) - m);
-    const float inv = 1.f / l;
-    for (int t = 0; t < p.K; ++t) y[t] = from_f<T>(expf(to_f(x[t]) - m) * inv);
+    for (int t = lane; t < p.K; t += 32) l += expf(E::get(x[t]) - m);
+    const float inv = 1.f / warp_sum(l);
+    __syncwarp();
+    for (int t = lane; t < p.K; t += 32) y[t] = E::put(expf(E::get(x[t]) - m) * inv);
 }
 
-// dx = y * (dy - sum_t y dy) over each row (the softmax's gradient; dx may be dy's tensor).
+// dx = y * (dy - sum_t y dy) over each row, one warp per row (dx may be dy's tensor).
 template <typename T>
-__global__ void __launch_bounds__(128) softmax_bwd_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    constexpr int NV = kRegK / 32;
+    const long long row = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     if (row >= p.rows) return;
+    const int lane = threadIdx.x & 31;
     const T* y = static_cast<const T*>(p.a) + row * p.K;
     const T* dy = static_cast<const T*>(p.b) + row * p.K;
     T* dx = static_cast<T*>(p.out0) + row * p.K;
+    if (p.K <= kRegK) {
+        float vy[NV], vd[NV];
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int t = lane + 32 * i;
+            vy[i] = t < p.K ? E::get(y[t]) : 0.f;
+            vd[i] = t < p.K ? E::get(dy[t]) : 0.f;
+            s = fmaf(vy[i], vd[i], s);
+        }
+        s = warp_sum(s);
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (lane + 32 * i < p.K) dx[lane + 32 * i] = E::put(vy[i] * (vd[i] - s));
+        return;
+    }
     float s = 0.f;
-    for (int t = 0; t < p.K; ++t) s = fmaf(to_f(y[t]), to_f(dy[t]), s);
-    for (int t = 0; t < p.K; ++t) dx[t] = from_f<T>(to_f(y[t]) * (to_f(dy[t]) - s));
+    for (int t = lane; t < p.K; t += 32) s = fmaf(E::get(y[t]), E::get(dy[t]), s);
+    s = warp_sum(s);
+    __syncwarp();
+    for (int t = lane; t < p.K; t += 32) dx[t] = E::put(E::get(y[t]) * (E::get(dy[t]) - s));
 }
 
-// Gather over a query's window: out_row = mul * sum_t w[row, t] src_(t-th neighbour).
-// dQ of the logits (w = dattn, src = k, mul = scale).
-template <typename T, int D>
-__global__ void __launch_bounds__(128) gather_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
-    const T* w = static_cast<const T*>(p.a) + row * p.K;
-    const T* src = static_cast<const T*>(p.b);
-    const Row r = decode(p, row);
-    int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float acc[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.f;
-    int t = 0, x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
-        for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2, ++t) {
-                x[2] = f[2] + p.d[2] * t2;
-                axpy_row<T, D>(acc, to_f(w[t]), src, row_at(p, r.b, x, r.h));
-            }
-        }
-    }
-    store_row<T, D>(static_cast<T*>(p.out0), row, acc, p.scale);
-}
+int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
 
-// Gather over a key's inverse window: out_j = mul * sum over queries i whose window holds j of
-// w[i, t(i, j)] src_i, t(i, j) the offset of j in i's window.  dK (w = dattn, src = q, mul = scale)
-// and dV (w = attn, src = dO, mul = 1); no atomics, every key row is written once.
-template <typename T, int D>
-__global__ void __launch_bounds__(128) scatter_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
-    const T* w = static_cast<const T*>(p.a);
-    const T* src = static_cast<const T*>(p.b);
-    const Row r = decode(p, row);
-    int lo[3], hi[3], cl[3];
-    for (int a = 0; a < 3; ++a) {
-        inverse_range(p, a, r.x[a], lo[a], hi[a]);
-        cl[a] = r.x[a] % p.d[a];
-    }
-    float acc[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.f;
-    int x[3], ta[3];
-    for (int i0 = lo[0]; i0 <= hi[0]; ++i0) {
-        x[0] = cl[0] + p.d[0] * i0;
-        ta[0] = (r.x[0] - first_nb(p, 0, x[0])) / p.d[0];
-        for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
-            x[1] = cl[1] + p.d[1] * i1;
-            ta[1] = (r.x[1] - first_nb(p, 1, x[1])) / p.d[1];
-            for (int i2 = lo[2]; i2 <= hi[2]; ++i2) {
-                x[2] = cl[2] + p.d[2] * i2;
-                ta[2] = (r.x[2] - first_nb(p, 2, x[2])) / p.d[2];
-                const long long qi = row_at(p, r.b, x, r.h);
-                const int t = (ta[0] * p.k[1] + ta[1]) * p.k[2] + ta[2];
-                axpy_row<T, D>(acc, to_f(w[qi * p.K + t]), src, qi);
-            }
-        }
-    }
-    store_row<T, D>(static_cast<T*>(p.out0), row, acc, p.scale);
-}
-
-// dattn[row, t] = dO_row . v_(t-th neighbour)  (the weights' gradient of AV)
-template <typename T, int D>
-__global__ void __launch_bounds__(128) av_bwd_attn_kernel(const UnfParams p) {
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= p.rows) return;
-    const T* dO = static_cast<const T*>(p.a);
-    const T* v = static_cast<const T*>(p.b);
-    T* dattn = static_cast<T*>(p.out0) + row * p.K;
-    const Row r = decode(p, row);
-    int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float g[D];
-    load_row<T, D>(dO, row, g);
-    int t = 0, x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
-        for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2, ++t) {
-                x[2] = f[2] + p.d[2] * t2;
-                dattn[t] = from_f<T>(dot_row<T, D>(g, v, row_at(p, r.b, x, r.h)));
-            }
-        }
-    }
-}
-
-int launch_rows(void (*kernel)(const UnfParams), const UnfParams& p, cudaStream_t s) {
-    if (p.rows == 0) return 0;
-    const long long blocks = (p.rows + 127) / 128;
-    kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s>>>(p);
-    return static_cast<int>(cudaGetLastError());
-}
-
-// Kernel selection by element type and head dim.
-enum Op { kQK, kAV, kDQ, kDKV, kDAttn };
+enum Op { kDot, kWsum, kScatter };
 
 template <typename T, int D>
 int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
+    using Ln = Lanes<T, D>;
+    if (p.rows == 0) return 0;
+    const dim3 grid(launch_blocks(p.rows * Ln::CPH)), block(kThreads);
     switch (op) {
-        case kQK: return launch_rows(qk_kernel<T, D>, p, s);
-        case kAV: return launch_rows(av_kernel<T, D>, p, s);
-        case kDQ: return launch_rows(gather_kernel<T, D>, p, s);
-        case kDKV: return launch_rows(scatter_kernel<T, D>, p, s);
-        case kDAttn: return launch_rows(av_bwd_attn_kernel<T, D>, p, s);
+        case kDot: dot_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
+        case kWsum: wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
+        case kScatter: scatter_kernel<T, D><<<grid, block, 0, s>>>(p); break;
     }
-    return static_cast<int>(cudaErrorInvalidValue);
+    return static_cast<int>(cudaGetLastError());
 }
 
 template <typename T>
@@ -339,21 +536,21 @@ int launch_op(Op op, const UnfParams& p, int elem, cudaStream_t s) {
 template <typename T>
 int launch_softmax_t(bool bwd, const UnfParams& p, cudaStream_t s) {
     if (p.rows == 0) return 0;
-    const long long blocks = (p.rows + 127) / 128;
+    const dim3 grid(launch_blocks(p.rows * 32)), block(kThreads);
     if (bwd)
-        softmax_bwd_kernel<T><<<dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s>>>(p);
+        softmax_bwd_kernel<T><<<grid, block, 0, s>>>(p);
     else
-        softmax_kernel<T><<<dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s>>>(p);
+        softmax_kernel<T><<<grid, block, 0, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
 }  // namespace
 
-int launch_unfused_qk(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kQK, p, elem, s); }
-int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kAV, p, elem, s); }
-int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDQ, p, elem, s); }
-int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDKV, p, elem, s); }
-int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDAttn, p, elem, s); }
+int launch_unfused_qk(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDot, p, elem, s); }
+int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kWsum, p, elem, s); }
+int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kWsum, p, elem, s); }
+int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kScatter, p, elem, s); }
+int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDot, p, elem, s); }
 int launch_unfused_softmax(const UnfParams& p, int elem, bool bwd, cudaStream_t s) {
     if (elem == 0) return launch_softmax_t<__nv_bfloat16>(bwd, p, s);
     if (elem == 2) return launch_softmax_t<__half>(bwd, p, s);

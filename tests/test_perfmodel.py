@@ -31,3 +31,21 @@ def test_useful_flops_and_bytes():
     assert b == pytest.approx(2.5 * f)
     kb = bench.kernel_bytes(w)
     assert kb["fwd"] == pytest.approx(1024 * 1024 * 8 * (4 * 64 + 4))
+
+
+def test_unfused_call_work_model():
+    """Per-call bytes and FLOPs of the unfused chain: the weights (R x K elements) cross HBM once per
+    producer and once per consumer, and the products sum to the fused path's useful FLOPs."""
+    w = nain.WORKLOADS["2d_bf16_1024x1024_k9"]
+    work = bench.unfused_call_work(w)
+    R = w.tokens * w.heads
+    RK = R * w.keys_per_query * 2
+    RD = R * w.D * 2
+    assert work["softmax"] == (2 * RK, 0.0)
+    assert work["qk"][0] == 2 * RD + RK and work["av"][0] == 2 * RD + RK
+    f_fwd, f_bwd = bench.useful_flops(w)
+    assert sum(work[c][1] for c in ("qk", "av")) == f_fwd
+    assert sum(work[c][1] for c in ("av_bwd", "qk_bwd")) == 8.0 * R * w.keys_per_query * w.D
+    # the fused backward's useful count adds the recomputed logits and probabilities (2 products)
+    assert f_bwd == 10.0 * R * w.keys_per_query * w.D
+    assert abs(bench.fp32_fma_tflops() - 80.55) < 0.01
