@@ -73,6 +73,7 @@ def fp32_fma_tflops(sm_mhz=None):
 
 
 UNFUSED_CALLS = ("qk", "softmax", "av", "av_bwd", "softmax_bwd", "qk_bwd")
+UNFUSED_CALLS_RPB = UNFUSED_CALLS + ("rpb_grad",)
 
 
 def unfused_call_work(w):
@@ -87,7 +88,8 @@ def unfused_call_work(w):
             "av": (2 * RD + RK, prod),                 # attn, v -> o
             "av_bwd": (3 * RD + 2 * RK, 2 * prod),     # dO, attn, v -> dattn, dv
             "softmax_bwd": (3 * RK, 0.0),              # y, dy -> dx
-            "qk_bwd": (4 * RD + RK, 2 * prod)}         # dattn, q, k -> dq, dk
+            "qk_bwd": (4 * RD + RK, 2 * prod),         # dattn, q, k -> dq, dk
+            "rpb_grad": (RK, 0.0)}                     # dattn -> the bias table's gradient (a few KB)
 
 
 def arithmetic_intensity(w, fused=True, elem_bytes=None):
@@ -277,13 +279,19 @@ class Step:
 class UnfusedStep:
     """Buffers and launches of one fwd + bwd step through the unfused operations."""
 
-    def __init__(self, w, t):
+    def __init__(self, w, t, rpb=False):
         import neighborhood_attention_fwd_gb300 as na
 
         self.na = na
         self.w = w
         self.t = t
         q = t["q"]
+        self.rpb = self.drpb = self.rpb_ws = None
+        if rpb:   # a seeded bias table, its gradient and the reduction's workspace, all preallocated
+            self.rpb = nain.make_rpb(w, device=q.device, seed=w.seed)
+            self.drpb = torch.empty_like(self.rpb)
+            nbytes = na.na_rpb_grad_workspace_size(w.B, w.spatial, w.heads, w.kernel)
+            self.rpb_ws = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
         self.attn = torch.empty(q.shape[:-1] + (w.keys_per_query,), dtype=q.dtype, device=q.device)
         self.dattn = torch.empty_like(self.attn)
         self.o = torch.empty_like(q)
@@ -299,7 +307,7 @@ class UnfusedStep:
                 ev[name].record(s)
 
         mark("start")
-        na.na_qk(t["q"], t["k"], self.attn, w.kernel, w.dilation, w.scale)
+        na.na_qk(t["q"], t["k"], self.attn, w.kernel, w.dilation, w.scale, rpb=self.rpb)
         mark("qk")
         na.na_softmax(self.attn, self.attn, w.kernel)
         mark("softmax")
@@ -311,8 +319,14 @@ class UnfusedStep:
         mark("softmax_bwd")
         na.na_qk_bwd(self.dattn, t["q"], t["k"], self.dq, self.dk, w.kernel, w.dilation, w.scale)
         mark("qk_bwd")
+        if self.rpb is not None:
+            na.na_rpb_grad(self.dattn, self.drpb, w.kernel, w.dilation, workspace=self.rpb_ws)
+            mark("rpb_grad")
 
-    LAUNCHES_PER_STEP = 8   # av_bwd and qk_bwd launch two kernels each
+    LAUNCHES_PER_STEP = 8   # av_bwd and qk_bwd launch two kernels each; the bias gradient two more
+
+    def launches(self):
+        return self.LAUNCHES_PER_STEP + (2 if self.rpb is not None else 0)
 
 
 def run_unfused(args, w, rank, world, dist):
@@ -322,12 +336,13 @@ def run_unfused(args, w, rank, world, dist):
 
     na.load()
     t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
-    step = UnfusedStep(w, t)
+    step = UnfusedStep(w, t, rpb=args.rpb)
+    calls_run = UNFUSED_CALLS_RPB if args.rpb else UNFUSED_CALLS
     tensor_bytes = t["q"].numel() * t["q"].element_size()
     flush = None
     if tensor_bytes < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    names = ("start",) + UNFUSED_CALLS
+    names = ("start",) + calls_run
     for _ in range(args.warmup):
         step.launch()
         if flush is not None:
@@ -369,7 +384,7 @@ def run_unfused(args, w, rank, world, dist):
     alu_tflops = fp32_fma_tflops(clk.get("sm_mhz"))
     work = unfused_call_work(w)
     calls = {}
-    for name in UNFUSED_CALLS:
+    for name in calls_run:
         nbytes, flops = work[name]
         t_b, t_f = nbytes / hbm, flops / (alu_tflops * 1e12)
         sec = ms[name] * 1e-3
@@ -379,21 +394,22 @@ def run_unfused(args, w, rank, world, dist):
             ach, peak, unit, bound = nbytes / sec / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
         calls[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                        "frac": ach / peak, "roof_ms": max(t_b, t_f) * 1e3, "alg_bytes": nbytes, "flops": flops}
-    dom = max(UNFUSED_CALLS, key=lambda k: ms[k])
+    dom = max(calls_run, key=lambda k: ms[k])
     roof_step = sum(c["roof_ms"] for c in calls.values())
-    e2e = run_e2e(args, w, t, step, UnfusedStep) if not args.no_e2e else None
+    e2e = run_e2e(args, w, t, step, lambda w_, t_: UnfusedStep(w_, t_, rpb=args.rpb)) if not args.no_e2e else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.dtype != "fp32" else "f32",
         "data": "synthetic (seeded N(0,1) inputs, dO = ones as loss = O.sum())" if w.dO == "ones"
                 else "synthetic (seeded N(0,1) inputs and dO)",
-        "config": {"workload": w.name, "path": "unfused", "B": w.B, "spatial": list(w.spatial), "heads": w.heads,
+        "config": {"workload": w.name, "path": "unfused" + ("+rpb" if args.rpb else ""), "B": w.B, "spatial": list(w.spatial), "heads": w.heads,
                    "D": w.D, "kernel": list(w.kernel), "dilation": list(w.dilation),
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps (256 MB write)"},
         "ms": {"fwd": ms["qk"] + ms["softmax"] + ms["av"],
-               "bwd": ms["av_bwd"] + ms["softmax_bwd"] + ms["qk_bwd"], "fwd_bwd": ms_step, "per_call": ms},
+               "bwd": ms["av_bwd"] + ms["softmax_bwd"] + ms["qk_bwd"] + ms.get("rpb_grad", 0.0), "fwd_bwd": ms_step,
+               "per_call": ms},
         "roofline": {"bound": calls[dom]["bound"], "achieved": calls[dom]["achieved"], "peak": calls[dom]["peak"],
                      "unit": calls[dom]["unit"], "frac": calls[dom]["frac"],
                      "traffic": load_traffic(w.name + ":unfused", dom), "kernel": dom,
@@ -403,7 +419,7 @@ def run_unfused(args, w, rank, world, dist):
         "calls": calls,
         "clocks": clk,
         "wall_s_timed_region": wall,
-        "gpu_launches": UnfusedStep.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": step.launches() * args.steps,
         "e2e": e2e,
     }
     return line, t
@@ -624,11 +640,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
                     help="the fused kernels (default) or the unfused chain of separate operations")
+    ap.add_argument("--rpb", action="store_true",
+                    help="with --path unfused: add a relative positional bias to the logits and time its gradient")
     ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default=None,
                     help="run a bf16 workload's shapes with fp16 or fp32 tensors instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    if args.rpb and args.path != "unfused":
+        ap.error("--rpb applies to --path unfused (the fused kernels take no bias)")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -188,9 +188,13 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
  * D in {16, 32, 64, 128} (else NA_ERR_UNSUPPORTED); sizes are validated as for na_fwd.
  */
 
-/* attn = scale * q . k over each query's window (the logits). */
-na_status na_qk(const void* q, const void* k, void* attn, int B, int ndim, const int* spatial, int heads, int D,
-                const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream);
+/* attn = scale * q . k over each query's window (the logits), plus, when rpb is not null, the relative
+ * positional bias of each pair.  The maintainer's profile in the same issue names the logits kernel
+ * QKRPB.  rpb: fp32 [heads, 2 k_0 - 1, .., 2 k_{n-1} - 1], caller-owned device memory, 4-byte aligned;
+ * the pair (query i, its window offset t) reads rpb[h, (c(key)_a - c(i)_a + k_a - 1)_a], c(.)_a the
+ * position's class index along axis a (its index divided by dilation[a]). */
+na_status na_qk(const void* q, const void* k, const float* rpb, void* attn, int B, int ndim, const int* spatial,
+                int heads, int D, const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream);
 
 /* o = sum over each query's window of attn * v. */
 na_status na_av(const void* attn, const void* v, void* o, int B, int ndim, const int* spatial, int heads, int D,
@@ -215,6 +219,19 @@ na_status na_qk_bwd(const void* dattn, const void* q, const void* k, void* dq, v
 na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn, void* dv, int B, int ndim,
                     const int* spatial, int heads, int D, const int* kernel, const int* dilation, na_dtype dtype,
                     void* stream);
+
+/* Bytes of device workspace na_rpb_grad needs for this problem (0 on invalid arguments). */
+size_t na_rpb_grad_workspace_size(int B, int ndim, const int* spatial, int heads, const int* kernel);
+
+/* Gradient of na_qk's bias table given the logits' gradient dattn [B, L.., heads, K] (dtype):
+ * drpb[h, r] = sum over batch, queries and window offsets at relative position r of dattn.
+ * drpb: fp32 [heads, 2 k_0 - 1, ..], overwritten.  Two stages through the workspace (per block of
+ * tokens, then over blocks in a fixed order): deterministic, no atomics.  With workspace null the
+ * library allocates it on the stream (cudaMallocAsync) and frees it after use; otherwise it needs
+ * na_rpb_grad_workspace_size bytes (NA_ERR_WORKSPACE if fewer), 16-byte aligned. */
+na_status na_rpb_grad(const void* dattn, float* drpb, int B, int ndim, const int* spatial, int heads,
+                      const int* kernel, const int* dilation, na_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,8 @@ from . import build as _build
 __all__ = [
     "NAError", "load", "na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv",
     "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
-    "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd",
+    "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad",
+    "na_rpb_grad_workspace_size",
 ]
 
 NA_BF16, NA_FP32, NA_FP16 = 0, 1, 2
@@ -55,6 +56,7 @@ def load(path: str | None = None):
     IP = ctypes.POINTER(ctypes.c_int)
     geo = [I, I, IP, I, I]                   # B, ndim, spatial, heads, D
     kd = [IP, IP, F]                         # kernel, dilation, scale
+    geo_nd = [I, I, IP, I]                   # B, ndim, spatial, heads
     lib.na_fwd.argtypes = [P, P, P, P, P] + geo + kd + [I, P]
     lib.na_bwd.argtypes = [P, P, P, P, P, P, P, P, P] + geo + kd + [I, P, ctypes.c_size_t, P]
     lib.na_bwd_delta.argtypes = [P, P, P] + geo + [I, P]
@@ -66,15 +68,17 @@ def load(path: str | None = None):
     lib.na_strerror.argtypes = [I]
     lib.na_strerror.restype = ctypes.c_char_p
     lib.na_plan_info.argtypes = [I, I, I, IP, I, I, IP, IP, ctypes.POINTER(ctypes.c_int64)]
-    geo_nd = [I, I, IP, I]                   # B, ndim, spatial, heads
-    lib.na_qk.argtypes = [P, P, P] + geo + kd + [I, P]
+    lib.na_qk.argtypes = [P, P, P, P] + geo + kd + [I, P]
+    lib.na_rpb_grad.argtypes = [P, P] + geo_nd + [IP, IP, I, P, ctypes.c_size_t, P]
+    lib.na_rpb_grad_workspace_size.argtypes = [I, I, IP, I, IP]
+    lib.na_rpb_grad_workspace_size.restype = ctypes.c_size_t
     lib.na_av.argtypes = [P, P, P] + geo + [IP, IP, I, P]
     lib.na_softmax.argtypes = [P, P] + geo_nd + [IP, I, P]
     lib.na_softmax_bwd.argtypes = [P, P, P] + geo_nd + [IP, I, P]
     lib.na_qk_bwd.argtypes = [P, P, P, P, P] + geo + kd + [I, P]
     lib.na_av_bwd.argtypes = [P, P, P, P, P] + geo + [IP, IP, I, P]
     for f in ("na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv", "na_device_status", "na_plan_info",
-              "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd"):
+              "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -255,17 +259,42 @@ def _attn_geometry(attn: torch.Tensor, kernel):
     return int(attn.shape[0]), ndim, tuple(int(s) for s in attn.shape[1:-2]), int(attn.shape[-2]), kernel
 
 
-def na_qk(q, k, attn, kernel, dilation=None, scale=None, stream=None):
-    """attn = scale * q . k over each query's window."""
+def _rpb_shape(heads, kernel):
+    return (heads,) + tuple(2 * int(x) - 1 for x in kernel)
+
+
+def na_qk(q, k, attn, kernel, dilation=None, scale=None, stream=None, rpb=None):
+    """attn = scale * q . k over each query's window, plus the relative positional bias rpb (fp32
+    [heads, 2k_0 - 1, ..]) when given."""
     B, ndim, spatial, heads, D = _geometry(q)
     _check(k, q.shape, q.dtype, "k")
     _check(q, q.shape, q.dtype, "q")
     kernel, dilation = _kd(ndim, kernel, dilation)
     _check(attn, tuple(q.shape[:-1]) + (_window_size(kernel),), q.dtype, "attn")
+    if rpb is not None:
+        _check(rpb, _rpb_shape(heads, kernel), torch.float32, "rpb")
     scale = D ** -0.5 if scale is None else float(scale)
-    st = load().na_qk(q.data_ptr(), k.data_ptr(), attn.data_ptr(), B, ndim, _ints(spatial), heads, D,
-                      _ints(kernel), _ints(dilation), scale, _dtype_code(q), _stream(stream))
+    st = load().na_qk(q.data_ptr(), k.data_ptr(), None if rpb is None else rpb.data_ptr(), attn.data_ptr(), B,
+                      ndim, _ints(spatial), heads, D, _ints(kernel), _ints(dilation), scale, _dtype_code(q),
+                      _stream(stream))
     _ok(st, "na_qk")
+
+
+def na_rpb_grad_workspace_size(B, spatial, heads, kernel) -> int:
+    kernel = (kernel,) * len(spatial) if isinstance(kernel, int) else tuple(kernel)
+    return int(load().na_rpb_grad_workspace_size(int(B), len(spatial), _ints(spatial), int(heads), _ints(kernel)))
+
+
+def na_rpb_grad(dattn, drpb, kernel, dilation=None, workspace=None, stream=None):
+    """drpb (fp32 [heads, 2k_0 - 1, ..]) = the bias table's gradient given the logits' gradient dattn."""
+    B, ndim, spatial, heads, kernel = _attn_geometry(dattn, kernel)
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    _check(dattn, dattn.shape, dattn.dtype, "dattn")
+    _check(drpb, _rpb_shape(heads, kernel), torch.float32, "drpb")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    st = load().na_rpb_grad(dattn.data_ptr(), drpb.data_ptr(), B, ndim, _ints(spatial), heads, _ints(kernel),
+                            _ints(dilation), _dtype_code(dattn), ws_ptr, ws_bytes, _stream(stream))
+    _ok(st, "na_rpb_grad")
 
 
 def na_av(attn, v, o, kernel, dilation=None, stream=None):

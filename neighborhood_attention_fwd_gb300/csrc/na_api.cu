@@ -709,15 +709,17 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
 // Unfused operations
 // ---------------------------------------------------------------------------------------------
 
-na_status na_qk(const void* q, const void* k, void* attn, int B, int ndim, const int* spatial, int heads, int D,
-                const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream) {
+na_status na_qk(const void* q, const void* k, const float* rpb, void* attn, int B, int ndim, const int* spatial,
+                int heads, int D, const int* kernel, const int* dilation, float scale, na_dtype dtype, void* stream) {
     na::UnfParams p;
     na_status st = unfused_params(B, ndim, spatial, heads, D, kernel, dilation, scale, dtype, true, p);
     if (st != NA_OK) return st;
     if ((st = check_ptrs({q, k, attn})) != NA_OK) return st;
+    if (rpb && (reinterpret_cast<uintptr_t>(rpb) & 3u)) return NA_ERR_ALIGNMENT;
     p.a = q;
     p.b = k;
     p.out0 = attn;
+    p.rpb = rpb;
     return cuda_status(na::launch_unfused_qk(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
 }
 
@@ -789,6 +791,40 @@ na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn
     p.b = dO;
     p.out0 = dv;
     return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
+}
+
+size_t na_rpb_grad_workspace_size(int B, int ndim, const int* spatial, int heads, const int* kernel) {
+    int ones[3] = {1, 1, 1};
+    Geom g;
+    if (make_geom(B, ndim, spatial, heads, 16, kernel, ones, g) != NA_OK) return 0;
+    const int K = g.k[0] * g.k[1] * g.k[2];
+    const int table = (2 * g.k[0] - 1) * (2 * g.k[1] - 1) * (2 * g.k[2] - 1);
+    const size_t bytes = na::rpb_grad_workspace_bytes(tokens_of(g) * g.B, g.heads, K, table);
+    return (bytes + 255) / 256 * 256;
+}
+
+na_status na_rpb_grad(const void* dattn, float* drpb, int B, int ndim, const int* spatial, int heads,
+                      const int* kernel, const int* dilation, na_dtype dtype, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, 0, kernel, dilation, 1.f, dtype, false, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({dattn, drpb})) != NA_OK) return st;
+    const size_t need = na_rpb_grad_workspace_size(B, ndim, spatial, heads, kernel);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* ws = workspace;
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need) return NA_ERR_WORKSPACE;
+        if (!aligned16(ws)) return NA_ERR_ALIGNMENT;
+    } else {
+        if (cudaMallocAsync(&ws, need, s) != cudaSuccess) return NA_ERR_WORKSPACE;
+        owned = true;
+    }
+    p.a = dattn;
+    st = cuda_status(na::launch_unfused_rpb_grad(p, elem_of(dtype), p.rows / p.heads, static_cast<float*>(ws), drpb, s));
+    if (owned && cudaFreeAsync(ws, s) != cudaSuccess && st == NA_OK) st = NA_ERR_CUDA;
+    return st;
 }
 
 }  // extern "C"

@@ -84,7 +84,12 @@ struct UnfParams {
     int heads, D, K;
     long long rows;     // B * tokens * heads
     float scale;        // qk: scale; gather, scatter: the factor of the sum (scale, or 1)
+    const float* rpb;   // qk: relative positional bias [heads, 2k0-1, 2k1-1, 2k2-1], or null
 };
+
+// Tokens per block of the bias-gradient reduction's first stage, and the size of its partial sums.
+int rpb_grad_tokens_per_block(int K);
+size_t rpb_grad_workspace_bytes(long long tokens, int heads, int K, int table);
 
 // Launchers (defined next to their kernels).  Return a cudaError_t as int.
 int launch_fwd_tc(const TcParams& p, cudaStream_t stream);
@@ -103,6 +108,10 @@ int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t stream);
 int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t stream);
 int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t stream);
 int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t stream);
+// drpb[h, r] = sum over (batch, query, offset) at relative position r of dattn (two stages through
+// `partial`, which holds rpb_grad_workspace_bytes).
+int launch_unfused_rpb_grad(const UnfParams& p, int elem, long long tokens, float* partial, float* drpb,
+                            cudaStream_t s);
 int launch_unfused_softmax(const UnfParams& p, int elem, bool bwd, cudaStream_t stream);
 
 // Kernel attributes that depend on the plan (dynamic smem opt-in); called before the launch.

@@ -164,6 +164,7 @@ __device__ __forceinline__ int first_nb(const UnfParams& p, int a, int i) {
 // row step between consecutive keys of the line (offset order t = (t0 k1 + t1) k2 + t2).
 struct Window {
     int f[3];
+    int rb[3];        // per axis: relative-position index of window offset 0 (class coordinates)
     long long b;
     int h;
     long long step;   // rows between keys t2 and t2 + 1
@@ -171,8 +172,15 @@ struct Window {
     __device__ void start(const UnfParams& p, const Row& r) {
         b = r.b;
         h = r.h;
-        for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
+        for (int a = 0; a < 3; ++a) {
+            f[a] = first_nb(p, a, r.x[a]);
+            rb[a] = f[a] / p.d[a] - r.x[a] / p.d[a] + p.k[a] - 1;
+        }
         step = static_cast<long long>(p.d[2]) * p.heads;
+    }
+    // Index into one head's bias table [2k0-1, 2k1-1, 2k2-1] of window offset (t0, t1, 0).
+    __device__ int rpb_line(const UnfParams& p, int t0, int t1) const {
+        return ((rb[0] + t0) * (2 * p.k[1] - 1) + rb[1] + t1) * (2 * p.k[2] - 1) + rb[2];
     }
     __device__ long long line_row(const UnfParams& p, int t0, int t1) const {
         const long long tok = ((b * p.L[0] + f[0] + p.d[0] * t0) * p.L[1] + f[1] + p.d[1] * t1) * p.L[2] + f[2];
@@ -226,9 +234,9 @@ __device__ __forceinline__ void reduce_scatter(float (&s)[G], int c) {
     for (int m = G; m < CPH; m <<= 1) s[0] += __shfl_xor_sync(0xffffffffu, s[0], m);
 }
 
-// out[row, t] = scale * a_row . b_(t-th neighbour of row)
-// Logits (a = q, b = k, scale) and the weights' gradient of AV (a = dO, b = v, scale 1).
-template <typename T, int D>
+// out[row, t] = scale * a_row . b_(t-th neighbour of row) (+ rpb[head, relative position of t])
+// Logits (a = q, b = k, scale, optional bias) and the weights' gradient of AV (a = dO, b = v, scale 1).
+template <typename T, int D, bool BIAS>
 __global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
     using E = Elem<T>;
     using Ln = Lanes<T, D>;
@@ -246,10 +254,14 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
     Window win;
     win.start(p, decode(p, ln.row));
     const long long kstep = win.step * D;
+    const float* bias = BIAS ? p.rpb + static_cast<long long>(win.h) * (2 * p.k[0] - 1) * (2 * p.k[1] - 1) *
+                                           (2 * p.k[2] - 1)
+                             : nullptr;
     int t = 0, tc = 0;
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const T* kp = Bm + win.line_row(p, t0, t1) * D;
+            const int bline = BIAS ? win.rpb_line(p, t0, t1) : 0;
             for (int t2 = 0; t2 < p.k[2]; t2 += G) {
                 const int n = min(G, p.k[2] - t2);
                 if (t + G > tc + kKC) {   // the stage is full: write it out
@@ -276,7 +288,9 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
                 }
                 reduce_scatter<G, CPH>(sg, ln.c);
                 const int g = ln.c % G;
-                if (ln.c < G && g < n) stage[ln.rl * SP + (t - tc + g)] = E::put(sg[0] * p.scale);
+                if (ln.c < G && g < n)
+                    stage[ln.rl * SP + (t - tc + g)] =
+                        E::put(BIAS ? fmaf(sg[0], p.scale, __ldg(bias + bline + t2 + g)) : sg[0] * p.scale);
                 t += n;
             }
         }
@@ -499,6 +513,74 @@ __global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p
     for (int t = lane; t < p.K; t += 32) dx[t] = E::put(E::get(y[t]) * (E::get(dy[t]) - s));
 }
 
+// Gradient of the bias table, first stage: block (chunk of tokens) sums dattn over its tokens'
+// (query, offset) pairs, for every head, into a shared-memory copy of the tables.  Consecutive
+// tokens with the same relative indices of window offset 0 (every interior query along a line) form
+// a run.  One thread per (head, window offset) sums its column over the run straight from global
+// memory -- a token's rows for all heads are contiguous, so the threads' loads are too -- and adds
+// the sum at that offset's table entry.  Distinct (head, offset) pairs of one run hit distinct
+// entries, and runs are separated by a barrier.  Fixed order, no atomics: the result does not
+// depend on scheduling.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rpb_grad_partial_kernel(const UnfParams p, long long tokens, int tpb,
+                                                                   float* partial) {
+    using E = Elem<T>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const int K = p.K, H = p.heads;
+    const int S1 = 2 * p.k[1] - 1, S2 = 2 * p.k[2] - 1, S = (2 * p.k[0] - 1) * S1 * S2;
+    float* tab = reinterpret_cast<float*>(smem_raw);                        // [heads][S]
+    int* rel = reinterpret_cast<int*>(tab + static_cast<size_t>(H) * S);    // [tpb][3]
+    const long long tok0 = static_cast<long long>(blockIdx.x) * tpb;
+    const int nt = static_cast<int>(min(static_cast<long long>(tpb), tokens - tok0));
+    const T* W = static_cast<const T*>(p.a) + tok0 * H * K;
+    for (int e = threadIdx.x; e < H * S; e += kThreads) tab[e] = 0.f;
+    for (int rr = threadIdx.x; rr < nt; rr += kThreads) {
+        const Row r = decode(p, (tok0 + rr) * H);
+        for (int a = 0; a < 3; ++a)
+            rel[rr * 3 + a] = first_nb(p, a, r.x[a]) / p.d[a] - r.x[a] / p.d[a] + p.k[a] - 1;
+    }
+    __syncthreads();
+    const int pairs = H * K;   // (head, offset) pairs of one token: its H * K contiguous weights
+    for (int rr = 0; rr < nt;) {
+        const int r0 = rel[rr * 3], r1 = rel[rr * 3 + 1], r2 = rel[rr * 3 + 2];
+        int end = rr + 1;
+        while (end < nt && rel[end * 3] == r0 && rel[end * 3 + 1] == r1 && rel[end * 3 + 2] == r2) ++end;
+        for (int pi = threadIdx.x; pi < pairs; pi += kThreads) {
+            const T* col = W + pi;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            int q = rr;
+            for (; q + 4 <= end; q += 4) {
+                a0 += E::get(col[static_cast<long long>(q) * pairs]);
+                a1 += E::get(col[static_cast<long long>(q + 1) * pairs]);
+                a2 += E::get(col[static_cast<long long>(q + 2) * pairs]);
+                a3 += E::get(col[static_cast<long long>(q + 3) * pairs]);
+            }
+            for (; q < end; ++q) a0 += E::get(col[static_cast<long long>(q) * pairs]);
+            const int h = pi / K, t = pi - h * K;
+            const int t2 = t % p.k[2], t1 = (t / p.k[2]) % p.k[1], t0 = t / (p.k[2] * p.k[1]);
+            tab[h * S + ((r0 + t0) * S1 + r1 + t1) * S2 + r2 + t2] += (a0 + a1) + (a2 + a3);
+        }
+        __syncthreads();
+        rr = end;
+    }
+    float* out = partial + static_cast<long long>(blockIdx.x) * H * S;
+    for (int e = threadIdx.x; e < H * S; e += kThreads) out[e] = tab[e];
+}
+
+// Second stage: drpb[e] = sum over chunks of partial[chunk][e], one warp per entry e: lane j sums
+// chunks j, j + 32, ... in order, then a fixed butterfly adds the lanes.
+__global__ void __launch_bounds__(kThreads) rpb_grad_sum_kernel(const float* partial, long long chunks, int entries,
+                                                                float* drpb) {
+    const int e = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);   // warp-uniform
+    if (e >= entries) return;
+    const int lane = threadIdx.x & 31;
+    float acc = 0.f;
+    for (long long c = lane; c < chunks; c += 32) acc += partial[c * entries + e];
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (lane == 0) drpb[e] = acc;
+}
+
 int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
 
 enum Op { kDot, kWsum, kScatter };
@@ -509,7 +591,12 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
     if (p.rows == 0) return 0;
     const dim3 grid(launch_blocks(p.rows * Ln::CPH)), block(kThreads);
     switch (op) {
-        case kDot: dot_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
+        case kDot:
+            if (p.rpb)
+                dot_kernel<T, D, true><<<grid, block, Ln::kStageBytes, s>>>(p);
+            else
+                dot_kernel<T, D, false><<<grid, block, Ln::kStageBytes, s>>>(p);
+            break;
         case kWsum: wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
         case kScatter: scatter_kernel<T, D><<<grid, block, 0, s>>>(p); break;
     }
@@ -551,6 +638,42 @@ int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t s) { return lau
 int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kWsum, p, elem, s); }
 int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kScatter, p, elem, s); }
 int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDot, p, elem, s); }
+// Tokens per block of the first stage (the partial sums are one set of tables per block).
+int rpb_grad_tokens_per_block(int K) { return K <= 1024 ? 1024 : 256; }
+
+size_t rpb_grad_workspace_bytes(long long tokens, int heads, int K, int table) {
+    const long long chunks = (tokens + rpb_grad_tokens_per_block(K) - 1) / rpb_grad_tokens_per_block(K);
+    return static_cast<size_t>(chunks) * heads * table * sizeof(float);
+}
+
+int launch_unfused_rpb_grad(const UnfParams& p, int elem, long long tokens, float* partial, float* drpb,
+                            cudaStream_t s) {
+    const int tpb = rpb_grad_tokens_per_block(p.K);
+    const long long chunks = (tokens + tpb - 1) / tpb;
+    const int table = (2 * p.k[0] - 1) * (2 * p.k[1] - 1) * (2 * p.k[2] - 1);
+    const int entries = p.heads * table;
+    if (tokens == 0) return static_cast<int>(cudaMemsetAsync(drpb, 0, sizeof(float) * entries, s));
+    const size_t smem = static_cast<size_t>(p.heads) * table * sizeof(float) + static_cast<size_t>(tpb) * 3 * sizeof(int);
+    if (smem > 227 * 1024) return static_cast<int>(cudaErrorInvalidValue);   // heads x table too large
+    const dim3 grid(static_cast<unsigned>(chunks));
+    auto run = [&](auto kernel) {
+        if (smem > 48 * 1024)   // many heads or very large windows: more than the default
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        kernel<<<grid, kThreads, smem, s>>>(p, tokens, tpb, partial);
+    };
+    if (elem == 0)
+        run(rpb_grad_partial_kernel<__nv_bfloat16>);
+    else if (elem == 2)
+        run(rpb_grad_partial_kernel<__half>);
+    else
+        run(rpb_grad_partial_kernel<float>);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return static_cast<int>(e);
+    rpb_grad_sum_kernel<<<launch_blocks(static_cast<long long>(entries) * 32), kThreads, 0, s>>>(partial, chunks,
+                                                                                                 entries, drpb);
+    return static_cast<int>(cudaGetLastError());
+}
+
 int launch_unfused_softmax(const UnfParams& p, int elem, bool bwd, cudaStream_t s) {
     if (elem == 0) return launch_softmax_t<__nv_bfloat16>(bwd, p, s);
     if (elem == 2) return launch_softmax_t<__half>(bwd, p, s);

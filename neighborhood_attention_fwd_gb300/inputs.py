@@ -107,6 +107,14 @@ def make_weights(w: Workload, kind: str = "randn", device="cpu", seed: int = 0):
     return x.to(w.torch_dtype())
 
 
+def make_rpb(w: Workload, device="cpu", seed: int = 0):
+    """A seeded relative-positional-bias table, fp32 [heads, 2k_0 - 1, ..], iid N(0, 1)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    shape = (w.heads,) + tuple(2 * k - 1 for k in w.kernel)
+    return torch.randn(shape, generator=gen, dtype=torch.float32, device=device)
+
+
 def small_workload(dtype: str, spatial, heads, D, kernel, dilation, B=1, dO="randn", seed=7) -> Workload:
     """An ad-hoc workload (parity sweeps)."""
     return Workload(f"adhoc_{dtype}_{'x'.join(map(str, spatial))}", dtype, B, tuple(spatial), heads, D,

@@ -18,6 +18,11 @@ oracle (``oracle.first_neighbour``):
 * qk_bwd:       dq_i = scale * sum_t dattn[i, t] k_{n(i, t)};  dk_j = scale * sum_{(i, t): n(i, t) = j} dattn[i, t] q_i
 * av_bwd:       dattn[i, t] = dO_i . v_{n(i, t)};  dv_j = sum_{(i, t): n(i, t) = j} attn[i, t] dO_i
 
+Relative positional bias (the maintainer's profile names the logits kernel QKRPB): an optional table
+rpb[heads, 2 k_0 - 1, .., 2 k_{n-1} - 1] adds rpb[h, (c(n(i, t))_a - c(i)_a + k_a - 1)_a] to attn[i, t],
+where c(.)_a is a position's class index along axis a (its index divided by the dilation).  Its
+gradient is drpb[h, r] = sum over (batch, query, offset) with relative position r of dattn[i, t].
+
 n(i, t) is the t-th key of query i's window: the window is the Cartesian product of the per-axis
 windows, and t = (t_0 k_1 + t_1) k_2 + t_2 orders its offsets with the first axis outermost.  The
 weight tensors are [B, L.., heads, K].
@@ -115,18 +120,57 @@ def _rows_of(rows, B, N, heads):
     return r // heads // N, (r // heads) % N, r % heads
 
 
-def qk(q, k, kernel, dilation, scale, rows=None):
-    """Attention logits: [B, L.., heads, K], or [len(rows), K] for sampled rows."""
+def relative_index(g, tok):
+    """[n, K] flat index into one head's bias table of every (query token, offset) pair: per axis the
+    key's class index minus the query's, plus k - 1, flattened with the first axis outermost."""
+    x = g.coords(tok)
+    n = x.shape[0]
+    idx = np.zeros((n,) + (1,) * len(g.kernel), dtype=np.int64)
+    for a, tab in enumerate(g.tabs):
+        d, k = g.dilation[a], g.kernel[a]
+        rel = tab[x[:, a]] // d - (x[:, a] // d)[:, None] + (k - 1)       # [n, k_a]
+        assert rel.min() >= 0 and rel.max() <= 2 * k - 2
+        span = int(np.prod([2 * kk - 1 for kk in g.kernel[a + 1:]]))
+        shape = [n] + [1] * len(g.kernel)
+        shape[1 + a] = k
+        idx = idx + (rel * span).reshape(shape)
+    return idx.reshape(n, g.K)
+
+
+def qk(q, k, kernel, dilation, scale, rows=None, rpb=None):
+    """Attention logits: [B, L.., heads, K], or [len(rows), K] for sampled rows.  rpb (optional):
+    [heads, 2 k_0 - 1, ..] bias table added to every logit at its relative position."""
     qf, kf = _split(q), _split(k)
     B, N, heads, _ = qf.shape
     g = Geometry(q.shape[1:-2], kernel, dilation)
+    table = None if rpb is None else _f64(rpb).reshape(heads, -1)
     if rows is None:
         nb = g.neighbours(np.arange(N))                       # [N, K]
         out = scale * np.einsum("bnhc,bnthc->bnht", _f64(qf), _f64(kf[:, nb]))
+        if table is not None:
+            rel = relative_index(g, np.arange(N))             # [N, K]
+            out = out + table[:, rel].transpose(1, 0, 2)[None]
         return out.reshape(tuple(q.shape[:-1]) + (g.K,))
     b, tok, h = _rows_of(rows, B, N, heads)
     nb = g.neighbours(tok)
-    return scale * np.einsum("rc,rtc->rt", _f64(qf[b, tok, h]), _f64(kf[b[:, None], nb, h[:, None]]))
+    out = scale * np.einsum("rc,rtc->rt", _f64(qf[b, tok, h]), _f64(kf[b[:, None], nb, h[:, None]]))
+    if table is not None:
+        out = out + table[h[:, None], relative_index(g, tok)]
+    return out
+
+
+def rpb_grad(dattn, kernel, dilation):
+    """Gradient of the bias table given the logits' gradient dattn [B, L.., heads, K]: a sum over
+    batch, queries and offsets of dattn at each relative position, [heads, 2 k_0 - 1, ..]."""
+    wf = _split(dattn)
+    B, N, heads, K = wf.shape
+    g = Geometry(dattn.shape[1:-2], kernel, dilation)
+    rel = relative_index(g, np.arange(N))                     # [N, K]
+    size = int(np.prod([2 * kk - 1 for kk in g.kernel]))
+    out = np.zeros((heads, size), dtype=np.float64)
+    for h in range(heads):
+        out[h] = np.bincount(rel.ravel(), weights=_f64(wf[:, :, h, :]).sum(axis=0).ravel(), minlength=size)
+    return out.reshape((heads,) + tuple(2 * kk - 1 for kk in g.kernel))
 
 
 def av(attn, v, kernel, dilation, rows=None):

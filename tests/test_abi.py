@@ -82,7 +82,8 @@ def test_unfused_entry_points_reject_bad_arguments(lib):
     f = ctypes.c_float
 
     def qk(ptr=16, kernel=(5, 5), D=32, dtype=0, scale=0.1):
-        return lib.na_qk(P(ptr), P(ptr), P(ptr), 1, 2, I((16, 16)), 2, D, I(kernel), I((1, 1)), f(scale), dtype, None)
+        return lib.na_qk(P(ptr), P(ptr), None, P(ptr), 1, 2, I((16, 16)), 2, D, I(kernel), I((1, 1)), f(scale), dtype,
+                         None)
 
     # only argument forms that fail validation are passed: a valid call would launch a kernel
     assert qk(ptr=None) == 1
@@ -100,6 +101,18 @@ def test_unfused_entry_points_reject_bad_arguments(lib):
                          None) == 1
     assert lib.na_av_bwd(P(16), P(16), P(16), P(16), P(16), 1, 2, I((16, 16)), 2, 32, I((5, 5)), I((1, 4)), 0,
                          None) == 1   # class of 4 positions < 5
+    assert lib.na_qk(P(16), P(16), P(18), P(16), 1, 2, I((16, 16)), 2, 32, I((5, 5)), I((1, 1)), f(0.1), 0,
+                     None) == 3       # misaligned bias table
+    assert lib.na_rpb_grad(P(16), None, 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, None, 0, None) == 1
+    assert lib.na_rpb_grad(P(16), P(16), 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, P(16), 8, None) == 6
+
+
+def test_rpb_grad_workspace_size(lib):
+    # 1024 x 1024 tokens, 8 heads, 9x9: 1024 tokens per block -> 1024 blocks of 8 x 289 fp32 partial sums
+    n = na.na_rpb_grad_workspace_size(1, (1024, 1024), 8, (9, 9))
+    blocks = 1024
+    assert n == (blocks * 8 * 289 * 4 + 255) // 256 * 256
+    assert na.na_rpb_grad_workspace_size(1, (16, 16), 2, (4, 5)) == 0      # even kernel: invalid
 
 
 @pytest.mark.parametrize("name", [n for n in nain.WORKLOADS if nain.WORKLOADS[n].dtype == "bf16"])

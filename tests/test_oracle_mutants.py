@@ -97,7 +97,12 @@ UNFUSED_MUTANTS = {
                                 "idx = idx + (tab[x[:, a]][:, ::-1] * self.strides[a]).reshape(shape)"),
     "dv_scatters_dO_with_dattn": ("dv = _scatter(af, gf, g, rows, B, N, heads)",
                                   "dv = _scatter(af, vf, g, rows, B, N, heads)"),
-    "qk_missing_scale_on_rows": ("return scale * np.einsum(\"rc,rtc->rt\"", "return np.einsum(\"rc,rtc->rt\""),
+    "qk_missing_scale_on_rows": ("out = scale * np.einsum(\"rc,rtc->rt\"", "out = np.einsum(\"rc,rtc->rt\""),
+    "rpb_relative_sign": ("rel = tab[x[:, a]] // d - (x[:, a] // d)[:, None] + (k - 1)",
+                          "rel = (x[:, a] // d)[:, None] - tab[x[:, a]] // d + (k - 1)"),
+    "rpb_axis_order": ("span = int(np.prod([2 * kk - 1 for kk in g.kernel[a + 1:]]))",
+                       "span = int(np.prod([2 * kk - 1 for kk in g.kernel[:a]]))"),
+    "rpb_grad_drops_batch": ("weights=_f64(wf[:, :, h, :]).sum(axis=0).ravel()", "weights=_f64(wf[0, :, h, :]).ravel()"),
 }
 
 
@@ -122,6 +127,12 @@ def unfused_pin_results(mod):
         checks[f"adjoint_{i}"] = lambda c=case: unpins.test_adjoint_identities(*c)
     for i in (2, 4, 6, 7):
         checks[f"rows_{i}"] = lambda c=pins.CASES[i]: unpins.test_sampled_rows_match_full(*c)
+    for i in (0, 2, 4, 6):
+        checks[f"rpb_dense_{i}"] = lambda c=pins.CASES[i]: unpins.test_rpb_chain_matches_dense_attention_with_bias(*c)
+    for i, case in enumerate(pins.CASES):
+        checks[f"rpb_adjoint_{i}"] = lambda c=case: unpins.test_rpb_grad_is_the_adjoint_of_the_bias(*c)
+    checks["rpb_counts"] = unpins.test_rpb_grad_counts_pairs_per_relative_position
+    checks["rpb_rows"] = unpins.test_rpb_sampled_rows_match_full
     saved = unpins.un
     unpins.un = mod
     try:

@@ -6,9 +6,11 @@ backward (the fused oracle is pinned on its own in test_oracle.py); every linear
 gradient must satisfy the adjoint identity <dy, A x> = <A^T dy, x>; the offset order of the weights
 is read back from an index-coded key tensor and compared with the window re-derived as "the k
 same-class positions nearest to i"; softmax_bwd is compared with central finite differences; and
-the sampled-row routes (inverse lists) must agree with the full scatter.  A dropped scale, a
-transposed offset order, a wrong inverse list or a sign error in the softmax gradient fails one of
-them.
+the sampled-row routes (inverse lists) must agree with the full scatter.  The relative positional
+bias is checked against dense attention whose bias is looked up from the two tokens' coordinates,
+and its gradient against the adjoint identity (the logits are affine in the table) and against
+closed-form pair counts.  A dropped scale, a transposed offset order, a wrong inverse list, a sign
+error in the softmax gradient or a mirrored bias index fails one of them.
 """
 import itertools
 
@@ -147,3 +149,83 @@ def test_inverse_lists_cover_every_pair_once():
             assert nb[qi, t] == j
             pairs.add((qi, t))
     assert len(pairs) == g.N * g.K
+
+
+# ---------------------------------------------------------------------------------------------
+# Relative positional bias
+# ---------------------------------------------------------------------------------------------
+
+def dense_bias(spatial, kernel, dilation, table):
+    """[heads, N, N] dense bias: for key j in query i's window (nearest-k-in-class characterisation),
+    table[h, ((y_a - x_a) / d_a + k_a - 1)_a] from the two tokens' coordinates; -inf elsewhere."""
+    coords = list(itertools.product(*[range(L) for L in spatial]))
+    N = len(coords)
+    heads = table.shape[0]
+    out = np.full((heads, N, N), -np.inf)
+    for i, x in enumerate(coords):
+        per_axis = [nearest_k(x[a], spatial[a], kernel[a], dilation[a]) for a in range(len(spatial))]
+        for y in itertools.product(*per_axis):
+            j = coords.index(y)
+            rel = tuple((y[a] - x[a]) // dilation[a] + kernel[a] - 1 for a in range(len(spatial)))
+            out[:, i, j] = table[(slice(None),) + rel]
+    return out
+
+
+@pytest.mark.parametrize("spatial,kernel,dilation,B,heads,D", [CASES[0], CASES[2], CASES[4], CASES[6]])
+def test_rpb_chain_matches_dense_attention_with_bias(spatial, kernel, dilation, B, heads, D):
+    q, k, v, _ = case_tensors(spatial, B, heads, D, 61)
+    table = rand((heads,) + tuple(2 * kk - 1 for kk in kernel), 62)
+    scale = 0.33
+    o = un.av(un.softmax(un.qk(q, k, kernel, dilation, scale, rpb=table)), v, kernel, dilation)
+    N = int(np.prod(spatial))
+    qf, kf, vf = (x.reshape(B, N, heads, D) for x in (q, k, v))
+    s = scale * np.einsum("bihc,bjhc->bhij", qf, kf) + dense_bias(spatial, kernel, dilation, table)[None]
+    p = np.exp(s - s.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    ref = np.einsum("bhij,bjhc->bihc", p, vf).reshape(o.shape)
+    assert np.abs(o - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("spatial,kernel,dilation,B,heads,D", CASES)
+def test_rpb_grad_is_the_adjoint_of_the_bias(spatial, kernel, dilation, B, heads, D):
+    """The logits are affine in the table: <dattn, qk(rpb) - qk(0)> = <rpb_grad(dattn), rpb>."""
+    q, k, _, _ = case_tensors(spatial, B, heads, D, 71)
+    K = int(np.prod(kernel))
+    table = rand((heads,) + tuple(2 * kk - 1 for kk in kernel), 72)
+    w = rand((B, *spatial, heads, K), 73)
+    diff = un.qk(q, k, kernel, dilation, 0.5, rpb=table) - un.qk(q, k, kernel, dilation, 0.5)
+    lhs = np.sum(w * diff)
+    rhs = np.sum(un.rpb_grad(w, kernel, dilation) * table)
+    assert abs(lhs - rhs) <= 1e-10 * max(1.0, abs(lhs))
+
+
+def test_rpb_constant_per_head_leaves_probabilities_unchanged():
+    spatial, kernel, dilation = (9, 10), (3, 5), (2, 1)
+    q, k, _, _ = case_tensors(spatial, 1, 3, 4, 81)
+    table = np.zeros((3, 5, 9)) + np.array([1.5, -2.0, 7.0])[:, None, None]
+    a = un.softmax(un.qk(q, k, kernel, dilation, 0.7, rpb=table))
+    b = un.softmax(un.qk(q, k, kernel, dilation, 0.7))
+    assert np.abs(a - b).max() <= 1e-14
+
+
+def test_rpb_sampled_rows_match_full():
+    spatial, kernel, dilation = (5, 4, 7), (1, 3, 3), (2, 1, 2)
+    q, k, _, _ = case_tensors(spatial, 2, 2, 4, 91)
+    table = rand((2, 1, 5, 5), 92)
+    total = 2 * int(np.prod(spatial)) * 2
+    rows = np.random.default_rng(93).choice(total, size=19, replace=False)
+    full = un.qk(q, k, kernel, dilation, 0.4, rpb=table).reshape(total, -1)[rows]
+    assert np.allclose(un.qk(q, k, kernel, dilation, 0.4, rows, rpb=table), full, rtol=0, atol=1e-12)
+
+
+def test_rpb_grad_counts_pairs_per_relative_position():
+    """With dattn = 1 everywhere, drpb counts the (batch, query, offset) pairs at each relative
+    position: summed over the table it is B * N * K per head, and in a 1D interior-only case each
+    of the k centred offsets gets every query."""
+    spatial, kernel, dilation = (9, 10), (3, 5), (2, 1)
+    g = un.Geometry(spatial, kernel, dilation)
+    ones = np.ones((2, *spatial, 3, g.K))
+    d = un.rpb_grad(ones, kernel, dilation)
+    assert np.allclose(d.reshape(3, -1).sum(-1), 2 * g.N * g.K)
+    d1 = un.rpb_grad(np.ones((1, 5, 1, 5)), (5,), (1,))      # L = k: every query's window is the whole axis
+    assert d1.reshape(-1).tolist() == [1, 2, 3, 4, 5, 4, 3, 2, 1]

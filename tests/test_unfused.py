@@ -166,7 +166,8 @@ def test_full_size_chain_sampled(cuda_lib):
     hp, hg = f32(probs), f32(grad)
     kern, dil, scale = w.kernel, w.dilation, w.scale
     attn = torch.empty_like(grad)
-    na.na_qk(t["q"], t["k"], attn, kern, dil, scale)
+    rpb = nain.make_rpb(w, device="cuda", seed=79)
+    na.na_qk(t["q"], t["k"], attn, kern, dil, scale, rpb=rpb)
     o2 = torch.empty_like(t["q"])
     na.na_av(probs, t["v"], o2, kern, dil)
     y = torch.empty_like(grad)
@@ -178,7 +179,7 @@ def test_full_size_chain_sampled(cuda_lib):
     dattn, dv2 = torch.empty_like(grad), torch.empty_like(t["q"])
     na.na_av_bwd(t["dO"], probs, t["v"], dattn, dv2, kern, dil)
     status_ok(na)
-    compare("attn", pick(attn), un.qk(h["q"], h["k"], kern, dil, scale, rows), tol)
+    compare("attn", pick(attn), un.qk(h["q"], h["k"], kern, dil, scale, rows, rpb=f32(rpb)), tol)
     compare("o", pick(o2), un.av(hp, h["v"], kern, dil, rows), tol)
     compare("softmax", pick(y), un.softmax(hg, rows), tol)
     compare("softmax_bwd", pick(dx), un.softmax_bwd(hp, hg, rows), tol)
@@ -188,3 +189,50 @@ def test_full_size_chain_sampled(cuda_lib):
     ra, rv = un.av_bwd(h["dO"], hp, h["v"], kern, dil, rows)
     compare("dattn", pick(dattn), ra, tol)
     compare("dv", pick(dv2), rv, tol)
+
+
+# ---------------------------------------------------------------------------------------------
+# Relative positional bias
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_rpb_logits_and_gradient_match_the_oracle(case, cuda_lib):
+    na = cuda_lib
+    w, t, wt = setup(case, seed=41)
+    tol = TOL[w.dtype]
+    dev = {k: v.cuda() for k, v in t.items()}
+    rpb = nain.make_rpb(w, seed=42)
+    attn = torch.empty_like(wt["logits"]).cuda()
+    na.na_qk(dev["q"], dev["k"], attn, w.kernel, w.dilation, w.scale, rpb=rpb.cuda())
+    drpb = torch.empty_like(rpb).cuda()
+    na.na_rpb_grad(wt["grad"].cuda(), drpb, w.kernel, w.dilation)
+    status_ok(na)
+    h = {k: f32(v) for k, v in t.items()}
+    compare("attn+rpb", to64(attn), un.qk(h["q"], h["k"], w.kernel, w.dilation, w.scale, rpb=f32(rpb)), tol)
+    compare("drpb", to64(drpb), un.rpb_grad(f32(wt["grad"]), w.kernel, w.dilation), TOL["fp32"])
+
+
+def test_rpb_grad_is_deterministic_and_takes_a_workspace(cuda_lib):
+    na = cuda_lib
+    w = nain.small_workload("bf16", (40, 37), 3, 32, (5, 7), (1, 2), B=2, seed=5)
+    g = nain.make_weights(w, "randn", device="cuda", seed=6)
+    a = torch.empty((3, 9, 13), dtype=torch.float32, device="cuda")
+    b = torch.empty_like(a)
+    na.na_rpb_grad(g, a, w.kernel, w.dilation)
+    nbytes = na.na_rpb_grad_workspace_size(w.B, w.spatial, w.heads, w.kernel)
+    ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+    na.na_rpb_grad(g, b, w.kernel, w.dilation, workspace=ws)
+    status_ok(na)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_rpb_grad_full_size(cuda_lib):
+    """The bias gradient over every query of the 512x512 shape (2M rows, 9x9) against the oracle."""
+    na = cuda_lib
+    w = nain.WORKLOADS["2d_bf16_512x512_k9"]
+    g = nain.make_weights(w, "randn", device="cuda", seed=8)
+    drpb = torch.empty((w.heads, 17, 17), dtype=torch.float32, device="cuda")
+    na.na_rpb_grad(g, drpb, w.kernel, w.dilation)
+    status_ok(na)
+    compare("drpb", to64(drpb), un.rpb_grad(f32(g), w.kernel, w.dilation), TOL["fp32"])
