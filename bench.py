@@ -76,6 +76,23 @@ UNFUSED_CALLS = ("qk", "softmax", "av", "av_bwd", "softmax_bwd", "qk_bwd")
 UNFUSED_CALLS_RPB = UNFUSED_CALLS + ("rpb_grad",)
 
 
+def growing_window_sizes(w):
+    """Kernel sizes along the first axis that grow from 1 to the full kernel over its length (the
+    user's "increasing kernel sizes along time"), the full kernel along the other axes."""
+    L0, k0 = w.spatial[0], w.kernel[0]
+    steps = k0 // 2 + 1
+    first = [1 + 2 * min(steps - 1, (i * steps) // L0) for i in range(L0)]
+    return [first] + [[k] * L for L, k in zip(w.spatial[1:], w.kernel[1:])]
+
+
+def masked_weights(w, sizes):
+    """Weights a variable-window mask sets to -inf (sizes along the first axis only)."""
+    rest_tokens = int(np.prod(w.spatial[1:])) if len(w.spatial) > 1 else 1
+    rest_k = int(np.prod(w.kernel[1:])) if len(w.kernel) > 1 else 1
+    K = w.keys_per_query
+    return float(sum(K - k0 * rest_k for k0 in sizes[0]) * rest_tokens * w.B * w.heads)
+
+
 def unfused_call_work(w):
     """Algorithmic bytes (inputs read once, outputs written once) and FLOPs of each unfused call.
     R = rows (tokens x heads); weights are R x K elements."""
@@ -89,7 +106,8 @@ def unfused_call_work(w):
             "av_bwd": (3 * RD + 2 * RK, 2 * prod),     # dO, attn, v -> dattn, dv
             "softmax_bwd": (3 * RK, 0.0),              # y, dy -> dx
             "qk_bwd": (4 * RD + RK, 2 * prod),         # dattn, q, k -> dq, dk
-            "rpb_grad": (RK, 0.0)}                     # dattn -> the bias table's gradient (a few KB)
+            "rpb_grad": (RK, 0.0),                     # dattn -> the bias table's gradient (a few KB)
+            "mask_window": (masked_weights(w, growing_window_sizes(w)) * s, 0.0)}   # -inf written, nothing read
 
 
 def arithmetic_intensity(w, fused=True, elem_bytes=None):
@@ -279,7 +297,7 @@ class Step:
 class UnfusedStep:
     """Buffers and launches of one fwd + bwd step through the unfused operations."""
 
-    def __init__(self, w, t, rpb=False):
+    def __init__(self, w, t, rpb=False, varwin=False):
         import neighborhood_attention_fwd_gb300 as na
 
         self.na = na
@@ -292,6 +310,7 @@ class UnfusedStep:
             self.drpb = torch.empty_like(self.rpb)
             nbytes = na.na_rpb_grad_workspace_size(w.B, w.spatial, w.heads, w.kernel)
             self.rpb_ws = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+        self.sizes = growing_window_sizes(w) if varwin else None
         self.attn = torch.empty(q.shape[:-1] + (w.keys_per_query,), dtype=q.dtype, device=q.device)
         self.dattn = torch.empty_like(self.attn)
         self.o = torch.empty_like(q)
@@ -309,6 +328,9 @@ class UnfusedStep:
         mark("start")
         na.na_qk(t["q"], t["k"], self.attn, w.kernel, w.dilation, w.scale, rpb=self.rpb)
         mark("qk")
+        if self.sizes is not None:
+            na.na_mask_window(self.attn, self.sizes, w.kernel, w.dilation)
+            mark("mask_window")
         na.na_softmax(self.attn, self.attn, w.kernel)
         mark("softmax")
         na.na_av(self.attn, t["v"], self.o, w.kernel, w.dilation)
@@ -326,7 +348,7 @@ class UnfusedStep:
     LAUNCHES_PER_STEP = 8   # av_bwd and qk_bwd launch two kernels each; the bias gradient two more
 
     def launches(self):
-        return self.LAUNCHES_PER_STEP + (2 if self.rpb is not None else 0)
+        return self.LAUNCHES_PER_STEP + (2 if self.rpb is not None else 0) + (1 if self.sizes is not None else 0)
 
 
 def run_unfused(args, w, rank, world, dist):
@@ -336,8 +358,10 @@ def run_unfused(args, w, rank, world, dist):
 
     na.load()
     t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
-    step = UnfusedStep(w, t, rpb=args.rpb)
+    step = UnfusedStep(w, t, rpb=args.rpb, varwin=args.varwin)
     calls_run = UNFUSED_CALLS_RPB if args.rpb else UNFUSED_CALLS
+    if args.varwin:
+        calls_run = calls_run[:1] + ("mask_window",) + calls_run[1:]
     tensor_bytes = t["q"].numel() * t["q"].element_size()
     flush = None
     if tensor_bytes < 2 * L2_BYTES:
@@ -396,18 +420,21 @@ def run_unfused(args, w, rank, world, dist):
                        "frac": ach / peak, "roof_ms": max(t_b, t_f) * 1e3, "alg_bytes": nbytes, "flops": flops}
     dom = max(calls_run, key=lambda k: ms[k])
     roof_step = sum(c["roof_ms"] for c in calls.values())
-    e2e = run_e2e(args, w, t, step, lambda w_, t_: UnfusedStep(w_, t_, rpb=args.rpb)) if not args.no_e2e else None
+    e2e = (run_e2e(args, w, t, step, lambda w_, t_: UnfusedStep(w_, t_, rpb=args.rpb, varwin=args.varwin))
+           if not args.no_e2e else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype if w.dtype != "fp32" else "f32",
         "data": "synthetic (seeded N(0,1) inputs, dO = ones as loss = O.sum())" if w.dO == "ones"
                 else "synthetic (seeded N(0,1) inputs and dO)",
-        "config": {"workload": w.name, "path": "unfused" + ("+rpb" if args.rpb else ""), "B": w.B, "spatial": list(w.spatial), "heads": w.heads,
+        "config": {"workload": w.name,
+                   "path": "unfused" + ("+rpb" if args.rpb else "") + ("+growing-window" if args.varwin else ""),
+                   "B": w.B, "spatial": list(w.spatial), "heads": w.heads,
                    "D": w.D, "kernel": list(w.kernel), "dilation": list(w.dilation),
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps (256 MB write)"},
-        "ms": {"fwd": ms["qk"] + ms["softmax"] + ms["av"],
+        "ms": {"fwd": ms["qk"] + ms.get("mask_window", 0.0) + ms["softmax"] + ms["av"],
                "bwd": ms["av_bwd"] + ms["softmax_bwd"] + ms["qk_bwd"] + ms.get("rpb_grad", 0.0), "fwd_bwd": ms_step,
                "per_call": ms},
         "roofline": {"bound": calls[dom]["bound"], "achieved": calls[dom]["achieved"], "peak": calls[dom]["peak"],
@@ -642,13 +669,15 @@ def main():
                     help="the fused kernels (default) or the unfused chain of separate operations")
     ap.add_argument("--rpb", action="store_true",
                     help="with --path unfused: add a relative positional bias to the logits and time its gradient")
+    ap.add_argument("--varwin", action="store_true",
+                    help="with --path unfused: mask the logits to kernel sizes that grow along the first axis")
     ap.add_argument("--dtype", choices=["bf16", "fp16", "fp32"], default=None,
                     help="run a bf16 workload's shapes with fp16 or fp32 tensors instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
-    if args.rpb and args.path != "unfused":
-        ap.error("--rpb applies to --path unfused (the fused kernels take no bias)")
+    if (args.rpb or args.varwin) and args.path != "unfused":
+        ap.error("--rpb and --varwin apply to --path unfused")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

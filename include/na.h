@@ -220,6 +220,18 @@ na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn
                     const int* spatial, int heads, int D, const int* kernel, const int* dilation, na_dtype dtype,
                     void* stream);
 
+/* Variable windows.  The user in the same issue asks for kernel sizes that change along time; the
+ * maintainer advises masking the unfused logits, which the user already does to na3d_qk's output.
+ * This sets attn[row, t] = -inf, in place, for every window offset t outside the query's own window:
+ * along each axis a, the window of size k_a(x_a) that the same shifted-window rule gives (nested in
+ * the full window of size kernel[a]).  sizes: device int32, caller-owned, 4-byte aligned, the per-
+ * position sizes of axis 0 (spatial[0] entries), then of axis 1, ...; each entry is clamped to
+ * [1, kernel[a]] and an even entry is lowered by one.  Offsets inside every row's window are not
+ * touched, and nothing else is read.  The softmax, the weighted sum and every gradient then treat the
+ * masked weights as absent (their probability and gradient are zero). */
+na_status na_mask_window(void* attn, const int* sizes, int B, int ndim, const int* spatial, int heads,
+                         const int* kernel, const int* dilation, na_dtype dtype, void* stream);
+
 /* Bytes of device workspace na_rpb_grad needs for this problem (0 on invalid arguments). */
 size_t na_rpb_grad_workspace_size(int B, int ndim, const int* spatial, int heads, const int* kernel);
 

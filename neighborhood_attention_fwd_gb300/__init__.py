@@ -23,7 +23,7 @@ __all__ = [
     "NAError", "load", "na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv",
     "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
     "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad",
-    "na_rpb_grad_workspace_size",
+    "na_rpb_grad_workspace_size", "na_mask_window",
 ]
 
 NA_BF16, NA_FP32, NA_FP16 = 0, 1, 2
@@ -72,13 +72,15 @@ def load(path: str | None = None):
     lib.na_rpb_grad.argtypes = [P, P] + geo_nd + [IP, IP, I, P, ctypes.c_size_t, P]
     lib.na_rpb_grad_workspace_size.argtypes = [I, I, IP, I, IP]
     lib.na_rpb_grad_workspace_size.restype = ctypes.c_size_t
+    lib.na_mask_window.argtypes = [P, P] + geo_nd + [IP, IP, I, P]
     lib.na_av.argtypes = [P, P, P] + geo + [IP, IP, I, P]
     lib.na_softmax.argtypes = [P, P] + geo_nd + [IP, I, P]
     lib.na_softmax_bwd.argtypes = [P, P, P] + geo_nd + [IP, I, P]
     lib.na_qk_bwd.argtypes = [P, P, P, P, P] + geo + kd + [I, P]
     lib.na_av_bwd.argtypes = [P, P, P, P, P] + geo + [IP, IP, I, P]
     for f in ("na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv", "na_device_status", "na_plan_info",
-              "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad"):
+              "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad",
+              "na_mask_window"):
         getattr(lib, f).restype = I
     _lib = lib
     return lib
@@ -356,3 +358,27 @@ def na_av_bwd(dO, attn, v, dattn, dv, kernel, dilation=None, stream=None):
                           _ints(spatial), heads, D, _ints(kernel), _ints(dilation), _dtype_code(v),
                           _stream(stream))
     _ok(st, "na_av_bwd")
+
+
+def na_mask_window(attn, sizes, kernel, dilation=None, stream=None):
+    """Set, in place, the logits outside each query's variable window to -inf.  sizes: one sequence or
+    tensor per axis, sizes[a][x] = the kernel size (odd, <= kernel[a]) of the queries at position x."""
+    B, ndim, spatial, heads, kernel = _attn_geometry(attn, kernel)
+    kernel, dilation = _kd(ndim, kernel, dilation)
+    _check(attn, attn.shape, attn.dtype, "attn")
+    if len(sizes) != ndim:
+        raise ValueError("sizes needs one entry per spatial axis")
+    parts = [torch.as_tensor(sz, dtype=torch.int32, device="cpu").reshape(-1) for sz in sizes]
+    for L, part in zip(spatial, parts):
+        if part.numel() != L:
+            raise ValueError("sizes[a] needs one entry per position along axis a")
+    # a copy from pageable host memory has finished when .to() returns, so the sizes are in place
+    # whichever stream the kernel runs on; the temporary must then outlive the launch on that stream
+    flat = torch.cat(parts).contiguous().to(attn.device)
+    st = load().na_mask_window(attn.data_ptr(), flat.data_ptr(), B, ndim, _ints(spatial), heads, _ints(kernel),
+                               _ints(dilation), _dtype_code(attn), _stream(stream))
+    _ok(st, "na_mask_window")
+    if isinstance(stream, torch.cuda.Stream):
+        flat.record_stream(stream)
+    elif stream is not None:
+        torch.cuda.ExternalStream(int(stream)).synchronize()

@@ -793,6 +793,29 @@ na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn
     return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
 }
 
+na_status na_mask_window(void* attn, const int* sizes, int B, int ndim, const int* spatial, int heads,
+                         const int* kernel, const int* dilation, na_dtype dtype, void* stream) {
+    na::UnfParams p;
+    na_status st = unfused_params(B, ndim, spatial, heads, 0, kernel, dilation, 1.f, dtype, false, p);
+    if (st != NA_OK) return st;
+    if ((st = check_ptrs({attn})) != NA_OK) return st;
+    if (!sizes) return NA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(sizes) & 3u) return NA_ERR_ALIGNMENT;
+    // embedded 3D: the real axes are the last ndim; their sizes follow one another in `sizes`
+    int off = 0;
+    for (int a = 0; a < 3; ++a) {
+        if (a < 3 - ndim) {
+            p.vk_off[a] = -1;
+        } else {
+            p.vk_off[a] = off;
+            off += spatial[a - (3 - ndim)];
+        }
+    }
+    p.vk = sizes;
+    p.out0 = attn;
+    return cuda_status(na::launch_unfused_mask_window(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
+}
+
 size_t na_rpb_grad_workspace_size(int B, int ndim, const int* spatial, int heads, const int* kernel) {
     int ones[3] = {1, 1, 1};
     Geom g;

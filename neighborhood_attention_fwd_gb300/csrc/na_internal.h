@@ -85,6 +85,8 @@ struct UnfParams {
     long long rows;     // B * tokens * heads
     float scale;        // qk: scale; gather, scatter: the factor of the sum (scale, or 1)
     const float* rpb;   // qk: relative positional bias [heads, 2k0-1, 2k1-1, 2k2-1], or null
+    const int* vk;      // mask: per-position kernel sizes, concatenated over the axes
+    int vk_off[3];      // mask: offset of each (embedded) axis in vk, -1 for an axis without one
 };
 
 // Tokens per block of the bias-gradient reduction's first stage, and the size of its partial sums.
@@ -112,6 +114,8 @@ int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t stream);
 // `partial`, which holds rpb_grad_workspace_bytes).
 int launch_unfused_rpb_grad(const UnfParams& p, int elem, long long tokens, float* partial, float* drpb,
                             cudaStream_t s);
+// attn[row, t] = -inf for every offset t outside the row's variable window (p.vk).
+int launch_unfused_mask_window(const UnfParams& p, int elem, cudaStream_t s);
 int launch_unfused_softmax(const UnfParams& p, int elem, bool bwd, cudaStream_t stream);
 
 // Kernel attributes that depend on the plan (dynamic smem opt-in); called before the launch.

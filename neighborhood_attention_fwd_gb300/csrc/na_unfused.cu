@@ -437,12 +437,9 @@ constexpr int kRegK = 128;
 // y = softmax(x) over each row of K weights, one warp per row (x and y may be the same tensor: every
 // read of the row happens before its first write).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) softmax_kernel(const UnfParams p) {
+__device__ __forceinline__ void softmax_row(const UnfParams& p, long long row, int lane) {
     using E = Elem<T>;
     constexpr int NV = kRegK / 32;
-    const long long row = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    if (row >= p.rows) return;   // warp-uniform
-    const int lane = threadIdx.x & 31;
     const T* x = static_cast<const T*>(p.a) + row * p.K;
     T* y = static_cast<T*>(p.out0) + row * p.K;
     if (p.K <= kRegK) {
@@ -476,16 +473,24 @@ __global__ void __launch_bounds__(kThreads) softmax_kernel(const UnfParams p) {
     const float inv = 1.f / warp_sum(l);
     __syncwarp();
     for (int t = lane; t < p.K; t += 32) y[t] = E::put(expf(E::get(x[t]) - m) * inv);
+    __syncwarp();
+}
+
+__device__ __forceinline__ long long warp_index() {
+    return (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) softmax_kernel(const UnfParams p) {
+    const long long row = warp_index();
+    if (row < p.rows) softmax_row<T>(p, row, threadIdx.x & 31);   // warp-uniform
 }
 
 // dx = y * (dy - sum_t y dy) over each row, one warp per row (dx may be dy's tensor).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p) {
+__device__ __forceinline__ void softmax_bwd_row(const UnfParams& p, long long row, int lane) {
     using E = Elem<T>;
     constexpr int NV = kRegK / 32;
-    const long long row = (static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x) >> 5;
-    if (row >= p.rows) return;
-    const int lane = threadIdx.x & 31;
     const T* y = static_cast<const T*>(p.a) + row * p.K;
     const T* dy = static_cast<const T*>(p.b) + row * p.K;
     T* dx = static_cast<T*>(p.out0) + row * p.K;
@@ -511,6 +516,13 @@ __global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p
     s = warp_sum(s);
     __syncwarp();
     for (int t = lane; t < p.K; t += 32) dx[t] = E::put(E::get(y[t]) * (E::get(dy[t]) - s));
+    __syncwarp();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p) {
+    const long long row = warp_index();
+    if (row < p.rows) softmax_bwd_row<T>(p, row, threadIdx.x & 31);
 }
 
 // Gradient of the bias table, first stage: block (chunk of tokens) sums dattn over its tokens'
@@ -579,6 +591,77 @@ __global__ void __launch_bounds__(kThreads) rpb_grad_sum_kernel(const float* par
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (lane == 0) drpb[e] = acc;
+}
+
+// Variable windows: attn[row, t] = -inf for every window offset t outside the row's own window of
+// size k_a(x_a) along each axis a (the same shifted-window rule, nested inside the full window).
+// One warp per token (its rows for every head are contiguous): the kept offsets form a box
+// [lo_a, hi_a] per axis, computed once per token, and only offsets outside it are written (nothing
+// is read).  A per-block table holds each offset's (t0, t1, t2), so the per-element test needs no
+// division.  Sizes are clamped to [1, k_a] and even sizes lowered by one.
+constexpr int kMaskTable = 4096;   // offsets covered by the table; larger windows decode per element
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) mask_window_kernel(const UnfParams p, long long tokens) {
+    using E = Elem<T>;
+    __shared__ uint32_t tdec[kMaskTable];   // t0 << 20 | t1 << 10 | t2
+    const int K = p.K, k1 = p.k[1], k2 = p.k[2];
+    const bool table = K <= kMaskTable && k1 <= 1024 && k2 <= 1024;   // the packed fields hold 10 bits
+    if (table)
+        for (int t = threadIdx.x; t < K; t += kThreads)
+            tdec[t] = static_cast<uint32_t>(t / (k1 * k2)) << 20 | static_cast<uint32_t>((t / k2) % k1) << 10 |
+                      static_cast<uint32_t>(t % k2);
+    __syncthreads();
+    const long long tok = warp_index();
+    if (tok >= tokens) return;   // warp-uniform
+    const int lane = threadIdx.x & 31;
+    int x[3];
+    if (tokens <= 0x7fffffffLL) {   // 32-bit decode
+        unsigned u = static_cast<unsigned>(tok);
+        x[2] = static_cast<int>(u % static_cast<unsigned>(p.L[2]));
+        u /= static_cast<unsigned>(p.L[2]);
+        x[1] = static_cast<int>(u % static_cast<unsigned>(p.L[1]));
+        u /= static_cast<unsigned>(p.L[1]);
+        x[0] = static_cast<int>(u % static_cast<unsigned>(p.L[0]));
+    } else {
+        long long u = tok;
+        x[2] = static_cast<int>(u % p.L[2]);
+        u /= p.L[2];
+        x[1] = static_cast<int>(u % p.L[1]);
+        u /= p.L[1];
+        x[0] = static_cast<int>(u % p.L[0]);
+    }
+    int lo[3], hi[3];
+    bool full = true;
+    for (int a = 0; a < 3; ++a) {
+        lo[a] = 0;
+        hi[a] = p.k[a] - 1;
+        if (p.vk_off[a] < 0) continue;
+        const int k = p.k[a], d = p.d[a], c = x[a] % d, j = x[a] / d, Lc = class_len(p.L[a], d, c);
+        int kv = min(max(__ldg(p.vk + p.vk_off[a] + x[a]), 1), k);
+        if ((kv & 1) == 0) --kv;
+        lo[a] = win_start(j, Lc, kv) - win_start(j, Lc, k);   // offset of the own window in the full one
+        hi[a] = lo[a] + kv - 1;
+        full = full && kv == k;
+    }
+    if (full) return;   // nothing to mask
+    const T ninf = E::put(-INFINITY);
+    T* out = static_cast<T*>(p.out0) + tok * p.heads * K;
+    for (int h = 0; h < p.heads; ++h, out += K)
+        for (int t = lane; t < K; t += 32) {
+            int t0, t1, t2;
+            if (table) {
+                const uint32_t dd = tdec[t];
+                t0 = static_cast<int>(dd >> 20);
+                t1 = static_cast<int>((dd >> 10) & 1023u);
+                t2 = static_cast<int>(dd & 1023u);
+            } else {
+                t0 = t / (k1 * k2);
+                t1 = (t / k2) % k1;
+                t2 = t % k2;
+            }
+            if (t0 < lo[0] || t0 > hi[0] || t1 < lo[1] || t1 > hi[1] || t2 < lo[2] || t2 > hi[2]) out[t] = ninf;
+        }
 }
 
 int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
@@ -671,6 +754,19 @@ int launch_unfused_rpb_grad(const UnfParams& p, int elem, long long tokens, floa
     if (e != cudaSuccess) return static_cast<int>(e);
     rpb_grad_sum_kernel<<<launch_blocks(static_cast<long long>(entries) * 32), kThreads, 0, s>>>(partial, chunks,
                                                                                                  entries, drpb);
+    return static_cast<int>(cudaGetLastError());
+}
+
+int launch_unfused_mask_window(const UnfParams& p, int elem, cudaStream_t s) {
+    if (p.rows == 0) return 0;
+    const long long tokens = p.rows / p.heads;
+    const dim3 grid(launch_blocks(tokens * 32)), block(kThreads);
+    if (elem == 0)
+        mask_window_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(p, tokens);
+    else if (elem == 2)
+        mask_window_kernel<__half><<<grid, block, 0, s>>>(p, tokens);
+    else
+        mask_window_kernel<float><<<grid, block, 0, s>>>(p, tokens);
     return static_cast<int>(cudaGetLastError());
 }
 

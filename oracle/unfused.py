@@ -23,6 +23,11 @@ rpb[heads, 2 k_0 - 1, .., 2 k_{n-1} - 1] adds rpb[h, (c(n(i, t))_a - c(i)_a + k_
 where c(.)_a is a position's class index along axis a (its index divided by the dilation).  Its
 gradient is drpb[h, r] = sum over (batch, query, offset) with relative position r of dattn[i, t].
 
+Variable windows (the user's request for kernel sizes that change along time, answered with "mask
+the weights" of the unfused logits): per axis a and position x, a kernel size k_a(x) <= k_a.  Query i
+keeps only the keys its own window of size k_a(i_a) (the same shifted-window rule, nested inside the
+full window) holds along every axis; mask_window sets the other logits to -inf.
+
 n(i, t) is the t-th key of query i's window: the window is the Cartesian product of the per-axis
 windows, and t = (t_0 k_1 + t_1) k_2 + t_2 orders its offsets with the first axis outermost.  The
 weight tensors are [B, L.., heads, K].
@@ -265,3 +270,27 @@ def av_bwd(dO, attn, v, kernel, dilation, rows=None):
     if rows is None:
         dv = dv.reshape(v.shape)
     return dattn, dv
+
+
+def mask_window(attn, sizes, kernel, dilation):
+    """Logits with every offset outside the query's variable window set to -inf.  sizes: one integer
+    array per axis, sizes[a][x] = the kernel size (odd, 1..kernel[a]) of queries at position x."""
+    out = np.array(attn, dtype=np.float64, copy=True)
+    B = out.shape[0]
+    spatial = tuple(out.shape[1:-2])
+    heads, K = out.shape[-2], out.shape[-1]
+    g = Geometry(spatial, kernel, dilation)
+    keys = g.coords(g.neighbours(np.arange(g.N)).ravel()).reshape(g.N, K, len(spatial))   # [N, K, ndim]
+    x = g.coords(np.arange(g.N))                                                          # [N, ndim]
+    keep = np.ones((g.N, K), dtype=bool)
+    for a, (L, d) in enumerate(zip(spatial, g.dilation)):
+        ka = np.asarray(sizes[a], dtype=np.int64)
+        first = np.array([first_neighbour(int(i), L, int(ka[i]), d) for i in range(L)])      # own window start
+        if (first < 0).any():
+            raise ValueError("invalid variable kernel size")
+        lo = first[x[:, a]][:, None]
+        hi = lo + d * (ka[x[:, a]][:, None] - 1)
+        keep &= (keys[:, :, a] >= lo) & (keys[:, :, a] <= hi)
+    flat = out.reshape(B, g.N, heads, K)
+    flat[np.broadcast_to(~keep[None, :, None, :], flat.shape)] = -np.inf
+    return out

@@ -107,6 +107,15 @@ def test_unfused_entry_points_reject_bad_arguments(lib):
     assert lib.na_rpb_grad(P(16), P(16), 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, P(16), 8, None) == 6
 
 
+def test_mask_window_rejects_bad_arguments(lib):
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    P = ctypes.c_void_p
+    assert lib.na_mask_window(P(16), None, 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, None) == 1
+    assert lib.na_mask_window(P(16), P(18), 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, None) == 3
+    assert lib.na_mask_window(None, P(16), 1, 2, I((16, 16)), 2, I((5, 5)), I((1, 1)), 0, None) == 1
+    assert lib.na_mask_window(P(16), P(16), 1, 2, I((16, 16)), 2, I((6, 5)), I((1, 1)), 0, None) == 1
+
+
 def test_rpb_grad_workspace_size(lib):
     # 1024 x 1024 tokens, 8 heads, 9x9: 1024 tokens per block -> 1024 blocks of 8 x 289 fp32 partial sums
     n = na.na_rpb_grad_workspace_size(1, (1024, 1024), 8, (9, 9))

@@ -102,6 +102,9 @@ UNFUSED_MUTANTS = {
                           "rel = (x[:, a] // d)[:, None] - tab[x[:, a]] // d + (k - 1)"),
     "rpb_axis_order": ("span = int(np.prod([2 * kk - 1 for kk in g.kernel[a + 1:]]))",
                        "span = int(np.prod([2 * kk - 1 for kk in g.kernel[:a]]))"),
+    "varwin_full_kernel_start": ("first = np.array([first_neighbour(int(i), L, int(ka[i]), d) for i in range(L)])",
+                                 "first = np.array([first_neighbour(int(i), L, int(g.kernel[a]), d) for i in range(L)])"),
+    "varwin_span_off_by_one": ("hi = lo + d * (ka[x[:, a]][:, None] - 1)", "hi = lo + d * ka[x[:, a]][:, None]"),
     "rpb_grad_drops_batch": ("weights=_f64(wf[:, :, h, :]).sum(axis=0).ravel()", "weights=_f64(wf[0, :, h, :]).ravel()"),
 }
 
@@ -132,6 +135,9 @@ def unfused_pin_results(mod):
     for i, case in enumerate(pins.CASES):
         checks[f"rpb_adjoint_{i}"] = lambda c=case: unpins.test_rpb_grad_is_the_adjoint_of_the_bias(*c)
     checks["rpb_counts"] = unpins.test_rpb_grad_counts_pairs_per_relative_position
+    for i, case in enumerate(unpins.VARWIN):
+        checks[f"varwin_{i}"] = lambda c=case: unpins.test_variable_window_chain_matches_dense_attention(*c)
+    checks["varwin_special"] = unpins.test_variable_window_special_cases
     checks["rpb_rows"] = unpins.test_rpb_sampled_rows_match_full
     saved = unpins.un
     unpins.un = mod

@@ -229,3 +229,62 @@ def test_rpb_grad_counts_pairs_per_relative_position():
     assert np.allclose(d.reshape(3, -1).sum(-1), 2 * g.N * g.K)
     d1 = un.rpb_grad(np.ones((1, 5, 1, 5)), (5,), (1,))      # L = k: every query's window is the whole axis
     assert d1.reshape(-1).tolist() == [1, 2, 3, 4, 5, 4, 3, 2, 1]
+
+
+# ---------------------------------------------------------------------------------------------
+# Variable windows (kernel sizes that change along an axis)
+# ---------------------------------------------------------------------------------------------
+
+def dense_variable_mask(spatial, sizes, dilation):
+    """[N, N] boolean: key j is kept for query i when, along every axis, j's coordinate is one of the
+    k_a(i) same-class positions nearest to i's (the nearest-k characterisation with the query's own k)."""
+    coords = list(itertools.product(*[range(L) for L in spatial]))
+    index = {c: n for n, c in enumerate(coords)}
+    N = len(coords)
+    out = np.zeros((N, N), dtype=bool)
+    for i, x in enumerate(coords):
+        per_axis = [nearest_k(x[a], spatial[a], int(sizes[a][x[a]]), dilation[a]) for a in range(len(spatial))]
+        for y in itertools.product(*per_axis):
+            out[i, index[y]] = True
+    return out
+
+
+VARWIN = [
+    # spatial, kernel, dilation, sizes per axis (None: the full kernel everywhere)
+    ((11,), (5,), (1,), [[1, 1, 3, 3, 5, 5, 5, 3, 3, 1, 1]]),
+    ((9, 10), (3, 5), (2, 1), [[1, 3, 1, 3, 3, 1, 3, 1, 3], None]),
+    ((6, 5, 7), (5, 3, 3), (1, 1, 2), [[1, 1, 3, 3, 5, 5], None, [3, 1, 3, 1, 3, 1, 3]]),
+]
+
+
+def _sizes(spatial, kernel, sizes):
+    return [np.full(L, k) if s is None else np.asarray(s) for L, k, s in zip(spatial, kernel, sizes)]
+
+
+@pytest.mark.parametrize("spatial,kernel,dilation,sizes", VARWIN)
+def test_variable_window_chain_matches_dense_attention(spatial, kernel, dilation, sizes):
+    B, heads, D = 2, 2, 3
+    q, k, v, _ = case_tensors(spatial, B, heads, D, 101)
+    sz = _sizes(spatial, kernel, sizes)
+    scale = 0.45
+    logits = un.mask_window(un.qk(q, k, kernel, dilation, scale), sz, kernel, dilation)
+    o = un.av(un.softmax(logits), v, kernel, dilation)
+    N = int(np.prod(spatial))
+    qf, kf, vf = (x.reshape(B, N, heads, D) for x in (q, k, v))
+    s = scale * np.einsum("bihc,bjhc->bhij", qf, kf)
+    s = np.where(dense_variable_mask(spatial, sz, dilation)[None, None], s, -np.inf)
+    p = np.exp(s - s.max(-1, keepdims=True))
+    p /= p.sum(-1, keepdims=True)
+    ref = np.einsum("bhij,bjhc->bihc", p, vf).reshape(o.shape)
+    assert np.abs(o - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_variable_window_special_cases():
+    spatial, kernel, dilation = (7, 8), (5, 3), (1, 2)
+    q, k, v, _ = case_tensors(spatial, 1, 2, 4, 111)
+    logits = un.qk(q, k, kernel, dilation, 0.5)
+    full = un.mask_window(logits, _sizes(spatial, kernel, [None, None]), kernel, dilation)
+    assert np.array_equal(full, logits)                        # the full kernel everywhere masks nothing
+    ones = [np.ones(7, dtype=int), np.ones(8, dtype=int)]
+    o = un.av(un.softmax(un.mask_window(logits, ones, kernel, dilation)), v, kernel, dilation)
+    assert np.abs(o - v).max() <= 1e-14                         # kernel 1: each query sees only itself

@@ -236,3 +236,70 @@ def test_rpb_grad_full_size(cuda_lib):
     na.na_rpb_grad(g, drpb, w.kernel, w.dilation)
     status_ok(na)
     compare("drpb", to64(drpb), un.rpb_grad(f32(g), w.kernel, w.dilation), TOL["fp32"])
+
+
+# ---------------------------------------------------------------------------------------------
+# Variable windows
+# ---------------------------------------------------------------------------------------------
+
+VARWIN = [
+    # dtype, spatial, heads, D, kernel, dilation, B, sizes per axis (None: the full kernel)
+    ("fp32", (11,), 2, 16, (5,), (1,), 2, [[1, 1, 3, 3, 5, 5, 5, 3, 3, 1, 1]]),
+    ("bf16", (9, 10), 2, 32, (3, 5), (2, 1), 1, [[1, 3, 1, 3, 3, 1, 3, 1, 3], None]),
+    ("fp16", (6, 5, 7), 1, 64, (5, 3, 3), (1, 1, 2), 1, [[1, 1, 3, 3, 5, 5], None, [3, 1, 3, 1, 3, 1, 3]]),
+    # kernel sizes that grow along time, the shape the user asks about (8 frames, 5x7x7 windows)
+    ("bf16", (8, 24, 20), 2, 32, (5, 7, 7), (1, 1, 1), 1, [[1, 1, 3, 3, 3, 5, 5, 5], None, None]),
+]
+
+
+def _varwin_ids(c):
+    return f"{c[0]}-{'x'.join(map(str, c[1]))}-k{'x'.join(map(str, c[4]))}-d{'x'.join(map(str, c[5]))}"
+
+
+def _full_sizes(spatial, kernel, sizes):
+    return [np.full(L, k) if s is None else np.asarray(s) for L, k, s in zip(spatial, kernel, sizes)]
+
+
+def compare_masked(name, got, ref, tol):
+    """The -inf pattern must match exactly; the finite entries follow the tolerance rule."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    ninf_g, ninf_r = np.isneginf(got), np.isneginf(ref)
+    assert np.array_equal(ninf_g, ninf_r), f"{name}: masked entries differ ({(ninf_g != ninf_r).sum()})"
+    compare(name, got[~ninf_g], ref[~ninf_r], tol)
+
+
+@pytest.mark.parametrize("case", VARWIN, ids=[_varwin_ids(c) for c in VARWIN])
+def test_variable_window_chain_matches_the_oracle(case, cuda_lib):
+    na = cuda_lib
+    dtype, spatial, heads, D, kernel, dilation, B, sizes = case
+    w = nain.small_workload(dtype, spatial, heads, D, kernel, dilation, B=B, seed=51)
+    t = nain.make_inputs(w, device="cpu")
+    tol = TOL[dtype]
+    sz = _full_sizes(spatial, kernel, sizes)
+    dev = {k: v.cuda() for k, v in t.items()}
+    q, k, v, dO = dev["q"], dev["k"], dev["v"], dev["dO"]
+    attn = torch.empty(q.shape[:-1] + (w.keys_per_query,), dtype=q.dtype, device="cuda")
+    na.na_qk(q, k, attn, kernel, dilation, w.scale)
+    na.na_mask_window(attn, sz, kernel, dilation)
+    logits = attn.clone()
+    na.na_softmax(attn, attn, kernel)
+    o = torch.empty_like(q)
+    na.na_av(attn, v, o, kernel, dilation)
+    dattn, dv = torch.empty_like(attn), torch.empty_like(v)
+    na.na_av_bwd(dO, attn, v, dattn, dv, kernel, dilation)
+    na.na_softmax_bwd(attn, dattn, dattn, kernel)
+    dq, dk = torch.empty_like(q), torch.empty_like(k)
+    na.na_qk_bwd(dattn, q, k, dq, dk, kernel, dilation, w.scale)
+    status_ok(na)
+
+    h = {key: f32(val) for key, val in t.items()}
+    ref_logits = un.mask_window(un.qk(h["q"], h["k"], kernel, dilation, w.scale), sz, kernel, dilation)
+    compare_masked("masked logits", to64(logits), ref_logits, tol)
+    y = un.softmax(ref_logits)
+    compare("O", to64(o), un.av(y, h["v"], kernel, dilation), tol)
+    ry, rv = un.av_bwd(h["dO"], y, h["v"], kernel, dilation)
+    rq, rk = un.qk_bwd(un.softmax_bwd(y, ry), h["q"], h["k"], kernel, dilation, w.scale)
+    compare("dQ", to64(dq), rq, tol, scale_ref=rv)
+    compare("dK", to64(dk), rk, tol, scale_ref=rv)
+    compare("dV", to64(dv), rv, tol)
