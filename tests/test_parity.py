@@ -99,6 +99,18 @@ def test_full_size_sampled_parity(name, cuda_lib):
     check_sampled(w, gpu, h, n=256)
 
 
+def test_full_size_fp16_headline_shape_sampled(cuda_lib):
+    """The 2D 1024x1024 / 9x9 shape with fp16 tensors (the dtype of the page's fast numbers), launched as
+    bench.py --dtype fp16 launches it, on sampled rows."""
+    import dataclasses
+
+    base = nain.WORKLOADS[nain.HEADLINE]
+    w = dataclasses.replace(base, name=base.name.replace("bf16", "fp16"), dtype="fp16")
+    t = nain.make_inputs(w, device="cuda")
+    gpu = run_gpu(w, t)
+    check_sampled(w, gpu, host(t), n=192)
+
+
 def test_full_size_fp32_workload(cuda_lib):
     w = nain.WORKLOADS["2d_fp32_16x16_k5"]
     t = nain.make_inputs(w, device="cpu")
