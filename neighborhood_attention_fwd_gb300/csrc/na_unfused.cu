@@ -721,8 +721,9 @@ int launch_unfused_av(const UnfParams& p, int elem, cudaStream_t s) { return lau
 int launch_unfused_gather(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kWsum, p, elem, s); }
 int launch_unfused_scatter(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kScatter, p, elem, s); }
 int launch_unfused_dattn(const UnfParams& p, int elem, cudaStream_t s) { return launch_op(kDot, p, elem, s); }
-// Tokens per block of the first stage (the partial sums are one set of tables per block).
-int rpb_grad_tokens_per_block(int K) { return K <= 1024 ? 1024 : 256; }
+// Tokens per block of the first stage (the partial sums are one set of tables per block): small
+// enough that even a 512x512 problem gives every SM several blocks to overlap their load latency.
+int rpb_grad_tokens_per_block(int K) { return K <= 1024 ? 256 : 64; }
 
 size_t rpb_grad_workspace_bytes(long long tokens, int heads, int K, int table) {
     const long long chunks = (tokens + rpb_grad_tokens_per_block(K) - 1) / rpb_grad_tokens_per_block(K);

@@ -117,9 +117,9 @@ def test_mask_window_rejects_bad_arguments(lib):
 
 
 def test_rpb_grad_workspace_size(lib):
-    # 1024 x 1024 tokens, 8 heads, 9x9: 1024 tokens per block -> 1024 blocks of 8 x 289 fp32 partial sums
+    # 1024 x 1024 tokens, 8 heads, 9x9: 256 tokens per block -> 4096 blocks of 8 x 289 fp32 partial sums
     n = na.na_rpb_grad_workspace_size(1, (1024, 1024), 8, (9, 9))
-    blocks = 1024
+    blocks = 4096
     assert n == (blocks * 8 * 289 * 4 + 255) // 256 * 256
     assert na.na_rpb_grad_workspace_size(1, (16, 16), 2, (4, 5)) == 0      # even kernel: invalid
 
