@@ -519,14 +519,23 @@ def run_ours(args, w, rank, world, dist):
         for which, name in ((0, "fwd"), (1, "dq"), (2, "dkdv")):
             tile_flops[name] = float(na.na_plan_info(which, w.B, w.spatial, w.heads, w.D, w.kernel,
                                                      w.dilation)["mma_flops"])
+    # the fp32 path runs on CUDA-core FMA units: its kernels' FLOPs (forward: S and PV; dQ: S, dP and
+    # dQ; dK/dV: S, dP, dV and dK, per (query, key) pair and channel) against the fp32 FMA peak
+    fma = w.dtype == "fp32"
+    alu_tflops = fp32_fma_tflops(clk.get("sm_mhz"))
+    if fma:
+        nkdh = float(w.tokens) * w.keys_per_query * w.D * w.heads
+        tile_flops = {"fwd": 4.0 * nkdh, "delta": 0.0, "dq": 6.0 * nkdh, "dkdv": 8.0 * nkdh}
     kernels = {}
     for name in ("fwd", "delta", "dq", "dkdv"):
         t_b = kb[name] / hbm
-        t_f = tile_flops[name] / ten
-        bound = "tensor" if t_f > t_b else "hbm"
+        t_f = tile_flops[name] / (alu_tflops * 1e12 if fma else ten)
+        bound = ("alu" if fma else "tensor") if t_f > t_b else "hbm"
         sec = ms[name] * 1e-3
         if bound == "tensor":
             ach, peak, unit = tile_flops[name] / sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        elif bound == "alu":
+            ach, peak, unit = tile_flops[name] / sec / 1e12, alu_tflops, "TFLOP/s"
         else:
             ach, peak, unit = kb[name] / sec / 1e9, peaks["hbm_gbs"], "GB/s"
         kernels[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
@@ -536,7 +545,8 @@ def run_ours(args, w, rank, world, dist):
     traffic = load_traffic(w.name, dom)
     roof_step = sum(kernels[k]["roof_ms"] for k in kernels)
     m_fwd, m_bwd = method_bytes(w)
-    useful_roof_ms = (max(f_fwd / ten, m_fwd / hbm) + max(f_bwd / ten, m_bwd / hbm)) * 1e3
+    fpeak = alu_tflops * 1e12 if fma else ten
+    useful_roof_ms = (max(f_fwd / fpeak, m_fwd / hbm) + max(f_bwd / fpeak, m_bwd / hbm)) * 1e3
 
     # --- end to end through the public API with host buffers
     e2e = run_e2e(args, w, t, step) if not args.no_e2e else None
@@ -556,7 +566,9 @@ def run_ours(args, w, rank, world, dist):
                    "bwd": f_bwd / ((ms["delta"] + ms["dq"] + ms["dkdv"]) * 1e-3) / 1e12},
         "roofline": {"bound": kernels[dom]["bound"], "achieved": kernels[dom]["achieved"],
                      "peak": kernels[dom]["peak"], "unit": kernels[dom]["unit"], "frac": kernels[dom]["frac"],
-                     "traffic": traffic, "kernel": dom, "peak_source": peaks["source"]},
+                     "traffic": traffic, "kernel": dom,
+                     "peak_source": "fp32 FMA peak from unit counts and the sampled clock"
+                                    if kernels[dom]["bound"] == "alu" else peaks["source"]},
         "roofline_step": {"tile_roof_ms": roof_step, "frac_tile": roof_step / ms_step,
                           "useful_roof_ms": useful_roof_ms, "frac_useful": useful_roof_ms / ms_step},
         "kernels": kernels,

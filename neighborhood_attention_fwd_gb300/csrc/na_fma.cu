@@ -5,8 +5,14 @@
 // large kernels"): per axis, a window of k positions of the query's residue class (dilation d),
 // starting at class index clamp(j - k/2, 0, Lc - k); the Cartesian product over axes.  The
 // maintainer's remark in that thread that fp32 attention is memory-bound ("FP32 peak FLOPS is
-// usually terrible") is why this path keeps one thread per row and lets L1/L2 absorb the window
-// overlap instead of tiling through shared memory.
+// usually terrible") is why this path lets L1/L2 absorb the window overlap instead of tiling
+// through shared memory.
+//
+// Lane layout: a row of D fp32 values is D/4 chunks of 16 bytes, and each row gets D/4
+// consecutive lanes, one per chunk.  Neighbouring rows (heads, then tokens) sit next to each other
+// in memory, so every row load of a warp is coalesced.  Dot products over D are a lane's chunk plus
+// a butterfly over the row's lanes (shuffles restricted to those lanes, so rows whose loops differ
+// in length never wait on each other).
 #include <cmath>
 
 #include <cuda_fp16.h>
@@ -18,6 +24,8 @@ namespace na {
 using namespace dev;
 
 namespace {
+
+constexpr int kFmaThreads = 256;
 
 struct RowIdx {
     long long b, tok;  // batch, spatial token index
@@ -39,156 +47,194 @@ __device__ __forceinline__ RowIdx decode_row(const FmaParams& p, long long row) 
     return r;
 }
 
-__device__ __forceinline__ long long row_of(const FmaParams& p, long long b, const int* x, int h) {
-    return ((b * p.L[0] + x[0]) * p.L[1] + x[1]) * static_cast<long long>(p.L[2]) * p.heads +
-           static_cast<long long>(x[2]) * p.heads + h;
-}
-
 // First neighbour (spatial index) of spatial index i along axis a.
 __device__ __forceinline__ int first_nb(const FmaParams& p, int a, int i) {
     const int d = p.d[a], c = i % d, j = i / d;
     return c + d * win_start(j, class_len(p.L[a], d, c), p.k[a]);
 }
 
+// The lanes of one row: CPH = D / 4 lanes per row, 32 / CPH rows per warp.  Lanes past the last
+// row repeat it and store nothing.
 template <int D>
-__device__ __forceinline__ void load_row(const float* base, long long row, float (&v)[D]) {
-    const float4* src = reinterpret_cast<const float4*>(base + row * D);
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-        const float4 t = __ldg(src + i);
-        v[4 * i] = t.x;
-        v[4 * i + 1] = t.y;
-        v[4 * i + 2] = t.z;
-        v[4 * i + 3] = t.w;
+struct RowLanes {
+    static constexpr int CPH = D / 4;
+    static constexpr int RPW = 32 / CPH;
+    int c, rl;
+    unsigned mask;     // the row's lanes
+    long long row;
+    bool store;
+
+    __device__ bool init(long long rows) {
+        const int lane = threadIdx.x & 31;
+        c = lane % CPH;
+        rl = lane / CPH;
+        mask = CPH == 32 ? 0xffffffffu : ((1u << CPH) - 1u) << (rl * CPH);
+        const long long row0 = (static_cast<long long>(blockIdx.x) * kFmaThreads + (threadIdx.x & ~31)) / CPH;
+        if (row0 >= rows) return false;   // the whole warp
+        row = row0 + rl;
+        store = row < rows;
+        if (!store) row = rows - 1;
+        return true;
     }
-}
-
-template <int D>
-__device__ __forceinline__ float dot_row(const float (&a)[D], const float* base, long long row) {
-    const float4* src = reinterpret_cast<const float4*>(base + row * D);
-    float acc = 0.f;
+    // sum over the row's lanes
+    __device__ float sum(float v) const {
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-        const float4 t = __ldg(src + i);
-        acc = fmaf(a[4 * i], t.x, acc);
-        acc = fmaf(a[4 * i + 1], t.y, acc);
-        acc = fmaf(a[4 * i + 2], t.z, acc);
-        acc = fmaf(a[4 * i + 3], t.w, acc);
+        for (int m = CPH / 2; m >= 1; m >>= 1) v += __shfl_xor_sync(mask, v, m);
+        return v;
     }
-    return acc;
+};
+
+__device__ __forceinline__ float4 ld4(const float* base, long long row, int D, int c) {
+    return __ldg(reinterpret_cast<const float4*>(base + row * D) + c);
 }
 
-template <int D>
-__device__ __forceinline__ void axpy_row(float (&acc)[D], float s, const float* base, long long row) {
-    const float4* src = reinterpret_cast<const float4*>(base + row * D);
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i) {
-        const float4 t = __ldg(src + i);
-        acc[4 * i] = fmaf(s, t.x, acc[4 * i]);
-        acc[4 * i + 1] = fmaf(s, t.y, acc[4 * i + 1]);
-        acc[4 * i + 2] = fmaf(s, t.z, acc[4 * i + 2]);
-        acc[4 * i + 3] = fmaf(s, t.w, acc[4 * i + 3]);
+__device__ __forceinline__ float dot4(const float4& a, const float4& b) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ void axpy4(float4& acc, float s, const float4& x) {
+    acc.x = fmaf(s, x.x, acc.x);
+    acc.y = fmaf(s, x.y, acc.y);
+    acc.z = fmaf(s, x.z, acc.z);
+    acc.w = fmaf(s, x.w, acc.w);
+}
+
+__device__ __forceinline__ void scale4(float4& acc, float s) {
+    acc.x *= s;
+    acc.y *= s;
+    acc.z *= s;
+    acc.w *= s;
+}
+
+// A row's window: the first key's row index along each line (t0, t1) and the step between keys.
+struct FmaWindow {
+    int f[3];
+    long long b;
+    int h;
+    __device__ void start(const FmaParams& p, const RowIdx& r) {
+        b = r.b;
+        h = r.h;
+        for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
     }
-}
+    __device__ long long line_row(const FmaParams& p, int t0, int t1) const {
+        const long long tok = ((b * p.L[0] + f[0] + p.d[0] * t0) * p.L[1] + f[1] + p.d[1] * t1) * p.L[2] + f[2];
+        return tok * p.heads + h;
+    }
+};
 
-template <int D>
-__device__ __forceinline__ void store_row(float* base, long long row, const float (&v)[D], float mul) {
-    float4* dst = reinterpret_cast<float4*>(base + row * D);
-#pragma unroll
-    for (int i = 0; i < D / 4; ++i)
-        dst[i] = make_float4(v[4 * i] * mul, v[4 * i + 1] * mul, v[4 * i + 2] * mul, v[4 * i + 3] * mul);
-}
+constexpr int kG = 4;   // keys per group: their loads issue together, and the forward rescales once per group
 
-// Forward: one thread per (batch, token, head) row, online softmax over the window.
+// Forward: online softmax over the window, one rescale per group of keys.
 template <int D>
-__global__ void __launch_bounds__(128) fwd_fma_kernel(const FmaParams p) {
-    const long long total = static_cast<long long>(p.B) * p.N * p.heads;
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= total) return;
+__global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p) {
+    const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
+    RowLanes<D> ln;
+    if (!ln.init(rows)) return;
     const float* q = static_cast<const float*>(p.q);
     const float* k = static_cast<const float*>(p.key);
     const float* v = static_cast<const float*>(p.value);
-    const RowIdx r = decode_row(p, row);
-    int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float qv[D], acc[D];
-    load_row<D>(q, row, qv);
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.f;
+    const float4 qc = ld4(q, ln.row, D, ln.c);
+    FmaWindow win;
+    win.start(p, decode_row(p, ln.row));
+    const long long kstep = static_cast<long long>(p.d[2]) * p.heads;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float m = -INFINITY, l = 0.f;
-    int x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2) {
-                x[2] = f[2] + p.d[2] * t2;
-                const long long kr = row_of(p, r.b, x, r.h);
-                const float s = p.scale * dot_row<D>(qv, k, kr);
-                const float mn = fmaxf(m, s);
-                const float corr = expf(m - mn);  // 0 on the first key (m = -inf)
-                const float pe = expf(s - mn);
-                l = l * corr + pe;
+            const long long r0 = win.line_row(p, t0, t1);
+            for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
+                const int n = min(kG, p.k[2] - t2);
+                float4 kc[kG], vc[kG];
 #pragma unroll
-                for (int c = 0; c < D; ++c) acc[c] *= corr;
-                axpy_row<D>(acc, pe, v, kr);
+                for (int g = 0; g < kG; ++g) {
+                    const long long kr = r0 + (t2 + min(g, n - 1)) * kstep;   // a valid key in every slot
+                    kc[g] = ld4(k, kr, D, ln.c);
+                    vc[g] = ld4(v, kr, D, ln.c);
+                }
+                float sg[kG];
+                float gm = -INFINITY;
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    sg[g] = g < n ? p.scale * ln.sum(dot4(qc, kc[g])) : -INFINITY;
+                    gm = fmaxf(gm, sg[g]);
+                }
+                const float mn = fmaxf(m, gm);
+                const float corr = expf(m - mn);   // 0 on the first group (m = -inf)
+                l *= corr;
+                scale4(acc, corr);
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    const float pe = expf(sg[g] - mn);   // 0 for the empty slots
+                    l += pe;
+                    axpy4(acc, pe, vc[g]);
+                }
                 m = mn;
             }
         }
+    if (ln.store) {
+        scale4(acc, 1.f / l);
+        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = acc;
+        if (ln.c == 0) static_cast<float*>(p.out1)[ln.row] = m + logf(l);
     }
-    store_row<D>(static_cast<float*>(p.out0), row, acc, 1.f / l);
-    static_cast<float*>(p.out1)[row] = m + logf(l);
 }
 
-// dQ: one thread per query row.
+// dQ = scale * sum_j dS_ij k_j with P = exp(scale q.k - LSE), dS = P (dO.v - Delta).
 template <int D>
-__global__ void __launch_bounds__(128) dq_fma_kernel(const FmaParams p) {
-    const long long total = static_cast<long long>(p.B) * p.N * p.heads;
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= total) return;
+__global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) {
+    const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
+    RowLanes<D> ln;
+    if (!ln.init(rows)) return;
     const float* q = static_cast<const float*>(p.q);
     const float* k = static_cast<const float*>(p.key);
     const float* v = static_cast<const float*>(p.value);
     const float* dO = static_cast<const float*>(p.dO);
-    const RowIdx r = decode_row(p, row);
-    int f[3];
-    for (int a = 0; a < 3; ++a) f[a] = first_nb(p, a, r.x[a]);
-    float qv[D], gv[D], acc[D];
-    load_row<D>(q, row, qv);
-    load_row<D>(dO, row, gv);
-#pragma unroll
-    for (int c = 0; c < D; ++c) acc[c] = 0.f;
-    const float lse = p.lse[row], dlt = p.delta[row];
-    int x[3];
-    for (int t0 = 0; t0 < p.k[0]; ++t0) {
-        x[0] = f[0] + p.d[0] * t0;
+    const float4 qc = ld4(q, ln.row, D, ln.c);
+    const float4 gc = ld4(dO, ln.row, D, ln.c);
+    const float lse = p.lse[ln.row], dlt = p.delta[ln.row];
+    FmaWindow win;
+    win.start(p, decode_row(p, ln.row));
+    const long long kstep = static_cast<long long>(p.d[2]) * p.heads;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
-            x[1] = f[1] + p.d[1] * t1;
-            for (int t2 = 0; t2 < p.k[2]; ++t2) {
-                x[2] = f[2] + p.d[2] * t2;
-                const long long kr = row_of(p, r.b, x, r.h);
-                const float pe = expf(p.scale * dot_row<D>(qv, k, kr) - lse);
-                const float ds = pe * (dot_row<D>(gv, v, kr) - dlt);
-                axpy_row<D>(acc, ds, k, kr);
+            const long long r0 = win.line_row(p, t0, t1);
+            for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
+                const int n = min(kG, p.k[2] - t2);
+                float4 kc[kG], vc[kG];
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    const long long kr = r0 + (t2 + min(g, n - 1)) * kstep;
+                    kc[g] = ld4(k, kr, D, ln.c);
+                    vc[g] = ld4(v, kr, D, ln.c);
+                }
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    const float s = ln.sum(dot4(qc, kc[g]));
+                    const float dp = ln.sum(dot4(gc, vc[g]));
+                    const float ds = g < n ? expf(fmaf(p.scale, s, -lse)) * (dp - dlt) : 0.f;
+                    axpy4(acc, ds, kc[g]);
+                }
             }
         }
+    if (ln.store) {
+        scale4(acc, p.scale);
+        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = acc;
     }
-    store_row<D>(static_cast<float*>(p.out0), row, acc, p.scale);
 }
 
-// dK, dV: one thread per key row, gathering over the queries whose windows hold the key.  Per axis
+// dK, dV: one row's lanes per key, gathering over the queries whose windows hold the key.  Per axis
 // those queries form the class-index interval [i_lo, i_hi]: i_lo = 0 if j < k else j - k/2, and
 // i_hi = Lc - 1 if j >= Lc - k else j + k/2 (the border keys are seen by more queries).
 template <int D>
-__global__ void __launch_bounds__(128) dkdv_fma_kernel(const FmaParams p) {
-    const long long total = static_cast<long long>(p.B) * p.N * p.heads;
-    const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= total) return;
+__global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p) {
+    const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
+    RowLanes<D> ln;
+    if (!ln.init(rows)) return;
     const float* q = static_cast<const float*>(p.q);
     const float* k = static_cast<const float*>(p.key);
     const float* v = static_cast<const float*>(p.value);
     const float* dO = static_cast<const float*>(p.dO);
-    const RowIdx r = decode_row(p, row);
+    const RowIdx r = decode_row(p, ln.row);
     int lo[3], hi[3], cl[3];
     for (int a = 0; a < 3; ++a) {
         const int d = p.d[a], c = r.x[a] % d, j = r.x[a] / d, Lc = class_len(p.L[a], d, c), ka = p.k[a];
@@ -196,31 +242,42 @@ __global__ void __launch_bounds__(128) dkdv_fma_kernel(const FmaParams p) {
         hi[a] = j >= Lc - ka ? Lc - 1 : j + ka / 2;
         cl[a] = c;
     }
-    float kv[D], vv[D], dk[D], dv[D];
-    load_row<D>(k, row, kv);
-    load_row<D>(v, row, vv);
-#pragma unroll
-    for (int c = 0; c < D; ++c) {
-        dk[c] = 0.f;
-        dv[c] = 0.f;
-    }
-    int x[3];
-    for (int i0 = lo[0]; i0 <= hi[0]; ++i0) {
-        x[0] = cl[0] + p.d[0] * i0;
+    const float4 kc = ld4(k, ln.row, D, ln.c);
+    const float4 vc = ld4(v, ln.row, D, ln.c);
+    float4 dk = make_float4(0.f, 0.f, 0.f, 0.f), dv = make_float4(0.f, 0.f, 0.f, 0.f);
+    const long long qstep = static_cast<long long>(p.d[2]) * p.heads;
+    for (int i0 = lo[0]; i0 <= hi[0]; ++i0)
         for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
-            x[1] = cl[1] + p.d[1] * i1;
-            for (int i2 = lo[2]; i2 <= hi[2]; ++i2) {
-                x[2] = cl[2] + p.d[2] * i2;
-                const long long qr = row_of(p, r.b, x, r.h);
-                const float pe = expf(p.scale * dot_row<D>(kv, q, qr) - p.lse[qr]);
-                const float ds = pe * (dot_row<D>(vv, dO, qr) - p.delta[qr]);
-                axpy_row<D>(dv, pe, dO, qr);
-                axpy_row<D>(dk, ds, q, qr);
+            const long long tok =
+                ((r.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] + cl[2];
+            const long long qr0 = tok * p.heads + r.h;   // query row of class index 0 along axis 2
+            for (int i2 = lo[2]; i2 <= hi[2]; i2 += kG) {
+                const int n = min(kG, hi[2] - i2 + 1);
+                float4 qc[kG], gc[kG];
+                float ls[kG], dl[kG];
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    const long long qr = qr0 + (i2 + min(g, n - 1)) * qstep;   // a valid query in every slot
+                    qc[g] = ld4(q, qr, D, ln.c);
+                    gc[g] = ld4(dO, qr, D, ln.c);
+                    ls[g] = __ldg(p.lse + qr);
+                    dl[g] = __ldg(p.delta + qr);
+                }
+#pragma unroll
+                for (int g = 0; g < kG; ++g) {
+                    const float s = ln.sum(dot4(kc, qc[g]));
+                    const float dp = ln.sum(dot4(vc, gc[g]));
+                    const float pe = g < n ? expf(fmaf(p.scale, s, -ls[g])) : 0.f;
+                    axpy4(dv, pe, gc[g]);
+                    axpy4(dk, pe * (dp - dl[g]), qc[g]);
+                }
             }
         }
+    if (ln.store) {
+        scale4(dk, p.scale);
+        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = dk;
+        reinterpret_cast<float4*>(static_cast<float*>(p.out1) + ln.row * D)[ln.c] = dv;
     }
-    store_row<D>(static_cast<float*>(p.out0), row, dk, p.scale);
-    store_row<D>(static_cast<float*>(p.out1), row, dv, 1.f);
 }
 
 // Delta = <dO, O> per row.  Each row is split over G = D*bytes/16 lanes (16 bytes each), reduced
@@ -251,12 +308,12 @@ __global__ void __launch_bounds__(256) delta_kernel(const T* __restrict__ o, con
 }
 
 
-template <typename F>
+template <int D, typename F>
 int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
     const long long total = static_cast<long long>(p.B) * p.N * p.heads;
     if (total == 0) return 0;
-    const long long blocks = (total + 127) / 128;
-    kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(128), 0, s>>>(p);
+    const long long blocks = (total * RowLanes<D>::CPH + kFmaThreads - 1) / kFmaThreads;
+    kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(kFmaThreads), 0, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
 
@@ -264,30 +321,30 @@ int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
 
 int launch_fwd_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows(fwd_fma_kernel<16>, p, s);
-        case 32: return launch_rows(fwd_fma_kernel<32>, p, s);
-        case 64: return launch_rows(fwd_fma_kernel<64>, p, s);
-        case 128: return launch_rows(fwd_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16>(fwd_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32>(fwd_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64>(fwd_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128>(fwd_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
 
 int launch_dq_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows(dq_fma_kernel<16>, p, s);
-        case 32: return launch_rows(dq_fma_kernel<32>, p, s);
-        case 64: return launch_rows(dq_fma_kernel<64>, p, s);
-        case 128: return launch_rows(dq_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16>(dq_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32>(dq_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64>(dq_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128>(dq_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
 
 int launch_dkdv_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows(dkdv_fma_kernel<16>, p, s);
-        case 32: return launch_rows(dkdv_fma_kernel<32>, p, s);
-        case 64: return launch_rows(dkdv_fma_kernel<64>, p, s);
-        case 128: return launch_rows(dkdv_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16>(dkdv_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32>(dkdv_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64>(dkdv_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128>(dkdv_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
