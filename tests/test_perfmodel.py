@@ -49,3 +49,19 @@ def test_unfused_call_work_model():
     # the fused backward's useful count adds the recomputed logits and probabilities (2 products)
     assert f_bwd == 10.0 * R * w.keys_per_query * w.D
     assert abs(bench.fp32_fma_tflops() - 80.55) < 0.01
+
+
+def test_growing_window_sizes_and_masked_count():
+    """The --varwin pattern grows from 1 to the full kernel along the first axis, and the masked-weight
+    count matches a direct count over every row."""
+    import numpy as np
+
+    w = nain.small_workload("bf16", (10, 6), 2, 16, (5, 3), (1, 1), B=2)
+    sizes = bench.growing_window_sizes(w)
+    assert sizes[0] == [1, 1, 1, 1, 3, 3, 3, 5, 5, 5]
+    assert sizes[1] == [3] * 6
+    direct = sum((w.keys_per_query - k0 * 3) * 6 for k0 in sizes[0]) * w.B * w.heads
+    assert bench.masked_weights(w, sizes) == direct
+    head = nain.WORKLOADS[nain.HEADLINE]
+    s = bench.growing_window_sizes(head)
+    assert s[0][0] == 1 and s[0][-1] == 9 and all(np.diff(s[0]) >= 0)
