@@ -54,13 +54,14 @@ __device__ __forceinline__ int first_nb(const FmaParams& p, int a, int i) {
 }
 
 // The lanes of one row: CPH = D / 4 lanes per row, 32 / CPH rows per warp.  Lanes past the last
-// row repeat it and store nothing.
-template <int D>
+// row repeat it and store nothing.  UNIFORM: every row of the warp runs the same loop (forward, dQ),
+// so the butterflies may name the whole warp; otherwise they name only the row's lanes.
+template <int D, bool UNIFORM>
 struct RowLanes {
     static constexpr int CPH = D / 4;
     static constexpr int RPW = 32 / CPH;
     int c, rl;
-    unsigned mask;     // the row's lanes
+    unsigned mask;     // the lanes that take part in a butterfly
     long long row;
     bool store;
 
@@ -68,7 +69,7 @@ struct RowLanes {
         const int lane = threadIdx.x & 31;
         c = lane % CPH;
         rl = lane / CPH;
-        mask = CPH == 32 ? 0xffffffffu : ((1u << CPH) - 1u) << (rl * CPH);
+        mask = (UNIFORM || CPH == 32) ? 0xffffffffu : ((1u << CPH) - 1u) << (rl * CPH);
         const long long row0 = (static_cast<long long>(blockIdx.x) * kFmaThreads + (threadIdx.x & ~31)) / CPH;
         if (row0 >= rows) return false;   // the whole warp
         row = row0 + rl;
@@ -84,9 +85,8 @@ struct RowLanes {
     }
 };
 
-__device__ __forceinline__ float4 ld4(const float* base, long long row, int D, int c) {
-    return __ldg(reinterpret_cast<const float4*>(base + row * D) + c);
-}
+constexpr float kLog2e = 1.4426950408889634f;   // log2(e)
+constexpr float kLn2 = 0.6931471805599453f;     // ln(2)
 
 __device__ __forceinline__ float dot4(const float4& a, const float4& b) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
@@ -106,7 +106,12 @@ __device__ __forceinline__ void scale4(float4& acc, float s) {
     acc.w *= s;
 }
 
-// A row's window: the first key's row index along each line (t0, t1) and the step between keys.
+// The lane's chunk of a row (row-major [rows, D] fp32): a float4 pointer.
+__device__ __forceinline__ const float4* chunk_ptr(const void* base, long long row, int D, int c) {
+    return reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * D) + c;
+}
+
+// A row's window: the first key's row index along each line (t0, t1); keys of a line are `step` rows apart.
 struct FmaWindow {
     int f[3];
     long long b;
@@ -124,47 +129,49 @@ struct FmaWindow {
 
 constexpr int kG = 4;   // keys per group: their loads issue together, and the forward rescales once per group
 
-// Forward: online softmax over the window, one rescale per group of keys.
+// Forward: online softmax over the window in log2 units (the scale carries log2 e), one rescale
+// per group of keys; LSE is stored in natural-log units.
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D> ln;
+    RowLanes<D, true> ln;
     if (!ln.init(rows)) return;
-    const float* q = static_cast<const float*>(p.q);
-    const float* k = static_cast<const float*>(p.key);
-    const float* v = static_cast<const float*>(p.value);
-    const float4 qc = ld4(q, ln.row, D, ln.c);
+    const float4 qc = __ldg(chunk_ptr(p.q, ln.row, D, ln.c));
     FmaWindow win;
     win.start(p, decode_row(p, ln.row));
-    const long long kstep = static_cast<long long>(p.d[2]) * p.heads;
+    const int kstep4 = p.d[2] * p.heads * (D / 4);   // float4s between consecutive keys of a line
+    const float sl2 = p.scale * kLog2e;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float m = -INFINITY, l = 0.f;
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const long long r0 = win.line_row(p, t0, t1);
+            const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
+            const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
             for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
                 const int n = min(kG, p.k[2] - t2);
                 float4 kc[kG], vc[kG];
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
-                    const long long kr = r0 + (t2 + min(g, n - 1)) * kstep;   // a valid key in every slot
-                    kc[g] = ld4(k, kr, D, ln.c);
-                    vc[g] = ld4(v, kr, D, ln.c);
+                    const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;   // a valid key in every slot
+                    kc[g] = __ldg(kl + o);
+                    vc[g] = __ldg(vl + o);
                 }
                 float sg[kG];
                 float gm = -INFINITY;
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
-                    sg[g] = g < n ? p.scale * ln.sum(dot4(qc, kc[g])) : -INFINITY;
+                    const float sv = sl2 * ln.sum(dot4(qc, kc[g]));
+                    sg[g] = g < n ? sv : -INFINITY;
                     gm = fmaxf(gm, sg[g]);
                 }
                 const float mn = fmaxf(m, gm);
-                const float corr = expf(m - mn);   // 0 on the first group (m = -inf)
+                const float corr = fast_exp2(m - mn);   // 0 on the first group (m = -inf)
                 l *= corr;
                 scale4(acc, corr);
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
-                    const float pe = expf(sg[g] - mn);   // 0 for the empty slots
+                    const float pe = fast_exp2(sg[g] - mn);   // 0 for the empty slots
                     l += pe;
                     axpy4(acc, pe, vc[g]);
                 }
@@ -174,7 +181,7 @@ __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p)
     if (ln.store) {
         scale4(acc, 1.f / l);
         reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = acc;
-        if (ln.c == 0) static_cast<float*>(p.out1)[ln.row] = m + logf(l);
+        if (ln.c == 0) static_cast<float*>(p.out1)[ln.row] = (m + __log2f(l)) * kLn2;
     }
 }
 
@@ -182,36 +189,35 @@ __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p)
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D> ln;
+    RowLanes<D, true> ln;
     if (!ln.init(rows)) return;
-    const float* q = static_cast<const float*>(p.q);
-    const float* k = static_cast<const float*>(p.key);
-    const float* v = static_cast<const float*>(p.value);
-    const float* dO = static_cast<const float*>(p.dO);
-    const float4 qc = ld4(q, ln.row, D, ln.c);
-    const float4 gc = ld4(dO, ln.row, D, ln.c);
-    const float lse = p.lse[ln.row], dlt = p.delta[ln.row];
+    const float4 qc = __ldg(chunk_ptr(p.q, ln.row, D, ln.c));
+    const float4 gc = __ldg(chunk_ptr(p.dO, ln.row, D, ln.c));
+    const float nl2 = -p.lse[ln.row] * kLog2e, dlt = p.delta[ln.row];
+    const float sl2 = p.scale * kLog2e;
     FmaWindow win;
     win.start(p, decode_row(p, ln.row));
-    const long long kstep = static_cast<long long>(p.d[2]) * p.heads;
+    const int kstep4 = p.d[2] * p.heads * (D / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const long long r0 = win.line_row(p, t0, t1);
+            const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
+            const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
             for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
                 const int n = min(kG, p.k[2] - t2);
                 float4 kc[kG], vc[kG];
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
-                    const long long kr = r0 + (t2 + min(g, n - 1)) * kstep;
-                    kc[g] = ld4(k, kr, D, ln.c);
-                    vc[g] = ld4(v, kr, D, ln.c);
+                    const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;
+                    kc[g] = __ldg(kl + o);
+                    vc[g] = __ldg(vl + o);
                 }
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
                     const float s = ln.sum(dot4(qc, kc[g]));
                     const float dp = ln.sum(dot4(gc, vc[g]));
-                    const float ds = g < n ? expf(fmaf(p.scale, s, -lse)) * (dp - dlt) : 0.f;
+                    const float ds = g < n ? fast_exp2(fmaf(sl2, s, nl2)) * (dp - dlt) : 0.f;
                     axpy4(acc, ds, kc[g]);
                 }
             }
@@ -228,12 +234,8 @@ __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) 
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D> ln;
+    RowLanes<D, false> ln;
     if (!ln.init(rows)) return;
-    const float* q = static_cast<const float*>(p.q);
-    const float* k = static_cast<const float*>(p.key);
-    const float* v = static_cast<const float*>(p.value);
-    const float* dO = static_cast<const float*>(p.dO);
     const RowIdx r = decode_row(p, ln.row);
     int lo[3], hi[3], cl[3];
     for (int a = 0; a < 3; ++a) {
@@ -242,32 +244,38 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
         hi[a] = j >= Lc - ka ? Lc - 1 : j + ka / 2;
         cl[a] = c;
     }
-    const float4 kc = ld4(k, ln.row, D, ln.c);
-    const float4 vc = ld4(v, ln.row, D, ln.c);
+    const float4 kc = __ldg(chunk_ptr(p.key, ln.row, D, ln.c));
+    const float4 vc = __ldg(chunk_ptr(p.value, ln.row, D, ln.c));
+    const float sl2 = p.scale * kLog2e;
     float4 dk = make_float4(0.f, 0.f, 0.f, 0.f), dv = make_float4(0.f, 0.f, 0.f, 0.f);
-    const long long qstep = static_cast<long long>(p.d[2]) * p.heads;
+    const int qstep = p.d[2] * p.heads;
     for (int i0 = lo[0]; i0 <= hi[0]; ++i0)
         for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
             const long long tok =
                 ((r.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] + cl[2];
             const long long qr0 = tok * p.heads + r.h;   // query row of class index 0 along axis 2
+            const float4* ql = chunk_ptr(p.q, qr0, D, ln.c);
+            const float4* gl = chunk_ptr(p.dO, qr0, D, ln.c);
+            const float* lsl = p.lse + qr0;
+            const float* dll = p.delta + qr0;
             for (int i2 = lo[2]; i2 <= hi[2]; i2 += kG) {
                 const int n = min(kG, hi[2] - i2 + 1);
                 float4 qc[kG], gc[kG];
                 float ls[kG], dl[kG];
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
-                    const long long qr = qr0 + (i2 + min(g, n - 1)) * qstep;   // a valid query in every slot
-                    qc[g] = ld4(q, qr, D, ln.c);
-                    gc[g] = ld4(dO, qr, D, ln.c);
-                    ls[g] = __ldg(p.lse + qr);
-                    dl[g] = __ldg(p.delta + qr);
+                    const int ii = i2 + min(g, n - 1);   // a valid query in every slot
+                    const long long oq = static_cast<long long>(ii) * qstep;
+                    qc[g] = __ldg(ql + oq * (D / 4));
+                    gc[g] = __ldg(gl + oq * (D / 4));
+                    ls[g] = __ldg(lsl + oq);
+                    dl[g] = __ldg(dll + oq);
                 }
 #pragma unroll
                 for (int g = 0; g < kG; ++g) {
                     const float s = ln.sum(dot4(kc, qc[g]));
                     const float dp = ln.sum(dot4(vc, gc[g]));
-                    const float pe = g < n ? expf(fmaf(p.scale, s, -ls[g])) : 0.f;
+                    const float pe = g < n ? fast_exp2(fmaf(sl2, s, -ls[g] * kLog2e)) : 0.f;
                     axpy4(dv, pe, gc[g]);
                     axpy4(dk, pe * (dp - dl[g]), qc[g]);
                 }
@@ -312,7 +320,7 @@ template <int D, typename F>
 int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
     const long long total = static_cast<long long>(p.B) * p.N * p.heads;
     if (total == 0) return 0;
-    const long long blocks = (total * RowLanes<D>::CPH + kFmaThreads - 1) / kFmaThreads;
+    const long long blocks = (total * (D / 4) + kFmaThreads - 1) / kFmaThreads;
     kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(kFmaThreads), 0, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }

@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 256;   // 8 warps per block
 constexpr int kKC = 128;        // window offsets staged per warp and pass
+constexpr float kLog2eF = 1.4426950408889634f;   // log2(e): exp(x) = 2^(x log2 e)
 
 // 16-byte chunks: EPC elements widened to fp32 and back (round to nearest even).
 template <typename T>
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
     E::unpack(ld16(A + ln.row * D + ln.c * EPC), af);
     Window win;
     win.start(p, decode(p, ln.row));
-    const long long kstep = win.step * D;
+    const int kstep = p.d[2] * p.heads * D;   // elements between consecutive keys of a line
     const float* bias = BIAS ? p.rpb + static_cast<long long>(win.h) * (2 * p.k[0] - 1) * (2 * p.k[1] - 1) *
                                            (2 * p.k[2] - 1)
                              : nullptr;
@@ -272,7 +273,8 @@ __global__ void __launch_bounds__(kThreads) dot_kernel(const UnfParams p) {
                 }
                 uint4 u[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) u[g] = g < n ? ld16(kp + (t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
+                for (int g = 0; g < G; ++g)
+                    u[g] = g < n ? ld16(kp + static_cast<long long>(t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
                 float sg[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads) wsum_kernel(const UnfParams p) {
     for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
     Window win;
     win.start(p, decode(p, ln.row));
-    const long long kstep = win.step * D;
+    const int kstep = p.d[2] * p.heads * D;   // elements between consecutive keys of a line
     int t = 0, tc = -kKC;
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
@@ -332,7 +334,8 @@ __global__ void __launch_bounds__(kThreads) wsum_kernel(const UnfParams p) {
                 }
                 uint4 u[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) u[g] = g < n ? ld16(kp + (t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
+                for (int g = 0; g < G; ++g)
+                    u[g] = g < n ? ld16(kp + static_cast<long long>(t2 + g) * kstep) : make_uint4(0, 0, 0, 0);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float w = g < n ? E::get(stage[ln.rl * SP + (t - tc + g)]) : 0.f;
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
         lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
         hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
     }
-    const long long qstep = static_cast<long long>(p.d[2]) * p.heads;
+    const int qstep = p.d[2] * p.heads;   // rows between consecutive queries of a line
     float acc[EPC];
 #pragma unroll
     for (int e = 0; e < EPC; ++e) acc[e] = 0.f;
@@ -386,6 +389,8 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
             const long long q0 =
                 ((r.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] + cl[2];
             const long long qrow0 = q0 * p.heads + r.h;   // query row of class index 0 along axis 2
+            const T* wl = W + qrow0 * p.K;                 // its weights
+            const T* sl = S + qrow0 * D;                   // and its row of src
             for (int i2 = lo[2]; i2 <= hi[2]; i2 += G) {
                 const int n = min(G, hi[2] - i2 + 1);
                 float w[G];
@@ -394,10 +399,10 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
                 for (int g = 0; g < G; ++g) {
                     if (g < n) {
                         const int ii = i2 + g;
-                        const long long qi = qrow0 + ii * qstep;
+                        const long long oq = static_cast<long long>(ii) * qstep;
                         const int t = ta01 * p.k[2] + jk[2] - win_start(ii, Lc[2], p.k[2]);
-                        w[g] = E::get(W[qi * p.K + t]);
-                        u[g] = ld16(S + qi * D);
+                        w[g] = E::get(wl[oq * p.K + t]);
+                        u[g] = ld16(sl + oq * D);
                     } else {
                         w[g] = 0.f;
                         u[g] = make_uint4(0, 0, 0, 0);
@@ -453,9 +458,10 @@ __device__ __forceinline__ void softmax_row(const UnfParams& p, long long row, i
         }
         m = warp_maxf(m);
         float l = 0.f;
+        const float ml2 = m * kLog2eF;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
-            v[i] = lane + 32 * i < p.K ? expf(v[i] - m) : 0.f;
+            v[i] = lane + 32 * i < p.K ? fast_exp2(fmaf(v[i], kLog2eF, -ml2)) : 0.f;
             l += v[i];
         }
         const float inv = 1.f / warp_sum(l);
@@ -469,10 +475,11 @@ __device__ __forceinline__ void softmax_row(const UnfParams& p, long long row, i
     for (int t = lane; t < p.K; t += 32) m = fmaxf(m, E::get(x[t]));
     m = warp_maxf(m);
     float l = 0.f;
-    for (int t = lane; t < p.K; t += 32) l += expf(E::get(x[t]) - m);
+    const float ml2 = m * kLog2eF;
+    for (int t = lane; t < p.K; t += 32) l += fast_exp2(fmaf(E::get(x[t]), kLog2eF, -ml2));
     const float inv = 1.f / warp_sum(l);
     __syncwarp();
-    for (int t = lane; t < p.K; t += 32) y[t] = E::put(expf(E::get(x[t]) - m) * inv);
+    for (int t = lane; t < p.K; t += 32) y[t] = E::put(fast_exp2(fmaf(E::get(x[t]), kLog2eF, -ml2)) * inv);
     __syncwarp();
 }
 
