@@ -4,9 +4,9 @@
 // Neighbourhood as read from NATTEN issue #161 ("Backward pass is very slow towards much tokens and
 // large kernels"): per axis, a window of k positions of the query's residue class (dilation d),
 // starting at class index clamp(j - k/2, 0, Lc - k); the Cartesian product over axes.  The
-// maintainer's remark in that thread that fp32 attention is memory-bound ("FP32 peak FLOPS is
-// usually terrible") is why this path lets L1/L2 absorb the window overlap instead of tiling
-// through shared memory.
+// maintainer's remark in that thread that fp32 attention is limited by memory rather than by
+// arithmetic, since the fp32 compute peak is low, is why this path lets L1/L2 absorb the window
+// overlap instead of tiling through shared memory.
 //
 // Lane layout: a row of D fp32 values is D/4 chunks of 16 bytes, and each row gets D/4
 // consecutive lanes, one per chunk.  Neighbouring rows (heads, then tokens) sit next to each other

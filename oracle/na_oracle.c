@@ -10,7 +10,7 @@
  *
  *   Neighbourhood.  The pages ("Backward pass is very slow towards much tokens and large
  *   kernels", NATTEN issue #161: the user's benchmark script and the maintainer's reply about
- *   the "cube receptive field") use na2d/na3d(query, key, value, kernel_size, dilation) but never
+ *   the cubic receptive field of each query) use na2d/na3d(query, key, value, kernel_size, dilation) but never
  *   write the window down.  The reading taken here, per spatial axis of length L with odd kernel
  *   size k (r = k/2) and dilation d:
  *     query index i belongs to residue class c = i mod d, at class index j = i div d;
