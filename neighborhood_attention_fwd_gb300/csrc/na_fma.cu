@@ -127,7 +127,11 @@ struct FmaWindow {
     }
 };
 
-constexpr int kG = 4;   // keys per group: their loads issue together, and the forward rescales once per group
+// Keys per group: their loads issue together (and the forward rescales once per group).  Larger
+// groups keep more loads in flight per warp but cost registers, hence resident warps; measured at
+// 1024x1024 9x9 fp32, one key per group suits the forward and two the backward kernels.
+constexpr int kGF = 1;
+constexpr int kGB = 2;
 
 // Forward: online softmax over the window in log2 units (the scale carries log2 e), one rescale
 // per group of keys; LSE is stored in natural-log units.
@@ -148,19 +152,19 @@ __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p)
             const long long r0 = win.line_row(p, t0, t1);
             const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
             const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
-            for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
-                const int n = min(kG, p.k[2] - t2);
-                float4 kc[kG], vc[kG];
+            for (int t2 = 0; t2 < p.k[2]; t2 += kGF) {
+                const int n = min(kGF, p.k[2] - t2);
+                float4 kc[kGF], vc[kGF];
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGF; ++g) {
                     const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;   // a valid key in every slot
                     kc[g] = __ldg(kl + o);
                     vc[g] = __ldg(vl + o);
                 }
-                float sg[kG];
+                float sg[kGF];
                 float gm = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGF; ++g) {
                     const float sv = sl2 * ln.sum(dot4(qc, kc[g]));
                     sg[g] = g < n ? sv : -INFINITY;
                     gm = fmaxf(gm, sg[g]);
@@ -170,7 +174,7 @@ __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p)
                 l *= corr;
                 scale4(acc, corr);
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGF; ++g) {
                     const float pe = fast_exp2(sg[g] - mn);   // 0 for the empty slots
                     l += pe;
                     axpy4(acc, pe, vc[g]);
@@ -204,17 +208,17 @@ __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) 
             const long long r0 = win.line_row(p, t0, t1);
             const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
             const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
-            for (int t2 = 0; t2 < p.k[2]; t2 += kG) {
-                const int n = min(kG, p.k[2] - t2);
-                float4 kc[kG], vc[kG];
+            for (int t2 = 0; t2 < p.k[2]; t2 += kGB) {
+                const int n = min(kGB, p.k[2] - t2);
+                float4 kc[kGB], vc[kGB];
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGB; ++g) {
                     const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;
                     kc[g] = __ldg(kl + o);
                     vc[g] = __ldg(vl + o);
                 }
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGB; ++g) {
                     const float s = ln.sum(dot4(qc, kc[g]));
                     const float dp = ln.sum(dot4(gc, vc[g]));
                     const float ds = g < n ? fast_exp2(fmaf(sl2, s, nl2)) * (dp - dlt) : 0.f;
@@ -258,12 +262,12 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
             const float4* gl = chunk_ptr(p.dO, qr0, D, ln.c);
             const float* lsl = p.lse + qr0;
             const float* dll = p.delta + qr0;
-            for (int i2 = lo[2]; i2 <= hi[2]; i2 += kG) {
-                const int n = min(kG, hi[2] - i2 + 1);
-                float4 qc[kG], gc[kG];
-                float ls[kG], dl[kG];
+            for (int i2 = lo[2]; i2 <= hi[2]; i2 += kGB) {
+                const int n = min(kGB, hi[2] - i2 + 1);
+                float4 qc[kGB], gc[kGB];
+                float ls[kGB], dl[kGB];
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGB; ++g) {
                     const int ii = i2 + min(g, n - 1);   // a valid query in every slot
                     const long long oq = static_cast<long long>(ii) * qstep;
                     qc[g] = __ldg(ql + oq * (D / 4));
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
                     dl[g] = __ldg(dll + oq);
                 }
 #pragma unroll
-                for (int g = 0; g < kG; ++g) {
+                for (int g = 0; g < kGB; ++g) {
                     const float s = ln.sum(dot4(kc, qc[g]));
                     const float dp = ln.sum(dot4(vc, gc[g]));
                     const float pe = g < n ? fast_exp2(fmaf(sl2, s, -ls[g] * kLog2e)) : 0.f;
