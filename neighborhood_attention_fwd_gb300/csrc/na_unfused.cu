@@ -361,7 +361,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
     using E = Elem<T>;
     using Ln = Lanes<T, D>;
-    constexpr int EPC = Ln::EPC, G = Group<Ln::CPH>::G < 4 ? 4 : Group<Ln::CPH>::G;
+    constexpr int EPC = Ln::EPC, G = 2;   // queries per group (larger groups cost resident warps: measured slower)
     Ln ln;
     if (!ln.init(p.rows)) return;
     if (ln.rl >= ln.nrows) return;   // no warp-wide operation follows
