@@ -240,7 +240,9 @@ size_t na_rpb_grad_workspace_size(int B, int ndim, const int* spatial, int heads
  * drpb: fp32 [heads, 2 k_0 - 1, ..], overwritten.  Two stages through the workspace (per block of
  * tokens, then over blocks in a fixed order): deterministic, no atomics.  With workspace null the
  * library allocates it on the stream (cudaMallocAsync) and frees it after use; otherwise it needs
- * na_rpb_grad_workspace_size bytes (NA_ERR_WORKSPACE if fewer), 16-byte aligned. */
+ * na_rpb_grad_workspace_size bytes (NA_ERR_WORKSPACE if fewer), 16-byte aligned.  Every head's table
+ * is reduced in one block's shared memory: heads * prod(2 k_a - 1) * 4 bytes must stay within about
+ * 224 KB (8 heads of a 9x9x9 window fit, of an 11x11x11 window not), else NA_ERR_UNSUPPORTED. */
 na_status na_rpb_grad(const void* dattn, float* drpb, int B, int ndim, const int* spatial, int heads,
                       const int* kernel, const int* dilation, na_dtype dtype, void* workspace, size_t workspace_bytes,
                       void* stream);

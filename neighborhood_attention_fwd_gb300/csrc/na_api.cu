@@ -833,6 +833,9 @@ na_status na_rpb_grad(const void* dattn, float* drpb, int B, int ndim, const int
     na_status st = unfused_params(B, ndim, spatial, heads, 0, kernel, dilation, 1.f, dtype, false, p);
     if (st != NA_OK) return st;
     if ((st = check_ptrs({dattn, drpb})) != NA_OK) return st;
+    // every head's table must fit one block's shared memory, with the per-token indices
+    const long long table = static_cast<long long>(2 * p.k[0] - 1) * (2 * p.k[1] - 1) * (2 * p.k[2] - 1);
+    if (static_cast<long long>(heads) * table * 4 + 256LL * 12 > 227LL * 1024) return NA_ERR_UNSUPPORTED;
     const size_t need = na_rpb_grad_workspace_size(B, ndim, spatial, heads, kernel);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ws = workspace;

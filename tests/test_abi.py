@@ -116,6 +116,14 @@ def test_mask_window_rejects_bad_arguments(lib):
     assert lib.na_mask_window(P(16), P(16), 1, 2, I((16, 16)), 2, I((6, 5)), I((1, 1)), 0, None) == 1
 
 
+def test_rpb_grad_rejects_tables_beyond_shared_memory(lib):
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    P = ctypes.c_void_p
+    # 8 heads x 33^3 fp32 entries (a 17x17x17 window) is 1.15 MB of tables: unsupported, before any launch
+    assert lib.na_rpb_grad(P(16), P(16), 1, 3, I((40, 40, 40)), 8, I((17, 17, 17)), I((1, 1, 1)), 0, None, 0,
+                           None) == 2
+
+
 def test_rpb_grad_workspace_size(lib):
     # 1024 x 1024 tokens, 8 heads, 9x9: 256 tokens per block -> 4096 blocks of 8 x 289 fp32 partial sums
     n = na.na_rpb_grad_workspace_size(1, (1024, 1024), 8, (9, 9))

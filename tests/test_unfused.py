@@ -303,3 +303,21 @@ def test_variable_window_chain_matches_the_oracle(case, cuda_lib):
     compare("dQ", to64(dq), rq, tol, scale_ref=rv)
     compare("dK", to64(dk), rk, tol, scale_ref=rv)
     compare("dV", to64(dv), rv, tol)
+
+
+def test_variable_window_mask_on_very_large_windows(cuda_lib):
+    """A 1D window of 4999 offsets is beyond the mask kernel's offset table (it decodes per element):
+    the mask on seeded logits matches the oracle's exactly, -inf pattern and kept values alike."""
+    na = cuda_lib
+    L, k = 5001, 4999
+    w = nain.small_workload("bf16", (L,), 1, 16, (k,), (1,), B=1, seed=61)
+    logits = nain.make_weights(w, "randn", seed=62)
+    sizes = [[1 + 2 * ((i * 7) % 2500) for i in range(L)]]           # odd sizes 1..4999, scattered
+    attn = logits.cuda()
+    na.na_mask_window(attn, sizes, w.kernel, w.dilation)
+    status_ok(na)
+    ref = un.mask_window(f32(logits), [np.asarray(sizes[0])], w.kernel, w.dilation)
+    got = to64(attn)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    keep = ~np.isneginf(ref)
+    assert np.array_equal(got[keep], ref[keep])
