@@ -8,11 +8,11 @@
 // arithmetic, since the fp32 compute peak is low, is why this path lets L1/L2 absorb the window
 // overlap instead of tiling through shared memory.
 //
-// Lane layout: a row of D fp32 values is D/4 chunks of 16 bytes, and each row gets D/4
-// consecutive lanes, one per chunk.  Neighbouring rows (heads, then tokens) sit next to each other
-// in memory, so every row load of a warp is coalesced.  Dot products over D are a lane's chunk plus
-// a butterfly over the row's lanes (shuffles restricted to those lanes, so rows whose loops differ
-// in length never wait on each other).
+// Lane layout: a row of D fp32 values is D/4 chunks of 16 bytes, spread over the row's consecutive
+// lanes (each lane holds kCPL of them, interleaved).  Neighbouring rows (heads, then tokens) sit next
+// to each other in memory, so every row load of a warp is coalesced.  Dot products over D are a
+// lane's chunks plus a butterfly over the row's lanes (shuffles restricted to those lanes where rows'
+// loops differ in length, so they never wait on each other).
 #include <cmath>
 
 #include <cuda_fp16.h>
@@ -53,12 +53,24 @@ __device__ __forceinline__ int first_nb(const FmaParams& p, int a, int i) {
     return c + d * win_start(j, class_len(p.L[a], d, c), p.k[a]);
 }
 
-// The lanes of one row: CPH = D / 4 lanes per row, 32 / CPH rows per warp.  Lanes past the last
-// row repeat it and store nothing.  UNIFORM: every row of the warp runs the same loop (forward, dQ),
-// so the butterflies may name the whole warp; otherwise they name only the row's lanes.
-template <int D, bool UNIFORM>
+// Chunks of 16 bytes per lane: a lane holds L of its row's D / 4 chunks, the row's lanes interleaved
+// (lane c owns chunks c, c + CPH, ...), so each load instruction of a row is still contiguous.  More
+// chunks per lane mean more FMAs per butterfly round but more registers; measured at 1024x1024 9x9
+// fp32, one chunk per lane suits the forward and dQ, two suit dK/dV.
+template <int D, int L>
+struct Chunks {
+    static constexpr int CPL = L < D / 4 ? L : D / 4;   // chunks per lane
+    static constexpr int CPH = D / 4 / CPL;             // lanes per row
+    float4 v[CPL];
+};
+constexpr int kCplF = 1, kCplQ = 1, kCplKV = 2;   // forward, dQ, dK/dV
+
+// The lanes of one row: CPH lanes per row, 32 / CPH rows per warp.  Lanes past the last row repeat
+// it and store nothing.  UNIFORM: every row of the warp runs the same loop (forward, dQ), so the
+// butterflies may name the whole warp; otherwise they name only the row's lanes.
+template <int D, bool UNIFORM, int L>
 struct RowLanes {
-    static constexpr int CPH = D / 4;
+    static constexpr int CPH = Chunks<D, L>::CPH;
     static constexpr int RPW = 32 / CPH;
     int c, rl;
     unsigned mask;     // the lanes that take part in a butterfly
@@ -69,7 +81,7 @@ struct RowLanes {
         const int lane = threadIdx.x & 31;
         c = lane % CPH;
         rl = lane / CPH;
-        mask = (UNIFORM || CPH == 32) ? 0xffffffffu : ((1u << CPH) - 1u) << (rl * CPH);
+        mask = (UNIFORM || CPH == 32) ? 0xffffffffu : ((CPH >= 32 ? 0u : (1u << CPH)) - 1u) << (rl * CPH);
         const long long row0 = (static_cast<long long>(blockIdx.x) * kFmaThreads + (threadIdx.x & ~31)) / CPH;
         if (row0 >= rows) return false;   // the whole warp
         row = row0 + rl;
@@ -106,9 +118,49 @@ __device__ __forceinline__ void scale4(float4& acc, float s) {
     acc.w *= s;
 }
 
-// The lane's chunk of a row (row-major [rows, D] fp32): a float4 pointer.
-__device__ __forceinline__ const float4* chunk_ptr(const void* base, long long row, int D, int c) {
+// The lane's first chunk of a row (row-major [rows, D] fp32); its others follow every CPH chunks.
+template <int D>
+__device__ __forceinline__ const float4* chunk_ptr(const void* base, long long row, int c) {
     return reinterpret_cast<const float4*>(static_cast<const float*>(base) + row * D) + c;
+}
+
+template <int D, int L>
+__device__ __forceinline__ void load_chunks(Chunks<D, L>& x, const float4* p) {
+#pragma unroll
+    for (int i = 0; i < Chunks<D, L>::CPL; ++i) x.v[i] = __ldg(p + i * Chunks<D, L>::CPH);
+}
+
+template <int D, int L>
+__device__ __forceinline__ float dot_chunks(const Chunks<D, L>& a, const Chunks<D, L>& b) {
+    float s = dot4(a.v[0], b.v[0]);
+#pragma unroll
+    for (int i = 1; i < Chunks<D, L>::CPL; ++i) s += dot4(a.v[i], b.v[i]);
+    return s;
+}
+
+template <int D, int L>
+__device__ __forceinline__ void axpy_chunks(Chunks<D, L>& acc, float s, const Chunks<D, L>& x) {
+#pragma unroll
+    for (int i = 0; i < Chunks<D, L>::CPL; ++i) axpy4(acc.v[i], s, x.v[i]);
+}
+
+template <int D, int L>
+__device__ __forceinline__ void scale_chunks(Chunks<D, L>& acc, float s) {
+#pragma unroll
+    for (int i = 0; i < Chunks<D, L>::CPL; ++i) scale4(acc.v[i], s);
+}
+
+template <int D, int L>
+__device__ __forceinline__ void zero_chunks(Chunks<D, L>& acc) {
+#pragma unroll
+    for (int i = 0; i < Chunks<D, L>::CPL; ++i) acc.v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+template <int D, int L>
+__device__ __forceinline__ void store_chunks(void* base, long long row, int c, const Chunks<D, L>& x) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + row * D) + c;
+#pragma unroll
+    for (int i = 0; i < Chunks<D, L>::CPL; ++i) p[i * Chunks<D, L>::CPH] = x.v[i];
 }
 
 // A row's window: the first key's row index along each line (t0, t1); keys of a line are `step` rows apart.
@@ -138,53 +190,55 @@ constexpr int kGB = 2;
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D, true> ln;
+    RowLanes<D, true, kCplF> ln;
     if (!ln.init(rows)) return;
-    const float4 qc = __ldg(chunk_ptr(p.q, ln.row, D, ln.c));
+    Chunks<D, kCplF> qc;
+    load_chunks<D, kCplF>(qc, chunk_ptr<D>(p.q, ln.row, ln.c));
     FmaWindow win;
     win.start(p, decode_row(p, ln.row));
     const int kstep4 = p.d[2] * p.heads * (D / 4);   // float4s between consecutive keys of a line
     const float sl2 = p.scale * kLog2e;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    Chunks<D, kCplF> acc;
+    zero_chunks<D, kCplF>(acc);
     float m = -INFINITY, l = 0.f;
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const long long r0 = win.line_row(p, t0, t1);
-            const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
-            const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
+            const float4* kl = chunk_ptr<D>(p.key, r0, ln.c);
+            const float4* vl = chunk_ptr<D>(p.value, r0, ln.c);
             for (int t2 = 0; t2 < p.k[2]; t2 += kGF) {
                 const int n = min(kGF, p.k[2] - t2);
-                float4 kc[kGF], vc[kGF];
+                Chunks<D, kCplF> kc[kGF], vc[kGF];
 #pragma unroll
                 for (int g = 0; g < kGF; ++g) {
                     const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;   // a valid key in every slot
-                    kc[g] = __ldg(kl + o);
-                    vc[g] = __ldg(vl + o);
+                    load_chunks<D, kCplF>(kc[g], kl + o);
+                    load_chunks<D, kCplF>(vc[g], vl + o);
                 }
                 float sg[kGF];
                 float gm = -INFINITY;
 #pragma unroll
                 for (int g = 0; g < kGF; ++g) {
-                    const float sv = sl2 * ln.sum(dot4(qc, kc[g]));
+                    const float sv = sl2 * ln.sum(dot_chunks<D, kCplF>(qc, kc[g]));
                     sg[g] = g < n ? sv : -INFINITY;
                     gm = fmaxf(gm, sg[g]);
                 }
                 const float mn = fmaxf(m, gm);
                 const float corr = fast_exp2(m - mn);   // 0 on the first group (m = -inf)
                 l *= corr;
-                scale4(acc, corr);
+                scale_chunks<D, kCplF>(acc, corr);
 #pragma unroll
                 for (int g = 0; g < kGF; ++g) {
                     const float pe = fast_exp2(sg[g] - mn);   // 0 for the empty slots
                     l += pe;
-                    axpy4(acc, pe, vc[g]);
+                    axpy_chunks<D, kCplF>(acc, pe, vc[g]);
                 }
                 m = mn;
             }
         }
     if (ln.store) {
-        scale4(acc, 1.f / l);
-        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = acc;
+        scale_chunks<D, kCplF>(acc, 1.f / l);
+        store_chunks<D, kCplF>(p.out0, ln.row, ln.c, acc);
         if (ln.c == 0) static_cast<float*>(p.out1)[ln.row] = (m + __log2f(l)) * kLn2;
     }
 }
@@ -193,42 +247,44 @@ __global__ void __launch_bounds__(kFmaThreads) fwd_fma_kernel(const FmaParams p)
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D, true> ln;
+    RowLanes<D, true, kCplQ> ln;
     if (!ln.init(rows)) return;
-    const float4 qc = __ldg(chunk_ptr(p.q, ln.row, D, ln.c));
-    const float4 gc = __ldg(chunk_ptr(p.dO, ln.row, D, ln.c));
+    Chunks<D, kCplQ> qc, gc;
+    load_chunks<D, kCplQ>(qc, chunk_ptr<D>(p.q, ln.row, ln.c));
+    load_chunks<D, kCplQ>(gc, chunk_ptr<D>(p.dO, ln.row, ln.c));
     const float nl2 = -p.lse[ln.row] * kLog2e, dlt = p.delta[ln.row];
     const float sl2 = p.scale * kLog2e;
     FmaWindow win;
     win.start(p, decode_row(p, ln.row));
     const int kstep4 = p.d[2] * p.heads * (D / 4);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    Chunks<D, kCplQ> acc;
+    zero_chunks<D, kCplQ>(acc);
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const long long r0 = win.line_row(p, t0, t1);
-            const float4* kl = chunk_ptr(p.key, r0, D, ln.c);
-            const float4* vl = chunk_ptr(p.value, r0, D, ln.c);
+            const float4* kl = chunk_ptr<D>(p.key, r0, ln.c);
+            const float4* vl = chunk_ptr<D>(p.value, r0, ln.c);
             for (int t2 = 0; t2 < p.k[2]; t2 += kGB) {
                 const int n = min(kGB, p.k[2] - t2);
-                float4 kc[kGB], vc[kGB];
+                Chunks<D, kCplQ> kc[kGB], vc[kGB];
 #pragma unroll
                 for (int g = 0; g < kGB; ++g) {
                     const long long o = static_cast<long long>(t2 + min(g, n - 1)) * kstep4;
-                    kc[g] = __ldg(kl + o);
-                    vc[g] = __ldg(vl + o);
+                    load_chunks<D, kCplQ>(kc[g], kl + o);
+                    load_chunks<D, kCplQ>(vc[g], vl + o);
                 }
 #pragma unroll
                 for (int g = 0; g < kGB; ++g) {
-                    const float s = ln.sum(dot4(qc, kc[g]));
-                    const float dp = ln.sum(dot4(gc, vc[g]));
+                    const float s = ln.sum(dot_chunks<D, kCplQ>(qc, kc[g]));
+                    const float dp = ln.sum(dot_chunks<D, kCplQ>(gc, vc[g]));
                     const float ds = g < n ? fast_exp2(fmaf(sl2, s, nl2)) * (dp - dlt) : 0.f;
-                    axpy4(acc, ds, kc[g]);
+                    axpy_chunks<D, kCplQ>(acc, ds, kc[g]);
                 }
             }
         }
     if (ln.store) {
-        scale4(acc, p.scale);
-        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = acc;
+        scale_chunks<D, kCplQ>(acc, p.scale);
+        store_chunks<D, kCplQ>(p.out0, ln.row, ln.c, acc);
     }
 }
 
@@ -238,7 +294,7 @@ __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) 
 template <int D>
 __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p) {
     const long long rows = static_cast<long long>(p.B) * p.N * p.heads;
-    RowLanes<D, false> ln;
+    RowLanes<D, false, kCplKV> ln;
     if (!ln.init(rows)) return;
     const RowIdx r = decode_row(p, ln.row);
     int lo[3], hi[3], cl[3];
@@ -248,47 +304,50 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
         hi[a] = j >= Lc - ka ? Lc - 1 : j + ka / 2;
         cl[a] = c;
     }
-    const float4 kc = __ldg(chunk_ptr(p.key, ln.row, D, ln.c));
-    const float4 vc = __ldg(chunk_ptr(p.value, ln.row, D, ln.c));
+    Chunks<D, kCplKV> kc, vc;
+    load_chunks<D, kCplKV>(kc, chunk_ptr<D>(p.key, ln.row, ln.c));
+    load_chunks<D, kCplKV>(vc, chunk_ptr<D>(p.value, ln.row, ln.c));
     const float sl2 = p.scale * kLog2e;
-    float4 dk = make_float4(0.f, 0.f, 0.f, 0.f), dv = make_float4(0.f, 0.f, 0.f, 0.f);
+    Chunks<D, kCplKV> dk, dv;
+    zero_chunks<D, kCplKV>(dk);
+    zero_chunks<D, kCplKV>(dv);
     const int qstep = p.d[2] * p.heads;
     for (int i0 = lo[0]; i0 <= hi[0]; ++i0)
         for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
             const long long tok =
                 ((r.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] + cl[2];
             const long long qr0 = tok * p.heads + r.h;   // query row of class index 0 along axis 2
-            const float4* ql = chunk_ptr(p.q, qr0, D, ln.c);
-            const float4* gl = chunk_ptr(p.dO, qr0, D, ln.c);
+            const float4* ql = chunk_ptr<D>(p.q, qr0, ln.c);
+            const float4* gl = chunk_ptr<D>(p.dO, qr0, ln.c);
             const float* lsl = p.lse + qr0;
             const float* dll = p.delta + qr0;
             for (int i2 = lo[2]; i2 <= hi[2]; i2 += kGB) {
                 const int n = min(kGB, hi[2] - i2 + 1);
-                float4 qc[kGB], gc[kGB];
+                Chunks<D, kCplKV> qc[kGB], gc[kGB];
                 float ls[kGB], dl[kGB];
 #pragma unroll
                 for (int g = 0; g < kGB; ++g) {
                     const int ii = i2 + min(g, n - 1);   // a valid query in every slot
                     const long long oq = static_cast<long long>(ii) * qstep;
-                    qc[g] = __ldg(ql + oq * (D / 4));
-                    gc[g] = __ldg(gl + oq * (D / 4));
+                    load_chunks<D, kCplKV>(qc[g], ql + oq * (D / 4));
+                    load_chunks<D, kCplKV>(gc[g], gl + oq * (D / 4));
                     ls[g] = __ldg(lsl + oq);
                     dl[g] = __ldg(dll + oq);
                 }
 #pragma unroll
                 for (int g = 0; g < kGB; ++g) {
-                    const float s = ln.sum(dot4(kc, qc[g]));
-                    const float dp = ln.sum(dot4(vc, gc[g]));
+                    const float s = ln.sum(dot_chunks<D, kCplKV>(kc, qc[g]));
+                    const float dp = ln.sum(dot_chunks<D, kCplKV>(vc, gc[g]));
                     const float pe = g < n ? fast_exp2(fmaf(sl2, s, -ls[g] * kLog2e)) : 0.f;
-                    axpy4(dv, pe, gc[g]);
-                    axpy4(dk, pe * (dp - dl[g]), qc[g]);
+                    axpy_chunks<D, kCplKV>(dv, pe, gc[g]);
+                    axpy_chunks<D, kCplKV>(dk, pe * (dp - dl[g]), qc[g]);
                 }
             }
         }
     if (ln.store) {
-        scale4(dk, p.scale);
-        reinterpret_cast<float4*>(static_cast<float*>(p.out0) + ln.row * D)[ln.c] = dk;
-        reinterpret_cast<float4*>(static_cast<float*>(p.out1) + ln.row * D)[ln.c] = dv;
+        scale_chunks<D, kCplKV>(dk, p.scale);
+        store_chunks<D, kCplKV>(p.out0, ln.row, ln.c, dk);
+        store_chunks<D, kCplKV>(p.out1, ln.row, ln.c, dv);
     }
 }
 
@@ -320,11 +379,11 @@ __global__ void __launch_bounds__(256) delta_kernel(const T* __restrict__ o, con
 }
 
 
-template <int D, typename F>
+template <int D, int L, typename F>
 int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
     const long long total = static_cast<long long>(p.B) * p.N * p.heads;
     if (total == 0) return 0;
-    const long long blocks = (total * (D / 4) + kFmaThreads - 1) / kFmaThreads;
+    const long long blocks = (total * Chunks<D, L>::CPH + kFmaThreads - 1) / kFmaThreads;
     kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(kFmaThreads), 0, s>>>(p);
     return static_cast<int>(cudaGetLastError());
 }
@@ -333,30 +392,30 @@ int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
 
 int launch_fwd_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows<16>(fwd_fma_kernel<16>, p, s);
-        case 32: return launch_rows<32>(fwd_fma_kernel<32>, p, s);
-        case 64: return launch_rows<64>(fwd_fma_kernel<64>, p, s);
-        case 128: return launch_rows<128>(fwd_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16, kCplF>(fwd_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32, kCplF>(fwd_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64, kCplF>(fwd_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128, kCplF>(fwd_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
 
 int launch_dq_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows<16>(dq_fma_kernel<16>, p, s);
-        case 32: return launch_rows<32>(dq_fma_kernel<32>, p, s);
-        case 64: return launch_rows<64>(dq_fma_kernel<64>, p, s);
-        case 128: return launch_rows<128>(dq_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16, kCplQ>(dq_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32, kCplQ>(dq_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64, kCplQ>(dq_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128, kCplQ>(dq_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
 
 int launch_dkdv_fma(const FmaParams& p, cudaStream_t s) {
     switch (p.D) {
-        case 16: return launch_rows<16>(dkdv_fma_kernel<16>, p, s);
-        case 32: return launch_rows<32>(dkdv_fma_kernel<32>, p, s);
-        case 64: return launch_rows<64>(dkdv_fma_kernel<64>, p, s);
-        case 128: return launch_rows<128>(dkdv_fma_kernel<128>, p, s);
+        case 16: return launch_rows<16, kCplKV>(dkdv_fma_kernel<16>, p, s);
+        case 32: return launch_rows<32, kCplKV>(dkdv_fma_kernel<32>, p, s);
+        case 64: return launch_rows<64, kCplKV>(dkdv_fma_kernel<64>, p, s);
+        case 128: return launch_rows<128, kCplKV>(dkdv_fma_kernel<128>, p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }
