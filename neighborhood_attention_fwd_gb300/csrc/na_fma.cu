@@ -179,11 +179,12 @@ struct FmaWindow {
     }
 };
 
-// Keys per group: their loads issue together (and the forward rescales once per group).  Larger
-// groups keep more loads in flight per warp but cost registers, hence resident warps; measured at
-// 1024x1024 9x9 fp32, one key per group suits the forward and two the backward kernels.
+// Keys (queries) per group: their loads issue together (and the forward rescales once per group).
+// Larger groups keep more loads in flight per warp but cost registers, hence resident warps;
+// measured at 1024x1024 9x9 fp32: one for the forward and dK/dV, two for dQ.
 constexpr int kGF = 1;
 constexpr int kGB = 2;
+constexpr int kGKV = 1;
 
 // Forward: online softmax over the window in log2 units (the scale carries log2 e), one rescale
 // per group of keys; LSE is stored in natural-log units.
@@ -321,12 +322,12 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
             const float4* gl = chunk_ptr<D>(p.dO, qr0, ln.c);
             const float* lsl = p.lse + qr0;
             const float* dll = p.delta + qr0;
-            for (int i2 = lo[2]; i2 <= hi[2]; i2 += kGB) {
-                const int n = min(kGB, hi[2] - i2 + 1);
-                Chunks<D, kCplKV> qc[kGB], gc[kGB];
-                float ls[kGB], dl[kGB];
+            for (int i2 = lo[2]; i2 <= hi[2]; i2 += kGKV) {
+                const int n = min(kGKV, hi[2] - i2 + 1);
+                Chunks<D, kCplKV> qc[kGKV], gc[kGKV];
+                float ls[kGKV], dl[kGKV];
 #pragma unroll
-                for (int g = 0; g < kGB; ++g) {
+                for (int g = 0; g < kGKV; ++g) {
                     const int ii = i2 + min(g, n - 1);   // a valid query in every slot
                     const long long oq = static_cast<long long>(ii) * qstep;
                     load_chunks<D, kCplKV>(qc[g], ql + oq * (D / 4));
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kFmaThreads) dkdv_fma_kernel(const FmaParams p
                     dl[g] = __ldg(dll + oq);
                 }
 #pragma unroll
-                for (int g = 0; g < kGB; ++g) {
+                for (int g = 0; g < kGKV; ++g) {
                     const float s = ln.sum(dot_chunks<D, kCplKV>(kc, qc[g]));
                     const float dp = ln.sum(dot_chunks<D, kCplKV>(vc, gc[g]));
                     const float pe = g < n ? fast_exp2(fmaf(sl2, s, -ls[g] * kLog2e)) : 0.f;
