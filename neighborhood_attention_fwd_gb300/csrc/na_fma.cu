@@ -65,13 +65,12 @@ struct Chunks {
 };
 constexpr int kCplF = 1, kCplQ = 1, kCplKV = 2;   // forward, dQ, dK/dV
 
-// The lanes of one row: CPH lanes per row, 32 / CPH rows per warp.  Lanes past the last row repeat
+// The lanes of one row: CPH lanes per row (so a warp holds 32 / CPH rows).  Lanes past the last row repeat
 // it and store nothing.  UNIFORM: every row of the warp runs the same loop (forward, dQ), so the
 // butterflies may name the whole warp; otherwise they name only the row's lanes.
 template <int D, bool UNIFORM, int L>
 struct RowLanes {
     static constexpr int CPH = Chunks<D, L>::CPH;
-    static constexpr int RPW = 32 / CPH;
     int c, rl;
     unsigned mask;     // the lanes that take part in a butterfly
     long long row;
