@@ -424,6 +424,7 @@ na_status unfused_params(int B, int ndim, const int* spatial, int heads, int D, 
     p.D = D;
     p.rows = tokens_of(g) * B * heads;
     p.scale = scale;
+    for (int c = 0; c < g.d[2]; ++c) p.strips2 += ((g.L[2] - c + g.d[2] - 1) / g.d[2] + 15) / 16;
     return NA_OK;
 }
 }  // namespace

@@ -87,6 +87,7 @@ struct UnfParams {
     const float* rpb;   // qk: relative positional bias [heads, 2k0-1, 2k1-1, 2k2-1], or null
     const int* vk;      // mask: per-position kernel sizes, concatenated over the axes
     int vk_off[3];      // mask: offset of each (embedded) axis in vk, -1 for an axis without one
+    int strips2;        // tensor-core logits: strips of 16 class positions along the innermost axis, summed over classes
 };
 
 // Tokens per block of the bias-gradient reduction's first stage, and the size of its partial sums.

@@ -20,6 +20,7 @@
 // (axis 0 outermost) selects key c + d (s + t_a) along each axis a, s the window start.  Every tensor
 // has the same element type (fp32, bf16 or fp16); arithmetic is fp32.
 #include <cmath>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -671,6 +672,137 @@ __global__ void __launch_bounds__(kThreads) mask_window_kernel(const UnfParams p
         }
 }
 
+// Tensor-core logits (bf16, fp16): a warp takes 16 consecutive positions of one residue class along
+// the innermost axis, for one head.  Those queries share their windows along the outer axes, and
+// along the innermost axis their windows lie in one span of at most 15 + k2 class positions.  Per
+// window line (t0, t1) the warp multiplies its 16 q rows by the span's key rows with warp-level MMAs
+// (m16n8k16, fp32 accumulation) and keeps, for each query, the k2 products of its own window.
+// Fragment layouts (PTX m16n8k16, row.col): with g = lane / 4 and q4 = lane % 4, A register i holds
+// row g + 8 (i & 1) and columns 2 q4 + 8 (i >> 1) + {0, 1}; B registers hold rows (keys) g of the
+// n-tile and columns 2 q4 + {0, 1} (+ 8); C holds rows g and g + 8, columns 2 q4 + {0, 1}.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if (F16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t ld32(const void* base, long long elem_off2) {
+    return __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + elem_off2));
+}
+
+constexpr int kMmaThreads = 128;   // 4 warps: each stages its 16 rows of K weights in shared memory
+
+template <typename T, int D, bool BIAS, bool STAGE>
+__global__ void __launch_bounds__(kMmaThreads) dot_mma_kernel(const UnfParams p) {
+    using E = Elem<T>;
+    constexpr bool F16 = sizeof(T) == 2 && !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int KS = D / 16;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const long long unit = (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5;
+    const long long units = static_cast<long long>(p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] *
+                                                              p.heads)) * p.L[0] * p.L[1] * p.strips2 * p.heads;
+    if (unit >= units) return;   // warp-uniform
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
+    long long u = unit;
+    const int h = static_cast<int>(u % p.heads);
+    u /= p.heads;
+    int s = static_cast<int>(u % p.strips2);
+    u /= p.strips2;
+    const int x1 = static_cast<int>(u % p.L[1]);
+    u /= p.L[1];
+    const int x0 = static_cast<int>(u % p.L[0]);
+    const long long b = u / p.L[0];
+    const int d2 = p.d[2], k2 = p.k[2];
+    int c2 = 0, Lc2 = 0;
+    for (c2 = 0; c2 < d2; ++c2) {   // the strip's class along the innermost axis
+        Lc2 = class_len(p.L[2], d2, c2);
+        const int n = (Lc2 + 15) >> 4;
+        if (s < n) break;
+        s -= n;
+    }
+    const int j0 = s * 16, nq = min(16, Lc2 - j0);
+    const int ws0 = win_start(j0, Lc2, k2);
+    const int span = win_start(j0 + nq - 1, Lc2, k2) - ws0 + k2;   // key positions the strip's windows cover
+    // this lane's two query rows (clamped to the last valid one for loads)
+    const int m0 = g, m1 = g + 8;
+    const int jq0 = j0 + min(m0, nq - 1), jq1 = j0 + min(m1, nq - 1);
+    const long long line_tok = (b * p.L[0] + x0) * p.L[1] + x1;
+    const long long r0 = (line_tok * p.L[2] + c2 + static_cast<long long>(d2) * jq0) * p.heads + h;
+    const long long r1 = (line_tok * p.L[2] + c2 + static_cast<long long>(d2) * jq1) * p.heads + h;
+    const int off0 = win_start(jq0, Lc2, k2) - ws0, off1 = win_start(jq1, Lc2, k2) - ws0;
+    uint32_t a[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int col = 16 * ks + 2 * q4;
+        a[ks][0] = ld32(p.a, r0 * D + col);
+        a[ks][1] = ld32(p.a, r1 * D + col);
+        a[ks][2] = ld32(p.a, r0 * D + col + 8);
+        a[ks][3] = ld32(p.a, r1 * D + col + 8);
+    }
+    // outer-axis windows (shared by the strip) and, with a bias, the relative indices
+    const int f0 = first_nb(p, 0, x0), f1 = first_nb(p, 1, x1);
+    const int S1 = 2 * p.k[1] - 1, S2b = 2 * k2 - 1;
+    const int rb0 = f0 / p.d[0] - x0 / p.d[0] + p.k[0] - 1, rb1 = f1 / p.d[1] - x1 / p.d[1] + p.k[1] - 1;
+    const int rbq0 = ws0 + off0 - jq0 + k2 - 1, rbq1 = ws0 + off1 - jq1 + k2 - 1;
+    const float* bias = BIAS ? p.rpb + static_cast<long long>(h) * (2 * p.k[0] - 1) * S1 * S2b : nullptr;
+    T* out = static_cast<T*>(p.out0);
+    T* stage = reinterpret_cast<T*>(smem_raw) + (threadIdx.x >> 5) * 16 * p.K;   // [16 rows][K]
+    const bool v0 = m0 < nq, v1 = m1 < nq;
+    const int ntiles = (span + 7) >> 3;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
+        for (int t1 = 0; t1 < p.k[1]; ++t1) {
+            const long long ktok0 = ((b * p.L[0] + f0 + p.d[0] * t0) * p.L[1] + f1 + p.d[1] * t1) * p.L[2] + c2 +
+                                    static_cast<long long>(d2) * ws0;   // the span's first key token
+            const int tline = (t0 * p.k[1] + t1) * k2;
+            const int bline = BIAS ? ((rb0 + t0) * S1 + rb1 + t1) * S2b : 0;
+            for (int nt = 0; nt < ntiles; ++nt) {
+                const int nk = min(nt * 8 + g, span - 1);   // this lane's key of the n-tile (clamped)
+                const long long kr = (ktok0 + static_cast<long long>(d2) * nk) * p.heads + h;
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int col = 16 * ks + 2 * q4;
+                    mma16816<F16>(c, a[ks], ld32(p.b, kr * D + col), ld32(p.b, kr * D + col + 8));
+                }
+                // keep each query's own window: span column n -> window offset n - off
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int n = nt * 8 + 2 * q4 + (e & 1);
+                    const bool second = e >= 2;
+                    const int t2 = n - (second ? off1 : off0);
+                    if ((second ? v1 : v0) && t2 >= 0 && t2 < k2) {
+                        float val = c[e] * p.scale;
+                        if (BIAS) val += __ldg(bias + bline + (second ? rbq1 : rbq0) + t2);
+                        if (STAGE)
+                            stage[(second ? m1 : m0) * p.K + tline + t2] = E::put(val);
+                        else
+                            out[(second ? r1 : r0) * p.K + tline + t2] = E::put(val);
+                    }
+                }
+            }
+        }
+    if (STAGE) {   // every weight of the strip's rows is staged: write each row's K values contiguously
+        __syncwarp();
+        const long long rbase = (line_tok * p.L[2] + c2 + static_cast<long long>(d2) * j0) * p.heads + h;
+        const long long rstep = static_cast<long long>(d2) * p.heads;   // rows between strip positions
+        for (int m = 0; m < nq; ++m) {
+            T* dst = out + (rbase + m * rstep) * p.K;
+            const T* src = stage + m * p.K;
+            for (int t = lane; t < p.K; t += 32) dst[t] = src[t];
+        }
+    }
+}
+
 int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
 
 enum Op { kDot, kWsum, kScatter };
@@ -682,10 +814,28 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
     const dim3 grid(launch_blocks(p.rows * Ln::CPH)), block(kThreads);
     switch (op) {
         case kDot:
-            if (p.rpb)
+            if (sizeof(T) == 2) {   // bf16, fp16: tensor-core logits, one warp per 16-position strip
+                const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                const size_t smem = static_cast<size_t>(kMmaThreads / 32) * 16 * p.K * sizeof(T);
+                auto run = [&](auto kernel, size_t bytes) {
+                    if (bytes > 48 * 1024)
+                        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+                    kernel<<<g2, b2, bytes, s>>>(p);
+                };
+                if (smem <= 200 * 1024) {   // stage the rows; past that, write each weight directly
+                    if (p.rpb) run(dot_mma_kernel<T, D, true, true>, smem);
+                    else run(dot_mma_kernel<T, D, false, true>, smem);
+                } else {
+                    if (p.rpb) run(dot_mma_kernel<T, D, true, false>, 0);
+                    else run(dot_mma_kernel<T, D, false, false>, 0);
+                }
+            } else if (p.rpb) {
                 dot_kernel<T, D, true><<<grid, block, Ln::kStageBytes, s>>>(p);
-            else
+            } else {
                 dot_kernel<T, D, false><<<grid, block, Ln::kStageBytes, s>>>(p);
+            }
             break;
         case kWsum: wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
         case kScatter: scatter_kernel<T, D><<<grid, block, 0, s>>>(p); break;
