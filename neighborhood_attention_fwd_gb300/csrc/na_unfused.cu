@@ -803,6 +803,147 @@ __global__ void __launch_bounds__(kMmaThreads) dot_mma_kernel(const UnfParams p)
     }
 }
 
+// The strip of a tensor-core warp: 16 consecutive positions of one residue class along the
+// innermost axis (nq of them valid), for one head.
+struct Strip {
+    long long b, line_tok;   // batch; token index of the strip's line without its innermost coordinate
+    int x0, x1, h, c2, Lc2, j0, nq, ws0, span;
+
+    __device__ bool init(const UnfParams& p, long long unit) {
+        const long long units = static_cast<long long>(p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] *
+                                                                 p.heads)) * p.L[0] * p.L[1] * p.strips2 * p.heads;
+        if (unit >= units) return false;
+        long long u = unit;
+        h = static_cast<int>(u % p.heads);
+        u /= p.heads;
+        int s = static_cast<int>(u % p.strips2);
+        u /= p.strips2;
+        x1 = static_cast<int>(u % p.L[1]);
+        u /= p.L[1];
+        x0 = static_cast<int>(u % p.L[0]);
+        b = u / p.L[0];
+        for (c2 = 0; c2 < p.d[2]; ++c2) {
+            Lc2 = class_len(p.L[2], p.d[2], c2);
+            const int n = (Lc2 + 15) >> 4;
+            if (s < n) break;
+            s -= n;
+        }
+        j0 = s * 16;
+        nq = min(16, Lc2 - j0);
+        ws0 = win_start(j0, Lc2, p.k[2]);
+        span = win_start(j0 + nq - 1, Lc2, p.k[2]) - ws0 + p.k[2];
+        line_tok = (b * p.L[0] + x0) * p.L[1] + x1;
+        return true;
+    }
+    // row index of strip position m (clamped to the last valid one)
+    __device__ long long row(const UnfParams& p, int m) const {
+        return (line_tok * p.L[2] + c2 + static_cast<long long>(p.d[2]) * (j0 + min(m, nq - 1))) * p.heads + h;
+    }
+    // offset of position m's window in the span
+    __device__ int off(const UnfParams& p, int m) const {
+        return win_start(j0 + min(m, nq - 1), Lc2, p.k[2]) - ws0;
+    }
+};
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t pack_b16(uint16_t lo, uint16_t hi) {
+    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// Tensor-core weighted sums (bf16, fp16): out_row = scale * sum_t w[row, t] src_(t-th neighbour).  Per
+// window line the warp's 16 rows form a banded A (the span x weights, zero outside each row's window)
+// from its staged weight rows, and the span's src rows, staged with a padded stride, give B through
+// ldmatrix.trans; m16n8k16 MMAs accumulate [16, D] in fp32.
+template <int D>
+struct WsumLayout {
+    static constexpr int kVStride = D + 8;   // staged src row stride (elements): conflict-free ldmatrix rows
+    __host__ __device__ static int span_pad(int k2) { return ((15 + k2) + 15) / 16 * 16; }
+    __host__ __device__ static size_t warp_bytes(int K, int k2) {
+        return (static_cast<size_t>(16) * K + static_cast<size_t>(span_pad(k2)) * kVStride) * 2;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMmaThreads) wsum_mma_kernel(const UnfParams p) {
+    constexpr bool F16 = !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int NT = D / 8, VS = WsumLayout<D>::kVStride;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Strip st;
+    if (!st.init(p, (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5)) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3, warp = threadIdx.x >> 5;
+    const int K = p.K, k2 = p.k[2], d2 = p.d[2];
+    const int spad = WsumLayout<D>::span_pad(k2);
+    uint16_t* ws = reinterpret_cast<uint16_t*>(smem_raw + warp * WsumLayout<D>::warp_bytes(K, k2));   // [16][K]
+    uint16_t* vs = ws + 16 * K;                                                                      // [spad][VS]
+    const uint16_t* W = static_cast<const uint16_t*>(p.a);
+    const uint16_t* S = static_cast<const uint16_t*>(p.b);
+    // the strip's weight rows (rows past the last valid one read as zero)
+    for (int m = 0; m < 16; ++m) {
+        const long long r = st.row(p, m);
+        for (int t = lane; t < K; t += 32) ws[m * K + t] = m < st.nq ? W[r * K + t] : uint16_t(0);
+    }
+    const int om0 = st.off(p, g), om1 = st.off(p, g + 8);
+    const int f0 = first_nb(p, 0, st.x0), f1 = first_nb(p, 1, st.x1);
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const uint32_t vs_addr = smem_u32(vs);
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
+        for (int t1 = 0; t1 < p.k[1]; ++t1) {
+            const long long ktok0 = ((st.b * p.L[0] + f0 + p.d[0] * t0) * p.L[1] + f1 + p.d[1] * t1) * p.L[2] +
+                                    st.c2 + static_cast<long long>(d2) * st.ws0;
+            const int tline = (t0 * p.k[1] + t1) * k2;
+            __syncwarp();   // the previous line's B reads are done
+            for (int idx = lane; idx < spad * (D / 8); idx += 32) {
+                const int n = idx / (D / 8), c8 = idx % (D / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (n < st.span) v = ld16(S + ((ktok0 + static_cast<long long>(d2) * n) * p.heads + st.h) * D + 8 * c8);
+                *reinterpret_cast<uint4*>(vs + n * VS + 8 * c8) = v;
+            }
+            __syncwarp();
+            for (int ks = 0; ks < spad / 16; ++ks) {
+                // A: banded weights, a[i] = rows g (+8), span columns 16 ks + 2 q4 (+8) + {0, 1}
+                uint32_t a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = g + 8 * (i & 1), om = (i & 1) ? om1 : om0;
+                    const int n = 16 * ks + 2 * q4 + 8 * (i >> 1);
+                    const int ta = n - om, tb = n + 1 - om;
+                    const uint16_t wa = (ta >= 0 && ta < k2) ? ws[m * K + tline + ta] : uint16_t(0);
+                    const uint16_t wb = (tb >= 0 && tb < k2) ? ws[m * K + tline + tb] : uint16_t(0);
+                    a[i] = pack_b16(wa, wb);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; nt += 2) {
+                    // four 8x8 tiles: keys [16 ks, +8) and [+8, +16) of channel blocks nt and nt + 1
+                    const int mi = lane >> 3, rr = lane & 7;
+                    const uint32_t addr =
+                        vs_addr + static_cast<uint32_t>(((16 * ks + 8 * (mi & 1) + rr) * VS + 8 * (nt + (mi >> 1))) * 2);
+                    uint32_t bfr[4];
+                    ldmatrix_x4_trans(bfr, addr);
+                    mma16816<F16>(acc[nt], a, bfr[0], bfr[1]);
+                    mma16816<F16>(acc[nt + 1], a, bfr[2], bfr[3]);
+                }
+            }
+        }
+    // rows g and g + 8, channels 8 nt + 2 q4 + {0, 1}
+    T* out = static_cast<T*>(p.out0);
+    const long long r0 = st.row(p, g), r1 = st.row(p, g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int col = 8 * nt + 2 * q4;
+        if (g < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r0 * D + col) = Elem<T>::pair(acc[nt][0] * p.scale, acc[nt][1] * p.scale);
+        if (g + 8 < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r1 * D + col) = Elem<T>::pair(acc[nt][2] * p.scale, acc[nt][3] * p.scale);
+    }
+}
+
 int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
 
 enum Op { kDot, kWsum, kScatter };
@@ -814,7 +955,7 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
     const dim3 grid(launch_blocks(p.rows * Ln::CPH)), block(kThreads);
     switch (op) {
         case kDot:
-            if (sizeof(T) == 2) {   // bf16, fp16: tensor-core logits, one warp per 16-position strip
+            if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core logits, one warp per 16-position strip
                 const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
                 const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
                 const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
@@ -831,13 +972,31 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
                     if (p.rpb) run(dot_mma_kernel<T, D, true, false>, 0);
                     else run(dot_mma_kernel<T, D, false, false>, 0);
                 }
-            } else if (p.rpb) {
-                dot_kernel<T, D, true><<<grid, block, Ln::kStageBytes, s>>>(p);
             } else {
-                dot_kernel<T, D, false><<<grid, block, Ln::kStageBytes, s>>>(p);
+                if (p.rpb)
+                    dot_kernel<T, D, true><<<grid, block, Ln::kStageBytes, s>>>(p);
+                else
+                    dot_kernel<T, D, false><<<grid, block, Ln::kStageBytes, s>>>(p);
             }
             break;
-        case kWsum: wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p); break;
+        case kWsum: {
+            bool done = false;
+            if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core weighted sums
+                const size_t smem = (kMmaThreads / 32) * WsumLayout<D>::warp_bytes(p.K, p.k[2]);
+                if (smem <= 200 * 1024) {
+                    const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                    const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                    const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                    if (smem > 48 * 1024)
+                        cudaFuncSetAttribute(wsum_mma_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+                    wsum_mma_kernel<T, D><<<g2, b2, smem, s>>>(p);
+                    done = true;
+                }
+            }
+            if (!done) wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p);
+            break;
+        }
         case kScatter: scatter_kernel<T, D><<<grid, block, 0, s>>>(p); break;
     }
     return static_cast<int>(cudaGetLastError());
