@@ -405,15 +405,17 @@ def run_unfused(args, w, rank, world, dist):
 
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
-    alu_tflops = fp32_fma_tflops(clk.get("sm_mhz"))
+    # bf16 / fp16 products run on the tensor cores (warp MMAs); fp32 products on CUDA-core FMA units
+    tensor = w.dtype in ("bf16", "fp16")
+    flop_peak = peaks["bf16_tflops"] if tensor else fp32_fma_tflops(clk.get("sm_mhz"))
     work = unfused_call_work(w)
     calls = {}
     for name in calls_run:
         nbytes, flops = work[name]
-        t_b, t_f = nbytes / hbm, flops / (alu_tflops * 1e12)
+        t_b, t_f = nbytes / hbm, flops / (flop_peak * 1e12)
         sec = ms[name] * 1e-3
         if t_f > t_b:
-            ach, peak, unit, bound = flops / sec / 1e12, alu_tflops, "TFLOP/s", "alu"
+            ach, peak, unit, bound = flops / sec / 1e12, flop_peak, "TFLOP/s", "tensor" if tensor else "alu"
         else:
             ach, peak, unit, bound = nbytes / sec / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
         calls[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,

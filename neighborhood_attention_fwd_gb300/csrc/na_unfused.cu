@@ -893,20 +893,21 @@ __global__ void __launch_bounds__(kMmaThreads) wsum_mma_kernel(const UnfParams p
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     const uint32_t vs_addr = smem_u32(vs);
+    const int nks = (st.span + 15) >> 4;   // k-steps this strip needs
     for (int t0 = 0; t0 < p.k[0]; ++t0)
         for (int t1 = 0; t1 < p.k[1]; ++t1) {
             const long long ktok0 = ((st.b * p.L[0] + f0 + p.d[0] * t0) * p.L[1] + f1 + p.d[1] * t1) * p.L[2] +
                                     st.c2 + static_cast<long long>(d2) * st.ws0;
             const int tline = (t0 * p.k[1] + t1) * k2;
             __syncwarp();   // the previous line's B reads are done
-            for (int idx = lane; idx < spad * (D / 8); idx += 32) {
+            for (int idx = lane; idx < 16 * nks * (D / 8); idx += 32) {
                 const int n = idx / (D / 8), c8 = idx % (D / 8);
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (n < st.span) v = ld16(S + ((ktok0 + static_cast<long long>(d2) * n) * p.heads + st.h) * D + 8 * c8);
                 *reinterpret_cast<uint4*>(vs + n * VS + 8 * c8) = v;
             }
             __syncwarp();
-            for (int ks = 0; ks < spad / 16; ++ks) {
+            for (int ks = 0; ks < nks; ++ks) {
                 // A: banded weights, a[i] = rows g (+8), span columns 16 ks + 2 q4 (+8) + {0, 1}
                 uint32_t a[4];
 #pragma unroll
@@ -932,6 +933,118 @@ __global__ void __launch_bounds__(kMmaThreads) wsum_mma_kernel(const UnfParams p
             }
         }
     // rows g and g + 8, channels 8 nt + 2 q4 + {0, 1}
+    T* out = static_cast<T*>(p.out0);
+    const long long r0 = st.row(p, g), r1 = st.row(p, g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int col = 8 * nt + 2 * q4;
+        if (g < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r0 * D + col) = Elem<T>::pair(acc[nt][0] * p.scale, acc[nt][1] * p.scale);
+        if (g + 8 < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r1 * D + col) = Elem<T>::pair(acc[nt][2] * p.scale, acc[nt][3] * p.scale);
+    }
+}
+
+// Tensor-core gathers over inverse windows (bf16, fp16): out_j = scale * sum over the queries i whose
+// windows hold key j of w[i, t(i, j)] src_i, for dK (dattn, q) and dV (attn, dO).  The warp is a
+// 16-key strip.  Its keys share their inverse ranges along the outer axes; along the innermost axis
+// their queries lie in one span [q_lo, q_hi].  Per query line (i0, i1) the warp stages, for every
+// query of the span, the k2 weights of its window line that lies on the strip's key line, and the
+// span's src rows; A[m, n] is query n's weight for key m (zero when key m is outside query n's
+// window), B the src rows through ldmatrix.trans.  Every key row is written once: no atomics.
+template <int D>
+struct ScatterLayout {
+    static constexpr int kVStride = D + 8;
+    __host__ __device__ static int span_pad(int k2) { return (16 + 2 * k2 + 15) / 16 * 16; }
+    __host__ __device__ static size_t warp_bytes(int k2) {
+        const size_t sp = static_cast<size_t>(span_pad(k2));
+        return (sp * k2 + sp * kVStride) * 2 + 16;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMmaThreads) scatter_mma_kernel(const UnfParams p) {
+    constexpr bool F16 = !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int NT = D / 8, VS = ScatterLayout<D>::kVStride;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    Strip st;
+    if (!st.init(p, (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5)) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3, warp = threadIdx.x >> 5;
+    const int K = p.K, k2 = p.k[2], d2 = p.d[2], r2 = k2 >> 1;
+    const int spad = ScatterLayout<D>::span_pad(k2);
+    uint16_t* vs = reinterpret_cast<uint16_t*>(smem_raw + warp * ScatterLayout<D>::warp_bytes(k2));   // [spad][VS]
+    uint16_t* wst = vs + spad * VS;                                                                   // [spad][k2]
+    const uint16_t* W = static_cast<const uint16_t*>(p.a);
+    const uint16_t* S = static_cast<const uint16_t*>(p.b);
+    // queries of the strip's keys along the innermost axis (class coordinates)
+    const int jl = st.j0 + st.nq - 1, Lc2 = st.Lc2;
+    const int q_lo = st.j0 < k2 ? 0 : st.j0 - r2;
+    const int q_hi = jl >= Lc2 - k2 ? Lc2 - 1 : jl + r2;
+    const int qspan = q_hi - q_lo + 1;   // <= 16 + 2 k2 (the layout's span_pad)
+    const int nks = (qspan + 15) >> 4;    // k-steps this strip needs (interior strips: fewer than span_pad / 16)
+    // outer axes: the keys' class, class index, class length and query ranges (shared by the strip)
+    int cl[2], jk[2], Lc[2], lo[2], hi[2];
+    const int xo[2] = {st.x0, st.x1};
+    for (int a = 0; a < 2; ++a) {
+        const int d = p.d[a], k = p.k[a];
+        cl[a] = xo[a] % d;
+        jk[a] = xo[a] / d;
+        Lc[a] = class_len(p.L[a], d, cl[a]);
+        lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
+        hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
+    }
+    const int jm0 = st.j0 + min(g, st.nq - 1), jm1 = st.j0 + min(g + 8, st.nq - 1);   // this lane's keys
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    const uint32_t vs_addr = smem_u32(vs);
+    for (int i0 = lo[0]; i0 <= hi[0]; ++i0) {
+        const int ta0 = jk[0] - win_start(i0, Lc[0], p.k[0]);
+        for (int i1 = lo[1]; i1 <= hi[1]; ++i1) {
+            const int wline = (ta0 * p.k[1] + jk[1] - win_start(i1, Lc[1], p.k[1])) * k2;
+            const long long qtok0 = ((st.b * p.L[0] + cl[0] + p.d[0] * i0) * p.L[1] + cl[1] + p.d[1] * i1) * p.L[2] +
+                                    st.c2 + static_cast<long long>(d2) * q_lo;   // the span's first query token
+            __syncwarp();   // the previous line's reads are done
+            for (int idx = lane; idx < 16 * nks * (D / 8); idx += 32) {
+                const int n = idx / (D / 8), c8 = idx % (D / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (n < qspan) v = ld16(S + ((qtok0 + static_cast<long long>(d2) * n) * p.heads + st.h) * D + 8 * c8);
+                *reinterpret_cast<uint4*>(vs + n * VS + 8 * c8) = v;
+            }
+            for (int idx = lane; idx < qspan * k2; idx += 32) {
+                const int n = idx / k2, u = idx - n * k2;
+                wst[idx] = W[((qtok0 + static_cast<long long>(d2) * n) * p.heads + st.h) * K + wline + u];
+            }
+            __syncwarp();
+            for (int ks = 0; ks < nks; ++ks) {
+                // A[m, n]: query n's weight for key m, a[i] = keys g (+8), queries 16 ks + 2 q4 (+8) + {0, 1}
+                uint32_t a[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int jm = (i & 1) ? jm1 : jm0;
+                    const int n = 16 * ks + 2 * q4 + 8 * (i >> 1);
+                    uint16_t e[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int nn = n + h2;
+                        const int u = jm - win_start(q_lo + nn, Lc2, k2);
+                        e[h2] = (nn < qspan && u >= 0 && u < k2) ? wst[nn * k2 + u] : uint16_t(0);
+                    }
+                    a[i] = pack_b16(e[0], e[1]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; nt += 2) {
+                    const int mi = lane >> 3, rr = lane & 7;
+                    const uint32_t addr =
+                        vs_addr + static_cast<uint32_t>(((16 * ks + 8 * (mi & 1) + rr) * VS + 8 * (nt + (mi >> 1))) * 2);
+                    uint32_t bfr[4];
+                    ldmatrix_x4_trans(bfr, addr);
+                    mma16816<F16>(acc[nt], a, bfr[0], bfr[1]);
+                    mma16816<F16>(acc[nt + 1], a, bfr[2], bfr[3]);
+                }
+            }
+        }
+    }
     T* out = static_cast<T*>(p.out0);
     const long long r0 = st.row(p, g), r1 = st.row(p, g + 8);
 #pragma unroll
@@ -997,7 +1110,24 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
             if (!done) wsum_kernel<T, D><<<grid, block, Ln::kStageBytes, s>>>(p);
             break;
         }
-        case kScatter: scatter_kernel<T, D><<<grid, block, 0, s>>>(p); break;
+        case kScatter: {
+            bool done = false;
+            if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core gathers over inverse windows
+                const size_t smem = (kMmaThreads / 32) * ScatterLayout<D>::warp_bytes(p.k[2]);
+                if (smem <= 200 * 1024) {
+                    const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                    const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                    const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                    if (smem > 48 * 1024)
+                        cudaFuncSetAttribute(scatter_mma_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+                    scatter_mma_kernel<T, D><<<g2, b2, smem, s>>>(p);
+                    done = true;
+                }
+            }
+            if (!done) scatter_kernel<T, D><<<grid, block, 0, s>>>(p);
+            break;
+        }
     }
     return static_cast<int>(cudaGetLastError());
 }
