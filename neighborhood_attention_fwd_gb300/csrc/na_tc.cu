@@ -9,11 +9,11 @@ uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D) { return tc_layout(
 int tc_tmem_cols(int which) { return which == 0 ? 256 : 512; }
 
 int tc_max_nc(int which, int D) {
-    // double-buffered score accumulators plus double-buffered tile accumulators; the forward keeps
-    // at most 4 groups (64 columns) of scores in registers
+    // double-buffered score accumulators plus double-buffered tile accumulators; the forward's P
+    // overwrites its scores, and its softmax takes a run of at most six groups (96 columns)
     const int cols = tc_tmem_cols(which);
     const int nc = which == 0 ? (cols - 2 * D) / 2 : (which == 1 ? (cols - 2 * D) / 4 : (cols - 4 * D) / 4);
-    const int cap = which == 0 ? 64 : 128;
+    const int cap = which == 0 ? 96 : 128;
     return (nc < cap ? nc : cap) / 16 * 16;
 }
 

@@ -26,8 +26,9 @@
 //   MMA warp      : per chunk the "score" products (and the bias products) into a double-buffered
 //                   TMEM accumulator, then the previous chunk's "update" products into a
 //                   double-buffered tile accumulator
-//   softmax warps : per chunk read scores from TMEM, write P (or dS) to a double-buffered smem
-//                   operand; per tile read the accumulator and store it.
+//   softmax warps : per chunk read scores from TMEM and write P (forward: into the same TMEM
+//                   buffer, over the scores; backward: dS, or P^T and dS^T, to a double-buffered
+//                   smem operand); per tile read the accumulator and store it.
 // Every mbarrier wait is bounded (see na_device.cuh); a wait that gives up records the site in the
 // status word and the CTA stops issuing work.
 #pragma once
@@ -99,7 +100,7 @@ template <bool F16>
 __host__ __device__ constexpr float masked_below() { return F16 ? -3.2e4f : -1.0e29f; }
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
-//   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [S] x {K, V};  P[2]
+//   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [S] x {K, V}   (P is written to TMEM)
 //   which 1 (dQ)  : tile ring [2] x {Q, dO}; chunk ring [S] x {K, V};  dS[2]
 //   which 2 (dKdV): tile ring [2] x {K, V};  chunk ring [S] x {Q, dO}; P^T[2], dS^T[2];
 //                   per chunk slot the -LSE (log2 units) and Delta of the chunk's queries
@@ -138,7 +139,7 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     L.p0 = o;
     L.p_op = pbytes;
     L.p_buf = nop * pbytes;
-    o += pbufs_of(which) * L.p_buf;
+    if (which != 0) o += pbufs_of(which) * L.p_buf;  // the forward's P lives in TMEM, over its scores
     L.abias = o;
     o += static_cast<uint32_t>(bg.na) * 4096u;
     L.bbias = o;
@@ -752,6 +753,16 @@ struct FwdIssuer {
                           idesc, 1u);
             }
     }
+    // O += P V with P read from TMEM: 16-bit pairs packed in NC / 2 columns from p_tmem, so the
+    // k-step kk (chunk columns 16 kk .. 16 kk + 15) starts at column p_tmem + 8 kk.
+    __device__ void p_tmem_x_chunk(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_off, bool accumulate) const {
+        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_mma(128, D, false, true, p.f16 != 0);
+        const uint32_t b = smem_u32(smem + b_off);
+        for (int kk = 0; kk < p.plan.NC / 16; ++kk)
+            umma_ts(d_tmem, p_tmem + 8u * kk, sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
+    }
     __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
         const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
         const uint32_t idesc = idesc_mma(128, D, false, true, p.f16 != 0);
@@ -812,7 +823,7 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
                 tc_fence_after();
                 const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
                 if (WHICH == 0) {
-                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
+                    mi.p_tmem_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
                 } else if (WHICH == 1) {
                     mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 0), q0.ci > 0);  // dQ += dS K
                 } else {
@@ -831,8 +842,10 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
         if (have && nq < 3) {
             const uint32_t qs = jS & 1, s = gS % kS, sb = gS & 1;
             if (!qready) qready = mbar_test(&bars[kQFull + qs], (jS >> 1) & 1);
+            // the forward's score buffer also holds that chunk's P: it is free once the product
+            // P V of chunk gS - 2 is done (the backward's softmax releases it after reading)
             if (qready && mbar_test(&bars[kKVFull + s], (gS / kS) & 1) &&
-                (gS < 2 || mbar_test(&bars[kSEmpty + sb], ((gS >> 1) - 1) & 1))) {
+                (gS < 2 || mbar_test(&bars[(WHICH == 0 ? kPEmpty : kSEmpty) + sb], ((gS >> 1) - 1) & 1))) {
                 tc_fence_after();
                 mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
                 mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
@@ -985,9 +998,7 @@ struct FwdCtx {
     unsigned* err;
     uint32_t tS0, tS_step;  // this warp's lanes of score buffer 0, and the offset of buffer 1
     uint32_t tO;            // this warp's lanes of the tile accumulator
-    uint32_t sP0, sP_step;  // P operand 0, and the offset of operand 1
-    uint32_t rowbase, sw;
-    int ngroups;       // 16-column groups per chunk
+    int ngroups;            // 16-column groups per chunk
     float sl2;
     uint64_t sl2x2;
     int lane;
@@ -996,50 +1007,59 @@ struct FwdCtx {
 // Groups [glo, glo + n) as a bit mask.
 __device__ __forceinline__ uint32_t run_mask(int glo, int n) { return ((1u << n) - 1u) << glo; }
 
-// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + N).  `nz` holds
-// the groups of this warp's rows of P buffer g & 1 that may be nonzero (its last run); groups in
-// nz outside the new run are zeroed, and nz becomes the new run.
-template <int D, int N, bool F16>
-__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, float& m, uint64_t (&lsum)[4],
-                                          uint32_t& nz) {
-    constexpr uint32_t kPB = pbufs_of(0);
-    const uint32_t sb = g & 1, pb = g % kPB;
-    uint32_t v[N > 0 ? N : 1][16];
-    const uint32_t tS = x.tS0 + sb * x.tS_step;
-#pragma unroll
-    for (int i = 0; i < N; ++i) tmem_ld16(tS + 16u * (glo + i), v[i]);
-    if (N > 0) {
-        tmem_ld_wait_all();
-#pragma unroll
-        for (int i = 0; i < N; ++i) reg_fence16(v[i]);
-    }
-    // the score buffer is free for the product of chunk g + 2
-    tc_fence_before();
-    __syncwarp();
-    if (x.lane == 0) mbar_arrive(&x.bars[kSEmpty + sb]);
-    // chunk row max (masked scores carry the -2^100 window bias), four independent chains
-    float cmax = -INFINITY;
-    if (N == 0) {
-        // no key of this warp's rows in the chunk: nothing to read, the running max is unchanged
+// A packed pair of the operand type back to fp32 (first element from the low half).
+template <bool F16>
+__device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
+    if constexpr (F16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v));
+        lo = f.x;
+        hi = f.y;
     } else {
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < N; ++i)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                mx[e] = fmax3(mx[e], fmaxf(__uint_as_float(v[i][4 * e]), __uint_as_float(v[i][4 * e + 1])),
-                              fmaxf(__uint_as_float(v[i][4 * e + 2]), __uint_as_float(v[i][4 * e + 3])));
-        cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        lo = __uint_as_float(v << 16);
+        hi = __uint_as_float(v & 0xffff0000u);
     }
+}
+
+// One part of a warp's run: groups [gb, gb + cnt) (cnt <= N) of the chunk's score buffer tS.  Their
+// scores are read and the running max is updated; when it moves by more than 2^8, O, the partial sums and the
+// chunk's groups [gb - gdone, gb) already written as P are rescaled.  Then P = exp2(S sl2 - m) is
+// written over the scores as packed 16-bit pairs: group gi's P takes columns 8 gi .. 8 gi + 7 of
+// the buffer, which held the scores of group gi / 2, read before this write (or outside the run).
+template <int D, int N, bool F16>
+__device__ __forceinline__ bool fwd_part(const FwdCtx& x, uint32_t g, uint32_t tS, int gb, int cnt, int gdone,
+                                         float& m, uint64_t (&lsum)[4]) {
+    uint32_t v[N][16];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        if (i < cnt) {
+            tmem_ld16(tS + 16u * (gb + i), v[i]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[i][e] = __float_as_uint(-INFINITY);
+        }
+    }
+    tmem_ld_wait_all();
+#pragma unroll
+    for (int i = 0; i < N; ++i) reg_fence16(v[i]);
+    // row max of the part (masked scores carry the -2^100 window bias), four independent chains
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            mx[e] = fmax3(mx[e], fmaxf(__uint_as_float(v[i][4 * e]), __uint_as_float(v[i][4 * e + 1])),
+                          fmaxf(__uint_as_float(v[i][4 * e + 2]), __uint_as_float(v[i][4 * e + 3])));
+    const float cmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     // running max (log2 units; the scale's sign is folded into the S product)
     const float cm2 = cmax > masked_below<F16>() ? cmax * x.sl2 : -INFINITY;  // no live key: -inf
     const float mnew = fmaxf(m, cm2);
     const bool rescale = (m != -INFINITY) && (mnew > m + kRescaleThreshold);
     const float alpha = rescale ? fast_exp2(m - mnew) : 1.f;
     if (m == -INFINITY || rescale) m = mnew;
-    if (N > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds the products of chunks g-1, g-2, ...: wait for the last one
-        if (!warp_wait(&x.bars[kPEmpty + (g - 1) % kPB], ((g - 1) / kPB) & 1, x.err, kSitePV)) return false;
+    if (__any_sync(0xffffffffu, rescale)) {
+        // O holds the products of chunks g-1, g-2, ...: wait for the last one (before a tile's first
+        // chunk that is the previous tile's, harmless; for g = 0 the parity test passes at once)
+        if (!warp_wait(&x.bars[kPEmpty + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, x.err, kSitePV)) return false;
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D; cc += 8) {
@@ -1050,25 +1070,29 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
             for (int e = 0; e < 8; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st8(x.tO + cc, r);
         }
+        if (gdone > 0) tmem_st_wait();  // the P groups of this chunk's first part are written
+        for (int gi = gb - gdone; gi < gb; ++gi) {
+            uint32_t r[8];
+            tmem_ld8(tS + 8u * gi, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float lo, hi;
+                unpack2<F16>(r[e], lo, hi);
+                r[e] = pack2<F16>(lo * alpha, hi * alpha);
+            }
+            tmem_st8(tS + 8u * gi, r);
+        }
         tmem_st_wait();
         const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
         for (int t = 0; t < 4; ++t) lsum[t] = f2_mul(lsum[t], a2);
     }
-    const uint32_t run = N > 0 ? run_mask(glo, N) : 0u, stale = nz & ~run;
-    nz = run;
-    if (N == 0 && stale == 0) {  // nothing to write: this warp's rows of the buffer are already zero
-        __syncwarp();
-        if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
-        return true;
-    }
-    // P buffer pb is free once the product of chunk g - kPB is done
-    if (g >= kPB && !warp_wait(&x.bars[kPEmpty + pb], ((g / kPB) - 1) & 1, x.err, kSitePV)) return false;
-    const uint32_t sP = x.sP0 + pb * x.sP_step;
     const float nm = m == -INFINITY ? 0.f : -m;  // masked scores are -inf: exp2 gives 0
     const uint64_t nm2 = f2(nm, nm);
 #pragma unroll
     for (int i = 0; i < N; ++i) {
+        if (i >= cnt) break;
         uint32_t w[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
@@ -1079,13 +1103,41 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
             lsum[(e >> 1) & 3] = f2_add(lsum[(e >> 1) & 3], pe);
             w[e >> 1] = x2_of<F16>(pe);
         }
-        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i)), w[0], w[1], w[2], w[3]);
-        st_shared_v4(sP + p_off(x.rowbase, x.sw, 2 * (glo + i) + 1), w[4], w[5], w[6], w[7]);
+        tmem_st8(tS + 8u * (gb + i), w);
     }
-    for (uint32_t z = stale; z; z &= z - 1) zero_group(sP, x.rowbase, x.sw, __ffs(z) - 1);
-    fence_proxy_async_smem();
+    return true;
+}
+
+// One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + n) (n <= 6):
+// runs of up to four groups in one part, longer runs in two parts of at most three (register
+// budget).  Groups outside the run hold scores, not P, so they are zeroed once every score of the
+// run has been read; then the P operand (score buffer g & 1) is released to the MMA warp.
+template <int D, bool F16>
+__device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, int n, float& m,
+                                          uint64_t (&lsum)[4]) {
+    const uint32_t tS = x.tS0 + (g & 1u) * x.tS_step;
+    bool ok = true;
+    switch (n) {
+        case 0: break;
+        case 1: ok = fwd_part<D, 1, F16>(x, g, tS, glo, 1, 0, m, lsum); break;
+        case 2: ok = fwd_part<D, 2, F16>(x, g, tS, glo, 2, 0, m, lsum); break;
+        case 3: ok = fwd_part<D, 3, F16>(x, g, tS, glo, 3, 0, m, lsum); break;
+        case 4: ok = fwd_part<D, 4, F16>(x, g, tS, glo, 4, 0, m, lsum); break;
+        default:
+            // groups [glo, glo + 3), then [glo + 3, glo + n); one loop body keeps register use at
+            // that of a single part
+#pragma unroll 1
+            for (int part = 0; part < 2 && ok; ++part)
+                ok = fwd_part<D, 3, F16>(x, g, tS, glo + 3 * part, part == 0 ? 3 : n - 3, 3 * part, m, lsum);
+            break;
+    }
+    if (!ok) return false;
+    for (int gi = 0; gi < x.ngroups; ++gi)
+        if (gi < glo || gi >= glo + n) tmem_st8_zero(tS + 8u * gi);
+    tmem_st_wait();
+    tc_fence_before();
     __syncwarp();
-    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + pb]);
+    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + (g & 1u)]);
     return true;
 }
 
@@ -1121,15 +1173,10 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.err = p.err;
     x.tS0 = tmem + tm_s(pl, 0) + lane_base;
     x.tS_step = tm_s(pl, 1) - tm_s(pl, 0);
-    x.sP0 = smem_u32(smem + lay.p(0, 0));
-    x.sP_step = lay.p(1, 0) - lay.p(0, 0);
-    x.rowbase = static_cast<uint32_t>(row) * 64u;
-    x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
     x.ngroups = pl.NC >> 4;
     x.sl2 = p.scale_log2;
     x.sl2x2 = f2(x.sl2, x.sl2);
     x.lane = lane;
-    uint32_t nz0 = run_mask(0, x.ngroups), nz1 = nz0, nz2 = nz0;  // groups of the P buffers that may be nonzero
     FwdEpilogue ep{false, false, 0.f, 0.f, 0, 0, 0};
     TileIter it = tile_iter_begin(p);
     bool started = false;
@@ -1150,16 +1197,7 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             tc_fence_after();
             int glo, n;
             chunk_range(pl, cur, wu, glo, n);
-            const uint32_t pb = g % pbufs_of(0);
-            uint32_t nz = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
-            switch (n) {
-                case 0: ok = fwd_chunk<D, 0, F16>(x, g, glo, m, lsum, nz); break;
-                case 1: ok = fwd_chunk<D, 1, F16>(x, g, glo, m, lsum, nz); break;
-                case 2: ok = fwd_chunk<D, 2, F16>(x, g, glo, m, lsum, nz); break;
-                case 3: ok = fwd_chunk<D, 3, F16>(x, g, glo, m, lsum, nz); break;
-                default: ok = fwd_chunk<D, 4, F16>(x, g, glo, m, lsum, nz); break;
-            }
-            if (pb == 0) nz0 = nz; else if (pb == 1) nz1 = nz; else nz2 = nz;
+            ok = fwd_chunk<D, F16>(x, g, glo, n, m, lsum);
             if (!ok) break;
         }
         if (!ok) break;

@@ -59,7 +59,7 @@ def replay(which, L, k, d, plan):
         if H[a] > 1:
             assert G[a] <= 32, "window-bias operand: at most two 16-column groups per axis"
     if which == 0:
-        assert NC <= 64, "the forward holds at most 4 groups of scores in registers"
+        assert NC <= 96, "the forward's softmax takes runs of at most six groups"
     Lcm = [-(-L[a] // d[a]) for a in range(3)]
     ntile = [-(-Lcm[a] // T[a]) for a in range(3)]
     nchk = [-(-H[a] // G[a]) for a in range(3)]
