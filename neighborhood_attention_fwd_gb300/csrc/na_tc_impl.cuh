@@ -50,9 +50,10 @@ constexpr int kMaxStages = 4;
 
 // Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
 // the copy latency.  dQ has the shared memory for a fourth chunk stage and a third P buffer (more
-// slack between unevenly loaded softmax warps).  The forward (two CTAs per SM) does not, and dK/dV
-// (two P operands) measured slower with a fourth stage: its per-column LSE/Delta gathers go
-// through L1, which shrinks as shared memory grows.
+// slack between unevenly loaded softmax warps).  The forward's two P operands are its two TMEM
+// score buffers (P is written over the scores), and dK/dV (two P operands in shared memory)
+// measured slower with a fourth stage: its per-column LSE/Delta gathers go through L1, which
+// shrinks as shared memory grows.
 __host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
 constexpr int kMaxPBufs = 3;
@@ -791,8 +792,9 @@ struct PendingUpdate {
 };
 
 // The MMA lane runs two streams: the score products of the next chunk (as soon as its K/V chunk is
-// loaded and its TMEM score buffer has been read by the softmax warps) and the update products of
-// the oldest scored chunk (as soon as its P operand is written).  Neither waits for the other, so
+// loaded and its TMEM score buffer is free: the forward writes P over the scores, so the buffer is
+// free once the product P V of the chunk two back is done) and the update products of the oldest
+// scored chunk (as soon as its P is written).  Neither waits for the other, so
 // one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
 // after kWaitLimitNs without progress the lane records an error and stops.
 template <int D, int WHICH>
