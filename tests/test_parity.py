@@ -64,6 +64,20 @@ def test_split_backward_matches_fused_entry_point(cuda_lib):
         assert torch.equal(a[key], b[key]), key
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_forward_rescales_on_a_wide_score_range(cuda_lib, dtype):
+    """q and k scaled by 3: scores spread over tens of log2 units, so the forward's running max moves
+    by more than its 2^8 threshold across chunks and between the two parts of a long run (2D 33x45
+    with a 9x9 window has runs of five 16-column groups), and O, and P already written, are rescaled.
+    Forward only: the rescales are the forward's."""
+    w = nain.small_workload(dtype, (33, 45), 2, 32, (9, 9), (1, 1), B=1, seed=21)
+    t = nain.make_inputs(w, device="cpu")
+    for key in ("q", "k"):
+        t[key] = (t[key].float() * 3.0).to(t[key].dtype)
+    gpu = run_gpu(w, {k: v.cuda() for k, v in t.items()}, want_bwd=False)
+    check_full(w, gpu, host(t), want_bwd=False)
+
+
 def test_backward_is_deterministic(cuda_lib):
     w = nain.small_workload("bf16", (40, 40), 2, 32, (9, 9), (1, 1), B=1, seed=4)
     t = {k: v.cuda() for k, v in nain.make_inputs(w, device="cpu").items()}
