@@ -1375,12 +1375,15 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             const uint32_t stale = nzq & ~run & (wg ? 0xaaaaaaaau : 0x55555555u);
             if (pb == 0) nz0 = run; else if (pb == 1) nz1 = run; else nz2 = run;
             if (mine == 0 && stale == 0) {
+                // nothing to write: the score buffer is released at once, but the arrival on the P
+                // operand waits for the products of chunk g - kPB, like every other arrival.  With two
+                // P buffers (dK/dV) an idle warp can otherwise reach chunk g + 2 while a slower warp
+                // still writes chunk g, and its arrival would complete chunk g's phase early.
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars[kSEmpty + sb]);
-                    mbar_arrive(&bars[kPFull + pb]);
-                }
+                if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
+                if (g >= kPB && !(ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV))) break;
+                if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
                 continue;
             }
             if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
