@@ -177,7 +177,8 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
  * Unfused operations.  NATTEN issue #161 ("Backward pass is very slow towards much tokens and large
  * kernels") times the chain na2d_qk -> softmax -> na2d_av beside the fused op, and the maintainer's
  * profile there lists its kernels (attention logits, AV, their gradients QGRAD, KGRAD, AGRAD, VGRAD,
- * softmax forward and backward).  These entry points compute that chain on CUDA cores.
+ * softmax forward and backward).  These entry points compute that chain: the bf16 and fp16 products
+ * on warp-level tensor-core MMAs, the fp32 products and the softmax on CUDA cores.
  *
  * Attention weights attn: [B, L.., heads, K] in the dtype of q, K = kernel[0] * ... * kernel[ndim-1];
  * the weight of window offset (t_0, .., t_{n-1}) (t_a < kernel[a], first axis outermost) sits at
