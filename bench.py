@@ -197,45 +197,71 @@ class ClockSampler:
 # Oracle (CPU baseline / reference arm)
 # ---------------------------------------------------------------------------------------------
 
-def oracle_sample(w, h, n_rows, seed=0):
-    """Time the oracle on a bounded sample: forward of n_rows query rows, dQ of n_rows rows and
-    dK/dV of n_rows rows.  Returns (seconds, useful FLOPs of the sample)."""
+# One sample size for both oracle legs (the GPU arm's cpu_baseline and --impl reference): the
+# oracle's dK/dV rows recompute the forward of every query in their inverse window, and those sets
+# overlap more as a sample gets denser, so its cost per row depends on the sample's density.
+CPU_SAMPLE_ROWS = 32768
+
+
+def oracle_sample(w, h, n_rows, seed=0, nthreads=None):
+    """Time the oracle on a bounded sample: forward of n_rows random query rows, dQ of the same rows
+    and dK/dV of the same n_rows key rows.  Returns (seconds, useful FLOPs of the sample, rows)."""
     import oracle
 
     rng = np.random.default_rng(seed)
     total = w.tokens * w.heads
     rows = np.sort(rng.choice(total, size=min(n_rows, total), replace=False)).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.na_fwd(h["q"], h["k"], h["v"], w.kernel, w.dilation, w.scale, rows=rows)
-    oracle.na_bwd(h["q"], h["k"], h["v"], h["dO"], w.kernel, w.dilation, w.scale, qrows=rows, krows=rows)
+    oracle.na_fwd(h["q"], h["k"], h["v"], w.kernel, w.dilation, w.scale, rows=rows, nthreads=nthreads)
+    oracle.na_bwd(h["q"], h["k"], h["v"], h["dO"], w.kernel, w.dilation, w.scale, qrows=rows, krows=rows,
+                  nthreads=nthreads)
     dt = time.perf_counter() - t0
     f_fwd, f_bwd = useful_flops(w)
     frac = len(rows) / float(total)
     return dt, (f_fwd + f_bwd) * frac, len(rows)
 
 
-def calibrate_oracle(w, h, target_s):
-    n = 64
-    dt, _, n = oracle_sample(w, h, n)
-    while dt < 0.5 and n < w.tokens * w.heads:
-        n *= 4
-        dt, _, n = oracle_sample(w, h, n)
-    return max(16, min(int(n * target_s / max(dt, 1e-6)), w.tokens * w.heads))
-
-
 def host_inputs(t):
     return {k: nain.to_oracle_array(v) for k, v in t.items()}
 
 
+def single_thread_forward(w, h, sample_rows=8192):
+    """One-thread oracle forward times: the small fp32 workload in full, and the given workload
+    extrapolated from a random sample of its query rows (ms for the whole forward)."""
+    import oracle
+
+    c1 = nain.WORKLOADS["2d_fp32_16x16_k5"]
+    hc = host_inputs(nain.make_inputs(c1, device="cpu"))
+    t0 = time.perf_counter()
+    oracle.na_fwd(hc["q"], hc["k"], hc["v"], c1.kernel, c1.dilation, c1.scale, nthreads=1)
+    c1_ms = (time.perf_counter() - t0) * 1e3
+    total = w.tokens * w.heads
+    rows = np.sort(np.random.default_rng(7).choice(total, size=min(sample_rows, total), replace=False))
+    t0 = time.perf_counter()
+    oracle.na_fwd(h["q"], h["k"], h["v"], w.kernel, w.dilation, w.scale, rows=rows.astype(np.int64), nthreads=1)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    return {f"{c1.name}_fwd_ms": c1_ms, f"{w.name}_fwd_ms_estimated": per_row * total * 1e3,
+            "sample_rows": int(len(rows)), "threads": 1}
+
+
 def cpu_baseline(w, t, target_s=15.0):
+    """The oracle on the host cores: repeated samples of CPU_SAMPLE_ROWS rows (after one untimed
+    sample) until about target_s seconds, plus the one-thread forward times."""
     import oracle
 
     h = host_inputs(t)
-    n = calibrate_oracle(w, h, target_s)
-    dt, flops, n = oracle_sample(w, h, n, seed=1)
-    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle forward of {n} random query rows and backward (dQ of the same {n} rows, "
-                      f"dK/dV of {n} key rows) of {w.name}; useful FLOPs of the sample / wall time"}
+    oracle_sample(w, h, CPU_SAMPLE_ROWS, seed=99)
+    dts, flops, seed = [], [], 1
+    while not dts or (sum(dts) < target_s and len(dts) < 50):
+        dt, fl, n = oracle_sample(w, h, CPU_SAMPLE_ROWS, seed=seed)
+        dts.append(dt)
+        flops.append(fl)
+        seed += 1
+    return {"value": sum(flops) / sum(dts) / 1e12, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(dts)} samples, each the fp64 oracle forward of {n} random query rows and backward "
+                      f"(dQ of the same rows, dK/dV of {n} key rows) of {w.name}; useful FLOPs of the samples / "
+                      f"their wall time",
+            "single_thread": single_thread_forward(w, h)}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -454,21 +480,19 @@ def run_unfused(args, w, rank, world, dist):
     return line, t
 
 
-def run_ours(args, w, rank, world, dist):
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
+def time_fused(w, t, steps, warmup, dev, dist):
+    """Time `steps` fused fwd + bwd steps of workload w on resident inputs t (after `warmup` untimed
+    steps), with per-kernel CUDA events on the launching stream and clocks sampled meanwhile.
+    Inputs smaller than twice L2 get a 256 MB flush write between steps, outside the events."""
     import neighborhood_attention_fwd_gb300 as na
 
-    na.load()
-    t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
     step = Step(w, t)
     tensor_bytes = t["q"].numel() * t["q"].element_size()
     flush = None
     if tensor_bytes < 2 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
     names = ["fwd0", "fwd1", "delta1", "dq1", "dkdv1"]
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step.launch()
         if flush is not None:
             flush.fill_(1.0)
@@ -476,7 +500,7 @@ def run_ours(args, w, rank, world, dist):
     if st != 0:
         raise RuntimeError(f"device status {st} ({raw:#x}) after warm-up")
 
-    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(args.steps)]
+    evs = [{n: torch.cuda.Event(enable_timing=True) for n in names} for _ in range(steps)]
     clocks = ClockSampler(dev.index)
     clocks.start()
     time.sleep(0.3)
@@ -484,7 +508,7 @@ def run_ours(args, w, rank, world, dist):
         dist.barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         step.launch(evs[i])
         if flush is not None:
             flush.fill_(float(i))
@@ -505,13 +529,15 @@ def run_ours(args, w, rank, world, dist):
         per["dkdv"].append(e["dq1"].elapsed_time(e["dkdv1"]))
         per["step"].append(e["fwd0"].elapsed_time(e["dkdv1"]))
     ms = {k: float(np.mean(v)) for k, v in per.items()}
-    ms_step = ranks_max(ms["step"], dist, dev)
+    return step, ms, clk, wall, flush is not None
 
-    f_fwd, f_bwd = useful_flops(w)
-    value = job_value(world, f_fwd + f_bwd, ms_step)
 
-    # --- roofline: per kernel, the slower of tile-level MMA FLOPs at the bf16 peak and the
-    # algorithmic bytes at HBM bandwidth
+def fused_roofline(w, ms, clk):
+    """Per-kernel roofline (the slower of tile-level MMA FLOPs at the bf16 peak and the algorithmic
+    bytes at HBM bandwidth; the fp32 path against the fp32 FMA peak) and the step's roofline at
+    tile-level and at useful FLOPs."""
+    import neighborhood_attention_fwd_gb300 as na
+
     peaks = load_peaks()
     hbm = peaks["hbm_gbs"] * 1e9
     ten = peaks["bf16_tflops"] * 1e12
@@ -543,12 +569,61 @@ def run_ours(args, w, rank, world, dist):
         kernels[name] = {"ms": ms[name], "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
                          "frac": ach / peak, "roof_ms": max(t_b, t_f) * 1e3, "tile_flops": tile_flops[name],
                          "alg_bytes": kb[name]}
-    dom = max(("fwd", "delta", "dq", "dkdv"), key=lambda k: ms[k])
-    traffic = load_traffic(w.name, dom)
-    roof_step = sum(kernels[k]["roof_ms"] for k in kernels)
+    f_fwd, f_bwd = useful_flops(w)
     m_fwd, m_bwd = method_bytes(w)
     fpeak = alu_tflops * 1e12 if fma else ten
     useful_roof_ms = (max(f_fwd / fpeak, m_fwd / hbm) + max(f_bwd / fpeak, m_bwd / hbm)) * 1e3
+    roof_step = sum(kernels[k]["roof_ms"] for k in kernels)
+    return kernels, roof_step, useful_roof_ms, peaks, alu_tflops
+
+
+# The other bf16 workloads timed beside the headline in the default run (fewer steps each).
+EXTRA_CONFIGS = ("3d_bf16_16x256x256_k3x5x5", "3d_bf16_b2_8x128x128_k5x7x7", "2d_bf16_2048x2048_k13_d2")
+
+
+def run_extra_configs(args, dev):
+    """Time each workload of EXTRA_CONFIGS with its own inputs (the headline's freed first):
+    per-kernel and per-phase ms, useful TFLOP/s, and the step against its tile-level and useful-FLOP
+    rooflines, with the clocks sampled during each timed region."""
+    out = {}
+    for name in EXTRA_CONFIGS:
+        w = nain.WORKLOADS[name]
+        t = nain.make_inputs(w, device=dev)
+        _, ms, clk, _, flushed = time_fused(w, t, args.config_steps, 3, dev, None)
+        kernels, roof_step, useful_roof_ms, _, _ = fused_roofline(w, ms, clk)
+        f_fwd, f_bwd = useful_flops(w)
+        out[name] = {
+            "ms": {"fwd": ms["fwd"], "bwd": ms["delta"] + ms["dq"] + ms["dkdv"], "fwd_bwd": ms["step"],
+                   "per_kernel": {k: ms[k] for k in ("fwd", "delta", "dq", "dkdv")}},
+            "value": (f_fwd + f_bwd) / (ms["step"] * 1e-3) / 1e12, "unit": UNIT,
+            "tile_roof_ms": roof_step, "frac_tile": roof_step / ms["step"],
+            "useful_roof_ms": useful_roof_ms, "frac_useful": useful_roof_ms / ms["step"],
+            "kernel_frac": {k: kernels[k]["frac"] for k in kernels},
+            "steps": args.config_steps, "warmup": 3,
+            "l2": "L2 flushed between steps (256 MB write)" if flushed else "inputs larger than L2",
+            "clocks": clk,
+        }
+        del t
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, w, rank, world, dist):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    import neighborhood_attention_fwd_gb300 as na
+
+    na.load()
+    t = nain.make_inputs(w, device=dev, seed=w.seed + rank)
+    step, ms, clk, wall, flushed = time_fused(w, t, args.steps, args.warmup, dev, dist)
+    ms_step = ranks_max(ms["step"], dist, dev)
+
+    f_fwd, f_bwd = useful_flops(w)
+    value = job_value(world, f_fwd + f_bwd, ms_step)
+
+    kernels, roof_step, useful_roof_ms, peaks, alu_tflops = fused_roofline(w, ms, clk)
+    dom = max(("fwd", "delta", "dq", "dkdv"), key=lambda k: ms[k])
+    traffic = load_traffic(w.name, dom)
 
     # --- end to end through the public API with host buffers
     e2e = run_e2e(args, w, t, step) if not args.no_e2e else None
@@ -561,7 +636,7 @@ def run_ours(args, w, rank, world, dist):
                 else "synthetic (seeded N(0,1) inputs and dO)",
         "config": {"workload": w.name, "B": w.B, "spatial": list(w.spatial), "heads": w.heads, "D": w.D,
                    "kernel": list(w.kernel), "dilation": list(w.dilation), "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2" if flush is None else "L2 flushed between steps (256 MB write)"},
+                   "l2": "L2 flushed between steps (256 MB write)" if flushed else "inputs larger than L2"},
         "ms": {"fwd": ms["fwd"], "bwd": ms["delta"] + ms["dq"] + ms["dkdv"], "fwd_bwd": ms_step,
                "per_kernel": {k: ms[k] for k in ("fwd", "delta", "dq", "dkdv")}},
         "tflops": {"fwd": f_fwd / (ms["fwd"] * 1e-3) / 1e12,
@@ -690,7 +765,7 @@ def run_reference(args, w, rank):
 
     t = nain.make_inputs(w, device="cpu")
     h = host_inputs(t)
-    n = calibrate_oracle(w, h, target_s=2.0)
+    n = CPU_SAMPLE_ROWS
     for i in range(args.warmup):
         oracle_sample(w, h, n, seed=100 + i)
     times, flops = [], []
@@ -725,6 +800,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other bf16 workloads timed beside the headline (the 'configs' key)")
+    ap.add_argument("--config-steps", type=int, default=10, help="timed steps of each extra workload")
     ap.add_argument("--path", choices=["fused", "unfused"], default="fused",
                     help="the fused kernels (default) or the unfused chain of separate operations")
     ap.add_argument("--rpb", action="store_true",
@@ -763,6 +841,12 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w, t, args.cpu_seconds)
+        # the other workloads, one GPU only: the headline's buffers are freed first
+        if (args.path == "fused" and world == 1 and not args.no_configs and args.dtype is None
+                and args.workload == nain.HEADLINE):
+            del t
+            torch.cuda.empty_cache()
+            line["configs"] = run_extra_configs(args, torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0))))
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
