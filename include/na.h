@@ -64,7 +64,10 @@ typedef enum {
  *   (every residue class holds at least k positions); scale finite (the workloads use D^-0.5).
  *   Every tensor pointer 16-byte aligned.
  * Supported (else NA_ERR_UNSUPPORTED):
- *   NA_BF16, NA_FP16: D in {16, 32, 64}; dilation[a] <= 8; per-axis halos within the TMA box limit.
+ *   NA_BF16, NA_FP16: D in {16, 32, 64}; dilation[a] <= 8 (the tensor-core kernels load a dilated
+ *   tile as one TMA box whose element stride is the dilation, and a TMA element stride is at most
+ *   8); a tile plan must exist whose boxes span at most
+ *   256 elements per axis (class positions times the dilation).
  *   NA_FP32: D in {16, 32, 64, 128}.
  */
 na_status na_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -156,6 +159,10 @@ na_status na_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
  * (0x5000 | wait site) for diagnostics.
  */
 na_status na_device_status(void* stream, uint32_t* raw);
+/* The library looks up, once per device, the device addresses of its file-scope arrays (this status
+ * word and na_bwd_noalloc's scratch) and keeps them for the life of the process.  A cudaDeviceReset,
+ * or anything else that destroys and recreates the device's primary context, invalidates those
+ * addresses: do not call the library on a device after resetting it. */
 
 /* Static description of a status code. */
 const char* na_strerror(na_status status);
