@@ -260,7 +260,11 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
             }
             if (skip) continue;
             int Hx[3];
-            for (int a = 0; a < 3; ++a) Hx[a] = max_halo(which, T[a], g.L[a], g.k[a], g.d[a]);
+            for (int a = 0; a < 3; ++a) {
+                Hx[a] = max_halo(which, T[a], g.L[a], g.k[a], g.d[a]);
+                if (Hx[a] >= (1 << 25)) skip = true;  // the kernels' chunk-count reciprocal is exact below 2^26
+            }
+            if (skip) continue;
             double tiles = 1;
             for (int a = 0; a < 3; ++a) tiles *= ceil_div(Lcm[a], T[a]);
             const int gmax0 = Hx[0] > 1 ? std::min(Hx[0], 32) : 1, gmax1 = Hx[1] > 1 ? std::min(Hx[1], 32) : 1;
@@ -363,6 +367,10 @@ na_status tc_common(int which, const Geom& g, float scale, na::TcParams& p) {
     // tiny positive one (uniform weights up to ~1e-28 relative) so that masked scores stay -inf
     p.neg = scale < 0.f ? 1u : 0u;
     p.scale_log2 = std::max(std::fabs(scale), 1e-30f) * 1.44269504088896340736f;
+    for (int a = 0; a < 3; ++a) {
+        for (int c = 0; c < 8; ++c) p.Lc_tab[a][c] = c < g.d[a] ? (g.L[a] - c + g.d[a] - 1) / g.d[a] : 0;
+        p.rcpG[a] = p.plan.G[a] == 1 ? 0u : static_cast<uint32_t>((1ull << 32) / static_cast<uint64_t>(p.plan.G[a]) + 1u);
+    }
     const int rad[8] = {g.heads, p.plan.ntile[2], p.plan.ntile[1], p.plan.ntile[0], g.d[2], g.d[1], g.d[0], g.B};
     for (int i = 0; i < 8; ++i) p.rad[i] = static_cast<uint32_t>(rad[i]);
     return status_ptr(&p.err);

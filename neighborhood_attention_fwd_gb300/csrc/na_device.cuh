@@ -90,6 +90,9 @@ constexpr uint32_t kSuspendNs = 100000;  // 0.1 ms per sleep; the status word is
 // Wait for the phase with the given parity to complete.  Gives up (returns false, records the
 // site in the status word) after kWaitLimitNs, or as soon as another CTA has recorded an error.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
+    // a phase that is already complete costs one test (~15 cycles; a try_wait with a suspend hint
+    // costs ~50 even then)
+    if (mbar_test(bar, parity)) return true;
     if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
     const unsigned long long t0 = globaltimer();
     for (;;) {

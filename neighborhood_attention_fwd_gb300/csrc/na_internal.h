@@ -55,6 +55,10 @@ struct TcParams {
     const float* lse;   // bwd: forward LSE
     const float* delta; // bwd: Delta = <dO, O>
     unsigned* err;      // device status word
+    // Per-tile decode without integer division (a 32-bit division by a runtime value costs the
+    // softmax warps hundreds of cycles at every tile boundary):
+    int Lc_tab[3][8];   // class length ceil((L - c) / d) per axis and residue class c < d (d <= 8)
+    uint32_t rcpG[3];   // floor(2^32 / G[a]) + 1 (0 for G[a] == 1): umulhi(x, rcpG[a]) == x / G[a] for x < 2^26
 };
 
 // Parameters of the CUDA-core kernels (fp32 path and the Delta prologue).

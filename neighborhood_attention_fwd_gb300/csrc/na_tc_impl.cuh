@@ -219,7 +219,7 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, int which, const 
     bool any = true;
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
-        c.Lc[a] = class_len(p.L[a], p.d[a], c.cls[a]);
+        c.Lc[a] = p.Lc_tab[a][c.cls[a]];
         c.t0[a] = t[a] * pl.T[a];
         if (c.t0[a] >= c.Lc[a]) any = false;
     }
@@ -237,7 +237,9 @@ __device__ __forceinline__ bool decode_tile(const TcParams& p, int which, const 
             hi = inv_hi(last, c.Lc[a], p.k[a]);
         }
         c.h0[a] = min(lo, max(0, c.Lc[a] - pl.H[a]));
-        c.nc[a] = min(pl.nchk[a], (hi - c.h0[a] + pl.G[a]) / pl.G[a]);
+        // chunks from the halo start to the last needed position: (hi - h0) / G + 1
+        const uint32_t x = static_cast<uint32_t>(hi - c.h0[a] + pl.G[a]);
+        c.nc[a] = min(pl.nchk[a], static_cast<int>(pl.G[a] == 1 ? x : __umulhi(x, p.rcpG[a])));
         c.C *= c.nc[a];
     }
     return true;
@@ -397,7 +399,9 @@ __device__ __forceinline__ void st_row32(uint32_t blk, int r, uint32_t bits, uin
                  bf16_pair(bits, 7, v));
 }
 
+// Whole-warp wait.  The common case, a phase that is already complete, takes one test and one vote.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
+    if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
     const bool ok = mbar_wait(bar, parity, err, site);
     return __all_sync(0xffffffffu, ok);
 }
