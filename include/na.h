@@ -164,6 +164,19 @@ na_status na_device_status(void* stream, uint32_t* raw);
  * or anything else that destroys and recreates the device's primary context, invalidates those
  * addresses: do not call the library on a device after resetting it. */
 
+/*
+ * Test hook for the bounded device-side waits (the pages have no counterpart; it exists so that the
+ * timeout path can be exercised without faulting a GPU).  For every later launch of the tensor-core
+ * kernels (NA_BF16, NA_FP16) in this process it sets the time limit of one wait to limit_ns
+ * (100 us .. 10 s; 0 restores the 2 s default) and, with withhold = 1, makes the first CTA skip the
+ * copy of its first halo chunk, so that the waits on that chunk run out.  Such a call leaves its
+ * outputs incomplete and na_device_status() then reports NA_ERR_TIMEOUT; the kernels stop issuing
+ * work, let the copies already issued land, free their tensor memory and return.  Call it again with
+ * (0, 0) to restore normal launches.  Process-wide; for tests only.
+ * Errors: NA_ERR_INVALID_ARG for a limit outside the range or withhold not 0 or 1.
+ */
+na_status na_debug_wait_hook(unsigned long long limit_ns, int withhold);
+
 /* Static description of a status code. */
 const char* na_strerror(na_status status);
 

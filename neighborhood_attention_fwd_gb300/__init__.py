@@ -23,7 +23,7 @@ __all__ = [
     "NAError", "load", "na_fwd", "na_bwd", "na_bwd_delta", "na_bwd_dq", "na_bwd_dkdv",
     "na_bwd_workspace_size", "na_device_status", "na_strerror", "na_plan_info", "library_path",
     "na_qk", "na_av", "na_softmax", "na_softmax_bwd", "na_qk_bwd", "na_av_bwd", "na_rpb_grad",
-    "na_rpb_grad_workspace_size", "na_mask_window",
+    "na_rpb_grad_workspace_size", "na_mask_window", "na_debug_wait_hook",
 ]
 
 NA_BF16, NA_FP32, NA_FP16 = 0, 1, 2
@@ -65,6 +65,7 @@ def load(path: str | None = None):
     lib.na_bwd_workspace_size.argtypes = [I, I, IP, I]
     lib.na_bwd_workspace_size.restype = ctypes.c_size_t
     lib.na_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.na_debug_wait_hook.argtypes = [ctypes.c_ulonglong, I]
     lib.na_strerror.argtypes = [I]
     lib.na_strerror.restype = ctypes.c_char_p
     lib.na_plan_info.argtypes = [I, I, I, IP, I, I, IP, IP, ctypes.POINTER(ctypes.c_int64)]
@@ -220,6 +221,12 @@ def na_device_status(stream=None):
     raw = ctypes.c_uint32(0)
     st = load().na_device_status(_stream(stream), ctypes.byref(raw))
     return int(st), int(raw.value)
+
+
+def na_debug_wait_hook(limit_ns: int = 0, withhold: bool = False) -> None:
+    """Test hook: the wait limit of later tensor-core launches (0: the 2 s default) and, with
+    withhold, the first CTA's first halo chunk left unfilled so that a wait runs out."""
+    _ok(load().na_debug_wait_hook(int(limit_ns), 1 if withhold else 0), "na_debug_wait_hook")
 
 
 PLAN_FIELDS = ("T1", "T2", "T3", "H1", "H2", "H3", "G1", "G2", "G3", "NC", "chunks_max", "ctas", "mma_flops",

@@ -7,11 +7,13 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
 
 #include "../../include/na.h"
+#include "na_device.cuh"
 #include "na_internal.h"
 
 namespace na {
@@ -65,6 +67,10 @@ na_status status_ptr(unsigned** out) {
     *out = g_status_ptr[dev];
     return NA_OK;
 }
+
+// Wait limit and test hook of the tensor-core kernels' launches (na_debug_wait_hook).
+std::atomic<unsigned long long> g_wait_ns{na::dev::kWaitLimitNs};
+std::atomic<uint32_t> g_withhold{0};
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -367,6 +373,8 @@ na_status tc_common(int which, const Geom& g, float scale, na::TcParams& p) {
     // tiny positive one (uniform weights up to ~1e-28 relative) so that masked scores stay -inf
     p.neg = scale < 0.f ? 1u : 0u;
     p.scale_log2 = std::max(std::fabs(scale), 1e-30f) * 1.44269504088896340736f;
+    p.wait_ns = g_wait_ns.load();
+    p.withhold = g_withhold.load();
     for (int a = 0; a < 3; ++a) {
         for (int c = 0; c < 8; ++c) p.Lc_tab[a][c] = c < g.d[a] ? (g.L[a] - c + g.d[a] - 1) / g.d[a] : 0;
         p.rcpG[a] = p.plan.G[a] == 1 ? 0u : static_cast<uint32_t>((1ull << 32) / static_cast<uint64_t>(p.plan.G[a]) + 1u);
@@ -651,6 +659,14 @@ na_status na_device_status(void* stream, uint32_t* raw) {
     }
     if (raw) *raw = word;
     return word ? NA_ERR_TIMEOUT : NA_OK;
+}
+
+na_status na_debug_wait_hook(unsigned long long limit_ns, int withhold) {
+    if (withhold != 0 && withhold != 1) return NA_ERR_INVALID_ARG;
+    if (limit_ns != 0 && (limit_ns < 100000ull || limit_ns > 10000000000ull)) return NA_ERR_INVALID_ARG;
+    g_wait_ns.store(limit_ns == 0 ? na::dev::kWaitLimitNs : limit_ns);
+    g_withhold.store(static_cast<uint32_t>(withhold));
+    return NA_OK;
 }
 
 const char* na_strerror(na_status s) {

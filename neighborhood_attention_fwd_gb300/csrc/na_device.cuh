@@ -19,7 +19,13 @@ enum WaitSite : unsigned {
     kSiteQ = 1, kSiteKV = 2, kSiteS = 3, kSiteP = 4, kSitePV = 5, kSiteEmpty = 6, kSiteFinal = 7, kSiteSt = 8,
 };
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // default limit of one wait: 2 s
+
+// Where a bounded wait reports and how long it may take (the launch's limit, normally kWaitLimitNs).
+struct WaitGuard {
+    unsigned* word;               // device status word
+    unsigned long long limit_ns;  // time limit of one wait
+};
 
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
@@ -87,9 +93,19 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 constexpr uint32_t kSuspendNs = 100000;  // 0.1 ms per sleep; the status word is polled between sleeps
 
+// Wait for the phase with the given parity without recording anything: false after limit_ns.  Used
+// on the way out, to let copies already issued land before the CTA's shared memory is released.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity, 1000u))
+        if (globaltimer() - t0 > limit_ns) return false;
+    return true;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns false, records the
-// site in the status word) after kWaitLimitNs, or as soon as another CTA has recorded an error.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
+// site in the status word) after the guard's limit, or as soon as another CTA has recorded an error.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
     // a phase that is already complete costs one test (~15 cycles; a try_wait with a suspend hint
     // costs ~50 even then)
     if (mbar_test(bar, parity)) return true;
@@ -97,9 +113,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     const unsigned long long t0 = globaltimer();
     for (;;) {
         if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
-        if (ld_volatile(err) != 0u) return false;
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            record_error(err, site);
+        if (ld_volatile(err.word) != 0u) return false;
+        if (globaltimer() - t0 > err.limit_ns) {
+            record_error(err.word, site);
             return false;
         }
     }

@@ -55,6 +55,8 @@ struct TcParams {
     const float* lse;   // bwd: forward LSE
     const float* delta; // bwd: Delta = <dO, O>
     unsigned* err;      // device status word
+    unsigned long long wait_ns;  // time limit of one bounded wait (kWaitLimitNs unless a test lowers it)
+    uint32_t withhold;  // test hook: 1 = CTA 0 never fills its first halo chunk, so a wait runs out
     // Per-tile decode without integer division (a 32-bit division by a runtime value costs the
     // softmax warps hundreds of cycles at every tile boundary):
     int Lc_tab[3][8];   // class length ceil((L - c) / d) per axis and residue class c < d (d <= 8)

@@ -400,7 +400,7 @@ __device__ __forceinline__ void st_row32(uint32_t blk, int r, uint32_t bits, uin
 }
 
 // Whole-warp wait.  The common case, a phase that is already complete, takes one test and one vote.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, unsigned* err, unsigned site) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
     if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
     const bool ok = mbar_wait(bar, parity, err, site);
     return __all_sync(0xffffffffu, ok);
@@ -566,7 +566,7 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
     constexpr int ntile = WHICH == 0 ? 1 : 2;
     constexpr int tmCk = WHICH == 0 ? 1 : 2, tmCv = WHICH == 0 ? 2 : 3;
     const int lane = threadIdx.x & 31;
-    unsigned* err = p.err;
+    const WaitGuard err{p.err, p.wait_ns};
     const TilePlan& pl = p.plan;
     const BiasGeom bg = bias_geom(pl);
     const uint32_t tile_bytes = 128u * D * 2u, chunk_bytes = static_cast<uint32_t>(pl.NC) * D * 2u;
@@ -630,7 +630,10 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
             if (g >= kS) ok = warp_wait(&bars[kKVEmpty + s], ((g / kS) - 1) & 1, err, kSiteEmpty);
             if (!ok) break;
             const int y0 = c.h0[0] + cur.o[0], z0 = c.h0[1] + cur.o[1], x0 = c.h0[2] + cur.o[2];
-            if (lane == 0) {
+            // test hook: CTA 0 never fills its first chunk (no copy, no arrival), so the waits on it
+            // run out after the launch's limit
+            const bool withheld = p.withhold != 0u && blockIdx.x == 0 && g == 0;
+            if (lane == 0 && !withheld) {
                 mbar_arrive_expect_tx(&bars[kKVFull + s], 2u * chunk_bytes);
                 tma_load_5d(smem + lay.chunk(s, 0), &p.tm[tmCk], &bars[kKVFull + s], c.h * D,
                             c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
@@ -653,10 +656,25 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
             cursor_next(pl, c, cur);
             if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, cur, f, lane);  // the next chunk's, in flight
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kKVFull + s]);
+            if (lane == 0 && !withheld) mbar_arrive(&bars[kKVFull + s]);
         }
         ++j;
     }
+    // Copies already issued must land before the CTA exits and its shared memory is reused (after an
+    // error the consumers stop early): wait for the last fill of every chunk slot and tile slot.
+    if (lane == 0) {
+        for (uint32_t k = 0; k < static_cast<uint32_t>(kS); ++k) {
+            if (g <= k) continue;
+            const uint32_t last = g - 1 - ((g - 1 - k) % kS);  // the last fill of slot k
+            if (!(p.withhold != 0u && blockIdx.x == 0 && last == 0)) mbar_drain(&bars[kKVFull + k], (last / kS) & 1, err.limit_ns);
+        }
+        for (uint32_t k = 0; k < 2; ++k) {
+            if (j <= k) continue;
+            const uint32_t last = j - 1 - ((j - 1 - k) & 1u);
+            mbar_drain(&bars[kQFull + k], (last >> 1) & 1, err.limit_ns);
+        }
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -800,12 +818,12 @@ struct PendingUpdate {
 // free once the product P V of the chunk two back is done) and the update products of the oldest
 // scored chunk (as soon as its P is written).  Neither waits for the other, so
 // one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
-// after kWaitLimitNs without progress the lane records an error and stops.
+// after the launch's wait limit without progress the lane records an error and stops.
 template <int D, int WHICH>
 __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
     constexpr int kS = stages_of(WHICH, D);
     constexpr uint32_t kPB = pbufs_of(WHICH);
-    unsigned* err = p.err;
+    const WaitGuard err{p.err, p.wait_ns};
     const TilePlan& pl = p.plan;
     const FwdIssuer<D> mi{p, smem, lay, bias_geom(pl)};
     const bool neg = p.neg != 0;
@@ -879,9 +897,9 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
             t_last = globaltimer();
             continue;
         }
-        if (ld_volatile(err) != 0u) break;
-        if (globaltimer() - t_last > kWaitLimitNs) {
-            record_error(err, kSiteP);
+        if (ld_volatile(err.word) != 0u) break;
+        if (globaltimer() - t_last > err.limit_ns) {
+            record_error(err.word, kSiteP);
             break;
         }
         __nanosleep(32);
@@ -892,7 +910,7 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
 template <int D, int WHICH>
 __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
     constexpr uint32_t kS = stages_of(WHICH, D);
-    unsigned* err = p.err;
+    const WaitGuard err{p.err, p.wait_ns};
     const TilePlan& pl = p.plan;
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
@@ -932,7 +950,7 @@ __device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& la
                             int u) {
     constexpr uint32_t kS = stages_of(WHICH, D);
     constexpr uint32_t kPB = pbufs_of(WHICH);
-    unsigned* err = p.err;
+    const WaitGuard err{p.err, p.wait_ns};
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
     TileIter it = tile_iter_begin(p);
@@ -1001,7 +1019,7 @@ __device__ __forceinline__ void zero_group(uint32_t sP, uint32_t rowbase, uint32
 
 struct FwdCtx {
     uint64_t* bars;
-    unsigned* err;
+    WaitGuard err;
     uint32_t tS0, tS_step;  // this warp's lanes of score buffer 0, and the offset of buffer 1
     uint32_t tO;            // this warp's lanes of the tile accumulator
     int ngroups;            // 16-column groups per chunk
@@ -1176,7 +1194,7 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     const TilePlan& pl = p.plan;
     FwdCtx x;
     x.bars = bars;
-    x.err = p.err;
+    x.err = WaitGuard{p.err, p.wait_ns};
     x.tS0 = tmem + tm_s(pl, 0) + lane_base;
     x.tS_step = tm_s(pl, 1) - tm_s(pl, 0);
     x.ngroups = pl.NC >> 4;
@@ -1310,7 +1328,7 @@ struct BwdEpilogue {
 template <int D, int WHICH, bool F16>
 __device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, const BwdEpilogue& e,
                                              uint32_t tmem_lanes, int wg, int lane) {
-    if (!warp_wait(&bars[kOFull + e.ob], (e.j >> 1) & 1, p.err, kSitePV)) return false;
+    if (!warp_wait(&bars[kOFull + e.ob], (e.j >> 1) & 1, WaitGuard{p.err, p.wait_ns}, kSitePV)) return false;
     tc_fence_after();
     const uint32_t acc = tmem_lanes + tm_acc<D>(WHICH, e.ob);
     const int c0 = wg * (D / 2);
@@ -1334,7 +1352,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    unsigned* err = p.err;
+    const WaitGuard err{p.err, p.wait_ns};
     const TilePlan& pl = p.plan;
     const int ngroups = pl.NC >> 4;
     BwdCtx x;
@@ -1502,10 +1520,15 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         bwd_softmax_loop<D, WHICH, F16>(p, smem, lay, bars, tmem);
     }
 
-    // teardown: every MMA of this CTA done before TMEM is freed (each issuing lane commits once)
+    // teardown: every TMEM access of the softmax warps and every MMA of this CTA done before TMEM is
+    // freed (each issuing lane commits once)
+    if (warp < kSoftWarps) {
+        tmem_st_wait();
+        tmem_ld_wait_all();
+    }
     if (warp >= kSoftWarps + 1 && lane == 0) {
         umma_commit(&bars[kFin]);
-        mbar_wait(&bars[kFin], 0, p.err, kSiteFinal);
+        mbar_wait(&bars[kFin], 0, WaitGuard{p.err, p.wait_ns}, kSiteFinal);
     }
     tc_fence_before();
     __syncthreads();
