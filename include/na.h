@@ -64,7 +64,7 @@ typedef enum {
  *   (every residue class holds at least k positions); scale finite (the workloads use D^-0.5).
  *   Every tensor pointer 16-byte aligned.
  * Supported (else NA_ERR_UNSUPPORTED):
- *   NA_BF16, NA_FP16: D in {16, 32, 64}; dilation[a] <= 8 (the tensor-core kernels load a dilated
+ *   NA_BF16, NA_FP16: D in {16, 32, 64, 128}; dilation[a] <= 8 (the tensor-core kernels load a dilated
  *   tile as one TMA box whose element stride is the dilation, and a TMA element stride is at most
  *   8); a tile plan must exist whose boxes span at most
  *   256 elements per axis (class positions times the dilation).

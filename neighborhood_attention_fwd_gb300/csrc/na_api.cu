@@ -18,7 +18,7 @@
 
 namespace na {
 uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D);
-int tc_tmem_cols(int which);
+int tc_tmem_cols(int which, int D);
 int tc_max_nc(int which, int D);
 }
 
@@ -247,7 +247,7 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
         }
     }
     const int D = g.D;
-    const int tmem_cols = na::tc_tmem_cols(which);
+    const int tmem_cols = na::tc_tmem_cols(which, D);
     const int ncmax = na::tc_max_nc(which, D);
     int Lcm[3];
     for (int a = 0; a < 3; ++a) Lcm[a] = ceil_div(g.L[a], g.d[a]);
@@ -330,20 +330,22 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
 }
 
 // Tensor map over a [B, L0, L1, L2, heads, D] bf16 tensor whose box is `e` class positions per axis
-// (element stride = dilation) and D channels of one head.
+// (element stride = dilation) and D channels of one head; at D = 128 the box is 64 channels (one
+// 128-byte swizzle row) and the kernels load the two halves of a head with two copies.
 na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int e[3], bool f16) {
     const cuuint64_t es = 2;
     const cuuint64_t hd = static_cast<cuuint64_t>(g.heads) * g.D;
     cuuint64_t dims[5] = {hd, static_cast<cuuint64_t>(g.L[2]), static_cast<cuuint64_t>(g.L[1]),
                           static_cast<cuuint64_t>(g.L[0]), static_cast<cuuint64_t>(g.B)};
     cuuint64_t strides[4] = {hd * es, hd * es * g.L[2], hd * es * g.L[2] * g.L[1], hd * es * g.L[2] * g.L[1] * g.L[0]};
-    cuuint32_t box[5] = {static_cast<cuuint32_t>(g.D), static_cast<cuuint32_t>(e[2] * g.d[2]),
+    const int dbox = g.D > 64 ? 64 : g.D;
+    cuuint32_t box[5] = {static_cast<cuuint32_t>(dbox), static_cast<cuuint32_t>(e[2] * g.d[2]),
                          static_cast<cuuint32_t>(e[1] * g.d[1]), static_cast<cuuint32_t>(e[0] * g.d[0]), 1};
     cuuint32_t estr[5] = {1, static_cast<cuuint32_t>(g.d[2]), static_cast<cuuint32_t>(g.d[1]),
                           static_cast<cuuint32_t>(g.d[0]), 1};
     for (int i = 0; i < 5; ++i)
         if (box[i] < 1 || box[i] > 256 || estr[i] > 8) return NA_ERR_UNSUPPORTED;
-    const int rowb = g.D * 2;
+    const int rowb = dbox * 2;
     const CUtensorMapSwizzle sw = rowb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                               : (rowb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     const CUresult r = g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
@@ -353,7 +355,7 @@ na_status encode_map(CUtensorMap* m, const void* base, const Geom& g, const int 
 }
 
 na_status tc_common(int which, const Geom& g, float scale, na::TcParams& p) {
-    if (g.D != 16 && g.D != 32 && g.D != 64) return NA_ERR_UNSUPPORTED;
+    if (g.D != 16 && g.D != 32 && g.D != 64 && g.D != 128) return NA_ERR_UNSUPPORTED;
     for (int a = 0; a < 3; ++a)
         if (g.d[a] > 8) return NA_ERR_UNSUPPORTED;
     std::memset(&p, 0, sizeof p);
@@ -688,7 +690,7 @@ na_status na_plan_info(int which, int B, int ndim, const int* spatial, int heads
     Geom g;
     na_status st = make_geom(B, ndim, spatial, heads, D, kernel, dilation, g);
     if (st != NA_OK) return st;
-    if (D != 16 && D != 32 && D != 64) return NA_ERR_UNSUPPORTED;
+    if (D != 16 && D != 32 && D != 64 && D != 128) return NA_ERR_UNSUPPORTED;
     TilePlan pl;
     if ((st = plan_tc(which, g, pl)) != NA_OK) return st;
     // chunks summed over every CTA (depends on the tile position along the two outer axes and class)

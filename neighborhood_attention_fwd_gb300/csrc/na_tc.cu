@@ -6,13 +6,15 @@ namespace na {
 
 uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D) { return tc_layout(which, pl, D).total + 1024u; }
 
-int tc_tmem_cols(int which) { return which == 0 ? 256 : 512; }
+int tc_tmem_cols(int which, int D) { return tmem_cols_of(which, D); }
 
 int tc_max_nc(int which, int D) {
-    // double-buffered score accumulators plus double-buffered tile accumulators; the forward's P
-    // overwrites its scores, and its softmax takes a run of at most six groups (96 columns)
-    const int cols = tc_tmem_cols(which);
-    const int nc = which == 0 ? (cols - 2 * D) / 2 : (which == 1 ? (cols - 2 * D) / 4 : (cols - 4 * D) / 4);
+    // double-buffered score accumulators (the backward's with their dP beside them) plus the tile
+    // accumulators; the forward's P overwrites its scores, and its softmax takes a run of at most six
+    // groups (96 columns)
+    const int cols = tc_tmem_cols(which, D);
+    const int acc = (which == 2 ? 2 : 1) * abufs_of(which, D) * D;
+    const int nc = which == 0 ? (cols - acc) / 2 : (cols - acc) / 4;
     const int cap = which == 0 ? 96 : 128;
     return (nc < cap ? nc : cap) / 16 * 16;
 }
@@ -24,6 +26,7 @@ int launch_bf16(const TcParams& p, cudaStream_t s) {
         case 16: return launch_tc<16, WHICH, false>(p, s);
         case 32: return launch_tc<32, WHICH, false>(p, s);
         case 64: return launch_tc<64, WHICH, false>(p, s);
+        case 128: return launch_tc<128, WHICH, false>(p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }

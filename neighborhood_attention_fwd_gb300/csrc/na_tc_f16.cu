@@ -11,6 +11,7 @@ int launch_f16(const TcParams& p, cudaStream_t s) {
         case 16: return launch_tc<16, WHICH, true>(p, s);
         case 32: return launch_tc<32, WHICH, true>(p, s);
         case 64: return launch_tc<64, WHICH, true>(p, s);
+        case 128: return launch_tc<128, WHICH, true>(p, s);
         default: return static_cast<int>(cudaErrorInvalidValue);
     }
 }

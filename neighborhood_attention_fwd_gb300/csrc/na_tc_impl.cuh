@@ -56,6 +56,17 @@ constexpr int kMaxStages = 4;
 // shrinks as shared memory grows.
 __host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
+// D = 128: every tensor of D channels is held as two halves of 64 channels (128-byte rows, the
+// 128-byte swizzle's width), each laid out exactly like a D = 64 operand; the products over D run
+// once per half.
+__host__ __device__ constexpr int dhalf_of(int D) { return D > 64 ? 64 : D; }
+// Tile-ring slots and tile-accumulator buffers.  At D = 128 the backward's tiles (two tensors of
+// 32 KB) leave shared memory for one tile slot, and dK/dV's accumulators (2 x 128 columns) fill half
+// of TMEM, so they are single-buffered and each tile's epilogue runs as soon as its chunks are done.
+__host__ __device__ constexpr int tslots_of(int which, int D) { return which != 0 && D > 64 ? 1 : 2; }
+__host__ __device__ constexpr int abufs_of(int which, int D) { return which == 2 && D > 64 ? 1 : 2; }
+// TMEM columns per CTA: the forward takes 256 (two CTAs per SM) up to D = 64.
+__host__ __device__ constexpr int tmem_cols_of(int which, int D) { return which == 0 && D <= 64 ? 256 : 512; }
 constexpr int kMaxPBufs = 3;
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
 // Warps that issue update products: the forward's one MMA warp issues everything; the backward has
@@ -108,6 +119,7 @@ __host__ __device__ constexpr float masked_below() { return F16 ? -3.2e4f : -1.0
 //   all: window-bias operands A (per tile) and B (constant).
 struct TcLayout {
     uint32_t tile0, tile_slot, tile_t;     // tile ring: tile0 + slot * tile_slot + tensor * tile_t
+    uint32_t tile_h, chunk_h;              // offset of the second 64-channel half of a tile / chunk tensor (D = 128)
     uint32_t chunk0, chunk_slot, chunk_t;  // chunk ring
     uint32_t p0, p_buf, p_op;              // P / dS operands
     uint32_t abias, bbias, bgroup;         // window-bias operands; bgroup = bytes of one B group
@@ -132,7 +144,9 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     L.tile0 = o;
     L.tile_t = tile;
     L.tile_slot = ntile * tile;
-    o += 2 * L.tile_slot;
+    L.tile_h = 128u * static_cast<uint32_t>(dhalf_of(D)) * 2u;
+    L.chunk_h = static_cast<uint32_t>(pl.NC) * static_cast<uint32_t>(dhalf_of(D)) * 2u;
+    o += static_cast<uint32_t>(tslots_of(which, D)) * L.tile_slot;
     L.chunk0 = o;
     L.chunk_t = chunk;
     L.chunk_slot = 2 * chunk;
@@ -563,6 +577,8 @@ __device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const
 template <int D, int WHICH>
 __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
     constexpr int kS = stages_of(WHICH, D);
+    constexpr uint32_t kTS = tslots_of(WHICH, D);
+    constexpr int kDH = dhalf_of(D);
     constexpr int ntile = WHICH == 0 ? 1 : 2;
     constexpr int tmCk = WHICH == 0 ? 1 : 2, tmCv = WHICH == 0 ? 2 : 3;
     const int lane = threadIdx.x & 31;
@@ -594,8 +610,8 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
     uint32_t j = 0, g = 0;
     bool ok = true;
     while (ok && next_tile(p, WHICH, it, started, c)) {
-        const uint32_t qs = j & 1;
-        if (j >= 2) ok = warp_wait(&bars[kQEmpty + qs], ((j >> 1) - 1) & 1, err, kSiteQ);
+        const uint32_t qs = j % kTS;
+        if (j >= kTS) ok = warp_wait(&bars[kQEmpty + qs], ((j / kTS) - 1) & 1, err, kSiteQ);
         if (!ok) break;
         // the bias operand A: rebuilt along the axes whose border situation changed, once every
         // score product of the previous tile (its last reader) is done
@@ -607,7 +623,7 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
             if (bg.nbg[a] > 0 && (!((built >> a) & 1u) || ns[a] != sig[a])) stale |= 1u << a;
         }
         if (stale) {
-            if (j >= 1) ok = warp_wait(&bars[kQEmpty + (qs ^ 1u)], ((j - 1) >> 1) & 1, err, kSiteQ);
+            if (j >= 1) ok = warp_wait(&bars[kQEmpty + (j - 1) % kTS], ((j - 1) / kTS) & 1, err, kSiteQ);
             if (!ok) break;
             build_bias_a(p, WHICH, c, bg, abias, lane, stale);
             fence_proxy_async_smem();
@@ -619,9 +635,11 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
         if (lane == 0) {
             mbar_arrive_expect_tx(&bars[kQFull + qs], ntile * tile_bytes);
             for (int tt = 0; tt < ntile; ++tt)
-                tma_load_5d(smem + lay.tile(qs, tt), &p.tm[tt], &bars[kQFull + qs], c.h * D,
-                            c.cls[2] + p.d[2] * c.t0[2], c.cls[1] + p.d[1] * c.t0[1], c.cls[0] + p.d[0] * c.t0[0],
-                            c.b);
+#pragma unroll
+                for (int hh = 0; hh < D / kDH; ++hh)
+                    tma_load_5d(smem + lay.tile(qs, tt) + hh * lay.tile_h, &p.tm[tt], &bars[kQFull + qs],
+                                c.h * D + hh * kDH, c.cls[2] + p.d[2] * c.t0[2], c.cls[1] + p.d[1] * c.t0[1],
+                                c.cls[0] + p.d[0] * c.t0[0], c.b);
         }
         ChunkCursor cur = cursor_begin();
         if (WHICH == 2) aux_fetch(p, c, cur, f, lane);
@@ -635,10 +653,15 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
             const bool withheld = p.withhold != 0u && blockIdx.x == 0 && g == 0;
             if (lane == 0 && !withheld) {
                 mbar_arrive_expect_tx(&bars[kKVFull + s], 2u * chunk_bytes);
-                tma_load_5d(smem + lay.chunk(s, 0), &p.tm[tmCk], &bars[kKVFull + s], c.h * D,
-                            c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
-                tma_load_5d(smem + lay.chunk(s, 1), &p.tm[tmCv], &bars[kKVFull + s], c.h * D,
-                            c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0, c.cls[0] + p.d[0] * y0, c.b);
+#pragma unroll
+                for (int hh = 0; hh < D / kDH; ++hh) {
+                    tma_load_5d(smem + lay.chunk(s, 0) + hh * lay.chunk_h, &p.tm[tmCk], &bars[kKVFull + s],
+                                c.h * D + hh * kDH, c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0,
+                                c.cls[0] + p.d[0] * y0, c.b);
+                    tma_load_5d(smem + lay.chunk(s, 1) + hh * lay.chunk_h, &p.tm[tmCv], &bars[kKVFull + s],
+                                c.h * D + hh * kDH, c.cls[2] + p.d[2] * x0, c.cls[1] + p.d[1] * z0,
+                                c.cls[0] + p.d[0] * y0, c.b);
+                }
             }
             if (WHICH == 2) {
                 float* l2 = reinterpret_cast<float*>(smem + lay.aux(s));
@@ -668,10 +691,10 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
             const uint32_t last = g - 1 - ((g - 1 - k) % kS);  // the last fill of slot k
             if (!(p.withhold != 0u && blockIdx.x == 0 && last == 0)) mbar_drain(&bars[kKVFull + k], (last / kS) & 1, err.limit_ns);
         }
-        for (uint32_t k = 0; k < 2; ++k) {
+        for (uint32_t k = 0; k < kTS; ++k) {
             if (j <= k) continue;
-            const uint32_t last = j - 1 - ((j - 1 - k) & 1u);
-            mbar_drain(&bars[kQFull + k], (last >> 1) & 1, err.limit_ns);
+            const uint32_t last = j - 1 - ((j - 1 - k) % kTS);
+            mbar_drain(&bars[kQFull + k], (last / kTS) & 1, err.limit_ns);
         }
     }
     __syncwarp();
@@ -691,13 +714,15 @@ struct MmaIssuer {
     uint64_t dk, dp, dmn, dbias;           // descriptor bases: K-major rows of D, P atoms, MN-major rows of D, bias blocks
     uint32_t idesc_s, idesc_sn, idesc_u;   // scores (N = NC), negated scores, updates (N = D)
     uint32_t nkk;                          // NC / 16
+    uint32_t tile_h, chunk_h;              // second 64-channel half of a tile / chunk tensor (D = 128)
     uint32_t abias, bbias, bgroup;
     int nbg[3], abase[3], bbase[3];
 
     __device__ static __forceinline__ uint64_t at(uint64_t base, uint32_t addr) { return base + (addr >> 4); }
 
     __device__ void init(const TcParams& p, uint8_t* smem, const TcLayout& lay) {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        constexpr int kDH = dhalf_of(D);
+        const uint32_t rowb = kDH * 2u, lay_ = swizzle_layout(kDH * 2), sbo = 8u * rowb;
         sbase = smem_u32(smem);
         dk = sdesc(0u, 16u, sbo, lay_);
         dp = sdesc(0u, 16u, 512u, 4u);
@@ -705,8 +730,10 @@ struct MmaIssuer {
         dbias = sdesc(0u, 16u, 256u, 6u);
         idesc_s = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0);
         idesc_sn = idesc_s | (1u << 13);
-        idesc_u = idesc_mma(128, D, false, true, p.f16 != 0);
+        idesc_u = idesc_mma(128, kDH, false, true, p.f16 != 0);
         nkk = static_cast<uint32_t>(p.plan.NC) / 16u;
+        tile_h = lay.tile_h;
+        chunk_h = lay.chunk_h;
         abias = sbase + lay.abias;
         bbias = sbase + lay.bbias;
         bgroup = lay.bgroup;
@@ -718,11 +745,16 @@ struct MmaIssuer {
         }
     }
 
-    // D_tmem = A_tile(128 x D) * B_chunk(NC x D)^T, both K-major; A negated when `neg`.
+    // D_tmem = A_tile(128 x D) * B_chunk(NC x D)^T, both K-major; A negated when `neg`.  K-step kk
+    // reads 16 channels of half kk / (64 / 16) (D = 128) at 32 bytes per step within the half.
     __device__ __forceinline__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
+        constexpr int kPerHalf = dhalf_of(D) / 16;
         const uint32_t a = sbase + a_off, b = sbase + b_off, id = neg ? idesc_sn : idesc_s;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) umma_bf16(d_tmem, at(dk, a + kk * 32u), at(dk, b + kk * 32u), id, kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t hh = static_cast<uint32_t>(kk / kPerHalf), r = static_cast<uint32_t>(kk % kPerHalf) * 32u;
+            umma_bf16(d_tmem, at(dk, a + hh * tile_h + r), at(dk, b + hh * chunk_h + r), id, kk > 0);
+        }
     }
     // D_tmem += A_bias(chunk) * B_bias^T along every masked axis: the window mask.
     __device__ __forceinline__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
@@ -735,13 +767,18 @@ struct MmaIssuer {
             if (nbg[ax] > 1) umma_bf16(d_tmem, at(dbias, ga + 4096u), at(dbias, gb + bgroup), idesc_s, 1u);
         }
     }
-    // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major.
+    // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major; at D = 128 one product
+    // of N = 64 per channel half, into accumulator columns [64 h, 64 h + 64).
     __device__ __forceinline__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
-        uint32_t a = sbase + p_off, b = sbase + b_off;
-        for (uint32_t kk = 0; kk < nkk; ++kk) {
-            umma_bf16(d_tmem, at(dp, a), at(dmn, b), idesc_u, (accumulate || kk > 0) ? 1u : 0u);
-            a += (kk & 1u) ? 8192u - 32u : 32u;
-            b += 16u * D * 2u;
+        constexpr int kDH = dhalf_of(D);
+#pragma unroll
+        for (int hh = 0; hh < D / kDH; ++hh) {
+            uint32_t a = sbase + p_off, b = sbase + b_off + static_cast<uint32_t>(hh) * chunk_h;
+            for (uint32_t kk = 0; kk < nkk; ++kk) {
+                umma_bf16(d_tmem + hh * kDH, at(dp, a), at(dmn, b), idesc_u, (accumulate || kk > 0) ? 1u : 0u);
+                a += (kk & 1u) ? 8192u - 32u : 32u;
+                b += 16u * kDH * 2u;
+            }
         }
     }
 };
@@ -757,13 +794,16 @@ struct FwdIssuer {
     BiasGeom bg;
 
     __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
+        constexpr int kDH = dhalf_of(D), kPerHalf = kDH / 16;
+        const uint32_t rowb = kDH * 2u, lay_ = swizzle_layout(kDH * 2), sbo = 8u * rowb;
         const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0) | (neg ? (1u << 13) : 0u);
         const uint32_t a = smem_u32(smem + a_off), b = smem_u32(smem + b_off);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16(d_tmem, sdesc(a + kk * 32u, 16u, sbo, lay_), sdesc(b + kk * 32u, 16u, sbo, lay_), idesc,
-                      kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t hh = static_cast<uint32_t>(kk / kPerHalf), r = static_cast<uint32_t>(kk % kPerHalf) * 32u;
+            umma_bf16(d_tmem, sdesc(a + hh * lay.tile_h + r, 16u, sbo, lay_),
+                      sdesc(b + hh * lay.chunk_h + r, 16u, sbo, lay_), idesc, kk > 0);
+        }
     }
     __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
         const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0);
@@ -779,21 +819,15 @@ struct FwdIssuer {
     // O += P V with P read from TMEM: 16-bit pairs packed in NC / 2 columns from p_tmem, so the
     // k-step kk (chunk columns 16 kk .. 16 kk + 15) starts at column p_tmem + 8 kk.
     __device__ void p_tmem_x_chunk(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_off, bool accumulate) const {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_mma(128, D, false, true, p.f16 != 0);
-        const uint32_t b = smem_u32(smem + b_off);
-        for (int kk = 0; kk < p.plan.NC / 16; ++kk)
-            umma_ts(d_tmem, p_tmem + 8u * kk, sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_), idesc,
-                    (accumulate || kk > 0) ? 1u : 0u);
-    }
-    __device__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
-        const uint32_t rowb = D * 2u, lay_ = swizzle_layout(D * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_mma(128, D, false, true, p.f16 != 0);
-        const uint32_t a = smem_u32(smem + p_off), b = smem_u32(smem + b_off);
-        for (int kk = 0; kk < p.plan.NC / 16; ++kk) {
-            const uint64_t ad = sdesc(a + (kk >> 1) * 8192u + (kk & 1) * 32u, 16u, 512u, 4u);
-            const uint64_t bd = sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_);
-            umma_bf16(d_tmem, ad, bd, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        constexpr int kDH = dhalf_of(D);
+        const uint32_t rowb = kDH * 2u, lay_ = swizzle_layout(kDH * 2), sbo = 8u * rowb;
+        const uint32_t idesc = idesc_mma(128, kDH, false, true, p.f16 != 0);
+#pragma unroll
+        for (int hh = 0; hh < D / kDH; ++hh) {
+            const uint32_t b = smem_u32(smem + b_off) + static_cast<uint32_t>(hh) * lay.chunk_h;
+            for (int kk = 0; kk < p.plan.NC / 16; ++kk)
+                umma_ts(d_tmem + hh * kDH, p_tmem + 8u * kk, sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_), idesc,
+                        (accumulate || kk > 0) ? 1u : 0u);
         }
     }
 };
@@ -805,7 +839,8 @@ __device__ __forceinline__ uint32_t tm_s(const TilePlan& pl, uint32_t b) { retur
 __device__ __forceinline__ uint32_t tm_dp(const TilePlan& pl, uint32_t b) { return (2 + b) * pl.NC; }
 template <int D>
 __device__ __forceinline__ uint32_t tm_acc(int which, uint32_t b) {
-    return which == 0 ? 256u - (2u - b) * D : (which == 1 ? 512u - (2u - b) * D : 512u - (4u - 2u * b) * D);
+    const uint32_t cols = static_cast<uint32_t>(tmem_cols_of(which, D));
+    return which == 2 ? cols - (2u * abufs_of(2, D) - 2u * b) * D : cols - (2u - b) * D;
 }
 
 struct PendingUpdate {
@@ -819,8 +854,9 @@ struct PendingUpdate {
 // scored chunk (as soon as its P is written).  Neither waits for the other, so
 // one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
 // after the launch's wait limit without progress the lane records an error and stops.
-template <int D, int WHICH>
+template <int D>
 __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr int WHICH = 0;
     constexpr int kS = stages_of(WHICH, D);
     constexpr uint32_t kPB = pbufs_of(WHICH);
     const WaitGuard err{p.err, p.wait_ns};
@@ -846,14 +882,7 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
                 (q0.ci != 0 || q0.j < 2 || mbar_test(&bars[kOEmpty + ob], ((q0.j >> 1) - 1) & 1))) {
                 tc_fence_after();
                 const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
-                if (WHICH == 0) {
-                    mi.p_tmem_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
-                } else if (WHICH == 1) {
-                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 0), q0.ci > 0);  // dQ += dS K
-                } else {
-                    mi.p_x_chunk(acc, lay.p(pb, 0), lay.chunk(q0.s, 1), q0.ci > 0);      // dV += P^T dO
-                    mi.p_x_chunk(acc + D, lay.p(pb, 1), lay.chunk(q0.s, 0), q0.ci > 0);  // dK += dS^T Q
-                }
+                mi.p_tmem_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
                 umma_commit(&bars[kPEmpty + pb]);
                 umma_commit(&bars[kKVEmpty + q0.s]);
                 if (q0.ci == q0.C - 1) umma_commit(&bars[kOFull + ob]);
@@ -920,9 +949,10 @@ __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
+    constexpr uint32_t kTS = tslots_of(WHICH, D);
     while (ok && next_tile(p, WHICH, it, started, c)) {
-        const uint32_t qs = j & 1;
-        if (!mbar_wait(&bars[kQFull + qs], (j >> 1) & 1, err, kSiteQ)) break;
+        const uint32_t qs = j % kTS;
+        if (!mbar_wait(&bars[kQFull + qs], (j / kTS) & 1, err, kSiteQ)) break;
         ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
             const uint32_t s = g % kS, sb = g & 1;
@@ -961,13 +991,14 @@ __device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& la
     const uint32_t op_p = WHICH == 2 ? static_cast<uint32_t>(u) : 0u;              // P^T or dS^T
     const uint32_t op_b = WHICH == 1 ? 0u : (u == 0 ? 1u : 0u);                    // K; dO or Q
     const uint32_t acc_off = WHICH == 2 && u == 1 ? static_cast<uint32_t>(D) : 0u;  // dK beside dV
+    constexpr uint32_t kAB = abufs_of(WHICH, D);
     while (ok && next_tile(p, WHICH, it, started, c)) {
-        const uint32_t ob = j & 1;
+        const uint32_t ob = j % kAB;
         const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + acc_off;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
             const uint32_t s = g % kS, pb = g % kPB;
             ok = mbar_wait(&bars[kPFull + pb], (g / kPB) & 1, err, kSiteP);
-            if (ok && ci == 0 && j >= 2) ok = mbar_wait(&bars[kOEmpty + ob], ((j >> 1) - 1) & 1, err, kSitePV);
+            if (ok && ci == 0 && j >= kAB) ok = mbar_wait(&bars[kOEmpty + ob], ((j / kAB) - 1) & 1, err, kSitePV);
             if (!ok) break;
             tc_fence_after();
             mi.p_x_chunk(acc, lay.p(pb, op_p), lay.chunk(s, op_b), ci > 0);
@@ -1178,7 +1209,10 @@ __device__ __forceinline__ bool fwd_epilogue(const TcParams& p, const FwdCtx& x,
                                              uint32_t tmem_lanes) {
     if (!warp_wait(&x.bars[kOFull + e.ob], (e.j >> 1) & 1, x.err, kSitePV)) return false;
     tc_fence_after();
-    store_row<D, F16>(tmem_lanes + tm_acc<D>(0, e.ob), 1.f / e.l, p.out0 + e.orow * D, e.valid);
+#pragma unroll
+    for (int hh = 0; hh < D / dhalf_of(D); ++hh)
+        store_row<dhalf_of(D), F16>(tmem_lanes + tm_acc<D>(0, e.ob) + hh * dhalf_of(D), 1.f / e.l,
+                                    p.out0 + e.orow * D + hh * dhalf_of(D), e.valid);
     tc_fence_before();
     __syncwarp();
     if (x.lane == 0) mbar_arrive(&x.bars[kOEmpty + e.ob]);
@@ -1328,7 +1362,8 @@ struct BwdEpilogue {
 template <int D, int WHICH, bool F16>
 __device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, const BwdEpilogue& e,
                                              uint32_t tmem_lanes, int wg, int lane) {
-    if (!warp_wait(&bars[kOFull + e.ob], (e.j >> 1) & 1, WaitGuard{p.err, p.wait_ns}, kSitePV)) return false;
+    constexpr uint32_t kAB = abufs_of(WHICH, D);
+    if (!warp_wait(&bars[kOFull + e.ob], (e.j / kAB) & 1, WaitGuard{p.err, p.wait_ns}, kSitePV)) return false;
     tc_fence_after();
     const uint32_t acc = tmem_lanes + tm_acc<D>(WHICH, e.ob);
     const int c0 = wg * (D / 2);
@@ -1371,7 +1406,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     while (ok && next_tile(p, WHICH, it, started, c)) {
         const RowGeom geo = row_geom(p, WHICH, c, row);
         const WarpUnion wu = warp_union(geo);
-        const uint32_t ob = j & 1;
+        const uint32_t ob = j % abufs_of(WHICH, D);
         float lse2 = 0.f, dlt = 0.f;
         if (WHICH == 1 && geo.valid) {
             lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
@@ -1436,9 +1471,14 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
         }
         if (!ok) break;
-        // the previous tile's epilogue, deferred until this tile's chunks are done
+        // the previous tile's epilogue, deferred until this tile's chunks are done; with a single
+        // accumulator buffer the next tile's first products wait for it, so it runs at once
         if (ep.live && !(ok = bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane))) break;
         ep = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
+        if (abufs_of(WHICH, D) == 1) {
+            if (!(ok = bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane))) break;
+            ep.live = false;
+        }
         ++j;
     }
     if (ok && ep.live) bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane);
@@ -1485,7 +1525,7 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
     constexpr int kSoftWarps = 4 * nwg_of(WHICH);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t tmem_cols = WHICH == 0 ? 256u : 512u;
+    const uint32_t tmem_cols = static_cast<uint32_t>(tmem_cols_of(WHICH, D));
 
     if (warp == kSoftWarps) {
         if (lane == 0) {
@@ -1507,8 +1547,11 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         producer_loop<D, WHICH>(p, smem, lay, bars);
     } else if (warp == kSoftWarps + 1) {
         if (lane == 0) {
-            if (WHICH == 0) mma_loop<D, WHICH>(p, smem, lay, bars, tmem);
-            else score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            if constexpr (WHICH == 0) {
+                mma_loop<D>(p, smem, lay, bars, tmem);
+            } else {
+                score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            }
         }
         __syncwarp();
     } else if (warp >= kSoftWarps + 2) {

@@ -39,6 +39,12 @@ SMALL = [
     ("fp16", (6, 20, 19), 2, 32, (3, 5, 5), (1, 1, 1), 1),
     ("fp16", (41, 38), 2, 64, (13, 13), (2, 2), 1),
     ("fp16", (16, 8), 1, 32, (1, 1), (1, 1), 1),            # k = 1
+    # D = 128: two 64-channel halves per operand; one forward CTA per SM; single-buffered dK/dV
+    ("bf16", (33, 30), 2, 128, (7, 5), (1, 2), 1),
+    ("bf16", (6, 12, 13), 1, 128, (3, 5, 5), (1, 1, 1), 2),
+    ("fp16", (33, 30), 2, 128, (7, 5), (1, 2), 1),
+    ("fp16", (6, 12, 13), 1, 128, (3, 5, 5), (1, 1, 1), 2),
+    ("bf16", (200,), 1, 128, (13,), (3,), 1),
 ]
 
 

@@ -25,7 +25,7 @@ def random_problem(rng):
         spatial.append(L)
         kernel.append(k)
         dilation.append(d)
-    return tuple(spatial), tuple(kernel), tuple(dilation), rng.choice([16, 32, 64])
+    return tuple(spatial), tuple(kernel), tuple(dilation), rng.choice([16, 32, 64, 128])
 
 
 def test_plans_fit_the_kernels_budgets(lib):
@@ -48,15 +48,20 @@ def test_plans_fit_the_kernels_budgets(lib):
             # the window-bias operand: at most two 16-column groups per chunk and masked axis
             assert all(1 <= G[a] <= min(H[a], 32) for a in range(3))
             assert p["smem_bytes"] <= 227 * 1024
-            if which == 0:
+            if which == 0 and D <= 64:
                 # two CTAs per SM: two score buffers (P written over them) and two accumulators in 256
                 # TMEM columns, a softmax run of at most six groups, and two CTAs' shared memory
                 assert p["tmem_cols"] == 256
                 assert 2 * NC + 2 * D <= 256 and NC <= 96
                 assert p["smem_bytes"] <= 113 * 1024
+            elif which == 0:
+                # D = 128: one CTA per SM with all 512 columns
+                assert p["tmem_cols"] == 512 and 2 * NC + 2 * D <= 512 and NC <= 96
             elif which == 1:
                 assert p["tmem_cols"] == 512 and 4 * NC + 2 * D <= 512  # S, dP (two each), dQ (two)
-            else:
+            elif D <= 64:
                 assert p["tmem_cols"] == 512 and 4 * NC + 4 * D <= 512  # S, dP, dV and dK (two each)
+            else:
+                assert p["tmem_cols"] == 512 and 4 * NC + 2 * D <= 512  # dV and dK single-buffered at D = 128
             assert p["ctas"] >= 1 and p["chunks_max"] >= 1 and p["chunks_total"] >= p["ctas"] // 2
     assert checked > 200

@@ -164,7 +164,7 @@ CASES = [
 def test_kernel_visits_exactly_the_neighbourhood(which, L, k, d):
     ndim = sum(1 for x in L if x > 1) or 1
     sp, kk, dd = L[3 - ndim:], k[3 - ndim:], d[3 - ndim:]
-    for D in (16, 32, 64):
+    for D in (16, 32, 64, 128):
         plan = na.na_plan_info(which, 1, sp, 1, D, kk, dd)
         got = replay(which, L, k, d, plan)
         exp = expected(which, L, k, d)
