@@ -767,6 +767,20 @@ struct MmaIssuer {
             if (nbg[ax] > 1) umma_bf16(d_tmem, at(dbias, ga + 4096u), at(dbias, gb + bgroup), idesc_s, 1u);
         }
     }
+    // D_tmem (+)= P(128 x NC) * B_chunk(NC x D), B MN-major, with P read from TMEM: 16-bit pairs packed
+    // in NC / 2 columns from a_tmem, so k-step kk (chunk columns 16 kk .. 16 kk + 15) starts at column
+    // a_tmem + 8 kk; at D = 128 one product per channel half.
+    __device__ __forceinline__ void pt_x_chunk(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_off, bool accumulate) const {
+        constexpr int kDH = dhalf_of(D);
+#pragma unroll
+        for (int hh = 0; hh < D / kDH; ++hh) {
+            uint32_t b = sbase + b_off + static_cast<uint32_t>(hh) * chunk_h;
+            for (uint32_t kk = 0; kk < nkk; ++kk) {
+                umma_ts(d_tmem + hh * kDH, a_tmem + 8u * kk, at(dmn, b), idesc_u, (accumulate || kk > 0) ? 1u : 0u);
+                b += 16u * kDH * 2u;
+            }
+        }
+    }
     // D_tmem (+)= P(128 x NC, 32-column atoms) * B_chunk(NC x D), B MN-major; at D = 128 one product
     // of N = 64 per channel half, into accumulator columns [64 h, 64 h + 64).
     __device__ __forceinline__ void p_x_chunk(uint32_t d_tmem, uint32_t p_off, uint32_t b_off, bool accumulate) const {
@@ -779,55 +793,6 @@ struct MmaIssuer {
                 a += (kk & 1u) ? 8192u - 32u : 32u;
                 b += 16u * kDH * 2u;
             }
-        }
-    }
-};
-
-// The forward's issuer: descriptors built in each call from the parameters.  (The forward's single
-// MMA lane runs a polling loop; measured on the 2048x2048 / 13x13 problem this form issues faster
-// there than the precomputed-descriptor form the backward issuers use.)
-template <int D>
-struct FwdIssuer {
-    const TcParams& p;
-    uint8_t* smem;
-    const TcLayout& lay;
-    BiasGeom bg;
-
-    __device__ void rows_x_chunk(uint32_t d_tmem, uint32_t a_off, uint32_t b_off, bool neg) const {
-        constexpr int kDH = dhalf_of(D), kPerHalf = kDH / 16;
-        const uint32_t rowb = kDH * 2u, lay_ = swizzle_layout(kDH * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0) | (neg ? (1u << 13) : 0u);
-        const uint32_t a = smem_u32(smem + a_off), b = smem_u32(smem + b_off);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t hh = static_cast<uint32_t>(kk / kPerHalf), r = static_cast<uint32_t>(kk % kPerHalf) * 32u;
-            umma_bf16(d_tmem, sdesc(a + hh * lay.tile_h + r, 16u, sbo, lay_),
-                      sdesc(b + hh * lay.chunk_h + r, 16u, sbo, lay_), idesc, kk > 0);
-        }
-    }
-    __device__ void add_bias(uint32_t d_tmem, const ChunkCursor& k) const {
-        const uint32_t idesc = idesc_mma(128, p.plan.NC, false, false, p.f16 != 0);
-        const uint32_t a = smem_u32(smem + lay.abias), b = smem_u32(smem + lay.bbias);
-        for (int ax = 0; ax < 3; ++ax)
-            for (int q = 0; q < bg.nbg[ax]; ++q) {
-                const uint32_t ga = static_cast<uint32_t>(bg.abase[ax] + k.ix[ax] * bg.nbg[ax] + q);
-                const uint32_t gb = static_cast<uint32_t>(bg.bbase[ax] + q);
-                umma_bf16(d_tmem, sdesc(a + ga * 4096u, 16u, 256u, 6u), sdesc(b + gb * lay.bgroup, 16u, 256u, 6u),
-                          idesc, 1u);
-            }
-    }
-    // O += P V with P read from TMEM: 16-bit pairs packed in NC / 2 columns from p_tmem, so the
-    // k-step kk (chunk columns 16 kk .. 16 kk + 15) starts at column p_tmem + 8 kk.
-    __device__ void p_tmem_x_chunk(uint32_t d_tmem, uint32_t p_tmem, uint32_t b_off, bool accumulate) const {
-        constexpr int kDH = dhalf_of(D);
-        const uint32_t rowb = kDH * 2u, lay_ = swizzle_layout(kDH * 2), sbo = 8u * rowb;
-        const uint32_t idesc = idesc_mma(128, kDH, false, true, p.f16 != 0);
-#pragma unroll
-        for (int hh = 0; hh < D / kDH; ++hh) {
-            const uint32_t b = smem_u32(smem + b_off) + static_cast<uint32_t>(hh) * lay.chunk_h;
-            for (int kk = 0; kk < p.plan.NC / 16; ++kk)
-                umma_ts(d_tmem + hh * kDH, p_tmem + 8u * kk, sdesc(b + kk * 16u * rowb, 16u * rowb, sbo, lay_), idesc,
-                        (accumulate || kk > 0) ? 1u : 0u);
         }
     }
 };
@@ -861,7 +826,8 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     constexpr uint32_t kPB = pbufs_of(WHICH);
     const WaitGuard err{p.err, p.wait_ns};
     const TilePlan& pl = p.plan;
-    const FwdIssuer<D> mi{p, smem, lay, bias_geom(pl)};
+    MmaIssuer<D> mi;
+    mi.init(p, smem, lay);
     const bool neg = p.neg != 0;
     TileIter it = tile_iter_begin(p);
     bool started = false;
@@ -873,7 +839,8 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     ChunkCursor cur = cursor_begin();
     PendingUpdate q0{}, q1{}, q2{};  // scored chunks awaiting their update, oldest first
     int nq = 0;
-    unsigned long long t_last = globaltimer();
+    unsigned long long t_last = 0;
+    uint32_t idle = 0;
     for (;;) {
         bool progress = false;
         if (nq > 0) {
@@ -882,7 +849,7 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
                 (q0.ci != 0 || q0.j < 2 || mbar_test(&bars[kOEmpty + ob], ((q0.j >> 1) - 1) & 1))) {
                 tc_fence_after();
                 const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
-                mi.p_tmem_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
+                mi.pt_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
                 umma_commit(&bars[kPEmpty + pb]);
                 umma_commit(&bars[kKVEmpty + q0.s]);
                 if (q0.ci == q0.C - 1) umma_commit(&bars[kOFull + ob]);
@@ -923,15 +890,20 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
         }
         if (!have && nq == 0) break;
         if (progress) {
-            t_last = globaltimer();
+            idle = 0;
             continue;
         }
-        if (ld_volatile(err.word) != 0u) break;
-        if (globaltimer() - t_last > err.limit_ns) {
-            record_error(err.word, kSiteP);
-            break;
+        // idle: spin on the barriers; the status word (a global load of some hundred cycles) and the
+        // time limit are checked every 64 passes
+        if ((++idle & 63u) == 0u) {
+            if (ld_volatile(err.word) != 0u) break;
+            const unsigned long long now = globaltimer();
+            if (idle == 64u) t_last = now;
+            else if (now - t_last > err.limit_ns) {
+                record_error(err.word, kSiteP);
+                break;
+            }
         }
-        __nanosleep(32);
     }
 }
 
