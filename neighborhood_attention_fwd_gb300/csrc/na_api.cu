@@ -408,6 +408,13 @@ na::FmaParams fma_params(const Geom& g, float scale) {
     p.D = g.D;
     p.N = tokens_of(g);
     p.scale = scale;
+    p.rows32 = static_cast<long long>(g.B) * p.N * g.heads < (1LL << 32) ? 1u : 0u;
+    p.fd_heads = na::make_fastdiv(static_cast<uint32_t>(g.heads));
+    p.fd_N = na::make_fastdiv(static_cast<uint32_t>(p.N));
+    for (int a = 0; a < 3; ++a) {
+        p.fd_L[a] = na::make_fastdiv(static_cast<uint32_t>(g.L[a]));
+        p.fd_d[a] = na::make_fastdiv(static_cast<uint32_t>(g.d[a]));
+    }
     return p;
 }
 
@@ -443,6 +450,17 @@ na_status unfused_params(int B, int ndim, const int* spatial, int heads, int D, 
     p.rows = tokens_of(g) * B * heads;
     p.scale = scale;
     for (int c = 0; c < g.d[2]; ++c) p.strips2 += ((g.L[2] - c + g.d[2] - 1) / g.d[2] + 15) / 16;
+    p.units = static_cast<long long>(B) * g.L[0] * g.L[1] * p.strips2 * heads;
+    p.small = p.rows < (1LL << 32) && p.units < (1LL << 32) ? 1u : 0u;
+    p.fd_heads = na::make_fastdiv(static_cast<uint32_t>(heads));
+    p.fd_strips2 = na::make_fastdiv(static_cast<uint32_t>(p.strips2));
+    for (int a = 0; a < 3; ++a) {
+        p.fd_L[a] = na::make_fastdiv(static_cast<uint32_t>(g.L[a]));
+        p.fd_d[a] = na::make_fastdiv(static_cast<uint32_t>(g.d[a]));
+    }
+    p.fd_K = na::make_fastdiv(static_cast<uint32_t>(p.K));
+    p.fd_k2 = na::make_fastdiv(static_cast<uint32_t>(g.k[2]));
+    p.fd_k12 = na::make_fastdiv(static_cast<uint32_t>(g.k[1] * g.k[2]));
     return NA_OK;
 }
 }  // namespace

@@ -35,6 +35,21 @@ struct RowIdx {
 
 __device__ __forceinline__ RowIdx decode_row(const FmaParams& p, long long row) {
     RowIdx r;
+    if (p.rows32) {
+        const uint32_t u = static_cast<uint32_t>(row);
+        const uint32_t bt = fdiv(u, p.fd_heads);
+        r.h = static_cast<int>(u - bt * p.fd_heads.d);
+        const uint32_t b = fdiv(bt, p.fd_N);
+        uint32_t t = bt - b * p.fd_N.d;
+        r.b = b;
+        r.tok = t;
+        for (int a = 2; a >= 0; --a) {
+            const uint32_t q = fdiv(t, p.fd_L[a]);
+            r.x[a] = static_cast<int>(t - q * p.fd_L[a].d);
+            t = q;
+        }
+        return r;
+    }
     r.h = static_cast<int>(row % p.heads);
     long long bt = row / p.heads;
     r.b = bt / p.N;
@@ -49,8 +64,9 @@ __device__ __forceinline__ RowIdx decode_row(const FmaParams& p, long long row) 
 
 // First neighbour (spatial index) of spatial index i along axis a.
 __device__ __forceinline__ int first_nb(const FmaParams& p, int a, int i) {
-    const int d = p.d[a], c = i % d, j = i / d;
-    return c + d * win_start(j, class_len(p.L[a], d, c), p.k[a]);
+    const int d = p.d[a], j = static_cast<int>(fdiv(static_cast<uint32_t>(i), p.fd_d[a])), c = i - j * d;
+    const int Lc = static_cast<int>(fdiv(static_cast<uint32_t>(p.L[a] - c + d - 1), p.fd_d[a]));
+    return c + d * win_start(j, Lc, p.k[a]);
 }
 
 // Chunks of 16 bytes per lane: a lane holds L of its row's D / 4 chunks, the row's lanes interleaved
@@ -302,7 +318,8 @@ __global__ void __launch_bounds__(kFmaThreads, 3) dkdv_fma_kernel(const FmaParam
     const RowIdx r = decode_row(p, ln.row);
     int lo[3], hi[3], cl[3];
     for (int a = 0; a < 3; ++a) {
-        const int d = p.d[a], c = r.x[a] % d, j = r.x[a] / d, Lc = class_len(p.L[a], d, c), ka = p.k[a];
+        const int d = p.d[a], j = static_cast<int>(fdiv(static_cast<uint32_t>(r.x[a]), p.fd_d[a])), c = r.x[a] - j * d;
+        const int Lc = static_cast<int>(fdiv(static_cast<uint32_t>(p.L[a] - c + d - 1), p.fd_d[a])), ka = p.k[a];
         lo[a] = j < ka ? 0 : j - ka / 2;
         hi[a] = j >= Lc - ka ? Lc - 1 : j + ka / 2;
         cl[a] = c;

@@ -12,6 +12,31 @@
 
 namespace na {
 
+// Division of 32-bit unsigned values by a divisor fixed for a launch, by multiplication (Granlund
+// and Montgomery, "Division by invariant integers using multiplication", 1994): with s = ceil(log2 d)
+// and m = floor(2^32 (2^s - d) / d) + 1, n / d = (t + ((n - t) >> 1)) >> (s - 1) where
+// t = umulhi(m, n), exact for every 32-bit n; d = 1 is a copy.  A hardware-free division by a
+// runtime divisor costs a thread ~74 cycles on this GPU, this ~10.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d, 0u, 0u};
+    if (d <= 1) return f;
+    uint32_t s = 0;
+    while ((1ull << s) < d) ++s;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << s) - d)) / d + 1ull);
+    f.s = s;
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    if (f.d <= 1u) return n;
+    const uint32_t t = __umulhi(f.m, n);
+    return (t + ((n - t) >> 1)) >> (f.s - 1u);
+}
+
 struct Geom {
     int B, heads, D;
     int L[3], k[3], d[3];
@@ -78,6 +103,9 @@ struct FmaParams {
     int B, heads, D;
     int64_t N;          // tokens per batch entry
     float scale;
+    // 32-bit row decode without division (used when B * N * heads < 2^32)
+    uint32_t rows32;
+    FastDiv fd_heads, fd_N, fd_L[3], fd_d[3];
 };
 
 // Parameters of the unfused operations (na_unfused.cu).  Rows are (batch, token, head) triples;
@@ -94,6 +122,10 @@ struct UnfParams {
     const int* vk;      // mask: per-position kernel sizes, concatenated over the axes
     int vk_off[3];      // mask: offset of each (embedded) axis in vk, -1 for an axis without one
     int strips2;        // tensor-core logits: strips of 16 class positions along the innermost axis, summed over classes
+    long long units;    // tensor-core kernels: strips of all lines, heads and batch entries (B L0 L1 strips2 heads)
+    // 32-bit decodes without division (rows and units < 2^32)
+    uint32_t small;
+    FastDiv fd_heads, fd_strips2, fd_L[3], fd_d[3], fd_K, fd_k2, fd_k12;
 };
 
 // Tokens per block of the bias-gradient reduction's first stage, and the size of its partial sums.

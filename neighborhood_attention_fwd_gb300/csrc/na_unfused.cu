@@ -146,6 +146,18 @@ struct Row {
 
 __device__ __forceinline__ Row decode(const UnfParams& p, long long row) {
     Row r;
+    if (p.small) {
+        uint32_t u = static_cast<uint32_t>(row), q = fdiv(u, p.fd_heads);
+        r.h = static_cast<int>(u - q * p.fd_heads.d);
+        u = q;
+        for (int a = 2; a >= 0; --a) {
+            q = fdiv(u, p.fd_L[a]);
+            r.x[a] = static_cast<int>(u - q * p.fd_L[a].d);
+            u = q;
+        }
+        r.b = u;
+        return r;
+    }
     r.h = static_cast<int>(row % p.heads);
     long long t = row / p.heads;
     for (int a = 2; a >= 0; --a) {
@@ -157,9 +169,45 @@ __device__ __forceinline__ Row decode(const UnfParams& p, long long row) {
 }
 
 // First neighbour (spatial index) of spatial index i along axis a.
+__device__ __forceinline__ int cidx(const UnfParams& p, int a, int i) {   // class index i / d
+    return static_cast<int>(fdiv(static_cast<uint32_t>(i), p.fd_d[a]));
+}
+__device__ __forceinline__ int clen(const UnfParams& p, int a, int c) {   // length of class c
+    return static_cast<int>(fdiv(static_cast<uint32_t>(p.L[a] - c + p.d[a] - 1), p.fd_d[a]));
+}
 __device__ __forceinline__ int first_nb(const UnfParams& p, int a, int i) {
-    const int d = p.d[a], c = i % d, j = i / d;
-    return c + d * win_start(j, class_len(p.L[a], d, c), p.k[a]);
+    const int d = p.d[a], j = cidx(p, a, i), c = i - j * d;
+    return c + d * win_start(j, clen(p, a, c), p.k[a]);
+}
+
+// A tensor-core warp's unit (head fastest, then strip along the innermost axis, the two outer axes,
+// batch).
+__device__ __forceinline__ void decode_unit(const UnfParams& p, long long unit, int& h, int& s, int& x1, int& x0,
+                                            long long& b) {
+    if (p.small) {
+        uint32_t u = static_cast<uint32_t>(unit), q = fdiv(u, p.fd_heads);
+        h = static_cast<int>(u - q * p.fd_heads.d);
+        u = q;
+        q = fdiv(u, p.fd_strips2);
+        s = static_cast<int>(u - q * p.fd_strips2.d);
+        u = q;
+        q = fdiv(u, p.fd_L[1]);
+        x1 = static_cast<int>(u - q * p.fd_L[1].d);
+        u = q;
+        q = fdiv(u, p.fd_L[0]);
+        x0 = static_cast<int>(u - q * p.fd_L[0].d);
+        b = q;
+        return;
+    }
+    long long u = unit;
+    h = static_cast<int>(u % p.heads);
+    u /= p.heads;
+    s = static_cast<int>(u % p.strips2);
+    u /= p.strips2;
+    x1 = static_cast<int>(u % p.L[1]);
+    u /= p.L[1];
+    x0 = static_cast<int>(u % p.L[0]);
+    b = u / p.L[0];
 }
 
 // A row's window, walked one key line (fixed t0, t1) at a time: the line's first key row and the
@@ -176,7 +224,7 @@ struct Window {
         h = r.h;
         for (int a = 0; a < 3; ++a) {
             f[a] = first_nb(p, a, r.x[a]);
-            rb[a] = f[a] / p.d[a] - r.x[a] / p.d[a] + p.k[a] - 1;
+            rb[a] = cidx(p, a, f[a]) - cidx(p, a, r.x[a]) + p.k[a] - 1;
         }
         step = static_cast<long long>(p.d[2]) * p.heads;
     }
@@ -201,18 +249,30 @@ struct Group {
 template <typename T, int SP>
 __device__ __forceinline__ void stage_store(T* out, const T* stage, long long row0, int nrows, int K, int tc,
                                             int clen, int lane) {
+    if (clen <= 0 || nrows <= 0) return;
+    int rr = 0, j = lane;   // idx = rr * clen + j, stepped by 32 without dividing
+    while (j >= clen) {
+        j -= clen;
+        ++rr;
+    }
     for (int idx = lane; idx < nrows * clen; idx += 32) {
-        const int rr = idx / clen, j = idx - rr * clen;
         out[(row0 + rr) * K + tc + j] = stage[rr * SP + j];
+        for (j += 32; j >= clen; j -= clen) ++rr;
     }
 }
 
 template <typename T, int SP>
 __device__ __forceinline__ void stage_load(T* stage, const T* in, long long row0, int nrows, int K, int tc, int clen,
                                            int lane) {
+    if (clen <= 0 || nrows <= 0) return;
+    int rr = 0, j = lane;   // idx = rr * clen + j, stepped by 32 without dividing
+    while (j >= clen) {
+        j -= clen;
+        ++rr;
+    }
     for (int idx = lane; idx < nrows * clen; idx += 32) {
-        const int rr = idx / clen, j = idx - rr * clen;
         stage[rr * SP + j] = in[(row0 + rr) * K + tc + j];
+        for (j += 32; j >= clen; j -= clen) ++rr;
     }
 }
 
@@ -373,9 +433,9 @@ __global__ void __launch_bounds__(kThreads) scatter_kernel(const UnfParams p) {
     int cl[3], jk[3], Lc[3], lo[3], hi[3];
     for (int a = 0; a < 3; ++a) {
         const int d = p.d[a], k = p.k[a];
-        cl[a] = r.x[a] % d;
-        jk[a] = r.x[a] / d;
-        Lc[a] = class_len(p.L[a], d, cl[a]);
+        jk[a] = cidx(p, a, r.x[a]);
+        cl[a] = r.x[a] - jk[a] * d;
+        Lc[a] = clen(p, a, cl[a]);
         lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
         hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
     }
@@ -557,7 +617,7 @@ __global__ void __launch_bounds__(kThreads) rpb_grad_partial_kernel(const UnfPar
     for (int rr = threadIdx.x; rr < nt; rr += kThreads) {
         const Row r = decode(p, (tok0 + rr) * H);
         for (int a = 0; a < 3; ++a)
-            rel[rr * 3 + a] = first_nb(p, a, r.x[a]) / p.d[a] - r.x[a] / p.d[a] + p.k[a] - 1;
+            rel[rr * 3 + a] = cidx(p, a, first_nb(p, a, r.x[a])) - cidx(p, a, r.x[a]) + p.k[a] - 1;
     }
     __syncthreads();
     const int pairs = H * K;   // (head, offset) pairs of one token: its H * K contiguous weights
@@ -576,8 +636,10 @@ __global__ void __launch_bounds__(kThreads) rpb_grad_partial_kernel(const UnfPar
                 a3 += E::get(col[static_cast<long long>(q + 3) * pairs]);
             }
             for (; q < end; ++q) a0 += E::get(col[static_cast<long long>(q) * pairs]);
-            const int h = pi / K, t = pi - h * K;
-            const int t2 = t % p.k[2], t1 = (t / p.k[2]) % p.k[1], t0 = t / (p.k[2] * p.k[1]);
+            const int h = static_cast<int>(fdiv(static_cast<uint32_t>(pi), p.fd_K)), t = pi - h * K;
+            const int t0 = static_cast<int>(fdiv(static_cast<uint32_t>(t), p.fd_k12));
+            const int t12 = t - t0 * p.k[1] * p.k[2];
+            const int t1 = static_cast<int>(fdiv(static_cast<uint32_t>(t12), p.fd_k2)), t2 = t12 - t1 * p.k[2];
             tab[h * S + ((r0 + t0) * S1 + r1 + t1) * S2 + r2 + t2] += (a0 + a1) + (a2 + a3);
         }
         __syncthreads();
@@ -645,7 +707,7 @@ __global__ void __launch_bounds__(kThreads) mask_window_kernel(const UnfParams p
         lo[a] = 0;
         hi[a] = p.k[a] - 1;
         if (p.vk_off[a] < 0) continue;
-        const int k = p.k[a], d = p.d[a], c = x[a] % d, j = x[a] / d, Lc = class_len(p.L[a], d, c);
+        const int k = p.k[a], d = p.d[a], j = cidx(p, a, x[a]), c = x[a] - j * d, Lc = clen(p, a, c);
         int kv = min(max(__ldg(p.vk + p.vk_off[a] + x[a]), 1), k);
         if ((kv & 1) == 0) --kv;
         lo[a] = win_start(j, Lc, kv) - win_start(j, Lc, k);   // offset of the own window in the full one
@@ -709,23 +771,15 @@ __global__ void __launch_bounds__(kMmaThreads) dot_mma_kernel(const UnfParams p)
     constexpr int KS = D / 16;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     const long long unit = (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5;
-    const long long units = static_cast<long long>(p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] *
-                                                              p.heads)) * p.L[0] * p.L[1] * p.strips2 * p.heads;
-    if (unit >= units) return;   // warp-uniform
+    if (unit >= p.units) return;   // warp-uniform
     const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3;
-    long long u = unit;
-    const int h = static_cast<int>(u % p.heads);
-    u /= p.heads;
-    int s = static_cast<int>(u % p.strips2);
-    u /= p.strips2;
-    const int x1 = static_cast<int>(u % p.L[1]);
-    u /= p.L[1];
-    const int x0 = static_cast<int>(u % p.L[0]);
-    const long long b = u / p.L[0];
+    int h, s, x1, x0;
+    long long b;
+    decode_unit(p, unit, h, s, x1, x0, b);
     const int d2 = p.d[2], k2 = p.k[2];
     int c2 = 0, Lc2 = 0;
     for (c2 = 0; c2 < d2; ++c2) {   // the strip's class along the innermost axis
-        Lc2 = class_len(p.L[2], d2, c2);
+        Lc2 = clen(p, 2, c2);
         const int n = (Lc2 + 15) >> 4;
         if (s < n) break;
         s -= n;
@@ -752,7 +806,7 @@ __global__ void __launch_bounds__(kMmaThreads) dot_mma_kernel(const UnfParams p)
     // outer-axis windows (shared by the strip) and, with a bias, the relative indices
     const int f0 = first_nb(p, 0, x0), f1 = first_nb(p, 1, x1);
     const int S1 = 2 * p.k[1] - 1, S2b = 2 * k2 - 1;
-    const int rb0 = f0 / p.d[0] - x0 / p.d[0] + p.k[0] - 1, rb1 = f1 / p.d[1] - x1 / p.d[1] + p.k[1] - 1;
+    const int rb0 = cidx(p, 0, f0) - cidx(p, 0, x0) + p.k[0] - 1, rb1 = cidx(p, 1, f1) - cidx(p, 1, x1) + p.k[1] - 1;
     const int rbq0 = ws0 + off0 - jq0 + k2 - 1, rbq1 = ws0 + off1 - jq1 + k2 - 1;
     const float* bias = BIAS ? p.rpb + static_cast<long long>(h) * (2 * p.k[0] - 1) * S1 * S2b : nullptr;
     T* out = static_cast<T*>(p.out0);
@@ -810,20 +864,11 @@ struct Strip {
     int x0, x1, h, c2, Lc2, j0, nq, ws0, span;
 
     __device__ bool init(const UnfParams& p, long long unit) {
-        const long long units = static_cast<long long>(p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] *
-                                                                 p.heads)) * p.L[0] * p.L[1] * p.strips2 * p.heads;
-        if (unit >= units) return false;
-        long long u = unit;
-        h = static_cast<int>(u % p.heads);
-        u /= p.heads;
-        int s = static_cast<int>(u % p.strips2);
-        u /= p.strips2;
-        x1 = static_cast<int>(u % p.L[1]);
-        u /= p.L[1];
-        x0 = static_cast<int>(u % p.L[0]);
-        b = u / p.L[0];
+        if (unit >= p.units) return false;
+        int s;
+        decode_unit(p, unit, h, s, x1, x0, b);
         for (c2 = 0; c2 < p.d[2]; ++c2) {
-            Lc2 = class_len(p.L[2], p.d[2], c2);
+            Lc2 = clen(p, 2, c2);
             const int n = (Lc2 + 15) >> 4;
             if (s < n) break;
             s -= n;
@@ -987,9 +1032,9 @@ __global__ void __launch_bounds__(kMmaThreads) scatter_mma_kernel(const UnfParam
     const int xo[2] = {st.x0, st.x1};
     for (int a = 0; a < 2; ++a) {
         const int d = p.d[a], k = p.k[a];
-        cl[a] = xo[a] % d;
-        jk[a] = xo[a] / d;
-        Lc[a] = class_len(p.L[a], d, cl[a]);
+        jk[a] = cidx(p, a, xo[a]);
+        cl[a] = xo[a] - jk[a] * d;
+        Lc[a] = clen(p, a, cl[a]);
         lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
         hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
     }
