@@ -68,7 +68,11 @@ __host__ __device__ constexpr int abufs_of(int which, int D) { return which == 2
 // TMEM columns per CTA: the forward takes 256 (two CTAs per SM) up to D = 64.
 __host__ __device__ constexpr int tmem_cols_of(int which, int D) { return which == 0 && D <= 64 ? 256 : 512; }
 constexpr int kMaxPBufs = 3;
-__host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : 2; }
+// Softmax warpgroups: the forward's four warps own one TMEM lane quarter each; in the backward
+// kBwdGroups warpgroups share every quarter's groups, warpgroup w taking groups w, w + kBwdGroups, ...
+constexpr int kBwdGroups = 2;
+static_assert(kBwdGroups >= 2, "the backward epilogue stores half of the D columns per warpgroup 0 and 1");
+__host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : kBwdGroups; }
 // Warps that issue update products: the forward's one MMA warp issues everything; the backward has
 // one issuing warp per update accumulator (dQ; or dV and dK) beside the warp issuing score products.
 // A single lane waits tens of cycles on each tcgen05.mma it issues, so products into independent
@@ -1257,7 +1261,7 @@ struct BwdCtx {
     uint64_t sl2x2;
 };
 
-// This warp's K (<= 2) groups g0, g0 + 2 of the chunk: their scores and dP values are read, the
+// This warp's K (<= 2) groups g0, g0 + kBwdGroups of the chunk: their scores and dP values are read, the
 // score buffer is released when these are the warp's last groups of the chunk (so the next chunk's
 // products can start), then P = exp2(S sl2 - LSE2) and dS = P (dP - Delta) are formed and stored.
 template <int WHICH, int K, bool F16>
@@ -1265,8 +1269,8 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
     uint32_t rs[K > 0 ? K : 1][16], rp[K > 0 ? K : 1][16];
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-        tmem_ld16(x.tS + 16u * (g0 + 2 * i), rs[i]);
-        tmem_ld16(x.tP + 16u * (g0 + 2 * i), rp[i]);
+        tmem_ld16(x.tS + 16u * (g0 + kBwdGroups * i), rs[i]);
+        tmem_ld16(x.tP + 16u * (g0 + kBwdGroups * i), rp[i]);
     }
     if (K > 0) {
         tmem_ld_wait_all();
@@ -1283,7 +1287,7 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
     }
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-        const int gi = g0 + 2 * i;
+        const int gi = g0 + kBwdGroups * i;
         uint32_t a[8], b[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -1323,6 +1327,13 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
     }
 }
 
+// Groups g with g mod kBwdGroups == w, as a 32-bit mask.
+__host__ __device__ constexpr uint32_t group_mask(int w) {
+    uint32_t m = 0u;
+    for (int g = w; g < 32; g += kBwdGroups) m |= 1u << g;
+    return m;
+}
+
 // A tile whose rows still have to be written; each warpgroup writes half of the D columns of its
 // quarter's rows (dQ, or dV and dK).
 struct BwdEpilogue {
@@ -1339,11 +1350,13 @@ __device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, 
     tc_fence_after();
     const uint32_t acc = tmem_lanes + tm_acc<D>(WHICH, e.ob);
     const int c0 = wg * (D / 2);
-    if (WHICH == 1) {
-        store_row<D / 2, F16>(acc + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dQ
-    } else {
-        store_row<D / 2, F16>(acc + c0, 1.f, p.out1 + e.orow * D + c0, e.valid);          // dV
-        store_row<D / 2, F16>(acc + D + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dK
+    if (wg < 2) {   // two warpgroups store half of the D columns each; any others only release
+        if (WHICH == 1) {
+            store_row<D / 2, F16>(acc + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dQ
+        } else {
+            store_row<D / 2, F16>(acc + c0, 1.f, p.out1 + e.orow * D + c0, e.valid);          // dV
+            store_row<D / 2, F16>(acc + D + c0, p.scale, p.out0 + e.orow * D + c0, e.valid);  // dK
+        }
     }
     tc_fence_before();
     __syncwarp();
@@ -1357,6 +1370,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     constexpr int kS = stages_of(WHICH, D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
+    const uint32_t gmask = group_mask(wg);    // this warpgroup's groups
     const int row = wq * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const WaitGuard err{p.err, p.wait_ns};
@@ -1395,13 +1409,13 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             tc_fence_after();
             int glo, n;
             chunk_range(pl, cur, wu, glo, n);
-            // this warpgroup's groups of the run: glo + wg, glo + wg + 2, ...; the groups of the
-            // quarter's last run in this buffer that the new run does not cover are zeroed, split
-            // between the warpgroups by parity
-            const int mine = n > wg ? (n - wg + 1) >> 1 : 0;
+            // this warpgroup's groups of the run: glo + wg, glo + wg + kBwdGroups, ...; the groups of
+            // the quarter's last run in this buffer that the new run does not cover are zeroed, split
+            // between the warpgroups by group index modulo kBwdGroups
+            const int mine = n > wg ? (n - wg + kBwdGroups - 1) / kBwdGroups : 0;
             const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
             const uint32_t nzq = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
-            const uint32_t stale = nzq & ~run & (wg ? 0xaaaaaaaau : 0x55555555u);
+            const uint32_t stale = nzq & ~run & gmask;
             if (pb == 0) nz0 = run; else if (pb == 1) nz1 = run; else nz2 = run;
             if (mine == 0 && stale == 0) {
                 // nothing to write: the score buffer is released at once, but the arrival on the P
@@ -1430,9 +1444,9 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             for (int k = 0; k < mine; k += 2) {
                 const bool last = k + 2 >= mine;
                 if (k + 1 < mine)
-                    bwd_groups<WHICH, 2, F16>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+                    bwd_groups<WHICH, 2, F16>(x, glo + wg + kBwdGroups * k, &bars[kSEmpty + sb], last, lane);
                 else
-                    bwd_groups<WHICH, 1, F16>(x, glo + wg + 2 * k, &bars[kSEmpty + sb], last, lane);
+                    bwd_groups<WHICH, 1, F16>(x, glo + wg + kBwdGroups * k, &bars[kSEmpty + sb], last, lane);
             }
             for (uint32_t z = stale; z; z &= z - 1) {
                 zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
