@@ -55,7 +55,14 @@ constexpr int kMaxStages = 4;
 // measured slower with a fourth stage: its per-column LSE/Delta gathers go through L1, which
 // shrinks as shared memory grows.
 __host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
-__host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 3 : 2; }
+// Backward chunk ownership.  dQ: the two warpgroups take alternate chunks (warpgroup w the chunks g
+// with g mod 2 == w), each covering its quarter's whole run, so the per-chunk work of waits, run
+// geometry and hand-offs is paid once per chunk and quarter; chunk g uses P buffer g mod 4, two per
+// warpgroup.  dK/dV: its two P operands per buffer leave shared memory for two buffers only, one per
+// warpgroup would stall on its own updates, so both warpgroups share every chunk's groups (measured at
+// 2D 1024^2 / 9x9: dQ 1.75 -> 1.61 ms alternating; dK/dV 2.37 -> 2.58 ms).
+__host__ __device__ constexpr bool alt_of(int which) { return which == 1; }
+__host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 4 : 2; }
 // D = 128: every tensor of D channels is held as two halves of 64 channels (128-byte rows, the
 // 128-byte swizzle's width), each laid out exactly like a D = 64 operand; the products over D run
 // once per half.
@@ -67,11 +74,16 @@ __host__ __device__ constexpr int tslots_of(int which, int D) { return which != 
 __host__ __device__ constexpr int abufs_of(int which, int D) { return which == 2 && D > 64 ? 1 : 2; }
 // TMEM columns per CTA: the forward takes 256 (two CTAs per SM) up to D = 64.
 __host__ __device__ constexpr int tmem_cols_of(int which, int D) { return which == 0 && D <= 64 ? 256 : 512; }
-constexpr int kMaxPBufs = 3;
+constexpr int kMaxPBufs = 4;
 // Softmax warpgroups: the forward's four warps own one TMEM lane quarter each; in the backward
 // kBwdGroups warpgroups share every quarter's groups, warpgroup w taking groups w, w + kBwdGroups, ...
 constexpr int kBwdGroups = 2;
 static_assert(kBwdGroups >= 2, "the backward epilogue stores half of the D columns per warpgroup 0 and 1");
+static_assert(kBwdGroups == 2, "alternate chunks pair two warpgroups");
+// Warps that read and release each chunk's scores and write its P operand.
+__host__ __device__ constexpr int chunk_warps_of(int which) { return which == 0 || alt_of(which) ? 4 : 4 * kBwdGroups; }
+// Distance between the groups one warp takes within a run.
+__host__ __device__ constexpr int group_stride_of(int which) { return alt_of(which) ? 1 : kBwdGroups; }
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : kBwdGroups; }
 // Warps that issue update products: the forward's one MMA warp issues everything; the backward has
 // one issuing warp per update accumulator (dQ; or dV and dK) beside the warp issuing score products.
@@ -1267,8 +1279,8 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
     uint32_t rs[K > 0 ? K : 1][16], rp[K > 0 ? K : 1][16];
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-        tmem_ld16(x.tS + 16u * (g0 + kBwdGroups * i), rs[i]);
-        tmem_ld16(x.tP + 16u * (g0 + kBwdGroups * i), rp[i]);
+        tmem_ld16(x.tS + 16u * (g0 + group_stride_of(WHICH) * i), rs[i]);
+        tmem_ld16(x.tP + 16u * (g0 + group_stride_of(WHICH) * i), rp[i]);
     }
     if (K > 0) {
         tmem_ld_wait_all();
@@ -1285,7 +1297,7 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
     }
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-        const int gi = g0 + kBwdGroups * i;
+        const int gi = g0 + group_stride_of(WHICH) * i;
         uint32_t a[8], b[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
@@ -1367,6 +1379,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                                  uint32_t tmem) {
     constexpr int kS = stages_of(WHICH, D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr bool kAlt = alt_of(WHICH);
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
     const uint32_t gmask = group_mask(wg);    // this warpgroup's groups
     const int row = wq * 32 + lane;
@@ -1402,6 +1415,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
             constexpr uint32_t kPB = pbufs_of(WHICH);
             const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
+            if (kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
             ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
             if (!ok) break;
             tc_fence_after();
@@ -1410,11 +1424,12 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             // this warpgroup's groups of the run: glo + wg, glo + wg + kBwdGroups, ...; the groups of
             // the quarter's last run in this buffer that the new run does not cover are zeroed, split
             // between the warpgroups by group index modulo kBwdGroups
-            const int mine = n > wg ? (n - wg + kBwdGroups - 1) / kBwdGroups : 0;
+            const int mine = kAlt ? n : (n > wg ? (n - wg + kBwdGroups - 1) / kBwdGroups : 0);
             const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
-            const uint32_t nzq = pb == 0 ? nz0 : (pb == 1 ? nz1 : nz2);
-            const uint32_t stale = nzq & ~run & gmask;
-            if (pb == 0) nz0 = run; else if (pb == 1) nz1 = run; else nz2 = run;
+            const uint32_t slot = kAlt ? pb >> 1 : pb;   // this warp's record of the buffer's last run
+            const uint32_t nzq = slot == 0 ? nz0 : (slot == 1 ? nz1 : nz2);
+            const uint32_t stale = nzq & ~run & (kAlt ? 0xffffffffu : gmask);
+            if (slot == 0) nz0 = run; else if (slot == 1) nz1 = run; else nz2 = run;
             if (mine == 0 && stale == 0) {
                 // nothing to write: the score buffer is released at once, but the arrival on the P
                 // operand waits for the products of chunk g - kPB, like every other arrival.  With two
@@ -1438,13 +1453,14 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                 x.l2 = smem_u32(smem + lay.aux(s));
                 x.dl = x.l2 + 4u * static_cast<uint32_t>(pl.NC);
             }
-            if (mine == 0) bwd_groups<WHICH, 0, F16>(x, glo + wg, &bars[kSEmpty + sb], true, lane);
+            const int first = glo + (kAlt ? 0 : wg);   // this warp's first group of the run
+            if (mine == 0) bwd_groups<WHICH, 0, F16>(x, first, &bars[kSEmpty + sb], true, lane);
             for (int k = 0; k < mine; k += 2) {
                 const bool last = k + 2 >= mine;
                 if (k + 1 < mine)
-                    bwd_groups<WHICH, 2, F16>(x, glo + wg + kBwdGroups * k, &bars[kSEmpty + sb], last, lane);
+                    bwd_groups<WHICH, 2, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
                 else
-                    bwd_groups<WHICH, 1, F16>(x, glo + wg + kBwdGroups * k, &bars[kSEmpty + sb], last, lane);
+                    bwd_groups<WHICH, 1, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
             }
             for (uint32_t z = stale; z; z &= z - 1) {
                 zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
@@ -1479,16 +1495,17 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
 template <int D, int WHICH>
 __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     constexpr uint32_t kSoft = 4 * nwg_of(WHICH);
+    constexpr uint32_t kChunkWarps = chunk_warps_of(WHICH);
     for (int i = 0; i < 2; ++i) {
         mbar_init(&bars[kQFull + i], 1);
         mbar_init(&bars[kQEmpty + i], 1);
         mbar_init(&bars[kSFull + i], 1);
-        mbar_init(&bars[kSEmpty + i], kSoft);
+        mbar_init(&bars[kSEmpty + i], kChunkWarps);
         mbar_init(&bars[kOFull + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
         mbar_init(&bars[kOEmpty + i], kSoft);
     }
     for (int i = 0; i < pbufs_of(WHICH); ++i) {
-        mbar_init(&bars[kPFull + i], kSoft);
+        mbar_init(&bars[kPFull + i], kChunkWarps);
         mbar_init(&bars[kPEmpty + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
     for (int s = 0; s < stages_of(WHICH, D); ++s) {
