@@ -1266,7 +1266,8 @@ struct BwdCtx {
     uint32_t tS, tP;     // this warp's lanes of the current score / dP buffers
     uint32_t sP0, sP1;   // P-side operands of the current buffer (dQ: dS; dK/dV: P^T, dS^T)
     uint32_t rowbase, sw;
-    uint32_t l2, dl;     // dK/dV: shared addresses of the chunk columns' -LSE (log2 units) and Delta
+    const float* l2;     // dK/dV: -LSE (log2 units) of the chunk columns
+    const float* dl;     // dK/dV: Delta of the chunk columns
     uint64_t nl2, dl2;   // dQ: -LSE (log2 units) and Delta of this row, packed twice
     uint64_t sl2x2;
 };
@@ -1303,8 +1304,8 @@ __device__ __forceinline__ void bwd_groups(const BwdCtx& x, int g0, uint64_t* se
         for (int e = 0; e < 16; e += 4) {
             uint64_t nlc[2] = {x.nl2, x.nl2}, dlc[2] = {x.dl2, x.dl2};
             if (WHICH == 2) {
-                const float4 lv = ld_shared_f4(x.l2 + 4u * static_cast<uint32_t>(16 * gi + e));
-                const float4 dv = ld_shared_f4(x.dl + 4u * static_cast<uint32_t>(16 * gi + e));
+                const float4 lv = *reinterpret_cast<const float4*>(x.l2 + 16 * gi + e);
+                const float4 dv = *reinterpret_cast<const float4*>(x.dl + 16 * gi + e);
                 nlc[0] = f2(lv.x, lv.y);
                 nlc[1] = f2(lv.z, lv.w);
                 dlc[0] = f2(dv.x, dv.y);
@@ -1391,8 +1392,8 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.rowbase = static_cast<uint32_t>(row) * 64u;
     x.sw = (static_cast<uint32_t>(row) >> 1) & 3u;
     x.sl2x2 = f2(p.scale_log2, p.scale_log2);
-    x.l2 = 0u;
-    x.dl = 0u;
+    x.l2 = nullptr;
+    x.dl = nullptr;
     uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0, nz2 = nz0;  // groups of the quarter's rows that may be nonzero
     BwdEpilogue ep{false, false, 0, 0, 0};
     TileIter it = tile_iter_begin(p);
@@ -1450,8 +1451,8 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             x.sP0 = smem_u32(smem + lay.p(pb, 0));
             x.sP1 = smem_u32(smem + lay.p(pb, 1));
             if (WHICH == 2) {
-                x.l2 = smem_u32(smem + lay.aux(s));
-                x.dl = x.l2 + 4u * static_cast<uint32_t>(pl.NC);
+                x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
+                x.dl = x.l2 + pl.NC;
             }
             const int first = glo + (kAlt ? 0 : wg);   // this warp's first group of the run
             if (mine == 0) bwd_groups<WHICH, 0, F16>(x, first, &bars[kSEmpty + sb], true, lane);
@@ -1488,8 +1489,11 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
 // Kernels
 // ---------------------------------------------------------------------------------------------
 
+// The dynamic shared base rounded up to 1024 bytes, as an offset from the __shared__ array itself, so
+// that pointers derived from it keep the shared address space (a round trip through an integer would
+// make every access through them a generic one).
 __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
-    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
 }
 
 template <int D, int WHICH>
