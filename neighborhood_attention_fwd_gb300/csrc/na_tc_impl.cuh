@@ -47,6 +47,10 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
 constexpr int kMaxStages = 4;
+// Decoded tile records in flight: the producer decodes every tile once and publishes it; the other
+// roles read it instead of decoding it themselves (a decode costs a warp hundreds of cycles, and at a
+// tile boundary it sits on the critical path of the MMA issuers and the softmax warps).
+constexpr uint32_t kTileRing = 4;
 
 // Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
 // the copy latency.  dQ has the shared memory for a fourth chunk stage and a third P buffer (more
@@ -140,6 +144,7 @@ struct TcLayout {
     uint32_t p0, p_buf, p_op;              // P / dS operands
     uint32_t abias, bbias, bgroup;         // window-bias operands; bgroup = bytes of one B group
     uint32_t aux0, aux_slot;               // dK/dV: per chunk slot -LSE (log2) and Delta
+    uint32_t tinfo;                        // ring of decoded tile records (kTileRing x 128 bytes)
     uint32_t bars, total;
     __host__ __device__ uint32_t tile(uint32_t slot, uint32_t t) const { return tile0 + slot * tile_slot + t * tile_t; }
     __host__ __device__ uint32_t chunk(uint32_t slot, uint32_t t) const {
@@ -179,6 +184,8 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     L.aux0 = o;
     L.aux_slot = which == 2 ? align_up(8u * static_cast<uint32_t>(pl.NC), 128) : 0u;
     o += align_up(stages_of(which, D) * L.aux_slot, 1024);
+    L.tinfo = o;
+    o += kTileRing * 128u;
     L.bars = o;
     o += 512;
     L.total = o;
@@ -189,8 +196,8 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
 enum Bar {
     kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kMaxStages, kSFull = 4 + 2 * kMaxStages,
     kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + kMaxPBufs, kOFull = kPEmpty + kMaxPBufs,
-    kOEmpty = kOFull + 2,
-    kFin = kOEmpty + 2, kNumBars = kFin + 1
+    kOEmpty = kOFull + 2, kTFull = kOEmpty + 2, kTEmpty = kTFull + kTileRing,
+    kFin = kTEmpty + kTileRing, kNumBars = kFin + 1
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -229,7 +236,7 @@ __device__ __forceinline__ void tile_iter_next(const TcParams& p, TileIter& it) 
 }
 
 // Per-tile decode of (head, tile, residue class, batch) and the halo it needs.
-struct Cta {
+struct alignas(16) Cta {
     int h, b;
     int cls[3], Lc[3], t0[3], h0[3];
     int nc[3], C;  // chunks actually needed along each axis, and in total
@@ -436,6 +443,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     return __all_sync(0xffffffffu, ok);
 }
 
+// Tile record j of this CTA from the producer's ring.  `warp`: the whole warp waits and reads (lane 0
+// releases the slot), else a single lane does.  Returns false after the last tile, or when a wait
+// gives up (then `ok` is false).
+__device__ __forceinline__ bool fetch_tile(uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t j,
+                                           const WaitGuard& err, bool warp, Cta& c, bool& ok) {
+    const uint32_t ts = j % kTileRing, par = (j / kTileRing) & 1u;
+    ok = warp ? warp_wait(&bars[kTFull + ts], par, err, kSiteQ) : mbar_wait(&bars[kTFull + ts], par, err, kSiteQ);
+    if (!ok) return false;
+    c = *reinterpret_cast<const Cta*>(smem + lay.tinfo + ts * 128u);
+    if (warp) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[kTEmpty + ts]);
+    } else {
+        mbar_arrive(&bars[kTEmpty + ts]);
+    }
+    return c.C > 0;
+}
+
 // Byte offset of block i (columns 8i .. 8i+7) of this row in a K-major operand stored as 32-column
 // atoms (128 rows x 64 B, 64-byte swizzle): rowbase = row * 64, sw = (row >> 1) & 3.
 __device__ __forceinline__ uint32_t p_off(uint32_t rowbase, uint32_t sw, int i) {
@@ -590,6 +615,25 @@ __device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const
     }
 }
 
+// Publish tile record j (c), or the end record (c == nullptr), once every reader of record
+// j - kTileRing has released its slot.
+__device__ __forceinline__ bool publish_tile(uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t j,
+                                             const WaitGuard& err, int lane, const Cta* c) {
+    const uint32_t ts = j % kTileRing;
+    if (j >= kTileRing && !warp_wait(&bars[kTEmpty + ts], ((j / kTileRing) - 1) & 1u, err, kSiteQ)) return false;
+    if (lane == 0) {
+        Cta* dst = reinterpret_cast<Cta*>(smem + lay.tinfo + ts * 128u);
+        if (c) {
+            *dst = *c;
+        } else {
+            dst->C = 0;
+        }
+        mbar_arrive(&bars[kTFull + ts]);
+    }
+    __syncwarp();
+    return true;
+}
+
 template <int D, int WHICH>
 __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars) {
     constexpr int kS = stages_of(WHICH, D);
@@ -626,6 +670,7 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
     uint32_t j = 0, g = 0;
     bool ok = true;
     while (ok && next_tile(p, WHICH, it, started, c)) {
+        if (!(ok = publish_tile(smem, lay, bars, j, err, lane, &c))) break;
         const uint32_t qs = j % kTS;
         if (j >= kTS) ok = warp_wait(&bars[kQEmpty + qs], ((j / kTS) - 1) & 1, err, kSiteQ);
         if (!ok) break;
@@ -698,6 +743,7 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
         }
         ++j;
     }
+    if (ok) publish_tile(smem, lay, bars, j, err, lane, nullptr);
     // Copies already issued must land before the CTA exits and its shared memory is reused (after an
     // error the consumers stop early): wait for the last fill of every chunk slot and tile slot.
     if (lane == 0) {
@@ -844,10 +890,9 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
     const bool neg = p.neg != 0;
-    TileIter it = tile_iter_begin(p);
-    bool started = false;
     Cta c;
-    bool have = next_tile(p, WHICH, it, started, c);
+    bool have = false, need = true;  // need: the next tile record has not been read yet
+    uint32_t jt = 0;                 // tile records read
     uint32_t jS = 0, gS = 0;
     int ciS = 0;
     bool qready = false;
@@ -858,6 +903,17 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
     uint32_t idle = 0;
     for (;;) {
         bool progress = false;
+        if (need) {
+            const uint32_t ts = jt % kTileRing;
+            if (mbar_test(&bars[kTFull + ts], (jt / kTileRing) & 1u)) {
+                c = *reinterpret_cast<const Cta*>(smem + lay.tinfo + ts * 128u);
+                mbar_arrive(&bars[kTEmpty + ts]);
+                ++jt;
+                need = false;
+                have = c.C > 0;
+                progress = true;
+            }
+        }
         if (nq > 0) {
             const uint32_t pb = q0.g % kPB, ob = q0.j & 1;
             if (mbar_test(&bars[kPFull + pb], (q0.g / kPB) & 1) &&
@@ -896,14 +952,15 @@ __device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, 
                     ++jS;
                     qready = false;
                     cur = cursor_begin();
-                    have = next_tile(p, WHICH, it, started, c);
+                    have = false;
+                    need = true;
                 } else {
                     cursor_next(pl, c, cur);
                 }
                 progress = true;
             }
         }
-        if (!have && nq == 0) break;
+        if (!have && !need && nq == 0) break;  // the end record was read and every update issued
         if (progress) {
             idle = 0;
             continue;
@@ -931,13 +988,11 @@ __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
     const bool neg = p.neg != 0;
-    TileIter it = tile_iter_begin(p);
-    bool started = false;
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
     constexpr uint32_t kTS = tslots_of(WHICH, D);
-    while (ok && next_tile(p, WHICH, it, started, c)) {
+    while (ok && fetch_tile(smem, lay, bars, j, err, false, c, ok)) {
         const uint32_t qs = j % kTS;
         if (!mbar_wait(&bars[kQFull + qs], (j / kTS) & 1, err, kSiteQ)) break;
         ChunkCursor cur = cursor_begin();
@@ -970,8 +1025,6 @@ __device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& la
     const WaitGuard err{p.err, p.wait_ns};
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
-    TileIter it = tile_iter_begin(p);
-    bool started = false;
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
@@ -979,7 +1032,7 @@ __device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& la
     const uint32_t op_b = WHICH == 1 ? 0u : (u == 0 ? 1u : 0u);                    // K; dO or Q
     const uint32_t acc_off = WHICH == 2 && u == 1 ? static_cast<uint32_t>(D) : 0u;  // dK beside dV
     constexpr uint32_t kAB = abufs_of(WHICH, D);
-    while (ok && next_tile(p, WHICH, it, started, c)) {
+    while (ok && fetch_tile(smem, lay, bars, j, err, false, c, ok)) {
         const uint32_t ob = j % kAB;
         const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + acc_off;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
@@ -1223,12 +1276,10 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2x2 = f2(x.sl2, x.sl2);
     x.lane = lane;
     FwdEpilogue ep{false, false, 0.f, 0.f, 0, 0, 0};
-    TileIter it = tile_iter_begin(p);
-    bool started = false;
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && next_tile(p, 0, it, started, c)) {
+    while (ok && fetch_tile(smem, lay, bars, j, x.err, true, c, ok)) {
         const RowGeom geo = row_geom(p, 0, c, row);
         const WarpUnion wu = warp_union(geo);
         const uint32_t ob = j & 1;
@@ -1396,12 +1447,10 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.dl = nullptr;
     uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0, nz2 = nz0;  // groups of the quarter's rows that may be nonzero
     BwdEpilogue ep{false, false, 0, 0, 0};
-    TileIter it = tile_iter_begin(p);
-    bool started = false;
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && next_tile(p, WHICH, it, started, c)) {
+    while (ok && fetch_tile(smem, lay, bars, j, err, true, c, ok)) {
         const RowGeom geo = row_geom(p, WHICH, c, row);
         const WarpUnion wu = warp_union(geo);
         const uint32_t ob = j % abufs_of(WHICH, D);
@@ -1515,6 +1564,10 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     for (int s = 0; s < stages_of(WHICH, D); ++s) {
         mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
         mbar_init(&bars[kKVEmpty + s], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
+    }
+    for (uint32_t t = 0; t < kTileRing; ++t) {
+        mbar_init(&bars[kTFull + t], 1);
+        mbar_init(&bars[kTEmpty + t], kSoft + 1 + nupd_of(WHICH));  // softmax warps, score/MMA lane, update lanes
     }
     mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
     fence_barrier_init();
