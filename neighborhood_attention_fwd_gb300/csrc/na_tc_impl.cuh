@@ -52,20 +52,15 @@ constexpr int kMaxStages = 4;
 // tile boundary it sits on the critical path of the MMA issuers and the softmax warps).
 constexpr uint32_t kTileRing = 4;
 
-// Halo chunk ring depth and P operand ring depth.  The chunk ring must cover the P pipeline plus
-// the copy latency.  dQ has the shared memory for a fourth chunk stage and a third P buffer (more
-// slack between unevenly loaded softmax warps).  The forward's two P operands are its two TMEM
-// score buffers (P is written over the scores), and dK/dV (two P operands in shared memory)
-// measured slower with a fourth stage: its per-column LSE/Delta gathers go through L1, which
-// shrinks as shared memory grows.
-__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 1 ? 4 : 3) : 2; }
-// Backward chunk ownership.  dQ: the two warpgroups take alternate chunks (warpgroup w the chunks g
-// with g mod 2 == w), each covering its quarter's whole run, so the per-chunk work of waits, run
-// geometry and hand-offs is paid once per chunk and quarter; chunk g uses P buffer g mod 4, two per
-// warpgroup.  dK/dV: its two P operands per buffer leave shared memory for two buffers only, one per
-// warpgroup would stall on its own updates, so both warpgroups share every chunk's groups (measured at
-// 2D 1024^2 / 9x9: dQ 1.75 -> 1.61 ms alternating; dK/dV 2.37 -> 2.58 ms).
-__host__ __device__ constexpr bool alt_of(int which) { return which == 1; }
+// Halo chunk ring depth.  The chunk ring must cover the P pipeline plus the copy latency: four
+// stages for the backward at D <= 32 (a third for the forward, whose two P operands are its two TMEM
+// score buffers: P is written over the scores), two at D >= 64.
+__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 0 ? 3 : 4) : 2; }
+// Backward chunk ownership: the two warpgroups take alternate chunks (warpgroup w the chunks g with
+// g mod 2 == w), each covering its quarter's whole run, so the per-chunk work of waits, run geometry
+// and hand-offs is paid once per chunk and quarter.  Chunk g uses P buffer g mod pbufs: dQ two per
+// warpgroup, dK/dV (two P operands per buffer) one per warpgroup.
+__host__ __device__ constexpr bool alt_of(int which) { return which != 0; }
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 4 : 2; }
 // D = 128: every tensor of D channels is held as two halves of 64 channels (128-byte rows, the
 // 128-byte swizzle's width), each laid out exactly like a D = 64 operand; the products over D run
