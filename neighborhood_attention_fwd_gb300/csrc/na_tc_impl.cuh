@@ -46,16 +46,17 @@ namespace {
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale running max until it is 2^8 off
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 5;
 // Decoded tile records in flight: the producer decodes every tile once and publishes it; the other
 // roles read it instead of decoding it themselves (a decode costs a warp hundreds of cycles, and at a
 // tile boundary it sits on the critical path of the MMA issuers and the softmax warps).
 constexpr uint32_t kTileRing = 4;
 
-// Halo chunk ring depth.  The chunk ring must cover the P pipeline plus the copy latency: four
-// stages for the backward at D <= 32 (a third for the forward, whose two P operands are its two TMEM
-// score buffers: P is written over the scores), two at D >= 64.
-__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 0 ? 3 : 4) : 2; }
+// Halo chunk ring depth.  The chunk ring must cover the P pipeline plus the copy latency: at
+// D <= 32 five stages for dQ, four for dK/dV (two P operands per chunk) and three for the forward,
+// whose two P operands are its two TMEM score buffers (P is written over the scores); two at
+// D >= 64.  (A fourth forward stage measured the same; a fifth dQ stage: 3D 16x256^2 dQ 2.19 -> 2.09 ms.)
+__host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ? (which == 0 ? 3 : (which == 1 ? 5 : 4)) : 2; }
 // Backward chunk ownership: the two warpgroups take alternate chunks (warpgroup w the chunks g with
 // g mod 2 == w), each covering its quarter's whole run, so the per-chunk work of waits, run geometry
 // and hand-offs is paid once per chunk and quarter.  Chunk g uses P buffer g mod pbufs: dQ two per
