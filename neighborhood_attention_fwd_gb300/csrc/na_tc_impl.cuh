@@ -586,28 +586,54 @@ __device__ void build_bias_a(const TcParams& p, int which, const Cta& c, const B
 // per-column LSE / Delta of each chunk.
 // ---------------------------------------------------------------------------------------------
 
-// dK/dV: LSE and Delta of the chunk columns lane + 32 i.  The loads read clamped (always valid)
-// positions and nothing consumes them until the chunk's slot is written, so their latency hides
-// behind the producer's next waits; `in` marks the columns inside the class.
+// dK/dV: LSE and Delta of the chunk columns lane + 32 i, loaded into registers one chunk before the
+// producer writes them into the chunk's slot (across tile boundaries too: the next tile is decoded
+// while the current one's last chunk is in flight), so their latency hides behind its waits.
+// Column i's element offset from the chunk origin is fixed for the launch (ce); a chunk adds its
+// origin and a tile its halo origin and head.  `in` marks the columns inside the class; the others
+// load nothing.
 struct AuxFetch {
-    int loc[4][3];
+    long long ce[4];   // element offset of column lane + 32 i from the chunk origin
+    long long ax[3];   // element step of one class position along each axis
+    int loc[4][3];     // local coordinates of column lane + 32 i
     float l[4], dl[4];
     uint32_t in;
 };
 
-__device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, const ChunkCursor& k, AuxFetch& f,
-                                          int lane) {
+__device__ __forceinline__ void aux_init(const TcParams& p, AuxFetch& f, int lane) {
+    const TilePlan& pl = p.plan;
+    const long long st[3] = {static_cast<long long>(p.L[1]) * p.L[2], p.L[2], 1};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) f.ax[a] = st[a] * p.d[a] * p.heads;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int cc = min(lane + 32 * i, pl.NC - 1);
+        f.loc[i][0] = cc / (pl.G[2] * pl.G[1]);
+        f.loc[i][1] = (cc / pl.G[2]) % pl.G[1];
+        f.loc[i][2] = cc % pl.G[2];
+        f.ce[i] = f.loc[i][0] * f.ax[0] + f.loc[i][1] * f.ax[1] + f.loc[i][2] * f.ax[2];
+    }
+}
+
+// Element index of the tile's halo origin (head c.h).
+__device__ __forceinline__ long long aux_tile_base(const TcParams& p, const Cta& c) {
+    return (((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * c.h0[0])) * p.L[1] +
+             (c.cls[1] + p.d[1] * c.h0[1])) * p.L[2] + (c.cls[2] + p.d[2] * c.h0[2])) * p.heads + c.h;
+}
+
+__device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, long long tb, const ChunkCursor& k,
+                                          AuxFetch& f, int lane) {
+    const long long e0 = tb + k.o[0] * f.ax[0] + k.o[1] * f.ax[1] + k.o[2] * f.ax[2];
+    const int lim0 = c.Lc[0] - c.h0[0] - k.o[0], lim1 = c.Lc[1] - c.h0[1] - k.o[1],
+              lim2 = c.Lc[2] - c.h0[2] - k.o[2];
     f.in = 0;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int j0 = c.h0[0] + k.o[0] + f.loc[i][0], j1 = c.h0[1] + k.o[1] + f.loc[i][1],
-                  j2 = c.h0[2] + k.o[2] + f.loc[i][2];
-        if (lane + 32 * i < p.plan.NC && j0 < c.Lc[0] && j1 < c.Lc[1] && j2 < c.Lc[2]) f.in |= 1u << i;
-        const int c0 = min(j0, c.Lc[0] - 1), c1 = min(j1, c.Lc[1] - 1), c2 = min(j2, c.Lc[2] - 1);
-        const long long tok = ((static_cast<long long>(c.b) * p.L[0] + (c.cls[0] + p.d[0] * c0)) * p.L[1] +
-                               (c.cls[1] + p.d[1] * c1)) * p.L[2] + (c.cls[2] + p.d[2] * c2);
-        f.l[i] = __ldg(p.lse + tok * p.heads + c.h);
-        f.dl[i] = __ldg(p.delta + tok * p.heads + c.h);
+        if (lane + 32 * i < p.plan.NC && f.loc[i][0] < lim0 && f.loc[i][1] < lim1 && f.loc[i][2] < lim2) {
+            f.in |= 1u << i;
+            f.l[i] = __ldg(p.lse + e0 + f.ce[i]);
+            f.dl[i] = __ldg(p.delta + e0 + f.ce[i]);
+        }
     }
 }
 
@@ -649,23 +675,17 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
     uint32_t built = 0;  // axes whose part of A holds the geometry of sig[]
     uint64_t sig[3] = {0, 0, 0};
     AuxFetch f;
-    if (WHICH == 2) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int col = lane + 32 * i;
-            const int cc = min(col, pl.NC - 1);
-            f.loc[i][0] = cc / (pl.G[2] * pl.G[1]);
-            f.loc[i][1] = (cc / pl.G[2]) % pl.G[1];
-            f.loc[i][2] = cc % pl.G[2];
-        }
-    }
+    if (WHICH == 2) aux_init(p, f, lane);
 
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
+    bool pre = false;       // dK/dV: c already holds the next tile and f its first chunk's LSE / Delta
+    long long tb = 0;       // dK/dV: element index of the tile's halo origin
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && next_tile(p, WHICH, it, started, c)) {
+    while (ok) {
+        if (!pre && !next_tile(p, WHICH, it, started, c)) break;
         if (!(ok = publish_tile(smem, lay, bars, j, err, lane, &c))) break;
         const uint32_t qs = j % kTS;
         if (j >= kTS) ok = warp_wait(&bars[kQEmpty + qs], ((j / kTS) - 1) & 1, err, kSiteQ);
@@ -699,7 +719,11 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
                                 c.cls[0] + p.d[0] * c.t0[0], c.b);
         }
         ChunkCursor cur = cursor_begin();
-        if (WHICH == 2) aux_fetch(p, c, cur, f, lane);
+        if (WHICH == 2 && !pre) {
+            tb = aux_tile_base(p, c);
+            aux_fetch(p, c, tb, cur, f, lane);
+        }
+        pre = false;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
             const uint32_t s = g % kS;
             if (g >= kS) ok = warp_wait(&bars[kKVEmpty + s], ((g / kS) - 1) & 1, err, kSiteEmpty);
@@ -733,11 +757,20 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
                 }
             }
             cursor_next(pl, c, cur);
-            if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, cur, f, lane);  // the next chunk's, in flight
+            if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, tb, cur, f, lane);  // the next chunk's, in flight
             __syncwarp();
             if (lane == 0 && !withheld) mbar_arrive(&bars[kKVFull + s]);
         }
+        if (!ok) break;
         ++j;
+        if constexpr (WHICH == 2) {
+            // the next tile, decoded now so that its first chunk's LSE / Delta are in flight while
+            // this tile's last chunk is consumed
+            if (!next_tile(p, WHICH, it, started, c)) break;
+            tb = aux_tile_base(p, c);
+            aux_fetch(p, c, tb, cursor_begin(), f, lane);
+            pre = true;
+        }
     }
     if (ok) publish_tile(smem, lay, bars, j, err, lane, nullptr);
     // Copies already issued must land before the CTA exits and its shared memory is reused (after an
