@@ -103,22 +103,26 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, unsig
     return true;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up (returns false, records the
-// site in the status word) after the guard's limit, or as soon as another CTA has recorded an error.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
-    // a phase that is already complete costs one test (~15 cycles; a try_wait with a suspend hint
-    // costs ~50 even then)
-    if (mbar_test(bar, parity)) return true;
-    if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
+// The blocking part of a wait, once a test found the phase incomplete: sleeps in try_wait until the
+// phase completes; gives up (returns false) after the guard's limit or as soon as any CTA has
+// recorded an error, recording this site unless an error is recorded already.  It is inlined at
+// every wait, so it is kept to one loop: the kernels' hot code has to stay small for the
+// instruction cache.
+__device__ __forceinline__ bool mbar_block(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
     const unsigned long long t0 = globaltimer();
-    for (;;) {
-        if (mbar_try_wait(bar, parity, kSuspendNs)) return true;
-        if (ld_volatile(err.word) != 0u) return false;
-        if (globaltimer() - t0 > err.limit_ns) {
+    while (!mbar_try_wait(bar, parity, kSuspendNs)) {
+        if (ld_volatile(err.word) != 0u || globaltimer() - t0 > err.limit_ns) {
             record_error(err.word, site);
             return false;
         }
     }
+    return true;
+}
+
+// Wait for the phase with the given parity to complete.  A phase that is already complete costs one
+// test (~15 cycles; a try_wait with a suspend hint costs ~50 even then).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
+    return mbar_test(bar, parity) || mbar_block(bar, parity, err, site);
 }
 
 // Named barrier among the first `nthreads` threads (ids 1..15; 0 is __syncthreads).

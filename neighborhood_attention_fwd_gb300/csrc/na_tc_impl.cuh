@@ -435,7 +435,7 @@ __device__ __forceinline__ void st_row32(uint32_t blk, int r, uint32_t bits, uin
 // Whole-warp wait.  The common case, a phase that is already complete, takes one test and one vote.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
     if (__all_sync(0xffffffffu, mbar_test(bar, parity))) return true;
-    const bool ok = mbar_wait(bar, parity, err, site);
+    const bool ok = mbar_block(bar, parity, err, site);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -1308,34 +1308,41 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && fetch_tile(smem, lay, bars, j, x.err, true, c, ok)) {
-        const RowGeom geo = row_geom(p, 0, c, row);
-        const WarpUnion wu = warp_union(geo);
-        const uint32_t ob = j & 1;
-        x.tO = tmem + tm_acc<D>(0, ob) + lane_base;
-        float m = -INFINITY;
-        uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (independent chains)
-        ChunkCursor cur = cursor_begin();
-        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            ok = warp_wait(&bars[kSFull + (g & 1)], (g >> 1) & 1, x.err, kSiteS);
-            if (!ok) break;
-            tc_fence_after();
-            int glo, n;
-            chunk_range(pl, cur, wu, glo, n);
-            ok = fwd_chunk<D, F16>(x, g, glo, n, m, lsum);
-            if (!ok) break;
-        }
+    for (;;) {
+        // one pass per tile, and one more after the last to store its rows (a single epilogue site)
+        const bool more = fetch_tile(smem, lay, bars, j, x.err, true, c, ok);
         if (!ok) break;
+        FwdEpilogue next{false, false, 0.f, 0.f, 0, 0, 0};
+        if (more) {
+            const RowGeom geo = row_geom(p, 0, c, row);
+            const WarpUnion wu = warp_union(geo);
+            const uint32_t ob = j & 1;
+            x.tO = tmem + tm_acc<D>(0, ob) + lane_base;
+            float m = -INFINITY;
+            uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (independent chains)
+            ChunkCursor cur = cursor_begin();
+            for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+                ok = warp_wait(&bars[kSFull + (g & 1)], (g >> 1) & 1, x.err, kSiteS);
+                if (!ok) break;
+                tc_fence_after();
+                int glo, n;
+                chunk_range(pl, cur, wu, glo, n);
+                ok = fwd_chunk<D, F16>(x, g, glo, n, m, lsum);
+                if (!ok) break;
+            }
+            if (!ok) break;
+            const uint64_t ls = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
+            float la, lb;
+            f2_split(ls, la, lb);
+            next = FwdEpilogue{true, geo.valid, m, la + lb, geo.token * p.heads + c.h, ob, j};
+        }
         // the previous tile's epilogue, deferred until this tile's chunks are done so that a warp
         // does not idle at the end of a tile while the slowest warp finishes it
         if (ep.live && !(ok = fwd_epilogue<D, F16>(p, x, ep, tmem + lane_base))) break;
-        const uint64_t ls = f2_add(f2_add(lsum[0], lsum[1]), f2_add(lsum[2], lsum[3]));
-        float la, lb;
-        f2_split(ls, la, lb);
-        ep = FwdEpilogue{true, geo.valid, m, la + lb, geo.token * p.heads + c.h, ob, j};
+        ep = next;
+        if (!more) break;
         ++j;
     }
-    if (ok && ep.live) fwd_epilogue<D, F16>(p, x, ep, tmem + lane_base);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1479,88 +1486,93 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     Cta c;
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok && fetch_tile(smem, lay, bars, j, err, true, c, ok)) {
-        const RowGeom geo = row_geom(p, WHICH, c, row);
-        const WarpUnion wu = warp_union(geo);
-        const uint32_t ob = j % abufs_of(WHICH, D);
-        float lse2 = 0.f, dlt = 0.f;
-        if (WHICH == 1 && geo.valid) {
-            lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
-            dlt = __ldg(p.delta + geo.token * p.heads + c.h);
-        }
-        x.nl2 = f2(-lse2, -lse2);
-        x.dl2 = f2(dlt, dlt);
-        ChunkCursor cur = cursor_begin();
-        for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            constexpr uint32_t kPB = pbufs_of(WHICH);
-            const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
-            if (kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
-            ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
-            if (!ok) break;
-            tc_fence_after();
-            int glo, n;
-            chunk_range(pl, cur, wu, glo, n);
-            // this warpgroup's groups of the run: glo + wg, glo + wg + kBwdGroups, ...; the groups of
-            // the quarter's last run in this buffer that the new run does not cover are zeroed, split
-            // between the warpgroups by group index modulo kBwdGroups
-            const int mine = kAlt ? n : (n > wg ? (n - wg + kBwdGroups - 1) / kBwdGroups : 0);
-            const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
-            const uint32_t slot = kAlt ? pb >> 1 : pb;   // this warp's record of the buffer's last run
-            const uint32_t nzq = slot == 0 ? nz0 : (slot == 1 ? nz1 : nz2);
-            const uint32_t stale = nzq & ~run & (kAlt ? 0xffffffffu : gmask);
-            if (slot == 0) nz0 = run; else if (slot == 1) nz1 = run; else nz2 = run;
-            if (mine == 0 && stale == 0) {
-                // nothing to write: the score buffer is released at once, but the arrival on the P
-                // operand waits for the products of chunk g - kPB, like every other arrival.  With two
-                // P buffers (dK/dV) an idle warp can otherwise reach chunk g + 2 while a slower warp
-                // still writes chunk g, and its arrival would complete chunk g's phase early.
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
-                if (g >= kPB && !(ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV))) break;
-                if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
-                continue;
-            }
-            if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
-            if (ok && g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
-            if (!ok) break;
-            x.tS = tmem + tm_s(pl, sb) + lane_base;
-            x.tP = tmem + tm_dp(pl, sb) + lane_base;
-            x.sP0 = smem_u32(smem + lay.p(pb, 0));
-            x.sP1 = smem_u32(smem + lay.p(pb, 1));
-            if (WHICH == 2) {
-                x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
-                x.dl = x.l2 + pl.NC;
-            }
-            const int first = glo + (kAlt ? 0 : wg);   // this warp's first group of the run
-            if (mine == 0) bwd_groups<WHICH, 0, F16>(x, first, &bars[kSEmpty + sb], true, lane);
-            for (int k = 0; k < mine; k += 2) {
-                const bool last = k + 2 >= mine;
-                if (k + 1 < mine)
-                    bwd_groups<WHICH, 2, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
-                else
-                    bwd_groups<WHICH, 1, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
-            }
-            for (uint32_t z = stale; z; z &= z - 1) {
-                zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
-                if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, __ffs(z) - 1);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
-        }
+    for (;;) {
+        // one pass per tile, and one more after the last to store its rows: the epilogue has a single
+        // call site (the kernels' hot code has to stay small for the instruction cache)
+        const bool more = fetch_tile(smem, lay, bars, j, err, true, c, ok);
         if (!ok) break;
+        BwdEpilogue next{false, false, 0, 0, 0};
+        if (more) {
+            const RowGeom geo = row_geom(p, WHICH, c, row);
+            const WarpUnion wu = warp_union(geo);
+            const uint32_t ob = j % abufs_of(WHICH, D);
+            float lse2 = 0.f, dlt = 0.f;
+            if (WHICH == 1 && geo.valid) {
+                lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
+                dlt = __ldg(p.delta + geo.token * p.heads + c.h);
+            }
+            x.nl2 = f2(-lse2, -lse2);
+            x.dl2 = f2(dlt, dlt);
+            ChunkCursor cur = cursor_begin();
+            for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+                constexpr uint32_t kPB = pbufs_of(WHICH);
+                const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
+                if (kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
+                ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
+                if (!ok) break;
+                tc_fence_after();
+                int glo, n;
+                chunk_range(pl, cur, wu, glo, n);
+                // this warpgroup's groups of the run: glo + wg, glo + wg + kBwdGroups, ...; the groups of
+                // the quarter's last run in this buffer that the new run does not cover are zeroed, split
+                // between the warpgroups by group index modulo kBwdGroups
+                const int mine = kAlt ? n : (n > wg ? (n - wg + kBwdGroups - 1) / kBwdGroups : 0);
+                const uint32_t run = n > 0 ? run_mask(glo, n) : 0u;
+                const uint32_t slot = kAlt ? pb >> 1 : pb;   // this warp's record of the buffer's last run
+                const uint32_t nzq = slot == 0 ? nz0 : (slot == 1 ? nz1 : nz2);
+                const uint32_t stale = nzq & ~run & (kAlt ? 0xffffffffu : gmask);
+                if (slot == 0) nz0 = run; else if (slot == 1) nz1 = run; else nz2 = run;
+                if (mine == 0 && stale == 0) {
+                    // nothing to write: the score buffer is released at once, but the arrival on the P
+                    // operand waits for the products of chunk g - kPB, like every other arrival.  With two
+                    // P buffers (dK/dV) an idle warp can otherwise reach chunk g + 2 while a slower warp
+                    // still writes chunk g, and its arrival would complete chunk g's phase early.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
+                    if (g >= kPB && !(ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV))) break;
+                    if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
+                    continue;
+                }
+                if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
+                if (ok && g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
+                if (!ok) break;
+                x.tS = tmem + tm_s(pl, sb) + lane_base;
+                x.tP = tmem + tm_dp(pl, sb) + lane_base;
+                x.sP0 = smem_u32(smem + lay.p(pb, 0));
+                x.sP1 = smem_u32(smem + lay.p(pb, 1));
+                if (WHICH == 2) {
+                    x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
+                    x.dl = x.l2 + pl.NC;
+                }
+                const int first = glo + (kAlt ? 0 : wg);   // this warp's first group of the run
+                if (mine == 0) bwd_groups<WHICH, 0, F16>(x, first, &bars[kSEmpty + sb], true, lane);
+                for (int k = 0; k < mine; k += 2) {
+                    const bool last = k + 2 >= mine;
+                    if (k + 1 < mine)
+                        bwd_groups<WHICH, 2, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
+                    else
+                        bwd_groups<WHICH, 1, F16>(x, first + group_stride_of(WHICH) * k, &bars[kSEmpty + sb], last, lane);
+                }
+                for (uint32_t z = stale; z; z &= z - 1) {
+                    zero_group(x.sP0, x.rowbase, x.sw, __ffs(z) - 1);
+                    if (WHICH == 2) zero_group(x.sP1, x.rowbase, x.sw, __ffs(z) - 1);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
+            }
+            if (!ok) break;
+            next = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
+        }
         // the previous tile's epilogue, deferred until this tile's chunks are done; with a single
         // accumulator buffer the next tile's first products wait for it, so it runs at once
+        if (abufs_of(WHICH, D) == 1) ep = next;
         if (ep.live && !(ok = bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane))) break;
-        ep = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
-        if (abufs_of(WHICH, D) == 1) {
-            if (!(ok = bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane))) break;
-            ep.live = false;
-        }
+        ep = abufs_of(WHICH, D) == 1 ? BwdEpilogue{false, false, 0, 0, 0} : next;
+        if (!more) break;
         ++j;
     }
-    if (ok && ep.live) bwd_epilogue<D, WHICH, F16>(p, bars, ep, tmem + lane_base, wg, lane);
 }
 
 // ---------------------------------------------------------------------------------------------
