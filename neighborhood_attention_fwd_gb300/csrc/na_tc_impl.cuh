@@ -131,7 +131,8 @@ __host__ __device__ constexpr float masked_below() { return F16 ? -3.2e4f : -1.0
 //   which 0 (fwd) : tile ring [2] x {Q};     chunk ring [S] x {K, V}   (P is written to TMEM)
 //   which 1 (dQ)  : tile ring [2] x {Q, dO}; chunk ring [S] x {K, V};  dS[2]
 //   which 2 (dKdV): tile ring [2] x {K, V};  chunk ring [S] x {Q, dO}; P^T[2], dS^T[2];
-//                   per chunk slot the -LSE (log2 units) and Delta of the chunk's queries
+//                   per softmax warpgroup two buffers of the -LSE (log2 units) and Delta of the
+//                   queries of its current chunk
 //   all: window-bias operands A (per tile) and B (constant).
 struct TcLayout {
     uint32_t tile0, tile_slot, tile_t;     // tile ring: tile0 + slot * tile_slot + tensor * tile_t
@@ -139,7 +140,7 @@ struct TcLayout {
     uint32_t chunk0, chunk_slot, chunk_t;  // chunk ring
     uint32_t p0, p_buf, p_op;              // P / dS operands
     uint32_t abias, bbias, bgroup;         // window-bias operands; bgroup = bytes of one B group
-    uint32_t aux0, aux_slot;               // dK/dV: per chunk slot -LSE (log2) and Delta
+    uint32_t aux0, aux_slot;               // dK/dV: -LSE (log2) and Delta, buffer 2 wg + b
     uint32_t tinfo;                        // ring of decoded tile records (kTileRing x 128 bytes)
     uint32_t bars, total;
     __host__ __device__ uint32_t tile(uint32_t slot, uint32_t t) const { return tile0 + slot * tile_slot + t * tile_t; }
@@ -179,7 +180,7 @@ __host__ __device__ inline TcLayout tc_layout(int which, const TilePlan& pl, int
     o += align_up(static_cast<uint32_t>(bg.nb) * L.bgroup, 1024);
     L.aux0 = o;
     L.aux_slot = which == 2 ? align_up(8u * static_cast<uint32_t>(pl.NC), 128) : 0u;
-    o += align_up(stages_of(which, D) * L.aux_slot, 1024);
+    o += align_up(2u * kBwdGroups * L.aux_slot, 1024);
     L.tinfo = o;
     o += kTileRing * 128u;
     L.bars = o;
@@ -193,7 +194,7 @@ enum Bar {
     kQFull = 0, kQEmpty = 2, kKVFull = 4, kKVEmpty = 4 + kMaxStages, kSFull = 4 + 2 * kMaxStages,
     kSEmpty = kSFull + 2, kPFull = kSEmpty + 2, kPEmpty = kPFull + kMaxPBufs, kOFull = kPEmpty + kMaxPBufs,
     kOEmpty = kOFull + 2, kTFull = kOEmpty + 2, kTEmpty = kTFull + kTileRing,
-    kFin = kTEmpty + kTileRing, kNumBars = kFin + 1
+    kFin = kTEmpty + kTileRing, kAuxSync = kFin + 1, kNumBars = kAuxSync + kBwdGroups
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -586,33 +587,30 @@ __device__ void build_bias_a(const TcParams& p, int which, const Cta& c, const B
 // per-column LSE / Delta of each chunk.
 // ---------------------------------------------------------------------------------------------
 
-// dK/dV: LSE and Delta of the chunk columns lane + 32 i, loaded into registers one chunk before the
-// producer writes them into the chunk's slot (across tile boundaries too: the next tile is decoded
-// while the current one's last chunk is in flight), so their latency hides behind its waits.
-// Column i's element offset from the chunk origin is fixed for the launch (ce); a chunk adds its
-// origin and a tile its halo origin and head.  `in` marks the columns inside the class; the others
-// load nothing.
-struct AuxFetch {
-    long long ce[4];   // element offset of column lane + 32 i from the chunk origin
+// dK/dV: the -LSE and Delta of one chunk column (the queries of a chunk are its columns).  The
+// softmax warpgroup that owns a chunk loads them, one column per thread (column 32 wq + lane), and
+// shares them through shared memory.  Column t's element offset from the chunk origin is fixed for
+// the launch (ce); a chunk adds its origin and a tile its halo origin and head.
+struct AuxCol {
+    long long ce;      // element offset of the column from the chunk origin
     long long ax[3];   // element step of one class position along each axis
-    int loc[4][3];     // local coordinates of column lane + 32 i
-    float l[4], dl[4];
-    uint32_t in;
+    int loc[3];        // local coordinates of the column in the chunk
+    bool col;          // t < NC
+    float l, dl;       // loaded values (valid when `in`)
+    bool in;           // the column is inside the class
 };
 
-__device__ __forceinline__ void aux_init(const TcParams& p, AuxFetch& f, int lane) {
+__device__ __forceinline__ void aux_init(const TcParams& p, AuxCol& a, int t) {
     const TilePlan& pl = p.plan;
     const long long st[3] = {static_cast<long long>(p.L[1]) * p.L[2], p.L[2], 1};
 #pragma unroll
-    for (int a = 0; a < 3; ++a) f.ax[a] = st[a] * p.d[a] * p.heads;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int cc = min(lane + 32 * i, pl.NC - 1);
-        f.loc[i][0] = cc / (pl.G[2] * pl.G[1]);
-        f.loc[i][1] = (cc / pl.G[2]) % pl.G[1];
-        f.loc[i][2] = cc % pl.G[2];
-        f.ce[i] = f.loc[i][0] * f.ax[0] + f.loc[i][1] * f.ax[1] + f.loc[i][2] * f.ax[2];
-    }
+    for (int i = 0; i < 3; ++i) a.ax[i] = st[i] * p.d[i] * p.heads;
+    a.col = t < pl.NC;
+    const int cc = min(t, pl.NC - 1);
+    a.loc[0] = cc / (pl.G[2] * pl.G[1]);
+    a.loc[1] = (cc / pl.G[2]) % pl.G[1];
+    a.loc[2] = cc % pl.G[2];
+    a.ce = a.loc[0] * a.ax[0] + a.loc[1] * a.ax[1] + a.loc[2] * a.ax[2];
 }
 
 // Element index of the tile's halo origin (head c.h).
@@ -621,19 +619,15 @@ __device__ __forceinline__ long long aux_tile_base(const TcParams& p, const Cta&
              (c.cls[1] + p.d[1] * c.h0[1])) * p.L[2] + (c.cls[2] + p.d[2] * c.h0[2])) * p.heads + c.h;
 }
 
-__device__ __forceinline__ void aux_fetch(const TcParams& p, const Cta& c, long long tb, const ChunkCursor& k,
-                                          AuxFetch& f, int lane) {
-    const long long e0 = tb + k.o[0] * f.ax[0] + k.o[1] * f.ax[1] + k.o[2] * f.ax[2];
-    const int lim0 = c.Lc[0] - c.h0[0] - k.o[0], lim1 = c.Lc[1] - c.h0[1] - k.o[1],
-              lim2 = c.Lc[2] - c.h0[2] - k.o[2];
-    f.in = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (lane + 32 * i < p.plan.NC && f.loc[i][0] < lim0 && f.loc[i][1] < lim1 && f.loc[i][2] < lim2) {
-            f.in |= 1u << i;
-            f.l[i] = __ldg(p.lse + e0 + f.ce[i]);
-            f.dl[i] = __ldg(p.delta + e0 + f.ce[i]);
-        }
+// Issue the loads of the column's LSE and Delta for the chunk at cursor k of tile c (base tb).
+__device__ __forceinline__ void aux_load(const TcParams& p, const Cta& c, long long tb, const ChunkCursor& k,
+                                         AuxCol& a) {
+    a.in = a.col && a.loc[0] < c.Lc[0] - c.h0[0] - k.o[0] && a.loc[1] < c.Lc[1] - c.h0[1] - k.o[1] &&
+           a.loc[2] < c.Lc[2] - c.h0[2] - k.o[2];
+    if (a.in) {
+        const long long e = tb + k.o[0] * a.ax[0] + k.o[1] * a.ax[1] + k.o[2] * a.ax[2] + a.ce;
+        a.l = __ldg(p.lse + e);
+        a.dl = __ldg(p.delta + e);
     }
 }
 
@@ -674,18 +668,12 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
     fence_proxy_async_smem();
     uint32_t built = 0;  // axes whose part of A holds the geometry of sig[]
     uint64_t sig[3] = {0, 0, 0};
-    AuxFetch f;
-    if (WHICH == 2) aux_init(p, f, lane);
-
     TileIter it = tile_iter_begin(p);
     bool started = false;
     Cta c;
-    bool pre = false;       // dK/dV: c already holds the next tile and f its first chunk's LSE / Delta
-    long long tb = 0;       // dK/dV: element index of the tile's halo origin
     uint32_t j = 0, g = 0;
     bool ok = true;
-    while (ok) {
-        if (!pre && !next_tile(p, WHICH, it, started, c)) break;
+    while (ok && next_tile(p, WHICH, it, started, c)) {
         if (!(ok = publish_tile(smem, lay, bars, j, err, lane, &c))) break;
         const uint32_t qs = j % kTS;
         if (j >= kTS) ok = warp_wait(&bars[kQEmpty + qs], ((j / kTS) - 1) & 1, err, kSiteQ);
@@ -719,11 +707,6 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
                                 c.cls[0] + p.d[0] * c.t0[0], c.b);
         }
         ChunkCursor cur = cursor_begin();
-        if (WHICH == 2 && !pre) {
-            tb = aux_tile_base(p, c);
-            aux_fetch(p, c, tb, cur, f, lane);
-        }
-        pre = false;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
             const uint32_t s = g % kS;
             if (g >= kS) ok = warp_wait(&bars[kKVEmpty + s], ((g / kS) - 1) & 1, err, kSiteEmpty);
@@ -744,33 +727,9 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
                                 c.cls[0] + p.d[0] * y0, c.b);
                 }
             }
-            if (WHICH == 2) {
-                const uint32_t l2 = smem_u32(smem + lay.aux(s)), dl = l2 + 4u * static_cast<uint32_t>(pl.NC);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int col = lane + 32 * i;
-                    if (col < pl.NC) {
-                        const bool in = (f.in >> i) & 1u;
-                        st_shared_f32(l2 + 4u * col, in ? -f.l[i] * kLog2e : -INFINITY);  // -LSE, log2 units; none outside
-                        st_shared_f32(dl + 4u * col, in ? f.dl[i] : 0.f);
-                    }
-                }
-            }
             cursor_next(pl, c, cur);
-            if (WHICH == 2 && ci + 1 < c.C) aux_fetch(p, c, tb, cur, f, lane);  // the next chunk's, in flight
-            __syncwarp();
-            if (lane == 0 && !withheld) mbar_arrive(&bars[kKVFull + s]);
         }
-        if (!ok) break;
         ++j;
-        if constexpr (WHICH == 2) {
-            // the next tile, decoded now so that its first chunk's LSE / Delta are in flight while
-            // this tile's last chunk is consumed
-            if (!next_tile(p, WHICH, it, started, c)) break;
-            tb = aux_tile_base(p, c);
-            aux_fetch(p, c, tb, cursor_begin(), f, lane);
-            pre = true;
-        }
     }
     if (ok) publish_tile(smem, lay, bars, j, err, lane, nullptr);
     // Copies already issued must land before the CTA exits and its shared memory is reused (after an
@@ -1465,7 +1424,6 @@ __device__ __forceinline__ bool bwd_epilogue(const TcParams& p, uint64_t* bars, 
 template <int D, int WHICH, bool F16>
 __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
                                  uint32_t tmem) {
-    constexpr int kS = stages_of(WHICH, D);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr bool kAlt = alt_of(WHICH);
     const int wq = warp & 3, wg = warp >> 2;  // lane quarter, warpgroup
@@ -1481,6 +1439,13 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
     x.sl2x2 = f2(p.scale_log2, p.scale_log2);
     x.l2 = nullptr;
     x.dl = nullptr;
+    // dK/dV: this thread's column of each chunk its warpgroup owns (loaded while the warp waits for
+    // the chunk's scores, then shared within the warpgroup)
+    static_assert(WHICH != 2 || alt_of(2), "the column exchange assumes alternate chunks");
+    AuxCol ac{};
+    long long tb = 0;
+    bool pre = false;  // ac already holds this chunk's values
+    if (WHICH == 2) aux_init(p, ac, row);
     uint32_t nz0 = run_mask(0, ngroups), nz1 = nz0, nz2 = nz0;  // groups of the quarter's rows that may be nonzero
     BwdEpilogue ep{false, false, 0, 0, 0};
     Cta c;
@@ -1496,6 +1461,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             const RowGeom geo = row_geom(p, WHICH, c, row);
             const WarpUnion wu = warp_union(geo);
             const uint32_t ob = j % abufs_of(WHICH, D);
+            if (WHICH == 2) tb = aux_tile_base(p, c);
             float lse2 = 0.f, dlt = 0.f;
             if (WHICH == 1 && geo.valid) {
                 lse2 = __ldg(p.lse + geo.token * p.heads + c.h) * kLog2e;
@@ -1506,11 +1472,37 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             ChunkCursor cur = cursor_begin();
             for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
                 constexpr uint32_t kPB = pbufs_of(WHICH);
-                const uint32_t sb = g & 1, s = g % kS, pb = g % kPB;
+                const uint32_t sb = g & 1, pb = g % kPB;
                 if (kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
+                // dK/dV: the column's values, unless the previous chunk of the warpgroup prefetched them
+                if (WHICH == 2 && !pre) aux_load(p, c, tb, cur, ac);
                 ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
                 if (!ok) break;
                 tc_fence_after();
+                if (WHICH == 2) {
+                    // the warpgroup's k-th chunk: its columns' -LSE (log2 units; none outside the class)
+                    // and Delta into buffer k mod 2; a buffer is rewritten only after every warp has
+                    // passed the exchange of the chunk in between, so after its last read
+                    const uint32_t k = g >> 1, buf = lay.aux(2u * static_cast<uint32_t>(wg) + (k & 1u));
+                    const uint32_t l2 = smem_u32(smem + buf), dl = l2 + 4u * static_cast<uint32_t>(pl.NC);
+                    if (ac.col) {
+                        st_shared_f32(l2 + 4u * static_cast<uint32_t>(row), ac.in ? -ac.l * kLog2e : -INFINITY);
+                        st_shared_f32(dl + 4u * static_cast<uint32_t>(row), ac.in ? ac.dl : 0.f);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars[kAuxSync + wg]);
+                    x.l2 = reinterpret_cast<const float*>(smem + buf);
+                    // the warpgroup's next chunk of this tile (g + 2): its loads are in flight while this
+                    // chunk is processed
+                    pre = ci + 2 < c.C;
+                    if (pre) {
+                        ChunkCursor nx = cur;
+                        cursor_next(pl, c, nx);
+                        cursor_next(pl, c, nx);
+                        aux_load(p, c, tb, nx, ac);
+                    }
+                    x.dl = x.l2 + pl.NC;
+                }
                 int glo, n;
                 chunk_range(pl, cur, wu, glo, n);
                 // this warpgroup's groups of the run: glo + wg, glo + wg + kBwdGroups, ...; the groups of
@@ -1532,19 +1524,18 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                     if (lane == 0) mbar_arrive(&bars[kSEmpty + sb]);
                     if (g >= kPB && !(ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV))) break;
                     if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
+                    // dK/dV: every warp passes the exchange before it writes the warpgroup's next buffer
+                    if (WHICH == 2 && !(ok = warp_wait(&bars[kAuxSync + wg], (g >> 1) & 1u, err, kSiteKV))) break;
                     continue;
                 }
-                if (WHICH == 2 && mine > 0) ok = warp_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);  // -LSE, Delta
-                if (ok && g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
+                if (g >= kPB) ok = warp_wait(&bars[kPEmpty + pb], ((g / kPB) - 1) & 1, err, kSitePV);
+                // dK/dV: every warp of the warpgroup has written its column of the exchange buffer
+                if (WHICH == 2 && ok) ok = warp_wait(&bars[kAuxSync + wg], (g >> 1) & 1u, err, kSiteKV);
                 if (!ok) break;
                 x.tS = tmem + tm_s(pl, sb) + lane_base;
                 x.tP = tmem + tm_dp(pl, sb) + lane_base;
                 x.sP0 = smem_u32(smem + lay.p(pb, 0));
                 x.sP1 = smem_u32(smem + lay.p(pb, 1));
-                if (WHICH == 2) {
-                    x.l2 = reinterpret_cast<const float*>(smem + lay.aux(s));
-                    x.dl = x.l2 + pl.NC;
-                }
                 const int first = glo + (kAlt ? 0 : wg);   // this warp's first group of the run
                 if (mine == 0) bwd_groups<WHICH, 0, F16>(x, first, &bars[kSEmpty + sb], true, lane);
                 for (int k = 0; k < mine; k += 2) {
@@ -1603,7 +1594,7 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kPEmpty + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
     for (int s = 0; s < stages_of(WHICH, D); ++s) {
-        mbar_init(&bars[kKVFull + s], 2);  // TMA bytes + the producer's arrive (after its aux writes)
+        mbar_init(&bars[kKVFull + s], 1);  // the producer's arrive with the TMA byte count
         mbar_init(&bars[kKVEmpty + s], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
     for (uint32_t t = 0; t < kTileRing; ++t) {
@@ -1611,6 +1602,8 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kTEmpty + t], kSoft + 1 + nupd_of(WHICH));  // softmax warps, score/MMA lane, update lanes
     }
     mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
+    if (WHICH == 2)
+        for (int w = 0; w < kBwdGroups; ++w) mbar_init(&bars[kAuxSync + w], 4);  // the warpgroup's warps
     fence_barrier_init();
 }
 
