@@ -126,6 +126,14 @@ struct UnfParams {
     // 32-bit decodes without division (rows and units < 2^32)
     uint32_t small;
     FastDiv fd_heads, fd_strips2, fd_L[3], fd_d[3], fd_K, fd_k2, fd_k12;
+    // Inverse-window gathers fed by TMA (tma = 1): per query line, the span's source rows (tm_src: the
+    // [B, L.., heads * D] tensor, srows span positions) and each span query's window weights on that line
+    // (tm_w: the [B, L.., heads * K] weights, a box of wb >= k2 + 7 offsets from an aligned start).
+    CUtensorMap tm_src, tm_w;
+    uint32_t tma, wb;
+    uint32_t srows;             // span rows copied per line: the largest span of any strip, rounded up to 16
+    unsigned* err;              // device status word (bounded waits)
+    unsigned long long wait_ns; // time limit of one wait
 };
 
 // Tokens per block of the bias-gradient reduction's first stage, and the size of its partial sums.

@@ -1102,6 +1102,144 @@ __global__ void __launch_bounds__(kMmaThreads) scatter_mma_kernel(const UnfParam
     }
 }
 
+// The same gather fed by TMA (bf16, fp16; D <= 64, tensor maps in p).  Per query line, one lane
+// copies the span's 32 source rows (swizzled as the row width allows) and each span query's window
+// weights on that line (a box of wb offsets from a 16-byte aligned start) into one of three stages
+// of the warp's ring, so the next two lines load while this one's products run; the banded A and
+// ldmatrix.trans B are built from the stage as above (B through the swizzle).  Waits are bounded: on
+// expiry the warp records the site, lets its copies in flight land and stops.
+template <int D>
+struct ScatterTmaLayout {
+    static constexpr int kStages = 3;
+    // span rows (srows, a multiple of 16) of 2 D bytes, each stage from a 1 KB boundary (swizzle atom)
+    __host__ __device__ static uint32_t src_bytes(int srows) { return (srows * 2u * D + 1023u) / 1024u * 1024u; }
+    __host__ __device__ static uint32_t w_bytes(int srows, int wb) { return 2u * srows * static_cast<uint32_t>(wb); }
+    __host__ __device__ static uint32_t warp_bytes(int srows, int wb) {
+        return (kStages * (src_bytes(srows) + w_bytes(srows, wb)) + 8u * kStages + 1023u) / 1024u * 1024u;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMmaThreads) scatter_tma_kernel(const __grid_constant__ UnfParams p) {
+    constexpr bool F16 = !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int NT = D / 8, S = ScatterTmaLayout<D>::kStages;
+    // swizzle of the source rows (2 D bytes each): 16-byte chunk c of row n sits at chunk c ^ ((n >> kSh) & kMask)
+    constexpr int kMask = 2 * D / 16 - 1, kSh = D == 64 ? 0 : (D == 32 ? 1 : 2);
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Strip st;
+    if (!st.init(p, (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5)) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3, warp = threadIdx.x >> 5;
+    const int K = p.K, k2 = p.k[2], d2 = p.d[2], r2 = k2 >> 1, wb = static_cast<int>(p.wb);
+    const int srows = static_cast<int>(p.srows);
+    const uint32_t kSrc = ScatterTmaLayout<D>::src_bytes(srows), wbytes = ScatterTmaLayout<D>::w_bytes(srows, wb);
+    unsigned char* wbase = smem + warp * ScatterTmaLayout<D>::warp_bytes(srows, wb);
+    const uint32_t src0 = smem_u32(wbase);
+    const uint16_t* wst0 = reinterpret_cast<const uint16_t*>(wbase + S * kSrc);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + S * (kSrc + wbytes));
+    const WaitGuard err{p.err, p.wait_ns};
+    // queries of the strip's keys along the innermost axis (class coordinates)
+    const int jl = st.j0 + st.nq - 1, Lc2 = st.Lc2;
+    const int q_lo = st.j0 < k2 ? 0 : st.j0 - r2;
+    const int q_hi = jl >= Lc2 - k2 ? Lc2 - 1 : jl + r2;
+    const int qspan = q_hi - q_lo + 1;  // <= srows, the rows of the box (the host takes the largest span)
+    const int nks = (qspan + 15) >> 4;
+    int cl[2], jk[2], Lc[2], lo[2], hi[2];
+    const int xo[2] = {st.x0, st.x1};
+    for (int a = 0; a < 2; ++a) {
+        const int d = p.d[a], k = p.k[a];
+        jk[a] = cidx(p, a, xo[a]);
+        cl[a] = xo[a] - jk[a] * d;
+        Lc[a] = clen(p, a, cl[a]);
+        lo[a] = jk[a] < k ? 0 : jk[a] - (k >> 1);
+        hi[a] = jk[a] >= Lc[a] - k ? Lc[a] - 1 : jk[a] + (k >> 1);
+    }
+    const int n1 = hi[1] - lo[1] + 1, nl = (hi[0] - lo[0] + 1) * n1;  // query lines (i0, i1)
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    // weight offset of line li's window line in the row of heads * K weights
+    auto wcol = [&](int li) {
+        const int i0 = lo[0] + li / n1, i1 = lo[1] + li % n1;
+        const int ta0 = jk[0] - win_start(i0, Lc[0], p.k[0]);
+        return st.h * K + (ta0 * p.k[1] + jk[1] - win_start(i1, Lc[1], p.k[1])) * k2;
+    };
+    auto issue = [&](int li) {
+        const int i0 = lo[0] + li / n1, i1 = lo[1] + li % n1, s = li % S;
+        const int x = st.c2 + d2 * q_lo, y = cl[1] + p.d[1] * i1, z = cl[0] + p.d[0] * i0;
+        mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(srows) * 2u * D + wbytes);
+        tma_load_5d(wbase + s * kSrc, &p.tm_src, &bars[s], st.h * D, x, y, z, static_cast<int>(st.b));
+        tma_load_5d(wbase + S * kSrc + s * wbytes, &p.tm_w, &bars[s], wcol(li) & ~7, x, y, z, static_cast<int>(st.b));
+    };
+    if (lane == 0)
+        for (int li = 0; li < S && li < nl; ++li) issue(li);
+    const int jm0 = st.j0 + min(g, st.nq - 1), jm1 = st.j0 + min(g + 8, st.nq - 1);  // this lane's keys
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    int li = 0;
+    bool ok = true;
+    for (; li < nl; ++li) {
+        const int s = li % S;
+        if (!__all_sync(0xffffffffu, mbar_test(&bars[s], (li / S) & 1)) &&
+            !__all_sync(0xffffffffu, mbar_block(&bars[s], (li / S) & 1, err, kSiteKV))) {
+            ok = false;
+            break;
+        }
+        const int wc = wcol(li);
+        const uint16_t* wst = wst0 + s * (wbytes / 2) + (wc & 7);  // query n's weight u at wst[n wb + u]
+        const uint32_t vs = src0 + s * kSrc;
+        for (int ks = 0; ks < nks; ++ks) {
+            // A[m, n]: query n's weight for key m, a[i] = keys g (+8), queries 16 ks + 2 q4 (+8) + {0, 1}
+            uint32_t a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int jm = (i & 1) ? jm1 : jm0;
+                const int n = 16 * ks + 2 * q4 + 8 * (i >> 1);
+                uint16_t e[2];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int nn = n + h2;
+                    const int u = jm - win_start(q_lo + nn, Lc2, k2);
+                    e[h2] = (nn < qspan && u >= 0 && u < k2) ? wst[nn * wb + u] : uint16_t(0);
+                }
+                a[i] = pack_b16(e[0], e[1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt += 2) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int n = 16 * ks + 8 * (mi & 1) + rr, c = nt + (mi >> 1);
+                const uint32_t addr = vs + static_cast<uint32_t>(n * 2 * D + ((c ^ ((n >> kSh) & kMask)) << 4));
+                uint32_t bfr[4];
+                ldmatrix_x4_trans(bfr, addr);
+                mma16816<F16>(acc[nt], a, bfr[0], bfr[1]);
+                mma16816<F16>(acc[nt + 1], a, bfr[2], bfr[3]);
+            }
+        }
+        __syncwarp();  // every lane is done with stage s
+        if (lane == 0 && li + S < nl) issue(li + S);
+    }
+    if (!ok) {
+        // the copies issued for lines li .. min(li + S, nl) - 1 land before the warp's shared memory is left
+        if (lane == 0)
+            for (int l = li; l < nl && l < li + S; ++l) mbar_drain(&bars[l % S], (l / S) & 1, err.limit_ns);
+        __syncwarp();
+        return;
+    }
+    T* out = static_cast<T*>(p.out0);
+    const long long r0 = st.row(p, g), r1 = st.row(p, g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int col = 8 * nt + 2 * q4;
+        if (g < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r0 * D + col) = Elem<T>::pair(acc[nt][0] * p.scale, acc[nt][1] * p.scale);
+        if (g + 8 < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r1 * D + col) = Elem<T>::pair(acc[nt][2] * p.scale, acc[nt][3] * p.scale);
+    }
+}
+
 int launch_blocks(long long threads_needed) { return static_cast<int>((threads_needed + kThreads - 1) / kThreads); }
 
 enum Op { kDot, kWsum, kScatter };
@@ -1157,9 +1295,23 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
         }
         case kScatter: {
             bool done = false;
+            if constexpr (sizeof(T) == 2 && D <= 64) {   // bf16, fp16 fed by TMA (tensor maps set by the host)
+                const size_t smem =
+                    (kMmaThreads / 32) * ScatterTmaLayout<D>::warp_bytes(static_cast<int>(p.srows), static_cast<int>(p.wb)) + 1024;
+                if (p.tma && smem <= 200 * 1024) {
+                    const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                    const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                    const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                    if (smem > 48 * 1024)
+                        cudaFuncSetAttribute(scatter_tma_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+                    scatter_tma_kernel<T, D><<<g2, b2, smem, s>>>(p);
+                    done = true;
+                }
+            }
             if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core gathers over inverse windows
                 const size_t smem = (kMmaThreads / 32) * ScatterLayout<D>::warp_bytes(p.k[2]);
-                if (smem <= 200 * 1024) {
+                if (!done && smem <= 200 * 1024) {
                     const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
                     const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
                     const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);

@@ -31,6 +31,18 @@ CASES = [
     ("fp16", (16, 8), 1, 64, (1, 1), (1, 1), 1),              # k = 1
 ]
 
+# Shapes whose weights rows (heads * K offsets) are a multiple of 16 bytes, the innermost kernel size at
+# most 17 and D at most 64: the inverse-window gathers (dK of na_qk_bwd, dV of na_av_bwd) take their
+# TMA-fed form, with source rows swizzled by 32, 64 or 128 bytes (D = 16, 32, 64).
+CASES_TMA = [
+    ("bf16", (13, 18), 8, 32, (5, 7), (1, 2), 2),
+    ("fp16", (6, 9, 10), 8, 64, (3, 5, 5), (1, 1, 2), 1),
+    ("bf16", (23, 29), 8, 16, (3, 5), (3, 2), 1),            # classes of unequal length
+    ("bf16", (9, 70), 8, 32, (3, 17), (1, 1), 1),            # innermost kernel 17: a 32-query span
+    ("fp16", (100,), 8, 16, (13,), (3,), 2),
+    ("bf16", (5, 7, 9), 8, 64, (5, 7, 9), (1, 1, 1), 1),      # kernel == extent: full attention
+]
+
 
 def _ids(c):
     return f"{c[0]}-{'x'.join(map(str, c[1]))}-h{c[2]}-D{c[3]}-k{'x'.join(map(str, c[4]))}-d{'x'.join(map(str, c[5]))}-B{c[6]}"
@@ -56,7 +68,7 @@ def status_ok(na):
     assert st == 0, f"device status {st} raw {raw:#x}"
 
 
-@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+@pytest.mark.parametrize("case", CASES + CASES_TMA, ids=[_ids(c) for c in CASES + CASES_TMA])
 def test_each_operation_matches_the_oracle(case, cuda_lib):
     na = cuda_lib
     w, t, wt = setup(case)
