@@ -464,52 +464,63 @@ na_status unfused_params(int B, int ndim, const int* spatial, int heads, int D, 
     return NA_OK;
 }
 
-// Tensor maps of the TMA-fed inverse-window gather (na_qk_bwd's dK, na_av_bwd's dV): src is q or dO,
-// w the weights.  Left off (p.tma = 0, the kernel without TMA runs) where TMA cannot describe the
+// Tensor maps of the TMA-fed weighted sums: with `inverse`, the inverse-window gathers (na_qk_bwd's dK,
+// na_av_bwd's dV; src is q or dO), else the window sums (na_av's O, na_qk_bwd's dQ; src is v or k); w
+// the weights.  Left off (p.tma = 0, the kernels without TMA run) where TMA cannot describe the
 // tensors: D > 64 (a source row wider than the 128-byte swizzle), dilation > 8 (the element stride),
 // a weights row of heads * K elements that is not a multiple of 16 bytes, misaligned pointers, or
 // spans longer than 64 positions.
-void unfused_gather_maps(na::UnfParams& p, int B, const void* src, const void* w, na_dtype dtype) {
+void unfused_tma_maps(na::UnfParams& p, int B, const void* src, const void* w, na_dtype dtype, bool inverse) {
     p.tma = 0;
     if (dtype == NA_FP32 || p.D > 64 || (static_cast<long long>(p.heads) * p.K) % 8 != 0) return;
     for (int a = 0; a < 3; ++a)
         if (p.d[a] > 8) return;
-    // rows copied per line: the largest span of queries over every 16-key strip of every class along the
-    // innermost axis (clamped windows at either border widen a strip's span up to about 2 k2 + 14)
+    // source rows copied per line: the largest span over every 16-position strip of every class along the
+    // innermost axis: of the keys in its queries' windows (at most 15 + k2), or of the queries whose
+    // windows hold its keys (clamped windows at either border widen that up to about 2 k2 + 14)
     const int k2 = p.k[2], r2 = k2 / 2;
     int span = 1;
     for (int c = 0; c < p.d[2]; ++c) {
         const int Lc = (p.L[2] - c + p.d[2] - 1) / p.d[2];
         for (int j0 = 0; j0 < Lc; j0 += 16) {
             const int jl = std::min(j0 + 15, Lc - 1);
-            const int lo = j0 < k2 ? 0 : j0 - r2, hi = jl >= Lc - k2 ? Lc - 1 : jl + r2;
+            int lo, hi;
+            if (inverse) {
+                lo = j0 < k2 ? 0 : j0 - r2;
+                hi = jl >= Lc - k2 ? Lc - 1 : jl + r2;
+            } else {
+                lo = std::max(0, std::min(j0 - r2, Lc - k2));
+                hi = std::max(0, std::min(jl - r2, Lc - k2)) + k2 - 1;
+            }
             span = std::max(span, hi - lo + 1);
         }
     }
-    const int srows = (span + 15) / 16 * 16;
+    const int srows = (span + 15) / 16 * 16, wrows = inverse ? srows : 16;
     if (srows > 64 || srows * p.d[2] > 256) return;
     if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(w)) & 15u) return;
     const int wb = (k2 + 7 + 7) / 8 * 8;  // >= k2 + 7 offsets from a 16-byte aligned start
     if (wb > 256 || get_encoder() != NA_OK || status_ptr(&p.err) != NA_OK) return;
     const CUtensorMapDataType ty = dtype == NA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t es = 2;
-    auto enc = [&](CUtensorMap* m, const void* base, cuuint64_t row, cuuint32_t inner, CUtensorMapSwizzle sw) {
+    auto enc = [&](CUtensorMap* m, const void* base, cuuint64_t row, cuuint32_t inner, int rows, CUtensorMapSwizzle sw) {
         cuuint64_t dims[5] = {row, static_cast<cuuint64_t>(p.L[2]), static_cast<cuuint64_t>(p.L[1]),
                               static_cast<cuuint64_t>(p.L[0]), static_cast<cuuint64_t>(B)};
         cuuint64_t strides[4] = {row * es, row * es * p.L[2], row * es * p.L[2] * p.L[1],
                                  row * es * p.L[2] * p.L[1] * p.L[0]};
-        cuuint32_t box[5] = {inner, static_cast<cuuint32_t>(srows * p.d[2]), 1, 1, 1};
+        cuuint32_t box[5] = {inner, static_cast<cuuint32_t>(rows * p.d[2]), 1, 1, 1};
         cuuint32_t estr[5] = {1, static_cast<cuuint32_t>(p.d[2]), 1, 1, 1};
         return g_encode(m, ty, 5, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     };
     const CUtensorMapSwizzle sw = p.D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                             : (p.D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-    if (!enc(&p.tm_src, src, static_cast<cuuint64_t>(p.heads) * p.D, static_cast<cuuint32_t>(p.D), sw)) return;
-    if (!enc(&p.tm_w, w, static_cast<cuuint64_t>(p.heads) * p.K, static_cast<cuuint32_t>(wb), CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!enc(&p.tm_src, src, static_cast<cuuint64_t>(p.heads) * p.D, static_cast<cuuint32_t>(p.D), srows, sw)) return;
+    if (!enc(&p.tm_w, w, static_cast<cuuint64_t>(p.heads) * p.K, static_cast<cuuint32_t>(wb), wrows,
+             CU_TENSOR_MAP_SWIZZLE_NONE))
         return;
     p.wb = static_cast<uint32_t>(wb);
     p.srows = static_cast<uint32_t>(srows);
+    p.wrows = static_cast<uint32_t>(wrows);
     p.wait_ns = g_wait_ns.load();
     p.tma = 1;
 }
@@ -827,6 +838,7 @@ na_status na_av(const void* attn, const void* v, void* o, int B, int ndim, const
     p.a = attn;
     p.b = v;
     p.out0 = o;
+    unfused_tma_maps(p, B, v, attn, dtype, false);
     return cuda_status(na::launch_unfused_av(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
 }
 
@@ -864,10 +876,11 @@ na_status na_qk_bwd(const void* dattn, const void* q, const void* k, void* dq, v
     p.a = dattn;
     p.b = k;
     p.out0 = dq;
+    unfused_tma_maps(p, B, k, dattn, dtype, false);
     if ((st = cuda_status(na::launch_unfused_gather(p, elem_of(dtype), s))) != NA_OK) return st;
     p.b = q;
     p.out0 = dk;
-    unfused_gather_maps(p, B, q, dattn, dtype);
+    unfused_tma_maps(p, B, q, dattn, dtype, true);
     return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
 }
 
@@ -886,7 +899,7 @@ na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn
     p.a = attn;
     p.b = dO;
     p.out0 = dv;
-    unfused_gather_maps(p, B, dO, attn, dtype);
+    unfused_tma_maps(p, B, dO, attn, dtype, true);
     return cuda_status(na::launch_unfused_scatter(p, elem_of(dtype), s));
 }
 

@@ -132,6 +132,7 @@ struct UnfParams {
     CUtensorMap tm_src, tm_w;
     uint32_t tma, wb;
     uint32_t srows;             // span rows copied per line: the largest span of any strip, rounded up to 16
+    uint32_t wrows;             // weight rows copied per line: srows (inverse-window gather) or 16 (weighted sum)
     unsigned* err;              // device status word (bounded waits)
     unsigned long long wait_ns; // time limit of one wait
 };

@@ -990,6 +990,119 @@ __global__ void __launch_bounds__(kMmaThreads) wsum_mma_kernel(const UnfParams p
     }
 }
 
+// The weighted sum fed by TMA (bf16, fp16; D <= 64, tensor maps in p).  Per window line (t0, t1) one
+// lane copies the span's source rows (srows rows, swizzled as the row width allows) and the strip's 16
+// rows of that line's k2 weights (a box of wb offsets from a 16-byte aligned start) into one of three
+// stages of the warp's ring; the banded A and ldmatrix.trans B come from the stage as above.  Rows
+// past the strip's queries or the span's keys hold real data or zeros: their weights are zero or their
+// results are not stored.  Waits are bounded as in the gather below.
+template <int D>
+struct WsumTmaLayout {
+    static constexpr int kStages = 3;
+    __host__ __device__ static uint32_t src_bytes(int srows) { return (srows * 2u * D + 1023u) / 1024u * 1024u; }
+    __host__ __device__ static uint32_t w_bytes(int wb) { return 32u * static_cast<uint32_t>(wb); }
+    __host__ __device__ static uint32_t warp_bytes(int srows, int wb) {
+        return (kStages * (src_bytes(srows) + w_bytes(wb)) + 8u * kStages + 1023u) / 1024u * 1024u;
+    }
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMmaThreads) wsum_tma_kernel(const __grid_constant__ UnfParams p) {
+    constexpr bool F16 = !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int NT = D / 8, S = WsumTmaLayout<D>::kStages;
+    // swizzle of the source rows (2 D bytes each): 16-byte chunk c of row n sits at chunk c ^ ((n >> kSh) & kMask)
+    constexpr int kMask = 2 * D / 16 - 1, kSh = D == 64 ? 0 : (D == 32 ? 1 : 2);
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Strip st;
+    if (!st.init(p, (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5)) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3, warp = threadIdx.x >> 5;
+    const int K = p.K, k2 = p.k[2], d2 = p.d[2], wb = static_cast<int>(p.wb), srows = static_cast<int>(p.srows);
+    const uint32_t kSrc = WsumTmaLayout<D>::src_bytes(srows), wbytes = WsumTmaLayout<D>::w_bytes(wb);
+    unsigned char* wbase = smem + warp * WsumTmaLayout<D>::warp_bytes(srows, wb);
+    const uint32_t src0 = smem_u32(wbase);
+    const uint16_t* wst0 = reinterpret_cast<const uint16_t*>(wbase + S * kSrc);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + S * (kSrc + wbytes));
+    const WaitGuard err{p.err, p.wait_ns};
+    const int om0 = st.off(p, g), om1 = st.off(p, g + 8);
+    const int f0 = first_nb(p, 0, st.x0), f1 = first_nb(p, 1, st.x1);
+    const int nl = p.k[0] * p.k[1];  // window lines (t0, t1)
+    const int nks = (st.span + 15) >> 4;  // k-steps this strip needs (span <= srows)
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    auto issue = [&](int li) {
+        const int t0 = li / p.k[1], t1 = li % p.k[1], s = li % S;
+        const int wc = st.h * K + (t0 * p.k[1] + t1) * k2;
+        mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(srows) * 2u * D + wbytes);
+        tma_load_5d(wbase + s * kSrc, &p.tm_src, &bars[s], st.h * D, st.c2 + d2 * st.ws0, f1 + p.d[1] * t1,
+                    f0 + p.d[0] * t0, static_cast<int>(st.b));
+        tma_load_5d(wbase + S * kSrc + s * wbytes, &p.tm_w, &bars[s], wc & ~7, st.c2 + d2 * st.j0, st.x1, st.x0,
+                    static_cast<int>(st.b));
+    };
+    if (lane == 0)
+        for (int li = 0; li < S && li < nl; ++li) issue(li);
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    int li = 0;
+    bool ok = true;
+    for (; li < nl; ++li) {
+        const int s = li % S;
+        if (!__all_sync(0xffffffffu, mbar_test(&bars[s], (li / S) & 1)) &&
+            !__all_sync(0xffffffffu, mbar_block(&bars[s], (li / S) & 1, err, kSiteKV))) {
+            ok = false;
+            break;
+        }
+        const int wc = st.h * K + li * k2;  // li = t0 k1 + t1: the line's first weight in the row
+        const uint16_t* wst = wst0 + s * (wbytes / 2) + (wc & 7);  // query m's weight u at wst[m wb + u]
+        const uint32_t vs = src0 + s * kSrc;
+        for (int ks = 0; ks < nks; ++ks) {
+            // A: banded weights, a[i] = rows g (+8), span columns 16 ks + 2 q4 (+8) + {0, 1}
+            uint32_t a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int m = g + 8 * (i & 1), om = (i & 1) ? om1 : om0;
+                const int n = 16 * ks + 2 * q4 + 8 * (i >> 1);
+                const int ta = n - om, tb = n + 1 - om;
+                const uint16_t wa = (ta >= 0 && ta < k2) ? wst[m * wb + ta] : uint16_t(0);
+                const uint16_t wbv = (tb >= 0 && tb < k2) ? wst[m * wb + tb] : uint16_t(0);
+                a[i] = pack_b16(wa, wbv);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; nt += 2) {
+                const int mi = lane >> 3, rr = lane & 7;
+                const int n = 16 * ks + 8 * (mi & 1) + rr, c = nt + (mi >> 1);
+                const uint32_t addr = vs + static_cast<uint32_t>(n * 2 * D + ((c ^ ((n >> kSh) & kMask)) << 4));
+                uint32_t bfr[4];
+                ldmatrix_x4_trans(bfr, addr);
+                mma16816<F16>(acc[nt], a, bfr[0], bfr[1]);
+                mma16816<F16>(acc[nt + 1], a, bfr[2], bfr[3]);
+            }
+        }
+        __syncwarp();  // every lane is done with stage s
+        if (lane == 0 && li + S < nl) issue(li + S);
+    }
+    if (!ok) {
+        if (lane == 0)
+            for (int l = li; l < nl && l < li + S; ++l) mbar_drain(&bars[l % S], (l / S) & 1, err.limit_ns);
+        __syncwarp();
+        return;
+    }
+    T* out = static_cast<T*>(p.out0);
+    const long long r0 = st.row(p, g), r1 = st.row(p, g + 8);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int col = 8 * nt + 2 * q4;
+        if (g < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r0 * D + col) = Elem<T>::pair(acc[nt][0] * p.scale, acc[nt][1] * p.scale);
+        if (g + 8 < st.nq)
+            *reinterpret_cast<uint32_t*>(out + r1 * D + col) = Elem<T>::pair(acc[nt][2] * p.scale, acc[nt][3] * p.scale);
+    }
+}
+
 // Tensor-core gathers over inverse windows (bf16, fp16): out_j = scale * sum over the queries i whose
 // windows hold key j of w[i, t(i, j)] src_i, for dK (dattn, q) and dV (attn, dO).  The warp is a
 // 16-key strip.  Its keys share their inverse ranges along the outer axes; along the innermost axis
@@ -1103,7 +1216,7 @@ __global__ void __launch_bounds__(kMmaThreads) scatter_mma_kernel(const UnfParam
 }
 
 // The same gather fed by TMA (bf16, fp16; D <= 64, tensor maps in p).  Per query line, one lane
-// copies the span's 32 source rows (swizzled as the row width allows) and each span query's window
+// copies the span's source rows (srows rows, swizzled as the row width allows) and each span query's window
 // weights on that line (a box of wb offsets from a 16-byte aligned start) into one of three stages
 // of the warp's ring, so the next two lines load while this one's products run; the banded A and
 // ldmatrix.trans B are built from the stage as above (B through the swizzle).  Waits are bounded: on
@@ -1277,9 +1390,23 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
             break;
         case kWsum: {
             bool done = false;
+            if constexpr (sizeof(T) == 2 && D <= 64) {   // bf16, fp16 fed by TMA (tensor maps set by the host)
+                const size_t smem =
+                    (kMmaThreads / 32) * WsumTmaLayout<D>::warp_bytes(static_cast<int>(p.srows), static_cast<int>(p.wb)) + 1024;
+                if (p.tma && smem <= 200 * 1024) {
+                    const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                    const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                    const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                    if (smem > 48 * 1024)
+                        cudaFuncSetAttribute(wsum_tma_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+                    wsum_tma_kernel<T, D><<<g2, b2, smem, s>>>(p);
+                    done = true;
+                }
+            }
             if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core weighted sums
                 const size_t smem = (kMmaThreads / 32) * WsumLayout<D>::warp_bytes(p.K, p.k[2]);
-                if (smem <= 200 * 1024) {
+                if (!done && smem <= 200 * 1024) {
                     const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
                     const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
                     const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
