@@ -472,7 +472,8 @@ na_status unfused_params(int B, int ndim, const int* spatial, int heads, int D, 
 // spans longer than 64 positions.
 void unfused_tma_maps(na::UnfParams& p, int B, const void* src, const void* w, na_dtype dtype, bool inverse) {
     p.tma = 0;
-    if (dtype == NA_FP32 || p.D > 64 || (static_cast<long long>(p.heads) * p.K) % 8 != 0) return;
+    // w null: only the source map (the logits kernels write the weights instead of reading them)
+    if (dtype == NA_FP32 || p.D > 64 || (w && (static_cast<long long>(p.heads) * p.K) % 8 != 0)) return;
     for (int a = 0; a < 3; ++a)
         if (p.d[a] > 8) return;
     // source rows copied per line: the largest span over every 16-position strip of every class along the
@@ -515,8 +516,8 @@ void unfused_tma_maps(na::UnfParams& p, int B, const void* src, const void* w, n
     const CUtensorMapSwizzle sw = p.D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                             : (p.D == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
     if (!enc(&p.tm_src, src, static_cast<cuuint64_t>(p.heads) * p.D, static_cast<cuuint32_t>(p.D), srows, sw)) return;
-    if (!enc(&p.tm_w, w, static_cast<cuuint64_t>(p.heads) * p.K, static_cast<cuuint32_t>(wb), wrows,
-             CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (w && !enc(&p.tm_w, w, static_cast<cuuint64_t>(p.heads) * p.K, static_cast<cuuint32_t>(wb), wrows,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
         return;
     p.wb = static_cast<uint32_t>(wb);
     p.srows = static_cast<uint32_t>(srows);
@@ -826,6 +827,7 @@ na_status na_qk(const void* q, const void* k, const float* rpb, void* attn, int 
     p.b = k;
     p.out0 = attn;
     p.rpb = rpb;
+    unfused_tma_maps(p, B, k, nullptr, dtype, false);
     return cuda_status(na::launch_unfused_qk(p, elem_of(dtype), static_cast<cudaStream_t>(stream)));
 }
 
@@ -895,6 +897,7 @@ na_status na_av_bwd(const void* dO, const void* attn, const void* v, void* dattn
     p.a = dO;
     p.b = v;
     p.out0 = dattn;
+    unfused_tma_maps(p, B, v, nullptr, dtype, false);
     if ((st = cuda_status(na::launch_unfused_dattn(p, elem_of(dtype), s))) != NA_OK) return st;
     p.a = attn;
     p.b = dO;

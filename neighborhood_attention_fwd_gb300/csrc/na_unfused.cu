@@ -896,6 +896,13 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                  : "r"(addr));
 }
 
+// 32-bit shared-memory load (volatile: it must not move above the wait for the copy that fills it)
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ uint32_t pack_b16(uint16_t lo, uint16_t hi) {
     return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
@@ -1100,6 +1107,128 @@ __global__ void __launch_bounds__(kMmaThreads) wsum_tma_kernel(const __grid_cons
             *reinterpret_cast<uint32_t*>(out + r0 * D + col) = Elem<T>::pair(acc[nt][0] * p.scale, acc[nt][1] * p.scale);
         if (g + 8 < st.nq)
             *reinterpret_cast<uint32_t*>(out + r1 * D + col) = Elem<T>::pair(acc[nt][2] * p.scale, acc[nt][3] * p.scale);
+    }
+}
+
+// The logits fed by TMA (bf16, fp16; D <= 64, the key map in p.tm_src): per window line one lane copies
+// the span's key rows (srows rows, swizzled as the row width allows) into one of three stages of the
+// warp's ring; B fragments are read from the stage through the swizzle.  The strip's weights are
+// staged in shared memory ([16][K]) and written row by row at the end.  Waits are bounded.
+template <int D>
+struct DotTmaLayout {
+    static constexpr int kStages = 3;
+    __host__ __device__ static uint32_t src_bytes(int srows) { return (srows * 2u * D + 1023u) / 1024u * 1024u; }
+    __host__ __device__ static uint32_t warp_bytes(int srows, int K, size_t elem) {
+        const uint32_t out = (16u * K * static_cast<uint32_t>(elem) + 15u) / 16u * 16u;
+        return (kStages * src_bytes(srows) + out + 8u * kStages + 1023u) / 1024u * 1024u;
+    }
+};
+
+template <typename T, int D, bool BIAS>
+__global__ void __launch_bounds__(kMmaThreads) dot_tma_kernel(const __grid_constant__ UnfParams p) {
+    using E = Elem<T>;
+    constexpr bool F16 = !std::is_same<T, __nv_bfloat16>::value;
+    constexpr int KS = D / 16, S = DotTmaLayout<D>::kStages;
+    constexpr int kMask = 2 * D / 16 - 1, kSh = D == 64 ? 0 : (D == 32 ? 1 : 2);
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Strip st;
+    if (!st.init(p, (static_cast<long long>(blockIdx.x) * kMmaThreads + threadIdx.x) >> 5)) return;
+    const int lane = threadIdx.x & 31, g = lane >> 2, q4 = lane & 3, warp = threadIdx.x >> 5;
+    const int d2 = p.d[2], k2 = p.k[2], srows = static_cast<int>(p.srows);
+    const uint32_t kSrc = DotTmaLayout<D>::src_bytes(srows);
+    unsigned char* wbase = smem + warp * DotTmaLayout<D>::warp_bytes(srows, p.K, sizeof(T));
+    const uint32_t src0 = smem_u32(wbase);
+    T* stage = reinterpret_cast<T*>(wbase + S * kSrc);   // [16 rows][K]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + DotTmaLayout<D>::warp_bytes(srows, p.K, sizeof(T)) - 8u * S);
+    const WaitGuard err{p.err, p.wait_ns};
+    const int m0 = g, m1 = g + 8;
+    const long long r0 = st.row(p, m0), r1 = st.row(p, m1);
+    const int off0 = st.off(p, m0), off1 = st.off(p, m1);
+    const int jq0 = st.j0 + min(m0, st.nq - 1), jq1 = st.j0 + min(m1, st.nq - 1);
+    uint32_t a[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const int col = 16 * ks + 2 * q4;
+        a[ks][0] = ld32(p.a, r0 * D + col);
+        a[ks][1] = ld32(p.a, r1 * D + col);
+        a[ks][2] = ld32(p.a, r0 * D + col + 8);
+        a[ks][3] = ld32(p.a, r1 * D + col + 8);
+    }
+    const int f0 = first_nb(p, 0, st.x0), f1 = first_nb(p, 1, st.x1);
+    const int S1 = 2 * p.k[1] - 1, S2b = 2 * k2 - 1;
+    const int rb0 = cidx(p, 0, f0) - cidx(p, 0, st.x0) + p.k[0] - 1, rb1 = cidx(p, 1, f1) - cidx(p, 1, st.x1) + p.k[1] - 1;
+    const int rbq0 = st.ws0 + off0 - jq0 + k2 - 1, rbq1 = st.ws0 + off1 - jq1 + k2 - 1;
+    const float* bias = BIAS ? p.rpb + static_cast<long long>(st.h) * (2 * p.k[0] - 1) * S1 * S2b : nullptr;
+    const bool v0 = m0 < st.nq, v1 = m1 < st.nq;
+    const int ntiles = (st.span + 7) >> 3;
+    const int nl = p.k[0] * p.k[1];
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    auto issue = [&](int li) {
+        const int t0 = li / p.k[1], t1 = li % p.k[1], s = li % S;
+        mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(srows) * 2u * D);
+        tma_load_5d(wbase + s * kSrc, &p.tm_src, &bars[s], st.h * D, st.c2 + d2 * st.ws0, f1 + p.d[1] * t1,
+                    f0 + p.d[0] * t0, static_cast<int>(st.b));
+    };
+    if (lane == 0)
+        for (int li = 0; li < S && li < nl; ++li) issue(li);
+    int li = 0;
+    bool ok = true;
+    for (; li < nl; ++li) {
+        const int s = li % S, t0 = li / p.k[1], t1 = li % p.k[1];
+        if (!__all_sync(0xffffffffu, mbar_test(&bars[s], (li / S) & 1)) &&
+            !__all_sync(0xffffffffu, mbar_block(&bars[s], (li / S) & 1, err, kSiteKV))) {
+            ok = false;
+            break;
+        }
+        const uint32_t vs = src0 + s * kSrc;
+        const int tline = li * k2;
+        const int bline = BIAS ? ((rb0 + t0) * S1 + rb1 + t1) * S2b : 0;
+        for (int nt = 0; nt < ntiles; ++nt) {
+            const int nk = nt * 8 + g;  // this lane's key row of the n-tile (rows past the span hold real data or zeros)
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                // B: key nk, channels 16 ks + 2 q4 (+ 8): 4 bytes in 16-byte chunks 2 ks and 2 ks + 1
+                const uint32_t rowa = vs + static_cast<uint32_t>(nk * 2 * D + 4 * q4);
+                const uint32_t sw = static_cast<uint32_t>((nk >> kSh) & kMask);
+                const uint32_t b0 = ld_shared_u32(rowa + (((2u * ks) ^ sw) << 4));
+                const uint32_t b1 = ld_shared_u32(rowa + (((2u * ks + 1u) ^ sw) << 4));
+                mma16816<F16>(c, a[ks], b0, b1);
+            }
+            // keep each query's own window: span column n -> window offset n - off
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int n = nt * 8 + 2 * q4 + (e & 1);
+                const bool second = e >= 2;
+                const int t2 = n - (second ? off1 : off0);
+                if ((second ? v1 : v0) && t2 >= 0 && t2 < k2) {
+                    float val = c[e] * p.scale;
+                    if (BIAS) val += __ldg(bias + bline + (second ? rbq1 : rbq0) + t2);
+                    stage[(second ? m1 : m0) * p.K + tline + t2] = E::put(val);
+                }
+            }
+        }
+        __syncwarp();  // every lane is done with stage s
+        if (lane == 0 && li + S < nl) issue(li + S);
+    }
+    if (!ok) {
+        if (lane == 0)
+            for (int l = li; l < nl && l < li + S; ++l) mbar_drain(&bars[l % S], (l / S) & 1, err.limit_ns);
+        __syncwarp();
+        return;
+    }
+    __syncwarp();
+    T* out = static_cast<T*>(p.out0);
+    const long long rbase = st.row(p, 0), rstep = static_cast<long long>(d2) * p.heads;  // rows between strip positions
+    for (int m = 0; m < st.nq; ++m) {
+        T* dst = out + (rbase + m * rstep) * p.K;
+        const T* src = stage + m * p.K;
+        for (int t = lane; t < p.K; t += 32) dst[t] = src[t];
     }
 }
 
@@ -1364,6 +1493,23 @@ int launch_op_td(Op op, const UnfParams& p, cudaStream_t s) {
     const dim3 grid(launch_blocks(p.rows * Ln::CPH)), block(kThreads);
     switch (op) {
         case kDot:
+            if constexpr (sizeof(T) == 2 && D <= 64) {   // bf16, fp16 fed by TMA (the key map set by the host)
+                const size_t smem =
+                    (kMmaThreads / 32) * DotTmaLayout<D>::warp_bytes(static_cast<int>(p.srows), p.K, sizeof(T)) + 1024;
+                if (p.tma && smem <= 200 * 1024) {
+                    const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
+                    const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
+                    const dim3 g2(static_cast<unsigned>((units * 32 + kMmaThreads - 1) / kMmaThreads)), b2(kMmaThreads);
+                    auto run = [&](auto kernel) {
+                        if (smem > 48 * 1024)
+                            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+                        kernel<<<g2, b2, smem, s>>>(p);
+                    };
+                    if (p.rpb) run(dot_tma_kernel<T, D, true>);
+                    else run(dot_tma_kernel<T, D, false>);
+                    return static_cast<int>(cudaGetLastError());
+                }
+            }
             if constexpr (sizeof(T) == 2) {   // bf16, fp16: tensor-core logits, one warp per 16-position strip
                 const long long batch = p.rows / (static_cast<long long>(p.L[0]) * p.L[1] * p.L[2] * p.heads);
                 const long long units = batch * p.L[0] * p.L[1] * p.strips2 * p.heads;
