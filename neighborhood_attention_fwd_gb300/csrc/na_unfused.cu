@@ -496,42 +496,62 @@ __device__ __forceinline__ float warp_maxf(float v) {
     return v;
 }
 
-// Rows of up to kRegK weights are held in registers (kRegK / 32 per lane) and read once; longer
-// rows are read again for each pass.
+// Rows of up to kRegK weights are held in registers and read once, two rows per warp (16 lanes each,
+// kRegK / 16 weights per lane); longer rows take a whole warp and are read again for each pass.
 constexpr int kRegK = 128;
 
-// y = softmax(x) over each row of K weights, one warp per row (x and y may be the same tensor: every
-// read of the row happens before its first write).
+__device__ __forceinline__ float half_sum(float v) {
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+__device__ __forceinline__ float half_maxf(float v) {
+#pragma unroll
+    for (int m = 8; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
+// y = softmax(x) over each row of K weights (x and y may be the same tensor: every read of a row
+// happens before its first write).  Rows of at most kRegK weights: two per warp, lanes 16 h .. 16 h + 15
+// on row 2 w + h (the warp's pair of rows, row2 = 2 w); longer rows: one per warp.
+template <typename T>
+__device__ __forceinline__ void softmax_pair(const UnfParams& p, long long row2, int lane) {
+    using E = Elem<T>;
+    constexpr int NV = kRegK / 16;
+    const long long row = row2 + (lane >> 4);
+    const bool live = row < p.rows;
+    const int l16 = lane & 15;
+    const T* x = static_cast<const T*>(p.a) + row * p.K;
+    T* y = static_cast<T*>(p.out0) + row * p.K;
+    float v[NV];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int t = l16 + 16 * i;
+        v[i] = live && t < p.K ? E::get(x[t]) : -INFINITY;
+        m = fmaxf(m, v[i]);
+    }
+    m = half_maxf(m);
+    float l = 0.f;
+    const float ml2 = m * kLog2eF;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        v[i] = live && l16 + 16 * i < p.K ? fast_exp2(fmaf(v[i], kLog2eF, -ml2)) : 0.f;
+        l += v[i];
+    }
+    const float inv = 1.f / half_sum(l);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        if (live && l16 + 16 * i < p.K) y[l16 + 16 * i] = E::put(v[i] * inv);
+}
+
 template <typename T>
 __device__ __forceinline__ void softmax_row(const UnfParams& p, long long row, int lane) {
     using E = Elem<T>;
-    constexpr int NV = kRegK / 32;
     const T* x = static_cast<const T*>(p.a) + row * p.K;
     T* y = static_cast<T*>(p.out0) + row * p.K;
-    if (p.K <= kRegK) {
-        float v[NV];
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int t = lane + 32 * i;
-            v[i] = t < p.K ? E::get(x[t]) : -INFINITY;
-            m = fmaxf(m, v[i]);
-        }
-        m = warp_maxf(m);
-        float l = 0.f;
-        const float ml2 = m * kLog2eF;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            v[i] = lane + 32 * i < p.K ? fast_exp2(fmaf(v[i], kLog2eF, -ml2)) : 0.f;
-            l += v[i];
-        }
-        const float inv = 1.f / warp_sum(l);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (lane + 32 * i < p.K) y[lane + 32 * i] = E::put(v[i] * inv);
-        return;
-    }
     float m = -INFINITY;
     for (int t = lane; t < p.K; t += 32) m = fmaxf(m, E::get(x[t]));
     m = warp_maxf(m);
@@ -550,35 +570,48 @@ __device__ __forceinline__ long long warp_index() {
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_kernel(const UnfParams p) {
-    const long long row = warp_index();
-    if (row < p.rows) softmax_row<T>(p, row, threadIdx.x & 31);   // warp-uniform
+    const long long w = warp_index();
+    if (p.K <= kRegK) {
+        if (2 * w < p.rows) softmax_pair<T>(p, 2 * w, threadIdx.x & 31);   // warp-uniform
+    } else if (w < p.rows) {
+        softmax_row<T>(p, w, threadIdx.x & 31);
+    }
 }
 
-// dx = y * (dy - sum_t y dy) over each row, one warp per row (dx may be dy's tensor).
+// dx = y * (dy - sum_t y dy) over each row (dx may be dy's tensor); rows of at most kRegK weights two
+// per warp as in the forward, longer rows one per warp.
 template <typename T>
-__device__ __forceinline__ void softmax_bwd_row(const UnfParams& p, long long row, int lane) {
+__device__ __forceinline__ void softmax_bwd_pair(const UnfParams& p, long long row2, int lane) {
     using E = Elem<T>;
-    constexpr int NV = kRegK / 32;
+    constexpr int NV = kRegK / 16;
+    const long long row = row2 + (lane >> 4);
+    const bool live = row < p.rows;
+    const int l16 = lane & 15;
     const T* y = static_cast<const T*>(p.a) + row * p.K;
     const T* dy = static_cast<const T*>(p.b) + row * p.K;
     T* dx = static_cast<T*>(p.out0) + row * p.K;
-    if (p.K <= kRegK) {
-        float vy[NV], vd[NV];
-        float s = 0.f;
+    float vy[NV], vd[NV];
+    float s = 0.f;
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            const int t = lane + 32 * i;
-            vy[i] = t < p.K ? E::get(y[t]) : 0.f;
-            vd[i] = t < p.K ? E::get(dy[t]) : 0.f;
-            s = fmaf(vy[i], vd[i], s);
-        }
-        s = warp_sum(s);
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            if (lane + 32 * i < p.K) dx[lane + 32 * i] = E::put(vy[i] * (vd[i] - s));
-        return;
+    for (int i = 0; i < NV; ++i) {
+        const int t = l16 + 16 * i;
+        vy[i] = live && t < p.K ? E::get(y[t]) : 0.f;
+        vd[i] = live && t < p.K ? E::get(dy[t]) : 0.f;
+        s = fmaf(vy[i], vd[i], s);
     }
+    s = half_sum(s);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        if (live && l16 + 16 * i < p.K) dx[l16 + 16 * i] = E::put(vy[i] * (vd[i] - s));
+}
+
+template <typename T>
+__device__ __forceinline__ void softmax_bwd_row(const UnfParams& p, long long row, int lane) {
+    using E = Elem<T>;
+    const T* y = static_cast<const T*>(p.a) + row * p.K;
+    const T* dy = static_cast<const T*>(p.b) + row * p.K;
+    T* dx = static_cast<T*>(p.out0) + row * p.K;
     float s = 0.f;
     for (int t = lane; t < p.K; t += 32) s = fmaf(E::get(y[t]), E::get(dy[t]), s);
     s = warp_sum(s);
@@ -589,8 +622,12 @@ __device__ __forceinline__ void softmax_bwd_row(const UnfParams& p, long long ro
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) softmax_bwd_kernel(const UnfParams p) {
-    const long long row = warp_index();
-    if (row < p.rows) softmax_bwd_row<T>(p, row, threadIdx.x & 31);
+    const long long w = warp_index();
+    if (p.K <= kRegK) {
+        if (2 * w < p.rows) softmax_bwd_pair<T>(p, 2 * w, threadIdx.x & 31);
+    } else if (w < p.rows) {
+        softmax_bwd_row<T>(p, w, threadIdx.x & 31);
+    }
 }
 
 // Gradient of the bias table, first stage: block (chunk of tokens) sums dattn over its tokens'
@@ -1622,7 +1659,8 @@ int launch_op(Op op, const UnfParams& p, int elem, cudaStream_t s) {
 template <typename T>
 int launch_softmax_t(bool bwd, const UnfParams& p, cudaStream_t s) {
     if (p.rows == 0) return 0;
-    const dim3 grid(launch_blocks(p.rows * 32)), block(kThreads);
+    const long long warps = p.K <= kRegK ? (p.rows + 1) / 2 : p.rows;  // rows of at most kRegK weights in pairs
+    const dim3 grid(launch_blocks(warps * 32)), block(kThreads);
     if (bwd)
         softmax_bwd_kernel<T><<<grid, block, 0, s>>>(p);
     else
