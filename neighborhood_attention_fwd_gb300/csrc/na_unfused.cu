@@ -1455,6 +1455,26 @@ __global__ void __launch_bounds__(kMmaThreads) scatter_tma_kernel(const __grid_c
     if (lane == 0)
         for (int li = 0; li < S && li < nl; ++li) issue(li);
     const int jm0 = st.j0 + min(g, st.nq - 1), jm1 = st.j0 + min(g + 8, st.nq - 1);  // this lane's keys
+    // the stage index of each of this lane's A elements (the same on every line): element h2 of a[i] at
+    // k-step ks is query n's weight for key jm, at n wb + u (u = jm - n's window start), or 0xffff
+    // (zero) outside query n's window or the span; two 16-bit entries per word
+    constexpr int kMaxKs = 4;  // srows <= 64
+    uint32_t aoff[kMaxKs][4];
+#pragma unroll
+    for (int ks = 0; ks < kMaxKs; ++ks)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int jm = (i & 1) ? jm1 : jm0;
+            uint32_t w2 = 0;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int nn = 16 * ks + 2 * q4 + 8 * (i >> 1) + h2;
+                const int u = jm - win_start(q_lo + nn, Lc2, k2);
+                const uint32_t o = (nn < qspan && u >= 0 && u < k2) ? static_cast<uint32_t>(nn * wb + u) : 0xffffu;
+                w2 |= o << (16 * h2);
+            }
+            aoff[ks][i] = w2;
+        }
     float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -1470,21 +1490,15 @@ __global__ void __launch_bounds__(kMmaThreads) scatter_tma_kernel(const __grid_c
         const int wc = wcol(li);
         const uint16_t* wst = wst0 + s * (wbytes / 2) + (wc & 7);  // query n's weight u at wst[n wb + u]
         const uint32_t vs = src0 + s * kSrc;
-        for (int ks = 0; ks < nks; ++ks) {
+#pragma unroll
+        for (int ks = 0; ks < kMaxKs; ++ks) {
+            if (ks >= nks) break;
             // A[m, n]: query n's weight for key m, a[i] = keys g (+8), queries 16 ks + 2 q4 (+8) + {0, 1}
             uint32_t a[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int jm = (i & 1) ? jm1 : jm0;
-                const int n = 16 * ks + 2 * q4 + 8 * (i >> 1);
-                uint16_t e[2];
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int nn = n + h2;
-                    const int u = jm - win_start(q_lo + nn, Lc2, k2);
-                    e[h2] = (nn < qspan && u >= 0 && u < k2) ? wst[nn * wb + u] : uint16_t(0);
-                }
-                a[i] = pack_b16(e[0], e[1]);
+                const uint32_t o0 = aoff[ks][i] & 0xffffu, o1 = aoff[ks][i] >> 16;
+                a[i] = pack_b16(o0 != 0xffffu ? wst[o0] : uint16_t(0), o1 != 0xffffu ? wst[o1] : uint16_t(0));
             }
 #pragma unroll
             for (int nt = 0; nt < NT; nt += 2) {
