@@ -125,6 +125,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return mbar_test(bar, parity) || mbar_block(bar, parity, err, site);
 }
 
+// A wait that spins on the phase test instead of sleeping, for the forward's issuing lanes: a chunk's
+// products are issued as soon as their operands are ready.  The status word and the time limit are
+// checked every 64 passes.
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
+    if (mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0u && (ld_volatile(err.word) != 0u || globaltimer() - t0 > err.limit_ns)) {
+            record_error(err.word, site);
+            return false;
+        }
+    }
+}
+
 // Named barrier among the first `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -191,6 +206,14 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Per-thread register budget of the executing warpgroup (every warp of the warpgroup executes it).
+// Raising waits until other warpgroups of the CTA have lowered theirs enough: the budgets of a CTA
+// must sum to no more than its launch registers.
+template <uint32_t N>
+__device__ __forceinline__ void reg_alloc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void reg_dealloc() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N)); }
 
 // D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 inputs, fp32 accumulation), issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,

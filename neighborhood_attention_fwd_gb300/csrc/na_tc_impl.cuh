@@ -85,12 +85,20 @@ __host__ __device__ constexpr int chunk_warps_of(int which) { return which == 0 
 // Distance between the groups one warp takes within a run.
 __host__ __device__ constexpr int group_stride_of(int which) { return alt_of(which) ? 1 : kBwdGroups; }
 __host__ __device__ constexpr int nwg_of(int which) { return which == 0 ? 1 : kBwdGroups; }
-// Warps that issue update products: the forward's one MMA warp issues everything; the backward has
-// one issuing warp per update accumulator (dQ; or dV and dK) beside the warp issuing score products.
-// A single lane waits tens of cycles on each tcgen05.mma it issues, so products into independent
-// accumulators are issued by different warps.
-__host__ __device__ constexpr int nupd_of(int which) { return which == 0 ? 0 : (which == 1 ? 1 : 2); }
-__host__ __device__ constexpr int threads_of(int which) { return 32 * (4 * nwg_of(which) + 2 + nupd_of(which)); }
+// Warps that issue update products (O, dQ; or dV and dK), one per accumulator, beside the warp issuing
+// score products.  A single lane waits tens of cycles on each tcgen05.mma it issues, and it shares its
+// SM sub-partition with softmax warps, so products into independent accumulators are issued by
+// different warps.
+__host__ __device__ constexpr int nupd_of(int which) { return which == 2 ? 2 : 1; }
+// The forward adds one idle warp so that its control warps fill the second warpgroup: the two
+// warpgroups then take different register budgets (setmaxnreg), the softmax warps the larger.
+__host__ __device__ constexpr int threads_of(int which) {
+    return 32 * (4 * nwg_of(which) + 2 + nupd_of(which) + (which == 0 ? 1 : 0));
+}
+// Forward register budgets per thread: softmax warpgroup and control warpgroup.  Two CTAs of 256
+// threads launch with 128 registers each; the two budgets sum to twice that.
+constexpr uint32_t kFwdSoftRegs = 160, kFwdCtrlRegs = 96;
+static_assert(kFwdSoftRegs + kFwdCtrlRegs == 2 * 128, "the forward's split must fit its launch registers");
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -750,10 +758,10 @@ __device__ void producer_loop(const TcParams& p, uint8_t* smem, const TcLayout& 
 }
 
 // ---------------------------------------------------------------------------------------------
-// MMA warp (lane 0): score products per chunk, update products of the previous chunk.
+// Issuing lanes: one for the score products of every chunk, one per update accumulator.
 // ---------------------------------------------------------------------------------------------
 
-// Issues the tensor-core products.  The MMA lane shares its SM sub-partition with softmax warps, so
+// Issues the tensor-core products.  An issuing lane shares its SM sub-partition with softmax warps, so
 // every instruction it spends per MMA counts: descriptors are built once with start address 0 and
 // offset per operand (the start-address field is the low 14 bits of the descriptor and holds
 // address >> 4; shared addresses are below 256 KB), and the instruction descriptors are constant.
@@ -857,117 +865,37 @@ __device__ __forceinline__ uint32_t tm_acc(int which, uint32_t b) {
     return which == 2 ? cols - (2u * abufs_of(2, D) - 2u * b) * D : cols - (2u - b) * D;
 }
 
-struct PendingUpdate {
-    uint32_t g, s, j;
-    int ci, C;
-};
-
-// The MMA lane runs two streams: the score products of the next chunk (as soon as its K/V chunk is
-// loaded and its TMEM score buffer is free: the forward writes P over the scores, so the buffer is
-// free once the product P V of the chunk two back is done) and the update products of the oldest
-// scored chunk (as soon as its P is written).  Neither waits for the other, so
-// one slow softmax warp does not hold back the next chunk's scores.  Waits poll without blocking;
-// after the launch's wait limit without progress the lane records an error and stops.
+// Forward: the update products O += P V of every chunk, issued by one lane as soon as the chunk's P is
+// written (and, for a tile's first chunk, its accumulator buffer has been read out).
 template <int D>
-__device__ void mma_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
-    constexpr int WHICH = 0;
-    constexpr int kS = stages_of(WHICH, D);
-    constexpr uint32_t kPB = pbufs_of(WHICH);
+__device__ void pv_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
+    constexpr uint32_t kS = stages_of(0, D);
     const WaitGuard err{p.err, p.wait_ns};
-    const TilePlan& pl = p.plan;
     MmaIssuer<D> mi;
     mi.init(p, smem, lay);
-    const bool neg = p.neg != 0;
     Cta c;
-    bool have = false, need = true;  // need: the next tile record has not been read yet
-    uint32_t jt = 0;                 // tile records read
-    uint32_t jS = 0, gS = 0;
-    int ciS = 0;
-    bool qready = false;
-    ChunkCursor cur = cursor_begin();
-    PendingUpdate q0{}, q1{}, q2{};  // scored chunks awaiting their update, oldest first
-    int nq = 0;
-    unsigned long long t_last = 0;
-    uint32_t idle = 0;
-    for (;;) {
-        bool progress = false;
-        if (need) {
-            const uint32_t ts = jt % kTileRing;
-            if (mbar_test(&bars[kTFull + ts], (jt / kTileRing) & 1u)) {
-                c = *reinterpret_cast<const Cta*>(smem + lay.tinfo + ts * 128u);
-                mbar_arrive(&bars[kTEmpty + ts]);
-                ++jt;
-                need = false;
-                have = c.C > 0;
-                progress = true;
-            }
+    uint32_t j = 0, g = 0;
+    bool ok = true;
+    while (ok && fetch_tile(smem, lay, bars, j, err, false, c, ok)) {
+        const uint32_t ob = j & 1u;
+        for (int ci = 0; ci < c.C; ++ci, ++g) {
+            const uint32_t pb = g & 1u, s = g % kS;
+            ok = mbar_spin(&bars[kPFull + pb], (g >> 1) & 1u, err, kSiteP);
+            if (ok && ci == 0 && j >= 2) ok = mbar_spin(&bars[kOEmpty + ob], ((j >> 1) - 1) & 1u, err, kSitePV);
+            if (!ok) break;
+            tc_fence_after();
+            mi.pt_x_chunk(tmem + tm_acc<D>(0, ob), tmem + tm_s(p.plan, pb), lay.chunk(s, 1), ci > 0);  // O += P V
+            umma_commit(&bars[kPEmpty + pb]);
+            umma_commit(&bars[kKVEmpty + s]);
+            if (ci == c.C - 1) umma_commit(&bars[kOFull + ob]);
         }
-        if (nq > 0) {
-            const uint32_t pb = q0.g % kPB, ob = q0.j & 1;
-            if (mbar_test(&bars[kPFull + pb], (q0.g / kPB) & 1) &&
-                (q0.ci != 0 || q0.j < 2 || mbar_test(&bars[kOEmpty + ob], ((q0.j >> 1) - 1) & 1))) {
-                tc_fence_after();
-                const uint32_t acc = tmem + tm_acc<D>(WHICH, ob);
-                mi.pt_x_chunk(acc, tmem + tm_s(pl, pb), lay.chunk(q0.s, 1), q0.ci > 0);  // O += P V
-                umma_commit(&bars[kPEmpty + pb]);
-                umma_commit(&bars[kKVEmpty + q0.s]);
-                if (q0.ci == q0.C - 1) umma_commit(&bars[kOFull + ob]);
-                q0 = q1;
-                q1 = q2;
-                --nq;
-                progress = true;
-            }
-        }
-        if (have && nq < 3) {
-            const uint32_t qs = jS & 1, s = gS % kS, sb = gS & 1;
-            if (!qready) qready = mbar_test(&bars[kQFull + qs], (jS >> 1) & 1);
-            // the forward's score buffer also holds that chunk's P: it is free once the product
-            // P V of chunk gS - 2 is done (the backward's softmax releases it after reading)
-            if (qready && mbar_test(&bars[kKVFull + s], (gS / kS) & 1) &&
-                (gS < 2 || mbar_test(&bars[(WHICH == 0 ? kPEmpty : kSEmpty) + sb], ((gS >> 1) - 1) & 1))) {
-                tc_fence_after();
-                mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S (or S^T)
-                mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
-                if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP
-                umma_commit(&bars[kSFull + sb]);
-                if (ciS == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
-                const PendingUpdate pu{gS, s, jS, ciS, c.C};
-                if (nq == 0) q0 = pu; else if (nq == 1) q1 = pu; else q2 = pu;
-                ++nq;
-                ++gS;
-                if (++ciS == c.C) {
-                    ciS = 0;
-                    ++jS;
-                    qready = false;
-                    cur = cursor_begin();
-                    have = false;
-                    need = true;
-                } else {
-                    cursor_next(pl, c, cur);
-                }
-                progress = true;
-            }
-        }
-        if (!have && !need && nq == 0) break;  // the end record was read and every update issued
-        if (progress) {
-            idle = 0;
-            continue;
-        }
-        // idle: spin on the barriers; the status word (a global load of some hundred cycles) and the
-        // time limit are checked every 64 passes
-        if ((++idle & 63u) == 0u) {
-            if (ld_volatile(err.word) != 0u) break;
-            const unsigned long long now = globaltimer();
-            if (idle == 64u) t_last = now;
-            else if (now - t_last > err.limit_ns) {
-                record_error(err.word, kSiteP);
-                break;
-            }
-        }
+        ++j;
     }
 }
 
-// Backward: the score products of every chunk, issued by one lane (S or S^T, the window bias, dP).
+// The score products of every chunk, issued by one lane: S (or S^T) and the window bias, and in the
+// backward dP (or dP^T).  The forward's score buffer also holds that chunk's P, so it is free once the
+// product P V of the chunk two back is done; the backward's softmax releases it after reading.
 template <int D, int WHICH>
 __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
     constexpr uint32_t kS = stages_of(WHICH, D);
@@ -986,13 +914,18 @@ __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay
         ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
             const uint32_t s = g % kS, sb = g & 1;
-            ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
-            if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            if constexpr (WHICH == 0) {
+                ok = mbar_spin(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
+                if (ok && g >= 2) ok = mbar_spin(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            } else {
+                ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
+                if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            }
             if (!ok) break;
             tc_fence_after();
             mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S or S^T
             mi.add_bias(tmem + tm_s(pl, sb), cur);                                          // + window bias
-            mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP or dP^T
+            if (WHICH != 0) mi.rows_x_chunk(tmem + tm_dp(pl, sb), lay.tile(qs, 1), lay.chunk(s, 1), false);  // dP or dP^T
             umma_commit(&bars[kSFull + sb]);
             if (ci == c.C - 1) umma_commit(&bars[kQEmpty + qs]);
         }
@@ -1194,7 +1127,7 @@ __device__ __forceinline__ bool fwd_part(const FwdCtx& x, uint32_t g, uint32_t t
 // One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + n) (n <= 6):
 // runs of up to four groups in one part, longer runs in two parts of at most three (register
 // budget).  Groups outside the run hold scores, not P, so they are zeroed once every score of the
-// run has been read; then the P operand (score buffer g & 1) is released to the MMA warp.
+// run has been read; then the P operand (score buffer g & 1) is released to the P V lane.
 template <int D, bool F16>
 __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, int n, float& m,
                                           uint64_t (&lsum)[4]) {
@@ -1599,7 +1532,7 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     }
     for (uint32_t t = 0; t < kTileRing; ++t) {
         mbar_init(&bars[kTFull + t], 1);
-        mbar_init(&bars[kTEmpty + t], kSoft + 1 + nupd_of(WHICH));  // softmax warps, score/MMA lane, update lanes
+        mbar_init(&bars[kTEmpty + t], kSoft + 1 + nupd_of(WHICH));  // softmax warps, score lane, update lanes
     }
     mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
     if (WHICH == 2)
@@ -1634,25 +1567,35 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    if (warp == kSoftWarps) {
-        producer_loop<D, WHICH>(p, smem, lay, bars);
-    } else if (warp == kSoftWarps + 1) {
-        if (lane == 0) {
-            if constexpr (WHICH == 0) {
-                mma_loop<D>(p, smem, lay, bars, tmem);
-            } else {
-                score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+    if constexpr (WHICH == 0) {
+        // each warpgroup's budget is set in the branch that runs its code
+        if (warp < kSoftWarps) {
+            reg_alloc<kFwdSoftRegs>();
+            fwd_softmax_loop<D, F16>(p, smem, lay, bars, tmem);
+        } else {
+            reg_dealloc<kFwdCtrlRegs>();
+            if (warp == kSoftWarps) {
+                producer_loop<D, WHICH>(p, smem, lay, bars);
+            } else if (warp == kSoftWarps + 1) {
+                if (lane == 0) score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+                __syncwarp();
+            } else if (warp == kSoftWarps + 2) {
+                if (lane == 0) pv_loop<D>(p, smem, lay, bars, tmem);
+                __syncwarp();
             }
         }
-        __syncwarp();
-    } else if (warp >= kSoftWarps + 2) {
-        if (lane == 0) update_loop<D, WHICH>(p, smem, lay, bars, tmem, warp - (kSoftWarps + 2));
-        __syncwarp();
-    } else if (WHICH == 0) {
-        fwd_softmax_loop<D, F16>(p, smem, lay, bars, tmem);
     } else {
-        bwd_softmax_loop<D, WHICH, F16>(p, smem, lay, bars, tmem);
+        if (warp == kSoftWarps) {
+            producer_loop<D, WHICH>(p, smem, lay, bars);
+        } else if (warp == kSoftWarps + 1) {
+            if (lane == 0) score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            __syncwarp();
+        } else if (warp >= kSoftWarps + 2) {
+            if (lane == 0) update_loop<D, WHICH>(p, smem, lay, bars, tmem, warp - (kSoftWarps + 2));
+            __syncwarp();
+        } else {
+            bwd_softmax_loop<D, WHICH, F16>(p, smem, lay, bars, tmem);
+        }
     }
 
     // teardown: every TMEM access of the softmax warps and every MMA of this CTA done before TMEM is
@@ -1661,7 +1604,7 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         tmem_st_wait();
         tmem_ld_wait_all();
     }
-    if (warp >= kSoftWarps + 1 && lane == 0) {
+    if (warp >= kSoftWarps + 1 && warp < kSoftWarps + 2 + nupd_of(WHICH) && lane == 0) {  // every issuing lane
         umma_commit(&bars[kFin]);
         mbar_wait(&bars[kFin], 0, WaitGuard{p.err, p.wait_ns}, kSiteFinal);
     }
