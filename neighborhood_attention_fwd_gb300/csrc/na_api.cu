@@ -415,6 +415,10 @@ na::FmaParams fma_params(const Geom& g, float scale) {
         p.fd_L[a] = na::make_fastdiv(static_cast<uint32_t>(g.L[a]));
         p.fd_d[a] = na::make_fastdiv(static_cast<uint32_t>(g.d[a]));
     }
+    const int lc2 = (g.L[2] + g.d[2] - 1) / g.d[2];   // class 0 is the longest
+    p.qc2 = (lc2 + 3) / 4;
+    p.fd_qc2 = na::make_fastdiv(static_cast<uint32_t>(p.qc2));
+    p.quads = static_cast<long long>(g.B) * g.L[0] * g.L[1] * g.d[2] * p.qc2 * g.heads;
     return p;
 }
 

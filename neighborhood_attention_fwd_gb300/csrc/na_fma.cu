@@ -304,6 +304,219 @@ __global__ void __launch_bounds__(kFmaThreads) dq_fma_kernel(const FmaParams p) 
     }
 }
 
+// Query quads.  A group of G = D/4 lanes (one 16-byte chunk of a row each) takes four consecutive
+// class positions of one residue class along the innermost axis, one head: their windows share
+// every line and, along the innermost axis, span at most k2 + 3 positions, so each key chunk a lane
+// loads serves four queries.  Heads are the fastest index, so a warp's groups load neighbouring rows.
+// The four partial dot products of a key are finished by a reduce-scatter over the group (two
+// exchange steps) and butterflies over the rest: afterwards the lanes c with c / (G/4) = r hold the
+// score of query r.
+constexpr int kQuad = 4;
+
+struct Quad {
+    long long tok0;   // token of class position 0 on the quad's line: ((b L0 + x0) L1 + x1) L2 + c2
+    long long b;
+    int x0, x1, c2, h, j0, nq, lc2;
+
+    __device__ bool init(const FmaParams& p, uint32_t u) {
+        uint32_t q = fdiv(u, p.fd_heads);
+        h = static_cast<int>(u - q * p.fd_heads.d);
+        u = q;
+        q = fdiv(u, p.fd_qc2);
+        const int s = static_cast<int>(u - q * p.fd_qc2.d);
+        u = q;
+        q = fdiv(u, p.fd_d[2]);
+        c2 = static_cast<int>(u - q * p.fd_d[2].d);
+        u = q;
+        q = fdiv(u, p.fd_L[1]);
+        x1 = static_cast<int>(u - q * p.fd_L[1].d);
+        u = q;
+        q = fdiv(u, p.fd_L[0]);
+        x0 = static_cast<int>(u - q * p.fd_L[0].d);
+        b = q;
+        lc2 = static_cast<int>(fdiv(static_cast<uint32_t>(p.L[2] - c2 + p.d[2] - 1), p.fd_d[2]));
+        j0 = kQuad * s;
+        if (j0 >= lc2) return false;   // past the end of a shorter class
+        nq = min(kQuad, lc2 - j0);
+        tok0 = ((b * p.L[0] + x0) * p.L[1] + x1) * p.L[2] + c2;
+        return true;
+    }
+    // class position of query r (the last valid one for r >= nq)
+    __device__ int j(int r) const { return j0 + min(r, nq - 1); }
+    __device__ long long row(const FmaParams& p, int r) const {
+        return (tok0 + static_cast<long long>(p.d[2]) * j(r)) * p.heads + h;
+    }
+};
+
+template <int G>
+struct QuadLanes {
+    int c, base;      // lane within the group; the group's first lane
+    unsigned mask;    // the group's lanes
+    __device__ QuadLanes() {
+        const int lane = threadIdx.x & 31;
+        c = lane & (G - 1);
+        base = lane & ~(G - 1);
+        mask = G == 32 ? 0xffffffffu : ((1u << G) - 1u) << base;
+    }
+    __device__ int rq() const { return c / (G / 4); }   // the query whose score this lane ends with
+    __device__ bool owner() const { return (c & (G / 4 - 1)) == 0; }
+    // the four partial sums of the lane -> the full sum of query rq() over the group
+    __device__ float reduce(const float (&v)[kQuad]) const {
+        const bool hi = (c & (G / 2)) != 0;
+        const float a0 = (hi ? v[2] : v[0]) + __shfl_xor_sync(mask, hi ? v[0] : v[2], G / 2);
+        const float a1 = (hi ? v[3] : v[1]) + __shfl_xor_sync(mask, hi ? v[1] : v[3], G / 2);
+        const bool lo = (c & (G / 4)) != 0;
+        float x = (lo ? a1 : a0) + __shfl_xor_sync(mask, lo ? a0 : a1, G / 4);
+#pragma unroll
+        for (int m = G / 8; m >= 1; m >>= 1) x += __shfl_xor_sync(mask, x, m);
+        return x;
+    }
+    // query r's value, from one of its lanes
+    __device__ float from(float v, int r) const { return __shfl_sync(mask, v, base + r * (G / 4)); }
+};
+
+// Forward over query quads: the online softmax takes the keys of a line in blocks of four (one max
+// and one rescale of the four accumulators per block).  Every query's window starts in the first
+// block of its first line (consecutive class positions start their windows at most one position
+// apart), so the running max is finite after that block.
+template <int D>
+__global__ void __launch_bounds__(kFmaThreads) fwd_fma_quad_kernel(const FmaParams p) {
+    constexpr int G = D / 4;
+    const QuadLanes<G> ql;
+    const long long unit = (static_cast<long long>(blockIdx.x) * kFmaThreads + threadIdx.x) / G;
+    Quad qd;
+    if (unit >= p.quads || !qd.init(p, static_cast<uint32_t>(unit))) return;   // the whole group
+    const int k2 = p.k[2], rq = ql.rq();
+    float4 qv[kQuad], acc[kQuad];
+    int ws[kQuad];
+#pragma unroll
+    for (int r = 0; r < kQuad; ++r) {
+        qv[r] = __ldg(chunk_ptr<D>(p.q, qd.row(p, r), ql.c));
+        acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ws[r] = win_start(qd.j(r), qd.lc2, k2);
+    }
+    const int u0 = ws[0], span = ws[kQuad - 1] - u0 + k2;
+    const int lo = (rq == 0 ? ws[0] : rq == 1 ? ws[1] : rq == 2 ? ws[2] : ws[3]) - u0, hi = lo + k2;
+    const int f0 = first_nb(p, 0, qd.x0), f1 = first_nb(p, 1, qd.x1);
+    const int kstep4 = p.d[2] * p.heads * G;   // float4s between consecutive class positions
+    const float sl2 = p.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
+        for (int t1 = 0; t1 < p.k[1]; ++t1) {
+            const long long tok = ((qd.b * p.L[0] + f0 + p.d[0] * t0) * p.L[1] + f1 + p.d[1] * t1) * p.L[2] + qd.c2 +
+                                  static_cast<long long>(p.d[2]) * u0;
+            const float4* kl = chunk_ptr<D>(p.key, tok * p.heads + qd.h, ql.c);
+            const float4* vl = chunk_ptr<D>(p.value, tok * p.heads + qd.h, ql.c);
+            for (int u = 0; u < span; u += 4) {
+                float4 kc[4], vc[4];
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) {
+                    const int o = min(u + kb, span - 1) * kstep4;   // a key inside the span in every slot
+                    kc[kb] = __ldg(kl + o);
+                    vc[kb] = __ldg(vl + o);
+                }
+                float sb[4];
+                float bm = -INFINITY;
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) {
+                    float pd[kQuad];
+#pragma unroll
+                    for (int r = 0; r < kQuad; ++r) pd[r] = dot4(qv[r], kc[kb]);
+                    const float sv = sl2 * ql.reduce(pd);
+                    sb[kb] = (u + kb >= lo && u + kb < hi) ? sv : -INFINITY;
+                    bm = fmaxf(bm, sb[kb]);
+                }
+                const float mn = fmaxf(m, bm);
+                const float corr = fast_exp2(m - mn);   // 0 on the first block (m = -inf)
+                l *= corr;
+                m = mn;
+#pragma unroll
+                for (int r = 0; r < kQuad; ++r) scale4(acc[r], ql.from(corr, r));
+#pragma unroll
+                for (int kb = 0; kb < 4; ++kb) {
+                    const float pe = fast_exp2(sb[kb] - mn);   // 0 outside the window
+                    l += pe;
+#pragma unroll
+                    for (int r = 0; r < kQuad; ++r) axpy4(acc[r], ql.from(pe, r), vc[kb]);
+                }
+            }
+        }
+#pragma unroll
+    for (int r = 0; r < kQuad; ++r) {
+        const float lr = ql.from(l, r);
+        if (r < qd.nq) {
+            scale4(acc[r], 1.f / lr);
+            *(reinterpret_cast<float4*>(static_cast<float*>(p.out0) + qd.row(p, r) * D) + ql.c) = acc[r];
+        }
+    }
+    if (ql.owner() && rq < qd.nq) static_cast<float*>(p.out1)[qd.row(p, rq)] = (m + __log2f(l)) * kLn2;
+}
+
+// dQ over query quads: per key, the four queries' scores and dO . v, then each query's
+// dS = P (dO . v - Delta) with P = exp(scale q . k - LSE), and dQ_r += dS_r k.
+template <int D>
+__global__ void __launch_bounds__(kFmaThreads) dq_fma_quad_kernel(const FmaParams p) {
+    constexpr int G = D / 4;
+    const QuadLanes<G> ql;
+    const long long unit = (static_cast<long long>(blockIdx.x) * kFmaThreads + threadIdx.x) / G;
+    Quad qd;
+    if (unit >= p.quads || !qd.init(p, static_cast<uint32_t>(unit))) return;   // the whole group
+    const int k2 = p.k[2], rq = ql.rq();
+    float4 qv[kQuad], gv[kQuad], acc[kQuad];
+    int ws[kQuad];
+#pragma unroll
+    for (int r = 0; r < kQuad; ++r) {
+        const long long row = qd.row(p, r);
+        qv[r] = __ldg(chunk_ptr<D>(p.q, row, ql.c));
+        gv[r] = __ldg(chunk_ptr<D>(p.dO, row, ql.c));
+        acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        ws[r] = win_start(qd.j(r), qd.lc2, k2);
+    }
+    const long long myrow = qd.row(p, rq);
+    const float nl2 = -p.lse[myrow] * kLog2e, dlt = p.delta[myrow];
+    const int u0 = ws[0], span = ws[kQuad - 1] - u0 + k2;
+    const int lo = (rq == 0 ? ws[0] : rq == 1 ? ws[1] : rq == 2 ? ws[2] : ws[3]) - u0, hi = lo + k2;
+    const int f0 = first_nb(p, 0, qd.x0), f1 = first_nb(p, 1, qd.x1);
+    const int kstep4 = p.d[2] * p.heads * G;
+    const float sl2 = p.scale * kLog2e;
+    for (int t0 = 0; t0 < p.k[0]; ++t0)
+        for (int t1 = 0; t1 < p.k[1]; ++t1) {
+            const long long tok = ((qd.b * p.L[0] + f0 + p.d[0] * t0) * p.L[1] + f1 + p.d[1] * t1) * p.L[2] + qd.c2 +
+                                  static_cast<long long>(p.d[2]) * u0;
+            const float4* kl = chunk_ptr<D>(p.key, tok * p.heads + qd.h, ql.c);
+            const float4* vl = chunk_ptr<D>(p.value, tok * p.heads + qd.h, ql.c);
+            for (int u = 0; u < span; u += 2) {
+                float4 kc[2], vc[2];
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const int o = min(u + kb, span - 1) * kstep4;
+                    kc[kb] = __ldg(kl + o);
+                    vc[kb] = __ldg(vl + o);
+                }
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    float ps[kQuad], pp[kQuad];
+#pragma unroll
+                    for (int r = 0; r < kQuad; ++r) {
+                        ps[r] = dot4(qv[r], kc[kb]);
+                        pp[r] = dot4(gv[r], vc[kb]);
+                    }
+                    const float sv = ql.reduce(ps), dp = ql.reduce(pp);
+                    const bool in = u + kb >= lo && u + kb < hi;
+                    const float ds = in ? fast_exp2(fmaf(sl2, sv, nl2)) * (dp - dlt) : 0.f;
+#pragma unroll
+                    for (int r = 0; r < kQuad; ++r) axpy4(acc[r], ql.from(ds, r), kc[kb]);
+                }
+            }
+        }
+#pragma unroll
+    for (int r = 0; r < kQuad; ++r)
+        if (r < qd.nq) {
+            scale4(acc[r], p.scale);
+            *(reinterpret_cast<float4*>(static_cast<float*>(p.out0) + qd.row(p, r) * D) + ql.c) = acc[r];
+        }
+}
+
 // dK, dV: one row's lanes per key, gathering over the queries whose windows hold the key.  Per axis
 // those queries form the class-index interval [i_lo, i_hi]: i_lo = 0 if j < k else j - k/2, and
 // i_hi = Lc - 1 if j >= Lc - k else j + k/2 (the border keys are seen by more queries).
@@ -409,9 +622,27 @@ int launch_rows(F kernel, const FmaParams& p, cudaStream_t s) {
     return static_cast<int>(cudaGetLastError());
 }
 
+// Query-quad kernels where the quad index fits the 32-bit decode.
+template <int D, typename F>
+int launch_quads(F kernel, const FmaParams& p, cudaStream_t s) {
+    if (p.quads == 0) return 0;
+    const long long blocks = (p.quads * (D / 4) + kFmaThreads - 1) / kFmaThreads;
+    kernel<<<dim3(static_cast<unsigned>(blocks)), dim3(kFmaThreads), 0, s>>>(p);
+    return static_cast<int>(cudaGetLastError());
+}
+
+bool quads_ok(const FmaParams& p) { return p.quads < (1LL << 32); }
+
 }  // namespace
 
 int launch_fwd_fma(const FmaParams& p, cudaStream_t s) {
+    if (quads_ok(p)) switch (p.D) {
+            case 16: return launch_quads<16>(fwd_fma_quad_kernel<16>, p, s);
+            case 32: return launch_quads<32>(fwd_fma_quad_kernel<32>, p, s);
+            case 64: return launch_quads<64>(fwd_fma_quad_kernel<64>, p, s);
+            case 128: return launch_quads<128>(fwd_fma_quad_kernel<128>, p, s);
+            default: return static_cast<int>(cudaErrorInvalidValue);
+        }
     switch (p.D) {
         case 16: return launch_rows<16, kCplF>(fwd_fma_kernel<16>, p, s);
         case 32: return launch_rows<32, kCplF>(fwd_fma_kernel<32>, p, s);
@@ -422,6 +653,13 @@ int launch_fwd_fma(const FmaParams& p, cudaStream_t s) {
 }
 
 int launch_dq_fma(const FmaParams& p, cudaStream_t s) {
+    if (quads_ok(p)) switch (p.D) {
+            case 16: return launch_quads<16>(dq_fma_quad_kernel<16>, p, s);
+            case 32: return launch_quads<32>(dq_fma_quad_kernel<32>, p, s);
+            case 64: return launch_quads<64>(dq_fma_quad_kernel<64>, p, s);
+            case 128: return launch_quads<128>(dq_fma_quad_kernel<128>, p, s);
+            default: return static_cast<int>(cudaErrorInvalidValue);
+        }
     switch (p.D) {
         case 16: return launch_rows<16, kCplQ>(dq_fma_kernel<16>, p, s);
         case 32: return launch_rows<32, kCplQ>(dq_fma_kernel<32>, p, s);

@@ -106,6 +106,11 @@ struct FmaParams {
     // 32-bit row decode without division (used when B * N * heads < 2^32)
     uint32_t rows32;
     FastDiv fd_heads, fd_N, fd_L[3], fd_d[3];
+    // query quads (four consecutive class positions along the innermost axis, one head): quads per
+    // class (of the longest class) and their total, B * L0 * L1 * d2 * qc2 * heads
+    int qc2;
+    FastDiv fd_qc2;
+    long long quads;
 };
 
 // Parameters of the unfused operations (na_unfused.cu).  Rows are (batch, token, head) triples;
