@@ -20,6 +20,8 @@ SMALL = [
     ("fp32", (9, 11, 10), 2, 16, (3, 5, 3), (2, 1, 3), 1),
     ("fp32", (12, 13), 1, 64, (5, 3), (1, 4), 1),
     ("fp32", (7, 9), 2, 128, (7, 9), (1, 1), 1),            # kernel == extent: full attention
+    ("fp32", (10, 23), 3, 64, (3, 7), (2, 3), 1),           # key quads over unequal classes (dK/dV quads from k2 >= 7)
+    ("fp32", (4, 6, 19), 2, 16, (3, 3, 9), (1, 2, 2), 2),   # quads of one class position past a class end
     ("bf16", (40, 37), 3, 32, (5, 7), (1, 1), 2),
     ("bf16", (33, 45), 2, 32, (9, 9), (1, 1), 1),
     ("bf16", (200,), 2, 32, (7,), (1,), 2),
