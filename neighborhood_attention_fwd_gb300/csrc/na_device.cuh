@@ -125,9 +125,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return mbar_test(bar, parity) || mbar_block(bar, parity, err, site);
 }
 
-// A wait that spins on the phase test instead of sleeping, for the forward's issuing lanes: a chunk's
-// products are issued as soon as their operands are ready.  The status word and the time limit are
-// checked every 64 passes.
+// A wait that spins on the phase test instead of sleeping, for the lanes that issue tensor-core
+// products: a chunk's products are issued as soon as their operands are ready.  The status word and
+// the time limit are checked every 64 passes.
 __device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const WaitGuard& err, unsigned site) {
     if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();

@@ -914,13 +914,9 @@ __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay
         ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
             const uint32_t s = g % kS, sb = g & 1;
-            if constexpr (WHICH == 0) {
-                ok = mbar_spin(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
-                if (ok && g >= 2) ok = mbar_spin(&bars[kPEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
-            } else {
-                ok = mbar_wait(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
-                if (ok && g >= 2) ok = mbar_wait(&bars[kSEmpty + sb], ((g >> 1) - 1) & 1, err, kSiteS);
-            }
+            ok = mbar_spin(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
+            if (ok && g >= 2)
+                ok = mbar_spin(&bars[(WHICH == 0 ? kPEmpty : kSEmpty) + sb], ((g >> 1) - 1) & 1, err, kSiteS);
             if (!ok) break;
             tc_fence_after();
             mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S or S^T
@@ -958,8 +954,8 @@ __device__ void update_loop(const TcParams& p, uint8_t* smem, const TcLayout& la
         const uint32_t acc = tmem + tm_acc<D>(WHICH, ob) + acc_off;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
             const uint32_t s = g % kS, pb = g % kPB;
-            ok = mbar_wait(&bars[kPFull + pb], (g / kPB) & 1, err, kSiteP);
-            if (ok && ci == 0 && j >= kAB) ok = mbar_wait(&bars[kOEmpty + ob], ((j / kAB) - 1) & 1, err, kSitePV);
+            ok = mbar_spin(&bars[kPFull + pb], (g / kPB) & 1, err, kSiteP);
+            if (ok && ci == 0 && j >= kAB) ok = mbar_spin(&bars[kOEmpty + ob], ((j / kAB) - 1) & 1, err, kSitePV);
             if (!ok) break;
             tc_fence_after();
             mi.p_x_chunk(acc, lay.p(pb, op_p), lay.chunk(s, op_b), ci > 0);
