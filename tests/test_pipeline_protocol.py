@@ -6,7 +6,9 @@ not toward the chunk the arriving warp means.  This model replays that protocol 
 checks that an update product never starts before every warp has finished writing its chunk.  It pins the
 dK/dV rule that a warp with nothing to write still waits for the products of chunk g - 2 before it
 arrives: without the wait (the `shortcut` variant) an idle warp runs ahead and completes chunk g's phase
-early, as seen on the GPU.  It also covers the forward, whose P is written over its scores in TMEM.
+early, as seen on the GPU.  It also covers the forward, whose P is written over its scores in TMEM and
+whose score and P V products come from two independent issuing lanes: a softmax warp that rescales the
+output accumulator in TMEM must find the P V product of the chunk before already done.
 """
 import random
 
@@ -30,17 +32,19 @@ class Bar:
         return (self.n & 1) != parity
 
 
-def run_model(variant, chunks, idle, rng, n_warps=8, n_issuers=2, n_p=2):
+def run_model(variant, chunks, idle, rng, n_warps=8, n_issuers=2, n_p=2, rescale_wait=True):
     """variant: 'backward' (the dK/dV protocol), 'shortcut' (idle warps arrive without the wait), or
     'forward' (P over the scores: the next score product waits for the P V product).  Returns the list
-    of violations (an update of chunk g that started before a warp finished writing chunk g)."""
+    of violations: an update of chunk g that started before a warp finished writing chunk g, or (forward)
+    a rescale of the output accumulator while the P V product of the chunk before was still running."""
     if variant == "forward":
-        n_issuers = 1  # one MMA lane issues the forward's P V products
+        n_issuers = 1  # one lane issues the forward's P V products, another its score products
     s_full = [Bar(1) for _ in range(2)]
     s_empty = [Bar(n_warps) for _ in range(2)]
     p_full = [Bar(n_warps) for _ in range(n_p)]
     p_empty = [Bar(n_issuers) for _ in range(n_p)]
     written = [-1] * n_warps  # last chunk each warp finished writing
+    pv_done = [False] * chunks  # the update product of each chunk has completed
     violations = []
 
     def delay(lo, hi):
@@ -62,6 +66,14 @@ def run_model(variant, chunks, idle, rng, n_warps=8, n_issuers=2, n_p=2):
             sb, pb = g & 1, g % n_p
             yield ("wait", s_full[sb], (g >> 1) & 1)
             yield delay(0, 2)  # read the run's scores
+            if variant == "forward" and g >= 1 and rng.random() < 0.3:
+                # the running max moved: rescale O, which the P V products of chunks g - 1, g - 2, ...
+                # accumulate into, after the last of them is done
+                if rescale_wait:
+                    yield ("wait", p_empty[(g - 1) % n_p], ((g - 1) // n_p) & 1)
+                if not pv_done[g - 1]:
+                    violations.append(("rescale", g, w))
+                yield delay(0, 2)
             if variant != "forward":
                 s_empty[sb].arrive()  # released as soon as they are read
             if w in idle and variant != "forward":  # the forward zeroes an idle warp's P rows: a write
@@ -83,6 +95,7 @@ def run_model(variant, chunks, idle, rng, n_warps=8, n_issuers=2, n_p=2):
                 if w not in idle and written[w] < g:
                     violations.append((u, g, w))
             yield delay(1, 5)
+            pv_done[g] = True
             p_empty[pb].arrive()
 
     agents = [score_lane()] + [softmax(w) for w in range(n_warps)]
@@ -138,3 +151,14 @@ def test_three_p_buffers_keep_the_shortcut_safe():
     for _ in range(300):
         idle = set(rng.sample(range(8), rng.randint(1, 6)))
         assert run_model("shortcut", 12, idle, rng, n_issuers=1, n_p=3) == []
+
+
+def test_a_rescale_without_the_wait_races_the_previous_update():
+    """The forward's rescale of O without waiting for chunk g - 1's P V product: with the P V lane
+    independent of the softmax warps, that product can still be running."""
+    rng = random.Random(5)
+    bad = 0
+    for _ in range(300):
+        idle = set(rng.sample(range(8), rng.randint(0, 6)))
+        bad += any(v[0] == "rescale" for v in run_model("forward", 12, idle, rng, rescale_wait=False))
+    assert bad > 0
