@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libna.so")
-SOURCES = ["na_api.cu", "na_fma.cu", "na_tc.cu", "na_tc_f16.cu", "na_unfused.cu"]
+SOURCES = ["na_api.cu", "na_fma.cu", "na_tc.cu", "na_tc_f16.cu", "na_tc_sb3.cu", "na_unfused.cu"]
 HEADERS = ["na_internal.h", "na_device.cuh", "na_tc_impl.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include")]

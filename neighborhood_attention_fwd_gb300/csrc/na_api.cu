@@ -19,7 +19,7 @@
 namespace na {
 uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D);
 int tc_tmem_cols(int which, int D);
-int tc_max_nc(int which, int D);
+int tc_max_nc(int which, int D, int sbufs);
 }
 
 namespace {
@@ -248,14 +248,14 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
     }
     const int D = g.D;
     const int tmem_cols = na::tc_tmem_cols(which, D);
-    const int ncmax = na::tc_max_nc(which, D);
     int Lcm[3];
     for (int a = 0; a < 3; ++a) Lcm[a] = ceil_div(g.L[a], g.d[a]);
     const int n_score = which == 0 ? 1 : 2, n_update = which == 2 ? 2 : 1;
 
+    // the cheapest plan whose chunks hold at most ncmax rows
+    auto search = [&](int ncmax, TilePlan& bp) {
     bool found = false;
     double best = 0;
-    TilePlan bp{};
     for (int T2 = 8; T2 <= 128; T2 *= 2)
         for (int T1 = 1; T1 * T2 <= 128; T1 *= 2) {
             const int T0 = 128 / (T1 * T2);
@@ -304,7 +304,22 @@ na_status plan_tc(int which, const Geom& g, TilePlan& out) {
                     }
             }
         }
-    if (!found) return NA_ERR_UNSUPPORTED;
+    return found;
+    };
+    TilePlan bp{};
+    if (!search(na::tc_max_nc(which, D, 2), bp)) return NA_ERR_UNSUPPORTED;
+    bp.sbufs = 2;
+    // A forward whose tiles walk ten or more chunks is bound by each score buffer's chain (the P V
+    // product of a chunk, then the score product of the chunk two later into the same buffer), not by
+    // the per-chunk costs: it takes three 64-column buffers instead (measured at 8x128x128 / (5, 7, 7),
+    // 10 chunks of 96 columns: 0.97 -> 0.80 ms; at 4-7 chunks per tile three buffers were 27-49% slower).
+    if (which == 0 && D <= 32 && bp.nchk[0] * bp.nchk[1] * bp.nchk[2] >= 10) {
+        TilePlan b3{};
+        if (search(na::tc_max_nc(which, D, 3), b3)) {
+            bp = b3;
+            bp.sbufs = 3;
+        }
+    }
     bp.tmem_cols = tmem_cols;
     // Shared memory: the layout, padded so that no more than 512 / tmem_cols CTAs fit on an SM
     // (their TMEM allocations then never wait on each other), and checked so that that many do fit.

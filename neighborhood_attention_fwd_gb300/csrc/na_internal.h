@@ -52,6 +52,7 @@ struct TilePlan {
     int nchk[3];     // chunks along each axis that cover the halo box
     int ntile[3];    // tiles per axis and residue class: ceil(ceil(L/d) / T)
     int tmem_cols;   // TMEM columns allocated per CTA (power of two)
+    int sbufs;       // score buffers in TMEM: 2, or 3 (the forward at D <= 32 with NC <= 64)
     int per_sm;      // persistent CTAs per SM (the grid is per_sm x SM count, at most `ctas`)
     int smem_bytes;  // dynamic shared memory per CTA (includes alignment slack)
     int64_t ctas;    // tiles (linearised: head fastest, then tile along axes 2,1,0, class 2,1,0, batch)
@@ -149,6 +150,7 @@ size_t rpb_grad_workspace_bytes(long long tokens, int heads, int K, int table);
 // Launchers (defined next to their kernels).  Return a cudaError_t as int.
 int launch_fwd_tc(const TcParams& p, cudaStream_t stream);
 int launch_fwd_tc_f16(const TcParams& p, cudaStream_t stream);
+int launch_fwd_tc_sb3(const TcParams& p, cudaStream_t stream);   // three score buffers, D <= 32
 int launch_dq_tc_f16(const TcParams& p, cudaStream_t stream);
 int launch_dkdv_tc_f16(const TcParams& p, cudaStream_t stream);
 int launch_dq_tc(const TcParams& p, cudaStream_t stream);

@@ -8,13 +8,13 @@ uint32_t tc_smem_bytes(int which, const TilePlan& pl, int D) { return tc_layout(
 
 int tc_tmem_cols(int which, int D) { return tmem_cols_of(which, D); }
 
-int tc_max_nc(int which, int D) {
-    // double-buffered score accumulators (the backward's with their dP beside them) plus the tile
-    // accumulators; the forward's P overwrites its scores, and its softmax takes a run of at most six
-    // groups (96 columns)
+int tc_max_nc(int which, int D, int sbufs) {
+    // the score accumulators (the backward's double-buffered with their dP beside them, the forward's
+    // two or three) plus the tile accumulators; the forward's P overwrites its scores, and its softmax
+    // takes a run of at most six groups (96 columns)
     const int cols = tc_tmem_cols(which, D);
     const int acc = (which == 2 ? 2 : 1) * abufs_of(which, D) * D;
-    const int nc = which == 0 ? (cols - acc) / 2 : (cols - acc) / 4;
+    const int nc = which == 0 ? (cols - acc) / sbufs : (cols - acc) / 4;
     const int cap = which == 0 ? 96 : 128;
     return (nc < cap ? nc : cap) / 16 * 16;
 }

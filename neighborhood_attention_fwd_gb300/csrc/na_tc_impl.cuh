@@ -63,6 +63,10 @@ __host__ __device__ constexpr int stages_of(int which, int D) { return D <= 32 ?
 // warpgroup, dK/dV (two P operands per buffer) one per warpgroup.
 __host__ __device__ constexpr bool alt_of(int which) { return which != 0; }
 __host__ __device__ constexpr int pbufs_of(int which) { return which == 1 ? 4 : 2; }
+// Score buffers in TMEM: two, or (the forward at D <= 32, when its plan asks for it) three.  Three
+// 64-column chunks and the two accumulators fill the forward's 256 columns; the score product into a
+// buffer then waits for the P V product of the chunk three back instead of two back.  The forward's P
+// buffers are its score buffers.
 // D = 128: every tensor of D channels is held as two halves of 64 channels (128-byte rows, the
 // 128-byte swizzle's width), each laid out exactly like a D = 64 operand; the products over D run
 // once per half.
@@ -204,6 +208,9 @@ enum Bar {
     kOEmpty = kOFull + 2, kTFull = kOEmpty + 2, kTEmpty = kTFull + kTileRing,
     kFin = kTEmpty + kTileRing, kAuxSync = kFin + 1, kNumBars = kAuxSync + kBwdGroups
 };
+// The forward's third score buffer (three-buffer plans) has its score-full barrier at kSFull + 2, the
+// first score-empty slot: the forward releases its buffers through the P V product's barrier and
+// never uses the score-empty ones.
 
 // ---------------------------------------------------------------------------------------------
 // Tile stream and tile geometry
@@ -854,7 +861,7 @@ struct MmaIssuer {
     }
 };
 
-// TMEM column bases.  fwd (256 columns): S[b] at b*NC, O[b] at 256 - (2 - b) * D.
+// TMEM column bases.  fwd (256 columns): S[b] at b*NC (b < 3 at D <= 32), O[b] at 256 - (2 - b) * D.
 // dQ (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dQ[b] at 512 - (2 - b) * D.
 // dKdV (512): S[b] at b*NC, dP[b] at (2 + b)*NC, dV[b] at 512 - (4 - 2b) * D, dK[b] = dV[b] + D.
 __device__ __forceinline__ uint32_t tm_s(const TilePlan& pl, uint32_t b) { return b * pl.NC; }
@@ -867,7 +874,7 @@ __device__ __forceinline__ uint32_t tm_acc(int which, uint32_t b) {
 
 // Forward: the update products O += P V of every chunk, issued by one lane as soon as the chunk's P is
 // written (and, for a tile's first chunk, its accumulator buffer has been read out).
-template <int D>
+template <int D, int SB>
 __device__ void pv_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
     constexpr uint32_t kS = stages_of(0, D);
     const WaitGuard err{p.err, p.wait_ns};
@@ -879,8 +886,9 @@ __device__ void pv_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, u
     while (ok && fetch_tile(smem, lay, bars, j, err, false, c, ok)) {
         const uint32_t ob = j & 1u;
         for (int ci = 0; ci < c.C; ++ci, ++g) {
-            const uint32_t pb = g & 1u, s = g % kS;
-            ok = mbar_spin(&bars[kPFull + pb], (g >> 1) & 1u, err, kSiteP);
+            constexpr uint32_t kSB = SB;
+            const uint32_t pb = g % kSB, s = g % kS;
+            ok = mbar_spin(&bars[kPFull + pb], (g / kSB) & 1u, err, kSiteP);
             if (ok && ci == 0 && j >= 2) ok = mbar_spin(&bars[kOEmpty + ob], ((j >> 1) - 1) & 1u, err, kSitePV);
             if (!ok) break;
             tc_fence_after();
@@ -896,7 +904,7 @@ __device__ void pv_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, u
 // The score products of every chunk, issued by one lane: S (or S^T) and the window bias, and in the
 // backward dP (or dP^T).  The forward's score buffer also holds that chunk's P, so it is free once the
 // product P V of the chunk two back is done; the backward's softmax releases it after reading.
-template <int D, int WHICH>
+template <int D, int WHICH, int SB>
 __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars, uint32_t tmem) {
     constexpr uint32_t kS = stages_of(WHICH, D);
     const WaitGuard err{p.err, p.wait_ns};
@@ -913,10 +921,11 @@ __device__ void score_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay
         if (!mbar_wait(&bars[kQFull + qs], (j / kTS) & 1, err, kSiteQ)) break;
         ChunkCursor cur = cursor_begin();
         for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-            const uint32_t s = g % kS, sb = g & 1;
+            constexpr uint32_t kSB = SB;
+            const uint32_t s = g % kS, sb = g % kSB;
             ok = mbar_spin(&bars[kKVFull + s], (g / kS) & 1, err, kSiteKV);
-            if (ok && g >= 2)
-                ok = mbar_spin(&bars[(WHICH == 0 ? kPEmpty : kSEmpty) + sb], ((g >> 1) - 1) & 1, err, kSiteS);
+            if (ok && g >= kSB)
+                ok = mbar_spin(&bars[(WHICH == 0 ? kPEmpty : kSEmpty) + sb], ((g / kSB) - 1) & 1, err, kSiteS);
             if (!ok) break;
             tc_fence_after();
             mi.rows_x_chunk(tmem + tm_s(pl, sb), lay.tile(qs, 0), lay.chunk(s, 0), neg);  // S or S^T
@@ -1037,7 +1046,7 @@ __device__ __forceinline__ void unpack2(uint32_t v, float& lo, float& hi) {
 // chunk's groups [gb - gdone, gb) already written as P are rescaled.  Then P = exp2(S sl2 - m) is
 // written over the scores as packed 16-bit pairs: group gi's P takes columns 8 gi .. 8 gi + 7 of
 // the buffer, which held the scores of group gi / 2, read before this write (or outside the run).
-template <int D, int N, bool F16>
+template <int D, int N, bool F16, int SB>
 __device__ __forceinline__ bool fwd_part(const FwdCtx& x, uint32_t g, uint32_t tS, int gb, int cnt, int gdone,
                                          float& m, uint64_t (&lsum)[4]) {
     uint32_t v[N][16];
@@ -1071,7 +1080,8 @@ __device__ __forceinline__ bool fwd_part(const FwdCtx& x, uint32_t g, uint32_t t
     if (__any_sync(0xffffffffu, rescale)) {
         // O holds the products of chunks g-1, g-2, ...: wait for the last one (before a tile's first
         // chunk that is the previous tile's, harmless; for g = 0 the parity test passes at once)
-        if (!warp_wait(&x.bars[kPEmpty + ((g - 1) & 1u)], ((g - 1) >> 1) & 1u, x.err, kSitePV)) return false;
+        constexpr uint32_t kSB = SB;
+        if (!warp_wait(&x.bars[kPEmpty + (g - 1) % kSB], ((g - 1) / kSB) & 1u, x.err, kSitePV)) return false;
         tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < D; cc += 8) {
@@ -1123,24 +1133,25 @@ __device__ __forceinline__ bool fwd_part(const FwdCtx& x, uint32_t g, uint32_t t
 // One chunk of the online softmax for a warp whose keys lie in groups [glo, glo + n) (n <= 6):
 // runs of up to four groups in one part, longer runs in two parts of at most three (register
 // budget).  Groups outside the run hold scores, not P, so they are zeroed once every score of the
-// run has been read; then the P operand (score buffer g & 1) is released to the P V lane.
-template <int D, bool F16>
+// run has been read; then the P operand (its score buffer) is released to the P V lane.
+template <int D, bool F16, int SB>
 __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, int n, float& m,
                                           uint64_t (&lsum)[4]) {
-    const uint32_t tS = x.tS0 + (g & 1u) * x.tS_step;
+    constexpr uint32_t kSB = SB;
+    const uint32_t tS = x.tS0 + (g % kSB) * x.tS_step;
     bool ok = true;
     switch (n) {
         case 0: break;
-        case 1: ok = fwd_part<D, 1, F16>(x, g, tS, glo, 1, 0, m, lsum); break;
-        case 2: ok = fwd_part<D, 2, F16>(x, g, tS, glo, 2, 0, m, lsum); break;
-        case 3: ok = fwd_part<D, 3, F16>(x, g, tS, glo, 3, 0, m, lsum); break;
-        case 4: ok = fwd_part<D, 4, F16>(x, g, tS, glo, 4, 0, m, lsum); break;
+        case 1: ok = fwd_part<D, 1, F16, SB>(x, g, tS, glo, 1, 0, m, lsum); break;
+        case 2: ok = fwd_part<D, 2, F16, SB>(x, g, tS, glo, 2, 0, m, lsum); break;
+        case 3: ok = fwd_part<D, 3, F16, SB>(x, g, tS, glo, 3, 0, m, lsum); break;
+        case 4: ok = fwd_part<D, 4, F16, SB>(x, g, tS, glo, 4, 0, m, lsum); break;
         default:
             // groups [glo, glo + 3), then [glo + 3, glo + n); one loop body keeps register use at
             // that of a single part
 #pragma unroll 1
             for (int part = 0; part < 2 && ok; ++part)
-                ok = fwd_part<D, 3, F16>(x, g, tS, glo + 3 * part, part == 0 ? 3 : n - 3, 3 * part, m, lsum);
+                ok = fwd_part<D, 3, F16, SB>(x, g, tS, glo + 3 * part, part == 0 ? 3 : n - 3, 3 * part, m, lsum);
             break;
     }
     if (!ok) return false;
@@ -1149,7 +1160,7 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     tmem_st_wait();
     tc_fence_before();
     __syncwarp();
-    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + (g & 1u)]);
+    if (x.lane == 0) mbar_arrive(&x.bars[kPFull + g % kSB]);
     return true;
 }
 
@@ -1177,7 +1188,7 @@ __device__ __forceinline__ bool fwd_epilogue(const TcParams& p, const FwdCtx& x,
     return true;
 }
 
-template <int D, bool F16>
+template <int D, bool F16, int SB>
 __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayout& lay, uint64_t* bars,
                                  uint32_t tmem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, row = warp * 32 + lane;
@@ -1210,12 +1221,12 @@ __device__ void fwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             uint64_t lsum[4] = {0ull, 0ull, 0ull, 0ull};  // four packed partial sums (independent chains)
             ChunkCursor cur = cursor_begin();
             for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
-                ok = warp_wait(&bars[kSFull + (g & 1)], (g >> 1) & 1, x.err, kSiteS);
+                ok = warp_wait(&bars[kSFull + g % SB], (g / SB) & 1, x.err, kSiteS);
                 if (!ok) break;
                 tc_fence_after();
                 int glo, n;
                 chunk_range(pl, cur, wu, glo, n);
-                ok = fwd_chunk<D, F16>(x, g, glo, n, m, lsum);
+                ok = fwd_chunk<D, F16, SB>(x, g, glo, n, m, lsum);
                 if (!ok) break;
             }
             if (!ok) break;
@@ -1506,7 +1517,7 @@ __device__ __forceinline__ uint8_t* aligned_smem(uint8_t* raw) {
     return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
 }
 
-template <int D, int WHICH>
+template <int D, int WHICH, int SB>
 __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     constexpr uint32_t kSoft = 4 * nwg_of(WHICH);
     constexpr uint32_t kChunkWarps = chunk_warps_of(WHICH);
@@ -1514,11 +1525,11 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
         mbar_init(&bars[kQFull + i], 1);
         mbar_init(&bars[kQEmpty + i], 1);
         mbar_init(&bars[kSFull + i], 1);
-        mbar_init(&bars[kSEmpty + i], kChunkWarps);
+        if (SB == 2) mbar_init(&bars[kSEmpty + i], kChunkWarps);  // (three buffers: slot 0 is the third score-full)
         mbar_init(&bars[kOFull + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
         mbar_init(&bars[kOEmpty + i], kSoft);
     }
-    for (int i = 0; i < pbufs_of(WHICH); ++i) {
+    for (int i = 0; i < (WHICH == 0 ? SB : pbufs_of(WHICH)); ++i) {
         mbar_init(&bars[kPFull + i], kChunkWarps);
         mbar_init(&bars[kPEmpty + i], nupd_of(WHICH) > 0 ? nupd_of(WHICH) : 1);
     }
@@ -1533,10 +1544,11 @@ __device__ __forceinline__ void init_barriers(uint64_t* bars) {
     mbar_init(&bars[kFin], 1 + nupd_of(WHICH));
     if (WHICH == 2)
         for (int w = 0; w < kBwdGroups; ++w) mbar_init(&bars[kAuxSync + w], 4);  // the warpgroup's warps
+    if (SB == 3) mbar_init(&bars[kSFull + 2], 1);                               // the forward's third score buffer
     fence_barrier_init();
 }
 
-template <int D, int WHICH, bool F16>
+template <int D, int WHICH, bool F16, int SB>
 __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = aligned_smem(smem_raw);
@@ -1550,7 +1562,7 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
 
     if (warp == kSoftWarps) {
         if (lane == 0) {
-            init_barriers<D, WHICH>(bars);
+            init_barriers<D, WHICH, SB>(bars);
             for (int m = 0; m < 4; ++m) tma_prefetch_desc(&p.tm[m]);
         }
         __syncwarp();
@@ -1567,16 +1579,16 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         // each warpgroup's budget is set in the branch that runs its code
         if (warp < kSoftWarps) {
             reg_alloc<kFwdSoftRegs>();
-            fwd_softmax_loop<D, F16>(p, smem, lay, bars, tmem);
+            fwd_softmax_loop<D, F16, SB>(p, smem, lay, bars, tmem);
         } else {
             reg_dealloc<kFwdCtrlRegs>();
             if (warp == kSoftWarps) {
                 producer_loop<D, WHICH>(p, smem, lay, bars);
             } else if (warp == kSoftWarps + 1) {
-                if (lane == 0) score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+                if (lane == 0) score_loop<D, WHICH, SB>(p, smem, lay, bars, tmem);
                 __syncwarp();
             } else if (warp == kSoftWarps + 2) {
-                if (lane == 0) pv_loop<D>(p, smem, lay, bars, tmem);
+                if (lane == 0) pv_loop<D, SB>(p, smem, lay, bars, tmem);
                 __syncwarp();
             }
         }
@@ -1584,7 +1596,7 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
         if (warp == kSoftWarps) {
             producer_loop<D, WHICH>(p, smem, lay, bars);
         } else if (warp == kSoftWarps + 1) {
-            if (lane == 0) score_loop<D, WHICH>(p, smem, lay, bars, tmem);
+            if (lane == 0) score_loop<D, WHICH, SB>(p, smem, lay, bars, tmem);
             __syncwarp();
         } else if (warp >= kSoftWarps + 2) {
             if (lane == 0) update_loop<D, WHICH>(p, smem, lay, bars, tmem, warp - (kSoftWarps + 2));
@@ -1612,10 +1624,10 @@ __global__ void __launch_bounds__(threads_of(WHICH), WHICH == 0 ? 2 : 1) tc_kern
     }
 }
 
-template <int D, int WHICH, bool F16>
-int launch_tc(const TcParams& p0, cudaStream_t stream) {
+template <int D, int WHICH, bool F16, int SB>
+int launch_tc_sb(const TcParams& p0, cudaStream_t stream) {
     const int smem = p0.plan.smem_bytes;
-    auto kernel = tc_kernel<D, WHICH, F16>;
+    auto kernel = tc_kernel<D, WHICH, F16, SB>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return static_cast<int>(e);
     if (p0.plan.ctas <= 0) return 0;
@@ -1634,6 +1646,16 @@ int launch_tc(const TcParams& p0, cudaStream_t stream) {
     }
     kernel<<<dim3(static_cast<unsigned>(grid)), dim3(threads_of(WHICH)), smem, stream>>>(p);
     return static_cast<int>(cudaGetLastError());
+}
+
+// The forward at D <= 32 comes in two forms, with two or three score buffers, as its plan says; the
+// three-buffer kernels are instantiated in a translation unit of their own (na_tc_sb3.cu).
+template <int D, int WHICH, bool F16>
+int launch_tc(const TcParams& p, cudaStream_t stream) {
+    if constexpr (WHICH == 0 && D <= 32) {
+        if (p.plan.sbufs == 3) return launch_fwd_tc_sb3(p, stream);
+    }
+    return launch_tc_sb<D, WHICH, F16, 2>(p, stream);
 }
 
 }  // namespace

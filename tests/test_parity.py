@@ -35,11 +35,13 @@ SMALL = [
     ("bf16", (5, 9, 33), 2, 32, (5, 9, 3), (1, 1, 8), 1),
     ("bf16", (16, 8), 1, 32, (1, 1), (1, 1), 1),            # k = 1: O = V, dQ = dK = 0
     ("bf16", (6, 5, 70), 1, 32, (3, 5, 1), (2, 1, 1), 3),   # short axes: windows touch both borders
+    ("bf16", (8, 20, 20), 1, 32, (5, 7, 7), (1, 1, 1), 1),  # long tiles: the forward's three score buffers
     # fp16 operands on the same tensor-core kernels
     ("fp16", (40, 37), 3, 32, (5, 7), (1, 1), 2),
     ("fp16", (300,), 1, 16, (13,), (3,), 1),
     ("fp16", (6, 20, 19), 2, 32, (3, 5, 5), (1, 1, 1), 1),
     ("fp16", (41, 38), 2, 64, (13, 13), (2, 2), 1),
+    ("fp16", (9, 17, 19), 2, 16, (5, 7, 7), (1, 1, 1), 1),  # three score buffers, D = 16
     ("fp16", (16, 8), 1, 32, (1, 1), (1, 1), 1),            # k = 1
     # D = 128: two 64-channel halves per operand; one forward CTA per SM; single-buffered dK/dV
     ("bf16", (33, 30), 2, 128, (7, 5), (1, 2), 1),
