@@ -41,6 +41,9 @@ CASES_TMA = [
     ("bf16", (9, 70), 8, 32, (3, 17), (1, 1), 1),            # innermost kernel 17: a 32-query span
     ("fp16", (100,), 8, 16, (13,), (3,), 2),
     ("bf16", (5, 7, 9), 8, 64, (5, 7, 9), (1, 1, 1), 1),      # kernel == extent: full attention
+    # several tensor-core logits strips (129 - k2 class positions each) along the innermost axis
+    ("bf16", (4, 300), 8, 32, (3, 9), (1, 1), 1),
+    ("fp16", (3, 261), 8, 16, (3, 7), (1, 2), 1),
 ]
 
 
