@@ -22,6 +22,7 @@ SMALL = [
     ("fp32", (7, 9), 2, 128, (7, 9), (1, 1), 1),            # kernel == extent: full attention
     ("fp32", (10, 23), 3, 64, (3, 7), (2, 3), 1),           # key quads over unequal classes (dK/dV quads from k2 >= 7)
     ("fp32", (4, 6, 19), 2, 16, (3, 3, 9), (1, 2, 2), 2),   # quads of one class position past a class end
+    ("fp32", (300,), 2, 32, (63,), (2,), 1),                # a 63-key window on the quad kernels
     ("bf16", (40, 37), 3, 32, (5, 7), (1, 1), 2),
     ("bf16", (33, 45), 2, 32, (9, 9), (1, 1), 1),
     ("bf16", (200,), 2, 32, (7,), (1,), 2),
@@ -36,6 +37,9 @@ SMALL = [
     ("bf16", (16, 8), 1, 32, (1, 1), (1, 1), 1),            # k = 1: O = V, dQ = dK = 0
     ("bf16", (6, 5, 70), 1, 32, (3, 5, 1), (2, 1, 1), 3),   # short axes: windows touch both borders
     ("bf16", (8, 20, 20), 1, 32, (5, 7, 7), (1, 1, 1), 1),  # long tiles: the forward's three score buffers
+    ("bf16", (1000,), 2, 32, (255,), (1,), 1),               # a 255-key window (10-16 chunks per tile)
+    ("fp16", (64, 64), 2, 32, (31, 31), (2, 2), 1),         # 31x31 windows, dilation 2 (three score buffers)
+    ("bf16", (40, 40), 1, 64, (39, 39), (1, 1), 1),         # windows of 39x39 on a 40x40 grid
     # fp16 operands on the same tensor-core kernels
     ("fp16", (40, 37), 3, 32, (5, 7), (1, 1), 2),
     ("fp16", (300,), 1, 16, (13,), (3,), 1),
