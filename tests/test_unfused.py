@@ -29,6 +29,9 @@ CASES = [
     ("fp16", (13, 18), 2, 32, (5, 7), (1, 2), 1),
     ("fp16", (5, 7, 9), 2, 16, (5, 7, 9), (1, 1, 1), 1),      # kernel == extent: full attention
     ("fp16", (16, 8), 1, 64, (1, 1), (1, 1), 1),              # k = 1
+    # rows of 129-256 weights: the softmax in blocks of 8 rows, and a tail of 5 rows (861 rows)
+    ("bf16", (7, 41), 3, 32, (5, 29), (1, 1), 1),
+    ("fp16", (6, 8, 30), 2, 16, (3, 5, 11), (1, 1, 2), 1),
 ]
 
 # Shapes whose weights rows (heads * K offsets) are a multiple of 16 bytes, the innermost kernel size at
