@@ -38,6 +38,7 @@ SMALL = [
     ("bf16", (6, 5, 70), 1, 32, (3, 5, 1), (2, 1, 1), 3),   # short axes: windows touch both borders
     ("bf16", (8, 20, 20), 1, 32, (5, 7, 7), (1, 1, 1), 1),  # long tiles: the forward's three score buffers
     ("bf16", (1000,), 2, 32, (255,), (1,), 1),               # a 255-key window (10-16 chunks per tile)
+    ("bf16", (96, 96), 8, 32, (7, 7), (1, 1), 1),            # 576 tiles: several tiles per persistent CTA
     ("fp16", (64, 64), 2, 32, (31, 31), (2, 2), 1),         # 31x31 windows, dilation 2 (three score buffers)
     ("bf16", (40, 40), 1, 64, (39, 39), (1, 1), 1),         # windows of 39x39 on a 40x40 grid
     # fp16 operands on the same tensor-core kernels
