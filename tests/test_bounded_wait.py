@@ -15,17 +15,21 @@ from na_testlib import check_full, host, run_gpu
 
 NA_ERR_TIMEOUT = 5
 # wait sites that can give up first when a halo chunk never arrives: the chunk itself, the scores
-# computed from it, the MMA lane's polling loop, the producer waiting to refill the slot
+# computed from it (or a free score buffer), the P operand, the producer waiting to refill the slot
 SITES = {2, 3, 4, 6}
+# a short-tile shape and a long-tile one (its forward plan takes three score buffers)
+SHAPES = {"short": ((40, 37), (5, 7), (1, 1)), "long": ((8, 20, 20), (5, 7, 7), (1, 1, 1))}
 
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("phase", ["fwd", "bwd"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-def test_a_wait_that_runs_out_is_reported_and_the_next_launch_is_clean(cuda_lib, phase, dtype):
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_a_wait_that_runs_out_is_reported_and_the_next_launch_is_clean(cuda_lib, phase, dtype, shape):
     import neighborhood_attention_fwd_gb300 as na
 
-    w = nain.small_workload(dtype, (40, 37), 2, 32, (5, 7), (1, 1), B=1, seed=31)
+    spatial, kernel, dilation = SHAPES[shape]
+    w = nain.small_workload(dtype, spatial, 2, 32, kernel, dilation, B=1, seed=31)
     t = {k: v.cuda() for k, v in nain.make_inputs(w, device="cpu").items()}
     q, k, v, dO = t["q"], t["k"], t["v"], t["dO"]
     o = torch.empty_like(q)
