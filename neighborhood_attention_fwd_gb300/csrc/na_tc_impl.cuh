@@ -408,6 +408,13 @@ __device__ __forceinline__ void cursor_next(const TilePlan& pl, const Cta& c, Ch
     }
 }
 
+// Steps a cursor N chunks on.
+template <int N>
+__device__ __forceinline__ void cursor_steps(const TilePlan& pl, const Cta& c, ChunkCursor& k) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) cursor_next(pl, c, k);
+}
+
 // The run of 16-column groups [glo, glo + n) of a chunk that holds every key (column) inside the
 // union of a warp's windows.  Chunk column = (y * G1 + z) * G2 + x for local coordinates (y, z, x).
 __device__ __forceinline__ void chunk_range(const TilePlan& pl, const ChunkCursor& k, const WarpUnion& u, int& glo,
@@ -1410,10 +1417,21 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
             x.nl2 = f2(-lse2, -lse2);
             x.dl2 = f2(dlt, dlt);
             ChunkCursor cur = cursor_begin();
-            for (int ci = 0; ci < c.C; ++ci, ++g, cursor_next(pl, c, cur)) {
+            // dQ visits only the warpgroup's chunks (its first of the tile, then every other one); dK/dV
+            // steps through every chunk and skips the other warpgroup's
+            constexpr bool kJump = kAlt && WHICH == 1;
+            constexpr int kStep = kJump ? 2 : 1;
+            const uint32_t gend = g + static_cast<uint32_t>(c.C);
+            int ci = 0;
+            if (kJump && (g & 1u) != static_cast<uint32_t>(wg)) {
+                ++ci;
+                ++g;
+                cursor_next(pl, c, cur);
+            }
+            for (; ci < c.C; ci += kStep, g += kStep, cursor_steps<kStep>(pl, c, cur)) {
                 constexpr uint32_t kPB = pbufs_of(WHICH);
                 const uint32_t sb = g & 1, pb = g % kPB;
-                if (kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
+                if (!kJump && kAlt && (g & 1u) != static_cast<uint32_t>(wg)) continue;   // the other warpgroup's chunk
                 // dK/dV: the column's values, unless the previous chunk of the warpgroup prefetched them
                 if (WHICH == 2 && !pre) aux_load(p, c, tb, cur, ac);
                 ok = warp_wait(&bars[kSFull + sb], (g >> 1) & 1, err, kSiteS);
@@ -1494,6 +1512,7 @@ __device__ void bwd_softmax_loop(const TcParams& p, uint8_t* smem, const TcLayou
                 if (lane == 0) mbar_arrive(&bars[kPFull + pb]);
             }
             if (!ok) break;
+            if (kJump) g = gend;
             next = BwdEpilogue{true, geo.valid, geo.token * p.heads + c.h, ob, j};
         }
         // the previous tile's epilogue, deferred until this tile's chunks are done; with a single
