@@ -1147,11 +1147,14 @@ __device__ __forceinline__ bool fwd_chunk(const FwdCtx& x, uint32_t g, int glo, 
     constexpr uint32_t kSB = SB;
     const uint32_t tS = x.tS0 + (g % kSB) * x.tS_step;
     bool ok = true;
+    // runs of one to three groups share the three-group part (its count is a run-time argument), so
+    // the softmax warps' hot code holds two part bodies instead of four: smaller code for the
+    // instruction cache, which the five roles of a CTA share
     switch (n) {
         case 0: break;
-        case 1: ok = fwd_part<D, 1, F16, SB>(x, g, tS, glo, 1, 0, m, lsum); break;
-        case 2: ok = fwd_part<D, 2, F16, SB>(x, g, tS, glo, 2, 0, m, lsum); break;
-        case 3: ok = fwd_part<D, 3, F16, SB>(x, g, tS, glo, 3, 0, m, lsum); break;
+        case 1:
+        case 2:
+        case 3: ok = fwd_part<D, 3, F16, SB>(x, g, tS, glo, n, 0, m, lsum); break;
         case 4: ok = fwd_part<D, 4, F16, SB>(x, g, tS, glo, 4, 0, m, lsum); break;
         default:
             // groups [glo, glo + 3), then [glo + 3, glo + n); one loop body keeps register use at
